@@ -1,0 +1,327 @@
+"""Plain CPU oracle of the Llama2 decoder forward (prefill and decode), fp64.
+
+TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and the
+cpu_baseline / reference legs of bench.py may import or call this module. The
+CUDA library never reaches it and it shares no code, constant or table with
+the CUDA library; the only module both sides use is the seeded input
+generator (llama2_decoder_forward_gb300.synth), which holds none of the
+method's arithmetic.
+
+Everything is computed in float64 from the stored input values (bf16 inputs are
+widened exactly); no intermediate value is rounded. Each step follows the
+pages' definition in their order, with numpy's matmul as the only library
+primitive:
+
+  embed -> for each layer [ h += attn(rmsnorm(h)); h += ffn(rmsnorm(h)) ]
+        -> logits = lm_head(rmsnorm(h))
+("Llama2架构与推理全解析" §2.3, the pseudocode of the main computation.)
+
+Readings taken where the pages are garbled or silent (listed again in the
+design notes):
+  * RMSNorm: y = x / sqrt(mean(x^2) + eps) * gamma; the operator between
+    mean(x^2) and eps was lost in extraction and is read as "+" (§1.2).
+  * RoPE pairs adjacent dims (2j, 2j+1) as one complex number, the form
+    f(q, m) = (W_q x_m) * e^{i m theta} of "Llama2架构全景解析" §1.1, with
+    theta_j = base^(-2j/d), j = 0 .. d/2-1 (§1.4: "high dims fast, low dims slow"
+    read as pair 0 fastest). Positions are 0-based.
+  * Only Q and K are rotated; the cache stores the rotated K and the plain V.
+  * Scores are scaled by 1/sqrt(head_dim); the causal mask lets a query at
+    position m see keys 0..m, the new token included (§2.3, §2.4).
+  * GQA: query head h reads K/V head floor(h / G), G = n_q / n_kv (§1.5).
+  * No biases anywhere; embedding and LM head are separate matrices (§2.3).
+  * Greedy choice: argmax, lowest index on ties (§2.5).
+
+Parity status: every function here is pinned by tests/test_oracle_pins.py
+(closed forms, invariants, library routines, brute force); the end-to-end
+logits on random weights have no printed value to match and rest on the pinned
+parts plus the decode-equals-prefill and paged-equals-contiguous checks.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+f64 = np.float64
+
+
+def as64(t) -> np.ndarray:
+    """Widen a torch tensor or array (fp32 / bf16) to float64 exactly."""
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            return t.detach().to("cpu", torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(t, dtype=f64)
+
+
+# --------------------------------------------------------------------------
+# Layer operations
+# --------------------------------------------------------------------------
+
+def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis, each token on its own
+    ("Llama2架构与推理全解析" §1.2): y = x / sqrt(mean(x^2) + eps) * gamma."""
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * gamma
+
+
+def linear(u: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """u @ W^T with W stored [out, in]; equal to the pages' x W with W [in, out]
+    (§1.3's SwiGLU(x) = (silu(x W_gate) * x W_up) W_down notation)."""
+    return u @ w.T
+
+
+def rope_frequencies(head_dim: int, theta: float) -> np.ndarray:
+    """theta_j = base^(-2j/d) for pair j = 0 .. d/2-1 (§1.4)."""
+    j = np.arange(head_dim // 2, dtype=f64)
+    return np.power(f64(theta), -2.0 * j / head_dim)
+
+
+def rope(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotate each adjacent pair (x[2j], x[2j+1]) of every head by angle
+    m * theta_j, m the token's position ("Llama2架构与推理全解析" §1.4;
+    "Llama2架构全景解析" §1.1). x: [rows, heads, d]; positions: [rows]."""
+    d = x.shape[-1]
+    phi = np.asarray(positions, dtype=f64)[:, None] * rope_frequencies(d, theta)[None, :]
+    c = np.cos(phi)[:, None, :]
+    s = np.sin(phi)[:, None, :]
+    a = x[..., 0::2]
+    b = x[..., 1::2]
+    out = np.empty_like(x, dtype=f64)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z * sigmoid(z) (§1.3)."""
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_ffn(u, w_gate, w_up, w_down) -> np.ndarray:
+    """SwiGLU(u) = (silu(u W_gate) * (u W_up)) W_down (§1.3)."""
+    return linear(silu(linear(u, w_gate)) * linear(u, w_up), w_down)
+
+
+def softmax(s: np.ndarray) -> np.ndarray:
+    """Softmax along the last axis with the row maximum subtracted before exp
+    (the logit-max subtraction of "LLM架构全景解析" §3.2)."""
+    z = s - np.max(s, axis=-1, keepdims=True)
+    e = np.exp(z)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """Scaled dot-product attention of one query over the given keys
+    (§2.3): p = softmax(K q / sqrt(d)); o = p V. q [d]; K, V [n, d]."""
+    d = q.shape[-1]
+    p = softmax((K @ q) / np.sqrt(f64(d)))
+    return p @ V
+
+
+def gqa_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, n_keys: int) -> np.ndarray:
+    """All query heads of one token over keys 0..n_keys-1 of its sequence (§1.5).
+    q [n_q, d]; K, V [n_kv, S, d]. Head h uses K/V head h // G."""
+    n_q = q.shape[0]
+    n_kv = K.shape[0]
+    G = n_q // n_kv
+    out = np.empty_like(q, dtype=f64)
+    for h in range(n_q):
+        g = h // G
+        out[h] = attend(q[h], K[g, :n_keys], V[g, :n_keys])
+    return out
+
+
+# --------------------------------------------------------------------------
+# One decoder layer
+# --------------------------------------------------------------------------
+
+def _split_qkv(qkv, n_q, n_kv, d):
+    rows = qkv.shape[0]
+    q = qkv[:, : n_q * d].reshape(rows, n_q, d)
+    k = qkv[:, n_q * d: (n_q + n_kv) * d].reshape(rows, n_kv, d)
+    v = qkv[:, (n_q + n_kv) * d:].reshape(rows, n_kv, d)
+    return q, k, v
+
+
+def layer_decode(x, lw, shape, K, V, positions):
+    """Decode step of one layer (§2.3 main computation, §2.4 KV cache).
+
+    x: [B, H] hidden input. lw: dict of float64 weights. K, V: per-sequence
+    caches [B, n_kv, S_cap, d] (float64, updated in place: the new token's
+    rotated K and its V are written at slot positions[b]). Returns the
+    layer output [B, H].
+    """
+    n_q, n_kv, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    pos = np.asarray(positions, dtype=np.int64)
+    u = rmsnorm(x, lw["attn_norm"], shape.rms_eps)
+    q, k, v = _split_qkv(linear(u, lw["wqkv"]), n_q, n_kv, d)
+    q = rope(q, pos, shape.rope_theta)
+    k = rope(k, pos, shape.rope_theta)
+    B = x.shape[0]
+    o = np.empty((B, n_q, d), dtype=f64)
+    for b in range(B):
+        m = int(pos[b])
+        K[b, :, m] = k[b]
+        V[b, :, m] = v[b]
+        o[b] = gqa_attention(q[b], K[b], V[b], m + 1)
+    h = x + linear(o.reshape(B, n_q * d), lw["wo"])
+    u2 = rmsnorm(h, lw["ffn_norm"], shape.rms_eps)
+    return h + swiglu_ffn(u2, lw["w_gate"], lw["w_up"], lw["w_down"])
+
+
+def layer_prefill(x, lw, shape, K, V, rows=None):
+    """Prefill of one layer for a fresh prompt (§2.1): x [B, T, H], token t at
+    position t. Writes rotated K and V of every prompt token into K, V
+    ([B, n_kv, S_cap, d], in place) and returns the output rows.
+
+    rows: optional list of token indices whose outputs are wanted (all by
+    default); K/V of every token are still computed, since later rows read them.
+    """
+    n_q, n_kv, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    B, T, H = x.shape
+    rows = list(range(T)) if rows is None else list(rows)
+    pos_all = np.arange(T)
+    out = np.empty((B, len(rows), H), dtype=f64)
+    q_rows = np.asarray(rows)
+    wq = lw["wqkv"][: n_q * d]
+    wkv = lw["wqkv"][n_q * d:]
+    for b in range(B):
+        u = rmsnorm(x[b], lw["attn_norm"], shape.rms_eps)
+        kv = linear(u, wkv)
+        k = kv[:, : n_kv * d].reshape(T, n_kv, d)
+        v = kv[:, n_kv * d:].reshape(T, n_kv, d)
+        k = rope(k, pos_all, shape.rope_theta)
+        K[b, :, :T] = np.transpose(k, (1, 0, 2))
+        V[b, :, :T] = np.transpose(v, (1, 0, 2))
+        q = linear(u[q_rows], wq).reshape(len(rows), n_q, d)
+        q = rope(q, q_rows, shape.rope_theta)
+        o = np.empty((len(rows), n_q, d), dtype=f64)
+        for i, t in enumerate(rows):
+            o[i] = gqa_attention(q[i], K[b], V[b], t + 1)
+        h = x[b, q_rows] + linear(o.reshape(len(rows), n_q * d), lw["wo"])
+        u2 = rmsnorm(h, lw["ffn_norm"], shape.rms_eps)
+        out[b] = h + swiglu_ffn(u2, lw["w_gate"], lw["w_up"], lw["w_down"])
+    return out
+
+
+# --------------------------------------------------------------------------
+# Whole model
+# --------------------------------------------------------------------------
+
+def embed(table: np.ndarray, tokens) -> np.ndarray:
+    """Row lookup in the [vocab, hidden] embedding table (§2.3)."""
+    return table[np.asarray(tokens, dtype=np.int64)]
+
+
+def lm_head(h, final_norm, w_lm, eps):
+    """logits = lm_head(rmsnorm(h)) with its own gain (§2.3 pseudocode)."""
+    return linear(rmsnorm(h, final_norm, eps), w_lm)
+
+
+def greedy(logits: np.ndarray) -> np.ndarray:
+    """Greedy choice: index of the largest logit, lowest index on ties (§2.5)."""
+    return np.argmax(logits, axis=-1).astype(np.int32)
+
+
+class Model:
+    """fp64 copy of a model's weights plus per-sequence caches."""
+
+    def __init__(self, shape, weights: dict, batch: int, capacity: int):
+        self.shape = shape
+        self.embed_t = as64(weights["embed"]) if weights.get("embed") is not None else None
+        self.final_norm = as64(weights["final_norm"]) if weights.get("final_norm") is not None else None
+        self.lm = as64(weights["lm_head"]) if weights.get("lm_head") is not None else None
+        self.layers = [{k: as64(v) for k, v in lw.items()} for lw in weights["layers"]]
+        n_kv, d = shape.n_kv_heads, shape.head_dim
+        self.K = [np.zeros((batch, n_kv, capacity, d)) for _ in self.layers]
+        self.V = [np.zeros((batch, n_kv, capacity, d)) for _ in self.layers]
+
+    def prefill(self, tokens):
+        """All prompt rows through every layer; returns logits of every row
+        [B, T, V] (the API keeps only the last row; the oracle keeps all)."""
+        h = embed(self.embed_t, tokens)
+        for l, lw in enumerate(self.layers):
+            h = layer_prefill(h, lw, self.shape, self.K[l], self.V[l])
+        return lm_head(h, self.final_norm, self.lm, self.shape.rms_eps)
+
+    def decode(self, tokens, positions):
+        """One token per sequence at its position; returns logits [B, V]."""
+        h = embed(self.embed_t, tokens)
+        for l, lw in enumerate(self.layers):
+            h = layer_decode(h, lw, self.shape, self.K[l], self.V[l], positions)
+        return lm_head(h, self.final_norm, self.lm, self.shape.rms_eps)
+
+
+def generate_greedy(model: Model, prompt, n_steps: int):
+    """Prefill, then n_steps greedy decode steps, each feeding the previous
+    choice (§3.4 generation loop). Returns (ids [B, n_steps+1], logits
+    [B, n_steps+1, V]) where entry 0 comes from the prefill's last row."""
+    prompt = np.asarray(prompt)
+    B, T = prompt.shape
+    lg = model.prefill(prompt)[:, -1]
+    ids = [greedy(lg)]
+    logits = [lg]
+    for s in range(n_steps):
+        pos = np.full(B, T + s)
+        lg = model.decode(ids[-1], pos)
+        ids.append(greedy(lg))
+        logits.append(lg)
+    return np.stack(ids, 1), np.stack(logits, 1)
+
+
+# --------------------------------------------------------------------------
+# Paged cache
+# --------------------------------------------------------------------------
+
+def gather_paged(pool: np.ndarray, table_row, n_tokens: int, page_size: int) -> np.ndarray:
+    """Logical cache of one sequence from a paged pool
+    ("Llama2架构全景解析" §2.3, PagedAttention): token m lives in page
+    table_row[m // P] at offset m % P. pool: [n_pages, n_kv, P, d].
+    Returns [n_kv, n_tokens, d]."""
+    n_kv, d = pool.shape[1], pool.shape[3]
+    out = np.empty((n_kv, n_tokens, d), dtype=f64)
+    for m in range(n_tokens):
+        out[:, m] = pool[int(table_row[m // page_size]), :, m % page_size]
+    return out
+
+
+def layer_decode_paged(x, lw, shape, Kpool, Vpool, table, positions, page_size):
+    """Decode step of one layer over a paged cache: gather each sequence's
+    pages into a logical contiguous cache, run layer_decode, and write the
+    new token's K/V back into its page slot."""
+    B = x.shape[0]
+    pos = np.asarray(positions, dtype=np.int64)
+    cap = int(pos.max()) + 1
+    n_kv, d = shape.n_kv_heads, shape.head_dim
+    K = np.zeros((B, n_kv, cap, d))
+    V = np.zeros((B, n_kv, cap, d))
+    for b in range(B):
+        n = int(pos[b])
+        K[b, :, :n] = gather_paged(Kpool, table[b], n, page_size)
+        V[b, :, :n] = gather_paged(Vpool, table[b], n, page_size)
+    out = layer_decode(x, lw, shape, K, V, pos)
+    for b in range(B):
+        m = int(pos[b])
+        page = int(table[b][m // page_size])
+        Kpool[page, :, m % page_size] = K[b, :, m]
+        Vpool[page, :, m % page_size] = V[b, :, m]
+    return out
+
+
+# --------------------------------------------------------------------------
+# Size facts
+# --------------------------------------------------------------------------
+
+def param_count(shape) -> int:
+    """Parameters of a model: embedding + LM head + per layer (Wqkv, Wo,
+    gate/up/down, two gains) + final gain."""
+    H, I, d = shape.hidden, shape.intermediate, shape.head_dim
+    per_layer = shape.qkv_rows * H + H * shape.n_q_heads * d + 3 * H * I + 2 * H
+    return 2 * shape.vocab * H + shape.n_layers * per_layer + H
+
+
+def kv_cache_bytes(shape, seq_len: int, bytes_per_elem: int) -> int:
+    """KV cache size = 2 x layers x KV heads x head dim x length x element
+    bytes ("Llama2架构与推理全解析" §2.4)."""
+    return 2 * shape.n_layers * shape.n_kv_heads * shape.head_dim * seq_len * bytes_per_elem

@@ -1,0 +1,354 @@
+"""Pins of the CPU oracle to facts other than itself: closed forms, invariants
+the pages state, library routines on special cases, brute force on tiny
+inputs and the numbers the pages print. CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+from oracle import llama_oracle as O
+from llama2_decoder_forward_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(7)
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_uniform_gamma_closed_form():
+    # gamma == c everywhere: RMS(y) = c * sqrt(ms / (ms + eps)).
+    x = rng.standard_normal((5, 64)) * 3.0
+    c, eps = 1.7, 1e-5
+    y = O.rmsnorm(x, np.full(64, c), eps)
+    ms = np.mean(x * x, axis=-1)
+    rms_y = np.sqrt(np.mean(y * y, axis=-1))
+    np.testing.assert_allclose(rms_y, c * np.sqrt(ms / (ms + eps)), rtol=1e-13)
+
+
+def test_rmsnorm_eps_inside_root_and_scale_invariance():
+    x = np.array([[3.0, 4.0]])            # mean(x^2) = 12.5
+    y = O.rmsnorm(x, np.ones(2), 0.5)
+    np.testing.assert_allclose(y, x / math.sqrt(13.0), rtol=1e-15)
+    # Scaling x by a leaves y unchanged up to eps: y(a z) / y(z) = sqrt((ms + eps) / (ms + eps / a^2)).
+    z = rng.standard_normal((3, 32))
+    ms = np.mean(z * z, axis=-1, keepdims=True)
+    ratio = O.rmsnorm(1e3 * z, np.ones(32), 1e-5) / O.rmsnorm(z, np.ones(32), 1e-5)
+    np.testing.assert_allclose(ratio, np.broadcast_to(np.sqrt((ms + 1e-5) / (ms + 1e-11)), ratio.shape),
+                               rtol=1e-13)
+
+
+def test_rmsnorm_matches_library_and_is_per_token():
+    x = rng.standard_normal((4, 48))
+    g = 1 + 0.1 * rng.standard_normal(48)
+    ref = F.rms_norm(torch.from_numpy(x), (48,), torch.from_numpy(g), eps=1e-5).numpy()
+    np.testing.assert_allclose(O.rmsnorm(x, g, 1e-5), ref, rtol=1e-13, atol=1e-14)
+    x2 = x.copy()
+    x2[1:] *= 5.0  # other tokens must not change token 0's output
+    np.testing.assert_array_equal(O.rmsnorm(x2, g, 1e-5)[0], O.rmsnorm(x, g, 1e-5)[0])
+
+
+# ---------------------------------------------------------------- RoPE
+
+def test_rope_hand_angles():
+    # d = 4, base 10000: theta_0 = 1, theta_1 = 10000^(-1/2) = 0.01.
+    np.testing.assert_allclose(O.rope_frequencies(4, 10000.0), [1.0, 0.01], rtol=1e-15)
+    e0 = np.array([[[1.0, 0.0, 0.0, 0.0]]])
+    y = O.rope(e0, [1], 10000.0)[0, 0]
+    np.testing.assert_allclose(y, [math.cos(1.0), math.sin(1.0), 0, 0], atol=1e-15)
+    e2 = np.array([[[0.0, 0.0, 1.0, 0.0]]])
+    y = O.rope(e2, [100], 10000.0)[0, 0]          # pair 1 turns by 100 * 0.01 = 1 rad
+    np.testing.assert_allclose(y, [0, 0, math.cos(1.0), math.sin(1.0)], atol=1e-14)
+    e1 = np.array([[[0.0, 1.0, 0.0, 0.0]]])       # (a, b) = (0, 1) -> (-sin, cos)
+    y = O.rope(e1, [2], 10000.0)[0, 0]
+    np.testing.assert_allclose(y[:2], [-math.sin(2.0), math.cos(2.0)], atol=1e-15)
+
+
+def test_rope_position_zero_is_identity_and_norm_preserved():
+    x = rng.standard_normal((6, 3, 64))
+    np.testing.assert_array_equal(O.rope(x, np.zeros(6), 10000.0), x)
+    y = O.rope(x, np.arange(6) * 517, 10000.0)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-13)
+
+
+def test_rope_relative_position_invariant():
+    # <R_m q, R_n k> depends only on m - n (§1.4).
+    d = 128
+    q = rng.standard_normal((1, 1, d))
+    k = rng.standard_normal((1, 1, d))
+    for delta in (0, 1, 7, 300):
+        vals = []
+        for n in (0, 5, 1000, 4000):
+            a = O.rope(q, [n + delta], 10000.0)[0, 0]
+            b = O.rope(k, [n], 10000.0)[0, 0]
+            vals.append(a @ b)
+        ref = O.rope(q, [delta], 10000.0)[0, 0] @ k[0, 0]
+        np.testing.assert_allclose(vals, ref, rtol=1e-9, atol=1e-9)
+
+
+def test_rope_matches_complex_form():
+    # f(q, m) = q * e^{i m theta}: pairs as complex numbers, via torch.polar.
+    d, T = 64, 9
+    x = torch.from_numpy(rng.standard_normal((T, 2, d)))
+    pos = torch.arange(T, dtype=torch.float64) * 37
+    freqs = 10000.0 ** (-torch.arange(0, d, 2, dtype=torch.float64) / d)
+    rot = torch.polar(torch.ones(T, d // 2, dtype=torch.float64), pos[:, None] * freqs[None])
+    xc = torch.view_as_complex(x.reshape(T, 2, d // 2, 2).contiguous())
+    ref = torch.view_as_real(xc * rot[:, None, :]).reshape(T, 2, d).numpy()
+    np.testing.assert_allclose(O.rope(x.numpy(), pos.numpy(), 10000.0), ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- softmax / attention
+
+def test_softmax_rows_sum_to_one_and_shift_invariant():
+    s = rng.standard_normal((7, 33)) * 10
+    p = O.softmax(s)
+    np.testing.assert_allclose(p.sum(-1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(O.softmax(s + 123.0), p, rtol=1e-12)
+    np.testing.assert_allclose(p, scipy.special.softmax(s, axis=-1), rtol=1e-13)
+    big = O.softmax(np.array([[1000.0, 1000.0, 999.0]]))   # no overflow
+    e = math.exp(-1)
+    np.testing.assert_allclose(big[0], [1 / (2 + e), 1 / (2 + e), e / (2 + e)], rtol=1e-14)
+
+
+def _brute_attend(q, K, V):
+    d = len(q)
+    s = [sum(q[i] * K[n][i] for i in range(d)) / math.sqrt(d) for n in range(len(K))]
+    mx = max(s)
+    w = [math.exp(x - mx) for x in s]
+    tot = sum(w)
+    return [sum(w[n] * V[n][i] for n in range(len(K))) / tot for i in range(len(V[0]))]
+
+
+def test_attention_brute_force_tiny():
+    q = rng.standard_normal(4)
+    K = rng.standard_normal((5, 4))
+    V = rng.standard_normal((5, 4))
+    np.testing.assert_allclose(O.attend(q, K, V), _brute_attend(q, K, V), rtol=1e-13)
+
+
+def test_attention_special_cases():
+    K = rng.standard_normal((6, 8))
+    V = rng.standard_normal((6, 8))
+    np.testing.assert_allclose(O.attend(np.zeros(8), K, V), V.mean(0), rtol=1e-13)
+    np.testing.assert_allclose(O.attend(rng.standard_normal(8), K[:1], V[:1]), V[0], rtol=1e-15)
+
+
+def test_gqa_group_one_is_mha_and_repeat_equivalence():
+    n_q, n_kv, S, d = 8, 2, 11, 16
+    q = rng.standard_normal((n_q, d))
+    K = rng.standard_normal((n_kv, S, d))
+    V = rng.standard_normal((n_kv, S, d))
+    g = O.gqa_attention(q, K, V, 9)
+    Kr, Vr = np.repeat(K, n_q // n_kv, 0), np.repeat(V, n_q // n_kv, 0)
+    mha = O.gqa_attention(q, Kr, Vr, 9)          # G = 1
+    np.testing.assert_allclose(g, mha, rtol=1e-14)
+    per_head = np.stack([O.attend(q[h], Kr[h, :9], Vr[h, :9]) for h in range(n_q)])
+    np.testing.assert_allclose(mha, per_head, rtol=1e-14)
+
+
+def test_causal_attention_matches_library_sdpa():
+    # All rows of a prompt vs torch's causal scaled_dot_product_attention.
+    n_q, n_kv, T, d = 4, 2, 7, 8
+    q = rng.standard_normal((n_q, T, d))
+    K = rng.standard_normal((n_kv, T, d))
+    V = rng.standard_normal((n_kv, T, d))
+    ours = np.stack([O.gqa_attention(q[:, t], K, V, t + 1) for t in range(T)], 1)
+    Kr = torch.from_numpy(np.repeat(K, 2, 0))
+    Vr = torch.from_numpy(np.repeat(V, 2, 0))
+    ref = F.scaled_dot_product_attention(torch.from_numpy(q), Kr, Vr, is_causal=True).numpy()
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- SwiGLU
+
+def test_silu_closed_form():
+    assert O.silu(np.array(0.0)) == 0.0
+    np.testing.assert_allclose(O.silu(np.array(1.0)), math.e / (1 + math.e), rtol=1e-15)
+    z = rng.standard_normal(100) * 6
+    np.testing.assert_allclose(O.silu(z), F.silu(torch.from_numpy(z)).numpy(), rtol=1e-13, atol=1e-15)
+
+
+def test_swiglu_gate_zero_and_orientation():
+    H, I = 6, 10
+    u = rng.standard_normal((3, H))
+    wu, wd = rng.standard_normal((I, H)), rng.standard_normal((H, I))
+    assert np.all(O.swiglu_ffn(u, np.zeros((I, H)), wu, wd) == 0.0)
+    # W stored [out, in]: a single 1 at W[o, i] copies input i to output o.
+    w = np.zeros((I, H))
+    w[3, 5] = 1.0
+    np.testing.assert_array_equal(O.linear(u, w)[:, 3], u[:, 5])
+    wg = rng.standard_normal((I, H))
+    a = F.silu(torch.from_numpy(u @ wg.T)).numpy() * (u @ wu.T)
+    np.testing.assert_allclose(O.swiglu_ffn(u, wg, wu, wd), a @ wd.T, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- whole layer vs library composition
+
+def _torch_layer_prefill(x, lw, shape):
+    """The layer built from torch library routines (rms_norm, linear, complex
+    RoPE, causal SDPA with repeated K/V heads, silu) in fp64."""
+    T = x.shape[0]
+    nq, nkv, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    t = {k: torch.from_numpy(v) for k, v in lw.items()}
+    xt = torch.from_numpy(x)
+    u = F.rms_norm(xt, (shape.hidden,), t["attn_norm"], eps=shape.rms_eps)
+    qkv = F.linear(u, t["wqkv"])
+    q = qkv[:, : nq * d].reshape(T, nq, d)
+    k = qkv[:, nq * d: (nq + nkv) * d].reshape(T, nkv, d)
+    v = qkv[:, (nq + nkv) * d:].reshape(T, nkv, d)
+    freqs = shape.rope_theta ** (-torch.arange(0, d, 2, dtype=torch.float64) / d)
+    rot = torch.polar(torch.ones(T, d // 2, dtype=torch.float64),
+                      torch.arange(T, dtype=torch.float64)[:, None] * freqs[None])
+
+    def rope(z):
+        zc = torch.view_as_complex(z.reshape(T, z.shape[1], d // 2, 2).contiguous())
+        return torch.view_as_real(zc * rot[:, None]).reshape(T, z.shape[1], d)
+
+    q, k = rope(q), rope(k)
+    G = nq // nkv
+    o = F.scaled_dot_product_attention(q.transpose(0, 1), k.transpose(0, 1).repeat_interleave(G, 0),
+                                       v.transpose(0, 1).repeat_interleave(G, 0), is_causal=True)
+    h = xt + F.linear(o.transpose(0, 1).reshape(T, nq * d), t["wo"])
+    u2 = F.rms_norm(h, (shape.hidden,), t["ffn_norm"], eps=shape.rms_eps)
+    ff = F.linear(F.silu(F.linear(u2, t["w_gate"])) * F.linear(u2, t["w_up"]), t["w_down"])
+    return (h + ff).numpy()
+
+
+@pytest.mark.parametrize("nq,nkv", [(4, 4), (4, 2), (8, 1)])
+def test_layer_matches_library_composition(nq, nkv):
+    shape = synth.Shape(1, 48, nq, nkv, 8, 40, 64, dtype="f32")   # n_q*d != hidden: no square weights
+    w = {k: O.as64(v) for k, v in synth.layer_weights(shape, 5, 0, std=0.2).items()}
+    x = rng.standard_normal((1, 9, 48))
+    K = np.zeros((1, nkv, 16, 8))
+    V = np.zeros((1, nkv, 16, 8))
+    ours = O.layer_prefill(x, w, shape, K, V)[0]
+    np.testing.assert_allclose(ours, _torch_layer_prefill(x[0], w, shape), rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- KV cache semantics
+
+def test_decode_step_equals_prefill_row():
+    # The cache only removes recompute (§2.4): decoding token t after a prefill
+    # of tokens 0..t-1 gives prefill row t.
+    shape = synth.TINY
+    w = synth.model_weights(shape, 1001)
+    toks = synth.token_ids(2, 10, shape.vocab, 1001).numpy()
+    full = O.Model(shape, w, 2, 16).prefill(toks)
+    m = O.Model(shape, w, 2, 16)
+    m.prefill(toks[:, :7])
+    for t in range(7, 10):
+        lg = m.decode(toks[:, t], np.full(2, t))
+        np.testing.assert_allclose(lg, full[:, t], rtol=1e-10, atol=1e-12)
+
+
+def test_paged_equals_contiguous():
+    shape = synth.Shape(1, 32, 4, 2, 8, 24, 16, dtype="f32")
+    lw = {k: O.as64(v) for k, v in synth.layer_weights(shape, 3, 0, std=0.3).items()}
+    P, B = 4, 3
+    lens = np.array([5, 9, 2])
+    x = rng.standard_normal((B, 32))
+    Kc = rng.standard_normal((B, 2, 16, 8))
+    Vc = rng.standard_normal((B, 2, 16, 8))
+    n_pages = [int(math.ceil((L + 1) / P)) for L in lens]
+    table, total = synth.page_table(n_pages, 4, 3)
+    table = table.numpy()
+    Kp = np.zeros((total, 2, P, 8))
+    Vp = np.zeros((total, 2, P, 8))
+    for b in range(B):
+        for m in range(lens[b]):
+            Kp[table[b, m // P], :, m % P] = Kc[b, :, m]
+            Vp[table[b, m // P], :, m % P] = Vc[b, :, m]
+    contig = O.layer_decode(x, lw, shape, Kc.copy(), Vc.copy(), lens)
+    paged = O.layer_decode_paged(x, lw, shape, Kp, Vp, table, lens, P)
+    np.testing.assert_allclose(paged, contig, rtol=1e-13)
+    for b in range(B):   # new token landed in its page slot
+        m = lens[b]
+        assert np.any(Kp[table[b, m // P], :, m % P] != 0)
+
+
+def test_greedy_lowest_index_on_tie():
+    assert list(O.greedy(np.array([[1.0, 3.0, 3.0, 2.0], [5.0, 5.0, 5.0, 5.0]]))) == [1, 0]
+
+
+# ---------------------------------------------------------------- sizes the pages print
+
+def _golden_table():
+    rows = {}
+    with open(os.path.join(GOLDEN, "size_table.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, *vals = line.split()
+                rows[k] = [float(v) for v in vals]
+    return rows
+
+
+def test_shapes_match_printed_size_table():
+    g = _golden_table()
+    for i, s in enumerate((synth.LLAMA2_7B, synth.LLAMA2_13B, synth.LLAMA2_70B)):
+        assert [s.n_layers, s.hidden, s.n_q_heads, s.n_kv_heads, s.intermediate, s.vocab] == [
+            g[k][i] for k in ("layers", "hidden", "heads", "kv_heads", "intermediate", "vocab")]
+    assert 1 - synth.LLAMA2_70B.n_kv_heads / synth.LLAMA2_70B.n_q_heads == g["gqa_kv_saving_70b"][0]
+
+
+def test_param_count_matches_printed_weight_sizes():
+    g = _golden_table()
+    assert O.param_count(synth.LLAMA2_7B) == 6_738_415_616          # the "7B"
+    for i, s in enumerate((synth.LLAMA2_7B, synth.LLAMA2_13B, synth.LLAMA2_70B)):
+        gb = O.param_count(s) * 2 / 1e9
+        assert abs(gb - g["weights_fp16_gb"][i]) / g["weights_fp16_gb"][i] < 0.05
+
+
+def test_kv_cache_formula_7b():
+    # 7B, 4096 tokens, fp16: exactly 2 GiB, the page's "about 2GB".
+    b = O.kv_cache_bytes(synth.LLAMA2_7B, 4096, 2)
+    assert b == 2 * 1024 ** 3
+    assert round(b / 1024 ** 3) == _golden_table()["kv_fp16_4096_gb"][0]
+
+
+def test_embed_and_head_match_library():
+    table = rng.standard_normal((20, 12))
+    toks = np.array([3, 0, 19, 3])
+    np.testing.assert_array_equal(O.embed(table, toks),
+                                  F.embedding(torch.from_numpy(toks), torch.from_numpy(table)).numpy())
+    h = rng.standard_normal((4, 12))
+    g = 1 + 0.1 * rng.standard_normal(12)
+    w = rng.standard_normal((20, 12))
+    ref = F.linear(F.rms_norm(torch.from_numpy(h), (12,), torch.from_numpy(g), eps=1e-5), torch.from_numpy(w))
+    np.testing.assert_allclose(O.lm_head(h, g, w, 1e-5), ref.numpy(), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- planted mistakes are caught
+
+def _half_split_rope(x, positions, theta):
+    d = x.shape[-1]
+    phi = np.asarray(positions, dtype=np.float64)[:, None] * O.rope_frequencies(d, theta)[None, :]
+    c, s = np.cos(phi)[:, None, :], np.sin(phi)[:, None, :]
+    a, b = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([a * c - b * s, a * s + b * c], -1)
+
+
+@pytest.mark.parametrize("mutant,pin", [
+    ("rope", "test_rope_hand_angles"),
+    ("rope", "test_rope_matches_complex_form"),
+    ("gqa", "test_causal_attention_matches_library_sdpa"),
+    ("scale", "test_attention_brute_force_tiny"),
+    ("eps", "test_rmsnorm_eps_inside_root_and_scale_invariance"),
+])
+def test_pins_catch_planted_mistakes(monkeypatch, mutant, pin):
+    if mutant == "rope":
+        monkeypatch.setattr(O, "rope", _half_split_rope)
+    elif mutant == "gqa":
+        def wrong_gqa(q, K, V, n):
+            return np.stack([O.attend(q[h], K[h % K.shape[0], :n], V[h % K.shape[0], :n])
+                             for h in range(q.shape[0])])
+        monkeypatch.setattr(O, "gqa_attention", wrong_gqa)
+    elif mutant == "scale":
+        monkeypatch.setattr(O, "attend", lambda q, K, V: O.softmax(K @ q) @ V)
+    elif mutant == "eps":
+        monkeypatch.setattr(O, "rmsnorm", lambda x, g, eps: x / (np.sqrt(np.mean(x * x, -1, keepdims=True)) + eps) * g)
+    with pytest.raises(AssertionError):
+        globals()[pin]()
