@@ -1,0 +1,272 @@
+/*
+ * llama_gb300.h -- C ABI of the GB300 (sm_103a) Llama2 decoder forward.
+ *
+ * The library computes the decoder-only forward pass of a Llama2-style model
+ * in its two phases ("Llama2架构与推理全解析" §2.1, Prefill and Decode):
+ *
+ *   h = embed(token_ids)
+ *   for each layer:  h = h + attn(rmsnorm(h), kv_cache)
+ *                    h = h + ffn(rmsnorm(h))
+ *   logits = lm_head(rmsnorm(h))
+ *
+ * (the main-computation pseudocode of §2.3), with RMSNorm (§1.2), SwiGLU
+ * (§1.3), RoPE (§1.4), grouped-query attention (§1.5) and a KV cache that the
+ * caller owns (§2.4). Prefill returns the first prediction and decode appends
+ * one token per sequence to the cache (§3.4 generation loop).
+ *
+ * Conventions shared by every entry point
+ *  - All device buffers are allocated by the caller (e.g. with PyTorch) and
+ *    passed as plain pointers; the library never allocates device memory. It
+ *    keeps a small host-side context whose device state lives in the caller's
+ *    workspace (llama_workspace_bytes).
+ *  - Row-major storage everywhere. Projection weights are [out, in]
+ *    (y = x W^T), which is the pages' x W with W stored [in, out].
+ *  - dtype LLAMA_BF16: weights, gains, embedding, LM head, KV cache are bf16;
+ *    dtype LLAMA_F32: all of them are fp32. In both cases the residual
+ *    stream (hidden) and the logits are fp32 and every reduction (GEMM,
+ *    softmax, norm statistics) accumulates in fp32.
+ *  - Token ids, positions and page-table entries are int32.
+ *  - Calls enqueue work on the context's stream and return without
+ *    synchronising, except llama_sync_status and llama_decode_step_host.
+ *  - Every entry point returns an llama_status code. Errors found on the
+ *    host (bad pointer, size, layout) are returned at once and nothing is
+ *    enqueued. Errors found by kernels (a token id >= vocab, a position past
+ *    the cache, a page id outside the pool, a device wait that ran out of
+ *    time) set a device status word; the offending access is skipped and the
+ *    next llama_sync_status returns LLAMA_ERR_DEVICE_CHECK. Nothing traps.
+ *  - One context per stream; a context is not thread-safe.
+ */
+#ifndef LLAMA_GB300_H
+#define LLAMA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum llama_status {
+  LLAMA_OK = 0,
+  LLAMA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad layout */
+  LLAMA_ERR_UNSUPPORTED = 2,   /* shape the kernels do not implement */
+  LLAMA_ERR_OUT_OF_RANGE = 3,  /* size above what the context was built for */
+  LLAMA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  LLAMA_ERR_DEVICE_CHECK = 5,  /* a kernel flagged bad data or a wait timeout */
+  LLAMA_ERR_WORKSPACE = 6      /* workspace null, misaligned or too small */
+} llama_status;
+
+typedef enum llama_dtype { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
+
+/* Device status word bits (llama_last_device_flags). */
+#define LLAMA_FLAG_TOKEN_RANGE 0x1u   /* token id outside [0, vocab) */
+#define LLAMA_FLAG_POS_RANGE 0x2u     /* position outside the cache */
+#define LLAMA_FLAG_PAGE_RANGE 0x4u    /* page id outside [0, n_pages) */
+#define LLAMA_FLAG_WAIT_TIMEOUT 0x8u  /* a bounded device wait expired */
+
+/* Model and sizing. Values of the size table ("Llama2架构与推理全解析" §1.6):
+ * 7B = {32, 4096, 32, 32, 128, 11008, 32000}, 70B = {80, 8192, 64, 8, 128,
+ * 28672, 32000}; rms_eps 1e-5 (§1.2 gives 1e-5 .. 1e-6), rope_theta 10000. */
+typedef struct llama_config {
+  int32_t n_layers;
+  int32_t hidden;        /* H */
+  int32_t n_q_heads;     /* query heads */
+  int32_t n_kv_heads;    /* K/V heads; n_q_heads % n_kv_heads == 0 (GQA, §1.5) */
+  int32_t head_dim;      /* d, even */
+  int32_t intermediate;  /* SwiGLU width I */
+  int32_t vocab;         /* V (ignored when has_embed_head == 0) */
+  float rms_eps;
+  float rope_theta;
+  int32_t dtype;         /* llama_dtype */
+  int32_t max_batch;     /* most sequences in one call */
+  int32_t max_tokens;    /* most prompt rows (B*T) in one prefill call */
+  int32_t max_seq;       /* positions 0 .. max_seq-1 may be used (RoPE table size) */
+  int32_t has_embed_head;/* 1: token ids in, logits out; 0: hidden in/out only */
+} llama_config;
+
+/* One layer's weights (device pointers, dtype of the config).
+ *   attn_norm, ffn_norm : [H]                       RMSNorm gains
+ *   wqkv                : [(n_q + 2 n_kv) d, H]     Q rows, then K rows, then V rows
+ *   wo                  : [H, n_q d]
+ *   w_gate, w_up        : [I, H]
+ *   w_down              : [H, I]
+ * The pointers must stay valid for the life of the context. */
+typedef struct llama_layer_weights {
+  const void* attn_norm;
+  const void* wqkv;
+  const void* wo;
+  const void* ffn_norm;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+} llama_layer_weights;
+
+/* Whole-model weights. embed and lm_head are separate [V, H] matrices (the
+ * pages: no weight tying); final_norm is [H]. All three may be NULL when
+ * has_embed_head == 0. layers is a HOST array of n_layers entries, read
+ * during llama_init only. */
+typedef struct llama_weights {
+  const void* embed;
+  const void* final_norm;
+  const void* lm_head;
+  const llama_layer_weights* layers;
+} llama_weights;
+
+/* KV cache, owned by the caller (device memory, dtype of the config).
+ * Contiguous (page_size == 0):
+ *   k, v : [n_layers][batch_capacity][n_kv][capacity][d]
+ *   sequence b of a call uses slot b; positions must be < capacity.
+ * Paged (page_size > 0, a multiple of 16; PagedAttention):
+ *   k, v       : [n_layers][n_pages][n_kv][page_size][d]
+ *   page_table : DEVICE int32 [batch][max_pages_per_seq]; token m of sequence
+ *                b lives in page page_table[b][m / page_size], slot
+ *                m % page_size.
+ * The cache stores the RoPE-rotated K and the plain V. */
+typedef struct llama_kv {
+  void* k;
+  void* v;
+  int32_t page_size;
+  int32_t capacity;
+  int32_t batch_capacity;
+  int32_t n_pages;
+  const int32_t* page_table;
+  int32_t max_pages_per_seq;
+} llama_kv;
+
+typedef struct llama_ctx llama_ctx;
+
+/* Bytes of device workspace llama_init needs for cfg (256-byte aligned). */
+int llama_workspace_bytes(const llama_config* cfg, size_t* bytes);
+
+/* Build a context. workspace: device buffer of at least
+ * llama_workspace_bytes bytes, 256-byte aligned, owned by the caller and
+ * untouched by anyone else while the context lives. stream: a cudaStream_t
+ * (NULL = legacy default stream). Enqueues the RoPE table fill on stream.
+ * On success *out receives the context (free with llama_free). */
+int llama_init(const llama_config* cfg, const llama_weights* w, void* workspace,
+               size_t workspace_bytes, void* stream, llama_ctx** out);
+
+/* Change the stream later calls enqueue on. */
+int llama_set_stream(llama_ctx* ctx, void* stream);
+
+/* Prefill a fresh prompt ("Llama2架构与推理全解析" §2.1): tokens is DEVICE
+ * int32 [B, T]; token t of each sequence sits at position t. Writes the
+ * rotated K and the V of positions 0..T-1 of every layer into kv, then
+ * the logits of each sequence's last row into logits (DEVICE fp32 [B, V]).
+ * next_ids (DEVICE int32 [B], may be NULL) receives the greedy choice
+ * (argmax, lowest index on ties; §2.5). */
+int llama_prefill(llama_ctx* ctx, const int32_t* tokens, int32_t B, int32_t T,
+                  const llama_kv* kv, float* logits, int32_t* next_ids);
+
+/* One decode step ("Llama2架构与推理全解析" §2.4, §3.4 decode_one): tokens and
+ * positions are DEVICE int32 [B]; sequence b's token is at position
+ * positions[b], its K/V are appended there, and it attends to keys
+ * 0..positions[b]. Writes logits (DEVICE fp32 [B, V]) and, if next_ids is not
+ * NULL, the greedy choice per sequence. */
+int llama_decode_step(llama_ctx* ctx, const int32_t* tokens, const int32_t* positions,
+                      int32_t B, const llama_kv* kv, float* logits, int32_t* next_ids);
+
+/* llama_decode_step with HOST buffers: copies tokens/positions (HOST int32
+ * [B]) to the device, runs the step, copies logits (HOST fp32 [B, V], may be
+ * NULL) and next_ids (HOST int32 [B], may be NULL) back, and synchronises the
+ * stream. Returns the status of the step including device flags. Host buffers
+ * should be pinned for asynchronous copies. */
+int llama_decode_step_host(llama_ctx* ctx, const int32_t* tokens_host,
+                           const int32_t* positions_host, int32_t B, const llama_kv* kv,
+                           float* logits_host, int32_t* next_ids_host);
+
+/* The layer stack alone on a hidden state (no embedding, final norm or LM
+ * head), for single-layer workloads. hidden is DEVICE fp32, updated in place.
+ *   llama_prefill_hidden: hidden [B*T, H], rows of sequence b at b*T .. b*T+T-1,
+ *                         fresh prompt at positions 0..T-1.
+ *   llama_decode_hidden : hidden [B, H], positions DEVICE int32 [B]. */
+int llama_prefill_hidden(llama_ctx* ctx, float* hidden, int32_t B, int32_t T,
+                         const llama_kv* kv);
+int llama_decode_hidden(llama_ctx* ctx, float* hidden, const int32_t* positions, int32_t B,
+                        const llama_kv* kv);
+
+/* Synchronise the stream, then read and clear the device status word.
+ * Returns LLAMA_OK, LLAMA_ERR_CUDA or LLAMA_ERR_DEVICE_CHECK. */
+int llama_sync_status(llama_ctx* ctx);
+
+/* Flags (LLAMA_FLAG_*) seen by the last llama_sync_status. */
+uint32_t llama_last_device_flags(const llama_ctx* ctx);
+
+/* Static description of a status code. */
+const char* llama_strerror(int status);
+
+/* Release the host context (the workspace stays the caller's). */
+int llama_free(llama_ctx* ctx);
+
+/* ---- Per-kernel timing. kind: one of LLAMA_KERNEL_* below. When enabled,
+ * every launch of that kernel class is bracketed by CUDA events on the
+ * context's stream; llama_profile_read returns the summed device time (ms)
+ * and the launch count since the last reset, synchronising the stream. */
+#define LLAMA_KERNEL_RMSNORM 0
+#define LLAMA_KERNEL_GEMM 1
+#define LLAMA_KERNEL_ROPE_APPEND 2
+#define LLAMA_KERNEL_ATTN_DECODE 3
+#define LLAMA_KERNEL_ATTN_PREFILL 4
+#define LLAMA_KERNEL_EMBED 5
+#define LLAMA_KERNEL_ARGMAX 6
+#define LLAMA_KERNEL_COUNT 7
+int llama_profile_enable(llama_ctx* ctx, uint32_t kind_mask);
+int llama_profile_read(llama_ctx* ctx, int32_t kind, double* total_ms, int64_t* launches);
+/* Launches of this library's kernels enqueued since context creation. */
+int64_t llama_launch_count(const llama_ctx* ctx);
+
+/* ---- Single operations, each one kernel (or one kernel plus its split
+ * combine) of the forward pass on caller buffers, enqueued on the context's
+ * stream. "T" below is the config dtype (bf16 or fp32). ---- */
+
+/* RMSNorm ("Llama2架构与推理全解析" §1.2): out[r] = x[r] / sqrt(mean(x[r]^2) + eps)
+ * * gamma over H columns. x fp32 [rows, H] (row r read at x + r*in_stride*H),
+ * gamma T [H], out T [rows, H]. in_stride >= 1 selects every in_stride-th row
+ * starting at row in_offset. */
+int llama_op_rmsnorm(llama_ctx* ctx, const float* x, int32_t rows, int32_t in_stride,
+                     int32_t in_offset, const void* gamma, void* out);
+
+/* Linear layer y = x W^T (§1.3 notation x W) with a fused epilogue.
+ *   x T [n_rows, K]; w T [M, K]; w_up T [M, K] (SWIGLU only).
+ *   epilogue LLAMA_EPI_STORE_F32 : out fp32 [n_rows, M] = x W^T
+ *            LLAMA_EPI_RESID_F32 : out fp32 [n_rows, M] += x W^T (residual add)
+ *            LLAMA_EPI_STORE_T   : out T [n_rows, M] = x W^T
+ *            LLAMA_EPI_SWIGLU    : out T [n_rows, M] = silu(x W^T) * (x W_up^T)
+ * bf16 runs on the tcgen05 tensor cores, fp32 on the CUDA cores. */
+#define LLAMA_EPI_STORE_F32 0
+#define LLAMA_EPI_RESID_F32 1
+#define LLAMA_EPI_STORE_T 2
+#define LLAMA_EPI_SWIGLU 3
+int llama_op_linear(llama_ctx* ctx, const void* x, int32_t n_rows, const void* w,
+                    const void* w_up, int32_t M, int32_t K, int32_t epilogue, void* out);
+
+/* RoPE + KV append (§1.4, §2.4): qkv fp32 [rows, (n_q + 2 n_kv) d] as the Q/K/V
+ * projection wrote it; row r is sequence r / rows_per_seq at position
+ * positions[r] (DEVICE int32 [rows]). Writes the rotated Q to q_out T
+ * [rows, n_q d], the rotated K and the V into layer `layer` of kv, and, if
+ * k_out/v_out are not NULL, also to k_out/v_out T [rows, n_kv d]. */
+int llama_op_rope_append(llama_ctx* ctx, const float* qkv, int32_t rows, int32_t rows_per_seq,
+                         const int32_t* positions, int32_t layer, const llama_kv* kv,
+                         void* q_out, void* k_out, void* v_out);
+
+/* Decode attention over the cache (§2.3, §2.4, §1.5): q T [B, n_q, d] (rotated),
+ * sequence b attends keys 0..positions[b] of layer `layer`; out T [B, n_q d]. */
+int llama_op_attention_decode(llama_ctx* ctx, const void* q, const int32_t* positions,
+                              int32_t B, int32_t layer, const llama_kv* kv, void* out);
+
+/* Causal prefill attention (§2.1, §2.3) of fresh prompts: q T [B*T, n_q, d],
+ * k, v T [B*T, n_kv, d] (k rotated); row t attends keys 0..t of its own
+ * sequence; out T [B*T, n_q d]. */
+int llama_op_attention_prefill(llama_ctx* ctx, const void* q, const void* k, const void* v,
+                               int32_t B, int32_t T, void* out);
+
+/* Embedding row lookup (§2.3): out fp32 [n, H] = table[tokens[i]]. */
+int llama_op_embed(llama_ctx* ctx, const int32_t* tokens, int32_t n, void* out);
+
+/* Greedy choice (§2.5): ids[b] = argmax_v logits[b, v], lowest index on ties. */
+int llama_op_argmax(llama_ctx* ctx, const float* logits, int32_t B, int32_t V, int32_t* ids);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LLAMA_GB300_H */

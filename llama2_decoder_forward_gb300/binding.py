@@ -1,0 +1,300 @@
+"""Python binding of the C ABI in include/llama_gb300.h.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+library. PyTorch tensors supply device memory and the stream; their data
+pointers go through ctypes. If the shared library is missing the binding
+raises at once; there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB
+
+c_int32 = ctypes.c_int32
+c_void_p = ctypes.c_void_p
+
+F32, BF16 = 0, 1
+EPI_STORE_F32, EPI_RESID_F32, EPI_STORE_T, EPI_SWIGLU = 0, 1, 2, 3
+KERNELS = ("rmsnorm", "gemm", "rope_append", "attn_decode", "attn_prefill", "embed", "argmax")
+FLAG_TOKEN_RANGE, FLAG_POS_RANGE, FLAG_PAGE_RANGE, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OUT_OF_RANGE", 4: "CUDA",
+          5: "DEVICE_CHECK", 6: "WORKSPACE"}
+
+
+class LlamaConfig(ctypes.Structure):
+    _fields_ = [("n_layers", c_int32), ("hidden", c_int32), ("n_q_heads", c_int32),
+                ("n_kv_heads", c_int32), ("head_dim", c_int32), ("intermediate", c_int32),
+                ("vocab", c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                ("dtype", c_int32), ("max_batch", c_int32), ("max_tokens", c_int32),
+                ("max_seq", c_int32), ("has_embed_head", c_int32)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in
+                ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", c_void_p), ("final_norm", c_void_p), ("lm_head", c_void_p),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class KV(ctypes.Structure):
+    _fields_ = [("k", c_void_p), ("v", c_void_p), ("page_size", c_int32), ("capacity", c_int32),
+                ("batch_capacity", c_int32), ("n_pages", c_int32), ("page_table", c_void_p),
+                ("max_pages_per_seq", c_int32)]
+
+
+_SIGS = {
+    "llama_workspace_bytes": (c_int32, [ctypes.POINTER(LlamaConfig), ctypes.POINTER(ctypes.c_size_t)]),
+    "llama_init": (c_int32, [ctypes.POINTER(LlamaConfig), ctypes.POINTER(Weights), c_void_p,
+                             ctypes.c_size_t, c_void_p, ctypes.POINTER(c_void_p)]),
+    "llama_set_stream": (c_int32, [c_void_p, c_void_p]),
+    "llama_prefill": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, ctypes.POINTER(KV), c_void_p,
+                                c_void_p]),
+    "llama_decode_step": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(KV),
+                                    c_void_p, c_void_p]),
+    "llama_decode_step_host": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(KV),
+                                         c_void_p, c_void_p]),
+    "llama_prefill_hidden": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, ctypes.POINTER(KV)]),
+    "llama_decode_hidden": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(KV)]),
+    "llama_sync_status": (c_int32, [c_void_p]),
+    "llama_last_device_flags": (ctypes.c_uint32, [c_void_p]),
+    "llama_strerror": (ctypes.c_char_p, [c_int32]),
+    "llama_free": (c_int32, [c_void_p]),
+    "llama_profile_enable": (c_int32, [c_void_p, ctypes.c_uint32]),
+    "llama_profile_read": (c_int32, [c_void_p, c_int32, ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_int64)]),
+    "llama_launch_count": (ctypes.c_int64, [c_void_p]),
+    "llama_op_rmsnorm": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p]),
+    "llama_op_linear": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_int32,
+                                  c_int32, c_void_p]),
+    "llama_op_rope_append": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32,
+                                       ctypes.POINTER(KV), c_void_p, c_void_p, c_void_p]),
+    "llama_op_attention_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32,
+                                            ctypes.POINTER(KV), c_void_p]),
+    "llama_op_attention_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
+                                             c_void_p]),
+    "llama_op_embed": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p]),
+    "llama_op_argmax": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError("libllama_gb300.so is not built (run llama2_decoder_forward_gb300"
+                               ".build.build_library() or __graft_entry__.build())")
+        l = ctypes.CDLL(LIB)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+class LlamaError(RuntimeError):
+    def __init__(self, rc, what, flags=0):
+        self.rc = rc
+        self.flags = flags
+        msg = "%s failed: %s (%s)" % (what, STATUS.get(rc, rc), lib().llama_strerror(rc).decode())
+        if flags:
+            msg += " device flags 0x%x" % flags
+        super().__init__(msg)
+
+
+def _p(t):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return c_void_p(s.cuda_stream)
+
+
+def make_config(shape, max_batch, max_tokens, max_seq, has_embed_head=True) -> LlamaConfig:
+    return LlamaConfig(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
+                       shape.head_dim, shape.intermediate, shape.vocab if has_embed_head else 0,
+                       shape.rms_eps, shape.rope_theta, F32 if shape.dtype == "f32" else BF16,
+                       max_batch, max_tokens, max_seq, 1 if has_embed_head else 0)
+
+
+def workspace_bytes(cfg: LlamaConfig) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().llama_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n))
+    if rc:
+        raise LlamaError(rc, "llama_workspace_bytes")
+    return n.value
+
+
+class KVCache:
+    """Caller-owned KV cache in the library's layout (torch device memory).
+
+    contiguous: k, v [n_layers, batch, n_kv, capacity, d]
+    paged     : k, v [n_layers, n_pages, n_kv, page_size, d] + page_table [B, max_pages] int32
+    """
+
+    def __init__(self, shape, *, batch=None, capacity=None, n_pages=None, page_size=0,
+                 page_table=None, dtype=None, device="cuda", k=None, v=None):
+        import torch
+        dt = dtype or shape.torch_dtype
+        L, nkv, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
+        self.page_size = page_size
+        self.page_table = page_table
+        if page_size == 0:
+            full = (L, batch, nkv, capacity, d)
+            self.batch, self.capacity, self.n_pages, self.max_pages = batch, capacity, 0, 0
+        else:
+            full = (L, n_pages, nkv, page_size, d)
+            self.batch, self.capacity, self.n_pages = 0, 0, n_pages
+            self.max_pages = page_table.shape[1]
+        self.k = k if k is not None else torch.zeros(full, dtype=dt, device=device)
+        self.v = v if v is not None else torch.zeros(full, dtype=dt, device=device)
+        assert tuple(self.k.shape) == full and tuple(self.v.shape) == full
+
+    def struct(self) -> KV:
+        return KV(self.k.data_ptr(), self.v.data_ptr(), self.page_size, self.capacity, self.batch,
+                  self.n_pages, None if self.page_table is None else self.page_table.data_ptr(),
+                  self.max_pages)
+
+
+class Model:
+    """A library context over device-resident weights.
+
+    weights: dict as produced by synth.model_weights / layer_weights, already
+    on the GPU ({"embed", "final_norm", "lm_head", "layers": [...]}); a
+    layer-only model passes {"layers": [...]} and has_embed_head=False.
+    """
+
+    def __init__(self, shape, weights, *, max_batch, max_tokens, max_seq, has_embed_head=True,
+                 stream=None):
+        import torch
+        self.shape = shape
+        self.weights = weights  # keep the tensors alive
+        self.cfg = make_config(shape, max_batch, max_tokens, max_seq, has_embed_head)
+        nbytes = workspace_bytes(self.cfg)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        layers = weights["layers"]
+        arr = (LayerWeights * len(layers))()
+        for i, lw in enumerate(layers):
+            arr[i] = LayerWeights(*[lw[n].data_ptr() for n in
+                                    ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")])
+        self._layers_arr = arr
+        w = Weights(_p(weights.get("embed")), _p(weights.get("final_norm")), _p(weights.get("lm_head")),
+                    ctypes.cast(arr, ctypes.POINTER(LayerWeights)))
+        ctx = c_void_p()
+        rc = lib().llama_init(ctypes.byref(self.cfg), ctypes.byref(w), _p(self.workspace), nbytes,
+                              _stream_handle(stream), ctypes.byref(ctx))
+        if rc:
+            raise LlamaError(rc, "llama_init")
+        self.ctx = ctx
+
+    def __del__(self):
+        ctx = getattr(self, "ctx", None)
+        if ctx is not None and _lib is not None:
+            _lib.llama_free(ctx)
+            self.ctx = None
+
+    def _chk(self, rc, what):
+        if rc:
+            raise LlamaError(rc, what)
+
+    def set_stream(self, stream):
+        self._chk(lib().llama_set_stream(self.ctx, _stream_handle(stream)), "llama_set_stream")
+
+    # ---- forward pass
+    def prefill(self, tokens, kv: KVCache, logits, next_ids=None):
+        B, T = tokens.shape
+        self._chk(lib().llama_prefill(self.ctx, _p(tokens), B, T, ctypes.byref(kv.struct()),
+                                      _p(logits), _p(next_ids)), "llama_prefill")
+
+    def decode_step(self, tokens, positions, kv: KVCache, logits, next_ids=None):
+        self._chk(lib().llama_decode_step(self.ctx, _p(tokens), _p(positions), tokens.shape[0],
+                                          ctypes.byref(kv.struct()), _p(logits), _p(next_ids)),
+                  "llama_decode_step")
+
+    def decode_step_host(self, tokens, positions, kv: KVCache, logits=None, next_ids=None):
+        rc = lib().llama_decode_step_host(self.ctx, _p(tokens), _p(positions), tokens.shape[0],
+                                          ctypes.byref(kv.struct()), _p(logits), _p(next_ids))
+        if rc:
+            raise LlamaError(rc, "llama_decode_step_host", lib().llama_last_device_flags(self.ctx))
+
+    def prefill_hidden(self, hidden, B, T, kv: KVCache):
+        self._chk(lib().llama_prefill_hidden(self.ctx, _p(hidden), B, T, ctypes.byref(kv.struct())),
+                  "llama_prefill_hidden")
+
+    def decode_hidden(self, hidden, positions, kv: KVCache):
+        self._chk(lib().llama_decode_hidden(self.ctx, _p(hidden), _p(positions), hidden.shape[0],
+                                            ctypes.byref(kv.struct())), "llama_decode_hidden")
+
+    def sync(self):
+        """Synchronise; raise LlamaError carrying the device flags on a kernel-side check."""
+        rc = lib().llama_sync_status(self.ctx)
+        if rc:
+            raise LlamaError(rc, "llama_sync_status", lib().llama_last_device_flags(self.ctx))
+
+    def sync_status(self):
+        rc = lib().llama_sync_status(self.ctx)
+        return rc, lib().llama_last_device_flags(self.ctx)
+
+    # ---- profiling
+    def profile(self, kinds):
+        mask = 0
+        for k in kinds:
+            mask |= 1 << KERNELS.index(k)
+        self._chk(lib().llama_profile_enable(self.ctx, mask), "llama_profile_enable")
+
+    def profile_read(self, kind):
+        ms = ctypes.c_double()
+        n = ctypes.c_int64()
+        self._chk(lib().llama_profile_read(self.ctx, KERNELS.index(kind), ctypes.byref(ms),
+                                           ctypes.byref(n)), "llama_profile_read")
+        return ms.value, n.value
+
+    def launch_count(self):
+        return lib().llama_launch_count(self.ctx)
+
+    # ---- single operations
+    def op_rmsnorm(self, x, gamma, out, rows=None, stride=1, offset=0):
+        rows = rows if rows is not None else x.shape[0]
+        self._chk(lib().llama_op_rmsnorm(self.ctx, _p(x), rows, stride, offset, _p(gamma), _p(out)),
+                  "llama_op_rmsnorm")
+
+    def op_linear(self, x, w, out, epilogue, w_up=None):
+        M, K = w.shape
+        self._chk(lib().llama_op_linear(self.ctx, _p(x), x.shape[0], _p(w), _p(w_up), M, K, epilogue,
+                                        _p(out)), "llama_op_linear")
+
+    def op_rope_append(self, qkv, rows_per_seq, positions, layer, kv: KVCache, q_out, k_out=None,
+                       v_out=None):
+        self._chk(lib().llama_op_rope_append(self.ctx, _p(qkv), qkv.shape[0], rows_per_seq,
+                                             _p(positions), layer, ctypes.byref(kv.struct()),
+                                             _p(q_out), _p(k_out), _p(v_out)), "llama_op_rope_append")
+
+    def op_attention_decode(self, q, positions, layer, kv: KVCache, out):
+        self._chk(lib().llama_op_attention_decode(self.ctx, _p(q), _p(positions), q.shape[0], layer,
+                                                  ctypes.byref(kv.struct()), _p(out)),
+                  "llama_op_attention_decode")
+
+    def op_attention_prefill(self, q, k, v, B, T, out):
+        self._chk(lib().llama_op_attention_prefill(self.ctx, _p(q), _p(k), _p(v), B, T, _p(out)),
+                  "llama_op_attention_prefill")
+
+    def op_embed(self, tokens, out):
+        self._chk(lib().llama_op_embed(self.ctx, _p(tokens), tokens.numel(), _p(out)), "llama_op_embed")
+
+    def op_argmax(self, logits, ids):
+        B, V = logits.shape
+        self._chk(lib().llama_op_argmax(self.ctx, _p(logits), B, V, _p(ids)), "llama_op_argmax")

@@ -1,0 +1,765 @@
+// C ABI of the library: configuration checks, the workspace layout, TMA
+// descriptors, and the host orchestration of prefill and decode
+// ("Llama2架构与推理全解析" §2.3 main computation, §2.1 two phases, §3.4
+// generation loop). Every step of the forward pass runs in this library's
+// kernels; the host only validates arguments and enqueues launches.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <tuple>
+#include <vector>
+
+#include "internal.h"
+
+using namespace llgb;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+constexpr int kMaxCounters = 8192;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+cudaError_t g_prep_err = cudaSuccess;
+
+bool load_encode() {
+  std::call_once(g_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    g_prep_err = gemm_prepare();
+    if (g_prep_err == cudaSuccess) g_prep_err = attn_prepare();
+  });
+  return g_encode != nullptr && g_prep_err == cudaSuccess;
+}
+
+int elem_size(int dtype) { return dtype == LLAMA_BF16 ? 2 : 4; }
+
+int sm_count_or_default() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    return n;
+  cudaGetLastError();
+  return 152;
+}
+
+// Workspace layout (byte offsets from the workspace base).
+struct Layout {
+  size_t status, counters, rope, x, u, qkv, q, kside, vside, o, a, u_last, logits, ids, tok, pos,
+      gpart, apart, total;
+  size_t gpart_bytes, apart_bytes;
+  int R;
+};
+
+int check_config(const llama_config* c) {
+  if (!c) return LLAMA_ERR_INVALID_ARG;
+  if (c->n_layers < 1 || c->hidden < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 ||
+      c->head_dim < 2 || c->intermediate < 1 || c->max_batch < 1 || c->max_tokens < 0 ||
+      c->max_seq < 1)
+    return LLAMA_ERR_INVALID_ARG;
+  if (c->has_embed_head != 0 && c->has_embed_head != 1) return LLAMA_ERR_INVALID_ARG;
+  if (c->has_embed_head && c->vocab < 1) return LLAMA_ERR_INVALID_ARG;
+  if (c->dtype != LLAMA_F32 && c->dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return LLAMA_ERR_INVALID_ARG;
+  if (c->n_q_heads % c->n_kv_heads != 0) return LLAMA_ERR_INVALID_ARG;
+  if (c->head_dim % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  // 16-byte row pitches for TMA and vector loads
+  if (c->hidden % 8 != 0 || c->intermediate % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (c->dtype == LLAMA_BF16) {
+    if (c->head_dim != 128) return LLAMA_ERR_UNSUPPORTED;
+    if (c->n_q_heads / c->n_kv_heads > 16) return LLAMA_ERR_UNSUPPORTED;
+  } else {
+    if (c->head_dim > 256) return LLAMA_ERR_UNSUPPORTED;
+    if ((size_t)(c->max_seq + c->head_dim + 32) * 4 > 200 * 1024) return LLAMA_ERR_UNSUPPORTED;
+  }
+  return LLAMA_OK;
+}
+
+Layout make_layout(const llama_config* c, int sm_count) {
+  Layout L{};
+  const size_t es = elem_size(c->dtype);
+  const int R = std::max(c->max_batch, c->max_tokens);
+  L.R = R;
+  const size_t H = c->hidden, d = c->head_dim, nq = c->n_q_heads, nkv = c->n_kv_heads,
+               I = c->intermediate, V = c->has_embed_head ? c->vocab : 0;
+  const size_t qkv_rows = (nq + 2 * nkv) * d;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  L.status = take(16);
+  L.counters = take(sizeof(int) * kMaxCounters);
+  L.rope = take((size_t)c->max_seq * (d / 2) * sizeof(float) * 2);
+  L.x = take((size_t)R * H * 4);
+  L.u = take((size_t)R * H * es);
+  L.qkv = take((size_t)R * qkv_rows * 4);
+  L.q = take((size_t)R * nq * d * es);
+  L.kside = take((size_t)std::max(c->max_tokens, 1) * nkv * d * es);
+  L.vside = take((size_t)std::max(c->max_tokens, 1) * nkv * d * es);
+  L.o = take((size_t)R * nq * d * es);
+  L.a = take((size_t)R * I * es);
+  L.u_last = take((size_t)c->max_batch * H * es);
+  L.logits = take((size_t)c->max_batch * std::max<size_t>(V, 1) * 4);
+  L.ids = take((size_t)c->max_batch * 4);
+  L.tok = take((size_t)c->max_batch * 4);
+  L.pos = take((size_t)c->max_batch * 4);
+  size_t gp = 0;
+  if (c->dtype == LLAMA_BF16) {
+    const int Ns[2] = {c->max_batch, std::max(c->max_tokens, 1)};
+    for (int N : Ns) {
+      gp = std::max(gp, gemm_partial_bytes((int)qkv_rows, N, (int)H, 0, sm_count));
+      gp = std::max(gp, gemm_partial_bytes((int)H, N, (int)(nq * d), 0, sm_count));
+      gp = std::max(gp, gemm_partial_bytes((int)I, N, (int)H, 1, sm_count));
+      gp = std::max(gp, gemm_partial_bytes((int)H, N, (int)I, 0, sm_count));
+      if (V) gp = std::max(gp, gemm_partial_bytes((int)V, std::min(N, c->max_batch), (int)H, 0, sm_count));
+    }
+  }
+  L.gpart_bytes = gp;
+  L.gpart = take(std::max<size_t>(gp, 16));
+  L.apart_bytes = attn_decode_partial_bytes(c->max_batch, (int)nq, (int)d, c->max_seq, sm_count,
+                                            (int)nkv);
+  L.apart = take(std::max<size_t>(L.apart_bytes, 16));
+  L.total = off;
+  return L;
+}
+
+struct Key2 {
+  const void* p;
+  uint64_t a, b, c, d, e, f;
+  bool operator<(const Key2& o) const {
+    return std::tie(p, a, b, c, d, e, f) < std::tie(o.p, o.a, o.b, o.c, o.d, o.e, o.f);
+  }
+};
+
+}  // namespace
+
+struct llama_ctx {
+  llama_config cfg;
+  cudaStream_t stream = nullptr;
+  int device = 0, sm_count = 152, es = 2;
+  const void *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+  std::vector<llama_layer_weights> layers;
+  char* ws = nullptr;
+  Layout L;
+  uint32_t* status = nullptr;
+  int* counters = nullptr;
+  float2* rope = nullptr;
+  std::map<Key2, CUtensorMap> maps;
+  uint32_t prof_mask = 0;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[LLAMA_KERNEL_COUNT];
+  size_t ev_used[LLAMA_KERNEL_COUNT] = {};
+  int64_t launches = 0;
+  uint32_t last_flags = 0;
+
+  template <typename T>
+  T* at(size_t off) const {
+    return reinterpret_cast<T*>(ws + off);
+  }
+};
+
+namespace {
+
+// 2D row-major [rows, cols] bf16 tensor, box {64, box_rows}, 128-byte swizzle.
+const CUtensorMap* map2d(llama_ctx* c, const void* ptr, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows) {
+  Key2 k{ptr, 2, rows, cols, box_rows, 0, 0};
+  auto it = c->maps.find(k);
+  if (it != c->maps.end()) return &it->second;
+  if (c->maps.size() > 4096) c->maps.clear();
+  CUtensorMap m;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return nullptr;
+  return &c->maps.emplace(k, m).first->second;
+}
+
+// 3D [d2][d1][d0] bf16 tensor (d0 innermost), box {64, b1, b2}, 128-byte swizzle.
+const CUtensorMap* map3d(llama_ctx* c, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint32_t b1, uint32_t b2) {
+  Key2 k{ptr, 3, d0, d1, d2, b1, b2};
+  auto it = c->maps.find(k);
+  if (it != c->maps.end()) return &it->second;
+  if (c->maps.size() > 4096) c->maps.clear();
+  CUtensorMap m;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {64, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return nullptr;
+  return &c->maps.emplace(k, m).first->second;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Bracket one kernel class with events when profiling is on.
+struct Prof {
+  llama_ctx* c;
+  int kind;
+  bool on;
+  cudaEvent_t e1 = nullptr;
+  Prof(llama_ctx* c_, int k) : c(c_), kind(k), on((c_->prof_mask >> k) & 1u) {
+    if (!on) return;
+    auto& v = c->ev[kind];
+    if (c->ev_used[kind] == v.size()) {
+      cudaEvent_t a, b;
+      if (cudaEventCreate(&a) != cudaSuccess) { on = false; return; }
+      if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); on = false; return; }
+      v.push_back({a, b});
+    }
+    auto& pr = v[c->ev_used[kind]++];
+    cudaEventRecord(pr.first, c->stream);
+    e1 = pr.second;
+  }
+  ~Prof() {
+    if (on) cudaEventRecord(e1, c->stream);
+  }
+};
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA; }
+
+int check_kv(const llama_ctx* c, const llama_kv* kv, int B) {
+  if (!kv || !kv->k || !kv->v) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(kv->k) || !aligned16(kv->v)) return LLAMA_ERR_INVALID_ARG;
+  const uint64_t nkv = c->cfg.n_kv_heads;
+  uint64_t rows;
+  if (kv->page_size == 0) {
+    if (kv->capacity < 1 || kv->batch_capacity < B) return LLAMA_ERR_INVALID_ARG;
+    rows = (uint64_t)kv->batch_capacity * nkv * kv->capacity;
+  } else {
+    if (kv->page_size < 0 || !kv->page_table || kv->n_pages < 1 || kv->max_pages_per_seq < 1)
+      return LLAMA_ERR_INVALID_ARG;
+    if (c->cfg.dtype == LLAMA_BF16 && kv->page_size % 16 != 0) return LLAMA_ERR_UNSUPPORTED;
+    rows = (uint64_t)kv->n_pages * nkv * kv->page_size;
+  }
+  if (rows + 64 >= (1ull << 31)) return LLAMA_ERR_UNSUPPORTED;  // int32 TMA row coordinates
+  return LLAMA_OK;
+}
+
+// ---------------------------------------------------------------- single steps
+int do_rmsnorm(llama_ctx* c, const float* x, int rows, int stride, int offset, const void* gamma,
+               void* out) {
+  Prof pf(c, LLAMA_KERNEL_RMSNORM);
+  c->launches++;
+  return cuda_rc(launch_rmsnorm(c->cfg.dtype, x, rows, stride, offset, gamma, c->cfg.hidden,
+                                c->cfg.rms_eps, out, c->stream));
+}
+
+int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, const void* wu,
+            int M, void* out, int ldo) {
+  GemmCall g{};
+  g.dtype = c->cfg.dtype;
+  g.epi = epi;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.x = x;
+  g.w = w;
+  g.w_up = wu;
+  g.out = out;
+  g.ldo = ldo;
+  g.partial = c->at<float>(c->L.gpart);
+  g.partial_bytes = c->L.gpart_bytes;
+  g.counters = c->counters;
+  g.n_counters = kMaxCounters;
+  g.status = c->status;
+  g.sm_count = c->sm_count;
+  if (c->cfg.dtype == LLAMA_BF16) {
+    if (!aligned16(x) || !aligned16(w) || (wu && !aligned16(wu))) return LLAMA_ERR_INVALID_ARG;
+    g.n_tile = gemm_n_tile(N);
+    g.map_w = map2d(c, w, M, K, 128);
+    g.map_up = wu ? map2d(c, wu, M, K, 128) : nullptr;
+    g.map_x = map2d(c, x, N, K, g.n_tile);
+    if (!g.map_w || !g.map_x || (wu && !g.map_up)) return LLAMA_ERR_CUDA;
+  }
+  Prof pf(c, LLAMA_KERNEL_GEMM);
+  c->launches++;
+  return cuda_rc(launch_gemm(g, c->stream));
+}
+
+int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
+                   const int32_t* positions, int layer, const llama_kv* kv, void* q_out,
+                   void* k_out, void* v_out) {
+  RopeAppendArgs a{};
+  a.qkv = qkv;
+  a.positions = positions;
+  a.rope = c->rope;
+  a.q_out = q_out;
+  a.k_out = k_out;
+  a.v_out = v_out;
+  a.k_cache = kv->k;
+  a.v_cache = kv->v;
+  a.page_table = kv->page_table;
+  a.status = c->status;
+  a.rows_per_seq = rows_per_seq;
+  a.n_q = c->cfg.n_q_heads;
+  a.n_kv = c->cfg.n_kv_heads;
+  a.head_dim = c->cfg.head_dim;
+  a.max_seq = c->cfg.max_seq;
+  a.layer = layer;
+  a.page_size = kv->page_size;
+  a.capacity = kv->capacity;
+  a.batch_cap = kv->batch_capacity;
+  a.n_pages = kv->n_pages;
+  a.max_pages = kv->max_pages_per_seq;
+  Prof pf(c, LLAMA_KERNEL_ROPE_APPEND);
+  c->launches++;
+  return cuda_rc(launch_rope_append(c->cfg.dtype, a, rows, c->stream));
+}
+
+int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B, int layer,
+                   const llama_kv* kv, void* out) {
+  AttnDecodeArgs a{};
+  a.q = q;
+  a.positions = positions;
+  a.k_cache = kv->k;
+  a.v_cache = kv->v;
+  a.page_table = kv->page_table;
+  a.out = out;
+  a.partial = c->at<float>(c->L.apart);
+  a.partial_bytes = c->L.apart_bytes;
+  a.status = c->status;
+  a.B = B;
+  a.n_q = c->cfg.n_q_heads;
+  a.n_kv = c->cfg.n_kv_heads;
+  a.head_dim = c->cfg.head_dim;
+  a.layer = layer;
+  a.page_size = kv->page_size;
+  a.capacity = kv->capacity;
+  a.batch_cap = kv->batch_capacity;
+  a.n_pages = kv->n_pages;
+  a.max_pages = kv->max_pages_per_seq;
+  const int cap_keys = kv->page_size ? kv->max_pages_per_seq * kv->page_size : kv->capacity;
+  a.max_keys = std::max(1, std::min(cap_keys, c->cfg.max_seq));
+  a.sm_count = c->sm_count;
+  if (c->cfg.dtype == LLAMA_BF16) {
+    const uint64_t d = c->cfg.head_dim, nkv = c->cfg.n_kv_heads;
+    const uint64_t rows = kv->page_size ? (uint64_t)kv->n_pages * nkv * kv->page_size
+                                        : (uint64_t)kv->batch_capacity * nkv * kv->capacity;
+    a.map_k = map3d(c, kv->k, d, rows, c->cfg.n_layers, 16, 1);
+    a.map_v = map3d(c, kv->v, d, rows, c->cfg.n_layers, 16, 1);
+    if (!a.map_k || !a.map_v) return LLAMA_ERR_CUDA;
+  }
+  Prof pf(c, LLAMA_KERNEL_ATTN_DECODE);
+  c->launches += attn_decode_launches(B, a.n_kv, a.max_keys, c->sm_count, c->cfg.dtype);
+  return cuda_rc(launch_attn_decode(c->cfg.dtype, a, c->stream));
+}
+
+int do_attn_prefill(llama_ctx* c, const void* q, const void* k, const void* v, int B, int T,
+                    void* out) {
+  AttnPrefillArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.status = c->status;
+  a.B = B;
+  a.T = T;
+  a.n_q = c->cfg.n_q_heads;
+  a.n_kv = c->cfg.n_kv_heads;
+  a.head_dim = c->cfg.head_dim;
+  if (c->cfg.dtype == LLAMA_BF16) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return LLAMA_ERR_INVALID_ARG;
+    const uint64_t d = c->cfg.head_dim, rows = (uint64_t)B * T;
+    a.map_q = map3d(c, q, d, c->cfg.n_q_heads, rows, 1, 64);
+    a.map_k = map3d(c, k, d, c->cfg.n_kv_heads, rows, 1, 64);
+    a.map_v = map3d(c, v, d, c->cfg.n_kv_heads, rows, 1, 64);
+    if (!a.map_q || !a.map_k || !a.map_v) return LLAMA_ERR_CUDA;
+  }
+  Prof pf(c, LLAMA_KERNEL_ATTN_PREFILL);
+  c->launches++;
+  return cuda_rc(launch_attn_prefill(c->cfg.dtype, a, c->stream));
+}
+
+#define TRY(expr)                   \
+  do {                              \
+    const int _rc = (expr);         \
+    if (_rc != LLAMA_OK) return _rc; \
+  } while (0)
+
+// One decoder layer on rows x[0..rows): h = h + attn(rmsnorm(h)); h = h + ffn(rmsnorm(h)).
+int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32_t* positions,
+              const llama_kv* kv, bool prefill) {
+  const llama_config& cf = c->cfg;
+  const llama_layer_weights& lw = c->layers[l];
+  const int H = cf.hidden, d = cf.head_dim, nq = cf.n_q_heads, nkv = cf.n_kv_heads,
+            I = cf.intermediate;
+  const int qkv_rows = (nq + 2 * nkv) * d;
+  void* u = c->at<void>(c->L.u);
+  float* qkv = c->at<float>(c->L.qkv);
+  void* q = c->at<void>(c->L.q);
+  void* o = c->at<void>(c->L.o);
+  void* a = c->at<void>(c->L.a);
+  TRY(do_rmsnorm(c, x, rows, 1, 0, lw.attn_norm, u));
+  TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows));
+  if (prefill) {
+    void* ks = c->at<void>(c->L.kside);
+    void* vs = c->at<void>(c->L.vside);
+    TRY(do_rope_append(c, qkv, rows, T, nullptr, l, kv, q, ks, vs));
+    TRY(do_attn_prefill(c, q, ks, vs, B, T, o));
+  } else {
+    TRY(do_rope_append(c, qkv, rows, 1, positions, l, kv, q, nullptr, nullptr));
+    TRY(do_attn_decode(c, q, positions, B, l, kv, o));
+  }
+  TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H));
+  TRY(do_rmsnorm(c, x, rows, 1, 0, lw.ffn_norm, u));
+  TRY(do_gemm(c, LLAMA_EPI_SWIGLU, u, rows, H, lw.w_gate, lw.w_up, I, a, I));
+  TRY(do_gemm(c, LLAMA_EPI_RESID_F32, a, rows, I, lw.w_down, nullptr, H, x, H));
+  return LLAMA_OK;
+}
+
+// Final RMSNorm + LM head (+ greedy choice) on rows stride*b + offset of x.
+int run_head(llama_ctx* c, const float* x, int B, int stride, int offset, float* logits,
+             int32_t* next_ids) {
+  const llama_config& cf = c->cfg;
+  void* ul = c->at<void>(c->L.u_last);
+  TRY(do_rmsnorm(c, x, B, stride, offset, c->final_norm, ul));
+  TRY(do_gemm(c, LLAMA_EPI_STORE_F32, ul, B, cf.hidden, c->lm_head, nullptr, cf.vocab, logits,
+              cf.vocab));
+  if (next_ids) {
+    Prof pf(c, LLAMA_KERNEL_ARGMAX);
+    c->launches++;
+    TRY(cuda_rc(launch_argmax(logits, B, cf.vocab, next_ids, c->stream)));
+  }
+  return LLAMA_OK;
+}
+
+int check_ctx(const llama_ctx* c) { return c ? LLAMA_OK : LLAMA_ERR_INVALID_ARG; }
+
+}  // namespace
+
+// ======================================================================== C ABI
+extern "C" {
+
+const char* llama_strerror(int s) {
+  switch (s) {
+    case LLAMA_OK: return "ok";
+    case LLAMA_ERR_INVALID_ARG: return "invalid argument";
+    case LLAMA_ERR_UNSUPPORTED: return "unsupported shape or layout";
+    case LLAMA_ERR_OUT_OF_RANGE: return "size above the context's limits";
+    case LLAMA_ERR_CUDA: return "CUDA call failed";
+    case LLAMA_ERR_DEVICE_CHECK: return "a kernel flagged bad input or a wait timeout";
+    case LLAMA_ERR_WORKSPACE: return "workspace null, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int llama_workspace_bytes(const llama_config* cfg, size_t* bytes) {
+  if (!bytes) return LLAMA_ERR_INVALID_ARG;
+  TRY(check_config(cfg));
+  *bytes = make_layout(cfg, sm_count_or_default()).total;
+  return LLAMA_OK;
+}
+
+int llama_init(const llama_config* cfg, const llama_weights* w, void* workspace,
+               size_t workspace_bytes, void* stream, llama_ctx** out) {
+  if (!out || !w) return LLAMA_ERR_INVALID_ARG;
+  *out = nullptr;
+  TRY(check_config(cfg));
+  if (!w->layers) return LLAMA_ERR_INVALID_ARG;
+  if (cfg->has_embed_head && (!w->embed || !w->final_norm || !w->lm_head))
+    return LLAMA_ERR_INVALID_ARG;
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const llama_layer_weights& lw = w->layers[l];
+    const void* ps[7] = {lw.attn_norm, lw.wqkv, lw.wo, lw.ffn_norm, lw.w_gate, lw.w_up, lw.w_down};
+    for (const void* p : ps)
+      if (!p || !aligned16(p)) return LLAMA_ERR_INVALID_ARG;
+  }
+  if (cfg->has_embed_head && (!aligned16(w->embed) || !aligned16(w->lm_head)))
+    return LLAMA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+    return LLAMA_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return LLAMA_ERR_CUDA;
+  }
+  if (!load_encode()) return LLAMA_ERR_CUDA;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  Layout L = make_layout(cfg, sms);
+  if (workspace_bytes < L.total) return LLAMA_ERR_WORKSPACE;
+  llama_ctx* c = new (std::nothrow) llama_ctx();
+  if (!c) return LLAMA_ERR_INVALID_ARG;
+  c->cfg = *cfg;
+  c->stream = reinterpret_cast<cudaStream_t>(stream);
+  c->device = dev;
+  c->sm_count = sms;
+  c->es = elem_size(cfg->dtype);
+  c->embed = w->embed;
+  c->final_norm = w->final_norm;
+  c->lm_head = w->lm_head;
+  c->layers.assign(w->layers, w->layers + cfg->n_layers);
+  c->ws = reinterpret_cast<char*>(workspace);
+  c->L = L;
+  c->status = c->at<uint32_t>(L.status);
+  c->counters = c->at<int>(L.counters);
+  c->rope = c->at<float2>(L.rope);
+  int rc = LLAMA_OK;
+  if (cudaMemsetAsync(c->ws, 0, L.rope, c->stream) != cudaSuccess) rc = LLAMA_ERR_CUDA;
+  if (rc == LLAMA_OK &&
+      launch_rope_table(c->rope, cfg->max_seq, cfg->head_dim, (double)cfg->rope_theta,
+                        c->stream) != cudaSuccess)
+    rc = LLAMA_ERR_CUDA;
+  c->launches = 1;
+  if (rc == LLAMA_OK && cfg->dtype == LLAMA_BF16) {  // weight descriptors
+    const uint64_t H = cfg->hidden, d = cfg->head_dim, nq = cfg->n_q_heads,
+                   nkv = cfg->n_kv_heads, I = cfg->intermediate;
+    for (const auto& lw : c->layers) {
+      if (!map2d(c, lw.wqkv, (nq + 2 * nkv) * d, H, 128) || !map2d(c, lw.wo, H, nq * d, 128) ||
+          !map2d(c, lw.w_gate, I, H, 128) || !map2d(c, lw.w_up, I, H, 128) ||
+          !map2d(c, lw.w_down, H, I, 128))
+        rc = LLAMA_ERR_CUDA;
+    }
+    if (cfg->has_embed_head && !map2d(c, c->lm_head, cfg->vocab, H, 128)) rc = LLAMA_ERR_CUDA;
+  }
+  if (rc != LLAMA_OK) {
+    delete c;
+    return rc;
+  }
+  *out = c;
+  return LLAMA_OK;
+}
+
+int llama_set_stream(llama_ctx* c, void* stream) {
+  TRY(check_ctx(c));
+  c->stream = reinterpret_cast<cudaStream_t>(stream);
+  return LLAMA_OK;
+}
+
+int llama_free(llama_ctx* c) {
+  if (!c) return LLAMA_ERR_INVALID_ARG;
+  for (auto& v : c->ev)
+    for (auto& pr : v) {
+      cudaEventDestroy(pr.first);
+      cudaEventDestroy(pr.second);
+    }
+  delete c;
+  return LLAMA_OK;
+}
+
+int llama_prefill(llama_ctx* c, const int32_t* tokens, int32_t B, int32_t T, const llama_kv* kv,
+                  float* logits, int32_t* next_ids) {
+  TRY(check_ctx(c));
+  const llama_config& cf = c->cfg;
+  if (!cf.has_embed_head) return LLAMA_ERR_UNSUPPORTED;
+  if (!tokens || !logits || B < 1 || T < 1) return LLAMA_ERR_INVALID_ARG;
+  if (B > cf.max_batch || (int64_t)B * T > cf.max_tokens || T > cf.max_seq)
+    return LLAMA_ERR_OUT_OF_RANGE;
+  TRY(check_kv(c, kv, B));
+  const int cap = kv->page_size ? kv->max_pages_per_seq * kv->page_size : kv->capacity;
+  if (T > cap) return LLAMA_ERR_OUT_OF_RANGE;
+  const int rows = B * T;
+  float* x = c->at<float>(c->L.x);
+  {
+    Prof pf(c, LLAMA_KERNEL_EMBED);
+    c->launches++;
+    TRY(cuda_rc(launch_embed(cf.dtype, tokens, c->embed, cf.vocab, cf.hidden, rows, x, c->status,
+                             c->stream)));
+  }
+  for (int l = 0; l < cf.n_layers; ++l) TRY(run_layer(c, l, x, rows, B, T, nullptr, kv, true));
+  return run_head(c, x, B, T, T - 1, logits, next_ids);
+}
+
+int llama_decode_step(llama_ctx* c, const int32_t* tokens, const int32_t* positions, int32_t B,
+                      const llama_kv* kv, float* logits, int32_t* next_ids) {
+  TRY(check_ctx(c));
+  const llama_config& cf = c->cfg;
+  if (!cf.has_embed_head) return LLAMA_ERR_UNSUPPORTED;
+  if (!tokens || !positions || !logits || B < 1) return LLAMA_ERR_INVALID_ARG;
+  if (B > cf.max_batch) return LLAMA_ERR_OUT_OF_RANGE;
+  TRY(check_kv(c, kv, B));
+  float* x = c->at<float>(c->L.x);
+  {
+    Prof pf(c, LLAMA_KERNEL_EMBED);
+    c->launches++;
+    TRY(cuda_rc(launch_embed(cf.dtype, tokens, c->embed, cf.vocab, cf.hidden, B, x, c->status,
+                             c->stream)));
+  }
+  for (int l = 0; l < cf.n_layers; ++l) TRY(run_layer(c, l, x, B, B, 1, positions, kv, false));
+  return run_head(c, x, B, 1, 0, logits, next_ids);
+}
+
+int llama_decode_step_host(llama_ctx* c, const int32_t* tokens_host,
+                           const int32_t* positions_host, int32_t B, const llama_kv* kv,
+                           float* logits_host, int32_t* next_ids_host) {
+  TRY(check_ctx(c));
+  if (!tokens_host || !positions_host || B < 1) return LLAMA_ERR_INVALID_ARG;
+  if (B > c->cfg.max_batch) return LLAMA_ERR_OUT_OF_RANGE;
+  int32_t* tok = c->at<int32_t>(c->L.tok);
+  int32_t* pos = c->at<int32_t>(c->L.pos);
+  float* lg = c->at<float>(c->L.logits);
+  int32_t* ids = c->at<int32_t>(c->L.ids);
+  const size_t nb = (size_t)B * sizeof(int32_t);
+  if (cudaMemcpyAsync(tok, tokens_host, nb, cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
+      cudaMemcpyAsync(pos, positions_host, nb, cudaMemcpyHostToDevice, c->stream) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  TRY(llama_decode_step(c, tok, pos, B, kv, lg, ids));
+  if (logits_host &&
+      cudaMemcpyAsync(logits_host, lg, (size_t)B * c->cfg.vocab * sizeof(float),
+                      cudaMemcpyDeviceToHost, c->stream) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  if (next_ids_host &&
+      cudaMemcpyAsync(next_ids_host, ids, nb, cudaMemcpyDeviceToHost, c->stream) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  return llama_sync_status(c);
+}
+
+int llama_prefill_hidden(llama_ctx* c, float* hidden, int32_t B, int32_t T, const llama_kv* kv) {
+  TRY(check_ctx(c));
+  const llama_config& cf = c->cfg;
+  if (!hidden || B < 1 || T < 1) return LLAMA_ERR_INVALID_ARG;
+  if (B > cf.max_batch || (int64_t)B * T > cf.max_tokens || T > cf.max_seq)
+    return LLAMA_ERR_OUT_OF_RANGE;
+  TRY(check_kv(c, kv, B));
+  const int cap = kv->page_size ? kv->max_pages_per_seq * kv->page_size : kv->capacity;
+  if (T > cap) return LLAMA_ERR_OUT_OF_RANGE;
+  for (int l = 0; l < cf.n_layers; ++l)
+    TRY(run_layer(c, l, hidden, B * T, B, T, nullptr, kv, true));
+  return LLAMA_OK;
+}
+
+int llama_decode_hidden(llama_ctx* c, float* hidden, const int32_t* positions, int32_t B,
+                        const llama_kv* kv) {
+  TRY(check_ctx(c));
+  if (!hidden || !positions || B < 1) return LLAMA_ERR_INVALID_ARG;
+  if (B > c->cfg.max_batch) return LLAMA_ERR_OUT_OF_RANGE;
+  TRY(check_kv(c, kv, B));
+  for (int l = 0; l < c->cfg.n_layers; ++l)
+    TRY(run_layer(c, l, hidden, B, B, 1, positions, kv, false));
+  return LLAMA_OK;
+}
+
+int llama_sync_status(llama_ctx* c) {
+  TRY(check_ctx(c));
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return LLAMA_ERR_CUDA;
+  uint32_t flags = 0;
+  if (cudaMemcpy(&flags, c->status, sizeof(flags), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  c->last_flags = flags;
+  if (flags) {
+    if (cudaMemset(c->status, 0, sizeof(uint32_t)) != cudaSuccess) return LLAMA_ERR_CUDA;
+    return LLAMA_ERR_DEVICE_CHECK;
+  }
+  return LLAMA_OK;
+}
+
+uint32_t llama_last_device_flags(const llama_ctx* c) { return c ? c->last_flags : 0u; }
+
+int llama_profile_enable(llama_ctx* c, uint32_t mask) {
+  TRY(check_ctx(c));
+  c->prof_mask = mask;
+  for (size_t& u : c->ev_used) u = 0;
+  return LLAMA_OK;
+}
+
+int llama_profile_read(llama_ctx* c, int32_t kind, double* total_ms, int64_t* launches) {
+  TRY(check_ctx(c));
+  if (kind < 0 || kind >= LLAMA_KERNEL_COUNT || !total_ms || !launches)
+    return LLAMA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return LLAMA_ERR_CUDA;
+  double tot = 0.0;
+  for (size_t i = 0; i < c->ev_used[kind]; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, c->ev[kind][i].first, c->ev[kind][i].second) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+    tot += ms;
+  }
+  *total_ms = tot;
+  *launches = (int64_t)c->ev_used[kind];
+  c->ev_used[kind] = 0;
+  return LLAMA_OK;
+}
+
+int64_t llama_launch_count(const llama_ctx* c) { return c ? c->launches : 0; }
+
+// ---------------------------------------------------------------- single operations
+int llama_op_rmsnorm(llama_ctx* c, const float* x, int32_t rows, int32_t in_stride,
+                     int32_t in_offset, const void* gamma, void* out) {
+  TRY(check_ctx(c));
+  if (!x || !gamma || !out || rows < 1 || in_stride < 1 || in_offset < 0)
+    return LLAMA_ERR_INVALID_ARG;
+  return do_rmsnorm(c, x, rows, in_stride, in_offset, gamma, out);
+}
+
+int llama_op_linear(llama_ctx* c, const void* x, int32_t n_rows, const void* w, const void* w_up,
+                    int32_t M, int32_t K, int32_t epilogue, void* out) {
+  TRY(check_ctx(c));
+  if (!x || !w || !out || n_rows < 1 || M < 1 || K < 1) return LLAMA_ERR_INVALID_ARG;
+  if (epilogue < LLAMA_EPI_STORE_F32 || epilogue > LLAMA_EPI_SWIGLU) return LLAMA_ERR_INVALID_ARG;
+  if (epilogue == LLAMA_EPI_SWIGLU && !w_up) return LLAMA_ERR_INVALID_ARG;
+  if (c->cfg.dtype == LLAMA_BF16 && K % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (n_rows > std::max(c->cfg.max_batch, c->cfg.max_tokens)) return LLAMA_ERR_OUT_OF_RANGE;
+  return do_gemm(c, epilogue, x, n_rows, K, w, epilogue == LLAMA_EPI_SWIGLU ? w_up : nullptr, M,
+                 out, M);
+}
+
+int llama_op_rope_append(llama_ctx* c, const float* qkv, int32_t rows, int32_t rows_per_seq,
+                         const int32_t* positions, int32_t layer, const llama_kv* kv, void* q_out,
+                         void* k_out, void* v_out) {
+  TRY(check_ctx(c));
+  if (!qkv || !q_out || rows < 1 || rows_per_seq < 1 || layer < 0 || layer >= c->cfg.n_layers)
+    return LLAMA_ERR_INVALID_ARG;
+  TRY(check_kv(c, kv, (rows + rows_per_seq - 1) / rows_per_seq));
+  return do_rope_append(c, qkv, rows, rows_per_seq, positions, layer, kv, q_out, k_out, v_out);
+}
+
+int llama_op_attention_decode(llama_ctx* c, const void* q, const int32_t* positions, int32_t B,
+                              int32_t layer, const llama_kv* kv, void* out) {
+  TRY(check_ctx(c));
+  if (!q || !positions || !out || B < 1 || layer < 0 || layer >= c->cfg.n_layers)
+    return LLAMA_ERR_INVALID_ARG;
+  if (B > c->cfg.max_batch) return LLAMA_ERR_OUT_OF_RANGE;
+  TRY(check_kv(c, kv, B));
+  return do_attn_decode(c, q, positions, B, layer, kv, out);
+}
+
+int llama_op_attention_prefill(llama_ctx* c, const void* q, const void* k, const void* v,
+                               int32_t B, int32_t T, void* out) {
+  TRY(check_ctx(c));
+  if (!q || !k || !v || !out || B < 1 || T < 1) return LLAMA_ERR_INVALID_ARG;
+  if (c->cfg.dtype == LLAMA_F32 && (size_t)(T + c->cfg.head_dim + 32) * 4 > 200 * 1024)
+    return LLAMA_ERR_OUT_OF_RANGE;
+  return do_attn_prefill(c, q, k, v, B, T, out);
+}
+
+int llama_op_embed(llama_ctx* c, const int32_t* tokens, int32_t n, void* out) {
+  TRY(check_ctx(c));
+  if (!c->cfg.has_embed_head) return LLAMA_ERR_UNSUPPORTED;
+  if (!tokens || !out || n < 1) return LLAMA_ERR_INVALID_ARG;
+  Prof pf(c, LLAMA_KERNEL_EMBED);
+  c->launches++;
+  return cuda_rc(launch_embed(c->cfg.dtype, tokens, c->embed, c->cfg.vocab, c->cfg.hidden, n,
+                              reinterpret_cast<float*>(out), c->status, c->stream));
+}
+
+int llama_op_argmax(llama_ctx* c, const float* logits, int32_t B, int32_t V, int32_t* ids) {
+  TRY(check_ctx(c));
+  if (!logits || !ids || B < 1 || V < 1) return LLAMA_ERR_INVALID_ARG;
+  Prof pf(c, LLAMA_KERNEL_ARGMAX);
+  c->launches++;
+  return cuda_rc(launch_argmax(logits, B, V, ids, c->stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Host-side declarations shared by the library's translation units: kernel
+// argument blocks and launcher entry points (all enqueue on a caller stream).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/llama_gb300.h"
+
+namespace llgb {
+
+// ------------------------------------------------------------------ RoPE + append
+struct RopeAppendArgs {
+  const float* qkv;          // [rows, (n_q + 2 n_kv) d] fp32
+  const int32_t* positions;  // [rows] or null (position = r % rows_per_seq)
+  const float2* rope;        // [max_seq, d/2] (cos, sin)
+  void* q_out;               // [rows, n_q d]
+  void* k_out;               // [rows, n_kv d] or null
+  void* v_out;               // [rows, n_kv d] or null
+  void* k_cache;
+  void* v_cache;
+  const int32_t* page_table;
+  uint32_t* status;
+  int rows_per_seq, n_q, n_kv, head_dim, max_seq, layer;
+  int page_size, capacity, batch_cap, n_pages, max_pages;
+};
+
+cudaError_t launch_embed(int dtype, const int32_t* tokens, const void* table, int V, int H, int n,
+                         float* out, uint32_t* status, cudaStream_t st);
+cudaError_t launch_rmsnorm(int dtype, const float* x, int rows, int in_stride, int in_offset,
+                           const void* gamma, int H, float eps, void* out, cudaStream_t st);
+cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double theta,
+                              cudaStream_t st);
+cudaError_t launch_rope_append(int dtype, const RopeAppendArgs& a, int rows, cudaStream_t st);
+cudaError_t launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st);
+
+// ------------------------------------------------------------------ GEMM
+// y[n, m] (epilogue) sum_k x[n, k] * w[m, k]; x has N rows, w has M rows.
+struct GemmCall {
+  int dtype;
+  int epi;                    // LLAMA_EPI_*
+  int M, N, K;
+  const void* x;              // [N, K]   (fp32 path)
+  const void* w;              // [M, K]
+  const void* w_up;           // [M, K]   (SWIGLU)
+  const CUtensorMap* map_w;   // bf16 path: weights, box {64, 128}, SWIZZLE_128B
+  const CUtensorMap* map_up;  // bf16 path, SWIGLU
+  const CUtensorMap* map_x;   // bf16 path: activations, box {64, n_tile}
+  int n_tile;                 // bf16 path: MMA N (multiple of 16, <= 256); map_x box rows
+  void* out;
+  int ldo;
+  float* partial;             // split-K partial sums (workspace)
+  size_t partial_bytes;
+  int* counters;              // split-K arrival counters (workspace, zeroed)
+  int n_counters;
+  uint32_t* status;
+  int sm_count;
+};
+// Tile width the bf16 GEMM uses for N activation rows.
+int gemm_n_tile(int N);
+// Bytes of split-K partials a call may need (upper bound for the workspace).
+size_t gemm_partial_bytes(int M, int N, int K, int dual, int sm_count);
+cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st);
+cudaError_t gemm_prepare();  // sets kernel attributes once per process
+
+// ------------------------------------------------------------------ attention
+struct AttnDecodeArgs {
+  const void* q;             // [B, n_q, d]
+  const int32_t* positions;  // [B]
+  const CUtensorMap* map_k;  // bf16: 3D {d, rows per layer, layers}, box {64, 16, 1}, SW128
+  const CUtensorMap* map_v;
+  const void* k_cache;       // fp32 path
+  const void* v_cache;
+  const int32_t* page_table;
+  void* out;                 // [B, n_q d]
+  float* partial;            // split partials (workspace)
+  size_t partial_bytes;
+  uint32_t* status;
+  int B, n_q, n_kv, head_dim, layer;
+  int page_size, capacity, batch_cap, n_pages, max_pages;
+  int max_keys;              // upper bound of positions[b] + 1 (sizes the split count)
+  int sm_count;
+};
+size_t attn_decode_partial_bytes(int B, int n_q, int head_dim, int max_keys, int sm_count,
+                                 int n_kv);
+cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t st);
+// Kernel launches one decode-attention call makes (1, or 2 with a split merge).
+int attn_decode_launches(int B, int n_kv, int max_keys, int sm_count, int dtype);
+
+struct AttnPrefillArgs {
+  const void* q;             // [B*T, n_q, d]
+  const void* k;             // [B*T, n_kv, d]
+  const void* v;
+  const CUtensorMap* map_q;  // bf16: 3D {d, heads, rows}, box {64, 1, 64}, SW128
+  const CUtensorMap* map_k;
+  const CUtensorMap* map_v;
+  void* out;                 // [B*T, n_q d]
+  uint32_t* status;
+  int B, T, n_q, n_kv, head_dim;
+};
+cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_t st);
+cudaError_t attn_prepare();
+
+}  // namespace llgb

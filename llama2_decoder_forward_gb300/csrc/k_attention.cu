@@ -1,0 +1,771 @@
+// Grouped-query scaled dot-product attention ("Llama2架构与推理全解析" §2.3:
+// scores q.k / sqrt(d), causal mask, softmax, weighted sum of V; §1.5 GQA:
+// query head h reads K/V head h / G; §2.4: decode reads the whole cache).
+//
+// Decode (bf16, head_dim 128): one CTA per (sequence, K/V head, key split).
+// A producer warp copies K and V of 16-key sub-tiles (one page of a paged
+// cache, or 16 consecutive slots of a contiguous one) from HBM into shared
+// memory with TMA (128-byte swizzle) into a 3-stage mbarrier ring; every
+// query head of the group shares the tile. Four consumer warps each take one
+// sub-tile per stage and run S = Q K^T and O += P V on mma.sync (the G query
+// heads are the 16-row M side, zero-padded), with an online softmax in fp32
+// (base-2 exponent, the running maximum subtracted before exp). The four
+// warps' (max, sum, O) are merged through shared memory; with several key
+// splits a small kernel merges the splits the same way.
+//
+// Prefill (bf16): FlashAttention-style: one CTA per (64 query rows, head,
+// sequence); K/V tiles of 64 keys via TMA, key tiles past the diagonal are
+// skipped, the diagonal tile is masked.
+//
+// fp32 configs use plain CUDA-core kernels (exact fp32, exp on the CUDA
+// math library) for both phases.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace llgb {
+
+constexpr int AD = 128;  // head_dim of the tensor-core kernels
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ======================================================================== decode
+constexpr int SUBK = 16;                               // keys per TMA box / page granule
+constexpr int DTILE = 64;                              // keys per stage
+constexpr int DSTAGES = 3;
+constexpr int DEC_THREADS = 160;                       // 4 consumer warps + producer warp
+constexpr uint32_t HALF_BYTES = SUBK * 128;            // 16 rows x 64 dims x bf16
+constexpr uint32_t SUB_BYTES = 2 * HALF_BYTES;         // 16 rows x 128 dims
+constexpr uint32_t DSTAGE_BYTES = 4 * SUB_BYTES * 2;   // 4 sub-tiles, K and V: 32 KB
+constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 256;
+
+struct DecParams {
+  const bf16* q;
+  const int32_t* positions;
+  const int32_t* page_table;
+  bf16* out;
+  float* part;
+  uint32_t* status;
+  int n_q, n_kv, G, layer;
+  int page_size, capacity, batch_cap, n_pages, max_pages;
+  int splits, keys_per_split;
+  float scale_log2;
+};
+
+// Number of keys sequence b attends (positions[b] + 1), clamped to the cache;
+// out-of-range positions are flagged by the RoPE/append kernel.
+__device__ __forceinline__ int decode_keys(int pos, int cap_keys) {
+  if (pos < 0) return 0;
+  return min(pos + 1, cap_keys);
+}
+
+// Row index (within one layer's [rows, d] view of the cache) of the 16-key
+// sub-tile starting at key k0 of sequence b, K/V head g. A page id outside the
+// pool is flagged and mapped to a row range that TMA fills with zeros.
+__device__ __forceinline__ int kv_row(const DecParams& p, int b, int g, int k0) {
+  if (p.page_size == 0) return (b * p.n_kv + g) * p.capacity + k0;
+  const int pi = k0 / p.page_size;
+  const int page = pi < p.max_pages ? p.page_table[(size_t)b * p.max_pages + pi] : -1;
+  if (page < 0 || page >= p.n_pages) {
+    flag(p.status, LLAMA_FLAG_PAGE_RANGE);
+    return -4 * SUBK;
+  }
+  return (page * p.n_kv + g) * p.page_size + (k0 % p.page_size);
+}
+
+__device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+__global__ void __launch_bounds__(DEC_THREADS, 2)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap mapK,
+                       const __grid_constant__ CUtensorMap mapV, DecParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + DSTAGES * DSTAGE_BYTES);
+  uint64_t* empty = full + DSTAGES;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + DSTAGES);
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
+  const int n_keys = decode_keys(p.positions[b], cap_keys);
+  const int kbeg = split * p.keys_per_split;
+  const int kend = min(n_keys, kbeg + p.keys_per_split);
+  if (kbeg >= kend) return;  // this split has no keys (the combine skips it)
+  const int n_sub = (kend - kbeg + SUBK - 1) / SUBK;
+  const int n_tiles = (n_sub + 3) / 4;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < DSTAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 4) {  // ------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % DSTAGES;
+        const uint32_t ph = (t / DSTAGES) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, p.status)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        const int nsub = min(4, n_sub - 4 * t);
+        uint8_t* st = smem + s * DSTAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], nsub * SUB_BYTES * 2);
+        for (int j = 0; j < nsub; ++j) {
+          const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
+          uint8_t* kd = st + j * SUB_BYTES;
+          uint8_t* vd = st + 4 * SUB_BYTES + j * SUB_BYTES;
+          tma_load_3d(kd, &mapK, &full[s], 0, row, p.layer);
+          tma_load_3d(kd + HALF_BYTES, &mapK, &full[s], 64, row, p.layer);
+          tma_load_3d(vd, &mapV, &full[s], 0, row, p.layer);
+          tma_load_3d(vd + HALF_BYTES, &mapV, &full[s], 64, row, p.layer);
+        }
+        ++issued;
+      }
+      if (!ok) {
+        for (int t = issued - 1; t >= 0 && t >= issued - DSTAGES; --t)
+          mbar_wait(&full[t % DSTAGES], (t / DSTAGES) & 1, p.status);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  const int G = p.G;
+  const int r0 = lane >> 2;
+  uint32_t qa[8][4];
+  {
+    const bf16* qb = p.q + ((size_t)b * p.n_q + (size_t)g * G) * AD;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int col = kk * 16 + 2 * (lane & 3);
+      qa[kk][0] = r0 < G ? *reinterpret_cast<const uint32_t*>(qb + r0 * AD + col) : 0u;
+      qa[kk][1] = r0 + 8 < G ? *reinterpret_cast<const uint32_t*>(qb + (r0 + 8) * AD + col) : 0u;
+      qa[kk][2] = r0 < G ? *reinterpret_cast<const uint32_t*>(qb + r0 * AD + col + 8) : 0u;
+      qa[kk][3] =
+          r0 + 8 < G ? *reinterpret_cast<const uint32_t*>(qb + (r0 + 8) * AD + col + 8) : 0u;
+    }
+  }
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  float oacc[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  const int mi = lane >> 3, rr = lane & 7;
+
+  for (int t = 0; t < n_tiles; ++t) {
+    const int s = t % DSTAGES;
+    const uint32_t ph = (t / DSTAGES) & 1;
+    if (*abort_flag) break;
+    if (!mbar_wait(&full[s], ph, p.status)) {
+      *abort_flag = 1;
+      break;
+    }
+    const int sub = 4 * t + warp;
+    if (sub < n_sub) {
+      uint8_t* st = smem + s * DSTAGE_BYTES;
+      const int k0 = kbeg + sub * SUBK;
+      const int nvalid = min(SUBK, kend - k0);
+      const uint32_t kbase = smem_u32(st + warp * SUB_BYTES);
+      uint8_t* vptr = st + 4 * SUB_BYTES + warp * SUB_BYTES;
+      if (nvalid < SUBK) {  // rows past the last key may hold anything: zero them
+        const int nz = (SUBK - nvalid) * 16;
+        for (int i = lane; i < nz; i += 32) {
+          const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
+          *reinterpret_cast<uint4*>(vptr + half * HALF_BYTES + row * 128 + chunk * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      const uint32_t vbase = smem_u32(vptr);
+      // S = Q K^T over 16 keys
+      float sc[2][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[0][i] = sc[1][i] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int half = kk >> 2;
+        const int chunk = (kk & 3) * 2 + (mi & 1);
+        const int row = ((mi >> 1) << 3) + rr;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + half * HALF_BYTES + swz128(row, chunk), b0, b1, b2, b3);
+        mma_bf16_16816(sc[0], qa[kk], b0, b1);
+        mma_bf16_16816(sc[1], qa[kk], b2, b3);
+      }
+      // online softmax in base 2
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int key = nb * 8 + 2 * (lane & 3) + (i & 1);
+          const float v = key < nvalid ? sc[nb][i] * p.scale_log2 : -INFINITY;
+          sc[nb][i] = v;
+          mx[i >> 1] = fmaxf(mx[i >> 1], v);
+        }
+      float corr[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        const float mnew = fmaxf(mrow[h], mx[h]);
+        corr[h] = mnew == -INFINITY ? 1.f : exp2f(mrow[h] - mnew);
+        mrow[h] = mnew;
+      }
+      float ps[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = i >> 1;
+          const float pv = mrow[h] == -INFINITY ? 0.f : exp2f(sc[nb][i] - mrow[h]);
+          sc[nb][i] = pv;
+          ps[h] += pv;
+        }
+      lrow[0] = lrow[0] * corr[0] + ps[0];
+      lrow[1] = lrow[1] * corr[1] + ps[1];
+#pragma unroll
+      for (int dn = 0; dn < 16; ++dn) {
+        oacc[dn][0] *= corr[0];
+        oacc[dn][1] *= corr[0];
+        oacc[dn][2] *= corr[1];
+        oacc[dn][3] *= corr[1];
+      }
+      uint32_t pa[4] = {pack_bf16(sc[0][0], sc[0][1]), pack_bf16(sc[0][2], sc[0][3]),
+                        pack_bf16(sc[1][0], sc[1][1]), pack_bf16(sc[1][2], sc[1][3])};
+      // O += P V
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        const int c16 = dp * 2 + (mi >> 1);
+        const int row = ((mi & 1) << 3) + rr;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + (c16 >> 3) * HALF_BYTES + swz128(row, c16 & 7), b0, b1, b2, b3);
+        mma_bf16_16816(oacc[2 * dp], pa, b0, b1);
+        mma_bf16_16816(oacc[2 * dp + 1], pa, b2, b3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ---------------------------------------------------------------- merge the 4 warps
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
+    lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
+  }
+  float* so = reinterpret_cast<float*>(smem);  // [4][16][128]
+  float* sm = so + 4 * 16 * AD;                // [4][16]
+  float* sl = sm + 64;                         // [4][16]
+  cons_bar();  // every consumer is done with the stage buffers
+#pragma unroll
+  for (int dn = 0; dn < 16; ++dn)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = r0 + (i >= 2 ? 8 : 0);
+      const int col = dn * 8 + 2 * (lane & 3) + (i & 1);
+      so[(warp * 16 + row) * AD + col] = oacc[dn][i];
+    }
+  if ((lane & 3) == 0) {
+    sm[warp * 16 + r0] = mrow[0];
+    sm[warp * 16 + r0 + 8] = mrow[1];
+    sl[warp * 16 + r0] = lrow[0];
+    sl[warp * 16 + r0 + 8] = lrow[1];
+  }
+  cons_bar();
+  if (*abort_flag) return;
+  const int t = threadIdx.x;  // output dim
+  for (int r = 0; r < G; ++r) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, sm[w * 16 + r]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float mw = sm[w * 16 + r];
+        const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        L += sl[w * 16 + r] * f;
+        O += so[(w * 16 + r) * AD + t] * f;
+      }
+    }
+    const size_t bh = (size_t)b * p.n_q + (size_t)g * G + r;
+    if (p.splits == 1) {
+      p.out[bh * AD + t] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    } else {
+      float* pp = p.part + (bh * p.splits + split) * (AD + 2);
+      pp[t] = O;
+      if (t == 0) {
+        pp[AD] = M;
+        pp[AD + 1] = L;
+      }
+    }
+  }
+}
+
+// Merge the key splits of (sequence, head) bh: rescale each split's sum and
+// output by 2^(m_s - max m) and normalise.
+__global__ void attn_combine_kernel(const float* __restrict__ part,
+                                    const int32_t* __restrict__ positions, int n_q, int splits,
+                                    int keys_per_split, int cap_keys, int d, void* out,
+                                    int out_f32) {
+  const int bh = blockIdx.x;
+  const int b = bh / n_q;
+  const int n_keys = decode_keys(positions[b], cap_keys);
+  const int used = min(splits, (n_keys + keys_per_split - 1) / keys_per_split);
+  const float* pp = part + (size_t)bh * splits * (d + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < used; ++s) M = fmaxf(M, pp[(size_t)s * (d + 2) + d]);
+  for (int t = threadIdx.x; t < d; t += blockDim.x) {
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < used; ++s) {
+        const float* ps = pp + (size_t)s * (d + 2);
+        const float f = ps[d] == -INFINITY ? 0.f : exp2f(ps[d] - M);
+        L += ps[d + 1] * f;
+        O += ps[t] * f;
+      }
+    }
+    const float v = L > 0.f ? O / L : 0.f;
+    if (out_f32)
+      reinterpret_cast<float*>(out)[(size_t)bh * d + t] = v;
+    else
+      reinterpret_cast<bf16*>(out)[(size_t)bh * d + t] = __float2bfloat16_rn(v);
+  }
+}
+
+// ======================================================================== prefill (bf16)
+constexpr int PQ = 64;  // query rows per CTA
+constexpr int PK = 64;  // keys per tile
+constexpr int PSTAGES = 2;
+constexpr int PRE_THREADS = 160;
+constexpr uint32_t PHALF = PK * 128;       // 64 rows x 64 dims bf16 = 8 KB
+constexpr uint32_t PTILE = 2 * PHALF;      // 64 x 128 = 16 KB
+constexpr size_t PRE_SMEM = PTILE + PSTAGES * 2 * PTILE + 1024 + 256;
+
+struct PreParams {
+  bf16* out;
+  uint32_t* status;
+  int T, n_q, n_kv, G, n_qtiles;
+  float scale_log2;
+};
+
+__global__ void __launch_bounds__(PRE_THREADS, 2)
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap mapQ,
+                        const __grid_constant__ CUtensorMap mapK,
+                        const __grid_constant__ CUtensorMap mapV, PreParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* qs = smem;
+  uint8_t* kvs = smem + PTILE;  // stage s: K at s*2*PTILE, V at s*2*PTILE + PTILE
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + PTILE + PSTAGES * 2 * PTILE);
+  uint64_t* full = qfull + 1;
+  uint64_t* empty = full + PSTAGES;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + PSTAGES);
+
+  const int qt = p.n_qtiles - 1 - (int)blockIdx.x;  // longest rows first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int g = h / p.G;
+  const int q0 = qt * PQ;
+  const int n_kt = min(qt + 1, (p.T + PK - 1) / PK);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rowbase = b * p.T;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qfull, 1);
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 4) {  // producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      mbar_arrive_expect_tx(qfull, PTILE);
+      tma_load_3d(qs, &mapQ, qfull, 0, h, rowbase + q0);
+      tma_load_3d(qs + PHALF, &mapQ, qfull, 64, h, rowbase + q0);
+      int issued = 0;
+      bool ok = true;
+      for (int kt = 0; kt < n_kt; ++kt) {
+        const int s = kt % PSTAGES;
+        const uint32_t ph = (kt / PSTAGES) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, p.status)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* ks = kvs + s * 2 * PTILE;
+        mbar_arrive_expect_tx(&full[s], 2 * PTILE);
+        tma_load_3d(ks, &mapK, &full[s], 0, g, rowbase + kt * PK);
+        tma_load_3d(ks + PHALF, &mapK, &full[s], 64, g, rowbase + kt * PK);
+        tma_load_3d(ks + PTILE, &mapV, &full[s], 0, g, rowbase + kt * PK);
+        tma_load_3d(ks + PTILE + PHALF, &mapV, &full[s], 64, g, rowbase + kt * PK);
+        ++issued;
+      }
+      mbar_wait(qfull, 0, p.status);
+      if (!ok) {
+        for (int t = issued - 1; t >= 0 && t >= issued - PSTAGES; --t)
+          mbar_wait(&full[t % PSTAGES], (t / PSTAGES) & 1, p.status);
+      }
+    }
+    return;
+  }
+
+  // consumers: warp w owns query rows q0 + 16w .. q0 + 16w + 15
+  const int mi = lane >> 3, rr = lane & 7;
+  const int r0 = lane >> 2;
+  const int myrow0 = q0 + warp * 16 + r0;  // rows myrow0 and myrow0 + 8
+  if (!mbar_wait(qfull, 0, p.status)) *abort_flag = 1;
+  uint32_t qa[8][4];
+  {
+    const uint32_t qb = smem_u32(qs);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int row = warp * 16 + ((mi & 1) << 3) + rr;
+      const int chunk = (kk & 3) * 2 + (mi >> 1);
+      ldsm_x4(qb + (kk >> 2) * PHALF + swz128(row, chunk), qa[kk][0], qa[kk][1], qa[kk][2],
+              qa[kk][3]);
+    }
+  }
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  float oacc[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+
+  for (int kt = 0; kt < n_kt; ++kt) {
+    const int s = kt % PSTAGES;
+    const uint32_t ph = (kt / PSTAGES) & 1;
+    if (*abort_flag) break;
+    if (!mbar_wait(&full[s], ph, p.status)) {
+      *abort_flag = 1;
+      break;
+    }
+    const uint32_t kb = smem_u32(kvs + s * 2 * PTILE);
+    const uint32_t vb = kb + PTILE;
+    float sc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        const int row = np * 16 + ((mi >> 1) << 3) + rr;
+        const int chunk = (kk & 3) * 2 + (mi & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + (kk >> 2) * PHALF + swz128(row, chunk), b0, b1, b2, b3);
+        mma_bf16_16816(sc[2 * np], qa[kk], b0, b1);
+        mma_bf16_16816(sc[2 * np + 1], qa[kk], b2, b3);
+      }
+    }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int key = kt * PK + nb * 8 + 2 * (lane & 3) + (i & 1);
+        const int row = myrow0 + (i >= 2 ? 8 : 0);
+        const float v = (key <= row && key < p.T) ? sc[nb][i] * p.scale_log2 : -INFINITY;
+        sc[nb][i] = v;
+        mx[i >> 1] = fmaxf(mx[i >> 1], v);
+      }
+    float corr[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
+      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
+      const float mnew = fmaxf(mrow[hh], mx[hh]);
+      corr[hh] = mnew == -INFINITY ? 1.f : exp2f(mrow[hh] - mnew);
+      mrow[hh] = mnew;
+    }
+    float ps[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int hh = i >> 1;
+        const float pv = mrow[hh] == -INFINITY ? 0.f : exp2f(sc[nb][i] - mrow[hh]);
+        sc[nb][i] = pv;
+        ps[hh] += pv;
+      }
+    lrow[0] = lrow[0] * corr[0] + ps[0];
+    lrow[1] = lrow[1] * corr[1] + ps[1];
+#pragma unroll
+    for (int dn = 0; dn < 16; ++dn) {
+      oacc[dn][0] *= corr[0];
+      oacc[dn][1] *= corr[0];
+      oacc[dn][2] *= corr[1];
+      oacc[dn][3] *= corr[1];
+    }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t pa[4] = {pack_bf16(sc[2 * ks][0], sc[2 * ks][1]),
+                        pack_bf16(sc[2 * ks][2], sc[2 * ks][3]),
+                        pack_bf16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]),
+                        pack_bf16(sc[2 * ks + 1][2], sc[2 * ks + 1][3])};
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        const int c16 = dp * 2 + (mi >> 1);
+        const int row = ks * 16 + ((mi & 1) << 3) + rr;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + (c16 >> 3) * PHALF + swz128(row, c16 & 7), b0, b1, b2, b3);
+        mma_bf16_16816(oacc[2 * dp], pa, b0, b1);
+        mma_bf16_16816(oacc[2 * dp + 1], pa, b2, b3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  if (*abort_flag) return;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    lrow[hh] += __shfl_xor_sync(0xffffffffu, lrow[hh], 1);
+    lrow[hh] += __shfl_xor_sync(0xffffffffu, lrow[hh], 2);
+  }
+  const size_t ld = (size_t)p.n_q * AD;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int row = myrow0 + hh * 8;
+    if (row >= p.T) continue;
+    const float inv = lrow[hh] > 0.f ? 1.f / lrow[hh] : 0.f;
+    bf16* dst = p.out + (size_t)(rowbase + row) * ld + (size_t)h * AD;
+#pragma unroll
+    for (int dn = 0; dn < 16; ++dn) {
+      const int col = dn * 8 + 2 * (lane & 3);
+      *reinterpret_cast<uint32_t*>(dst + col) =
+          pack_bf16(oacc[dn][2 * hh] * inv, oacc[dn][2 * hh + 1] * inv);
+    }
+  }
+}
+
+// ======================================================================== fp32 CUDA-core kernels
+// Decode: one CTA per (query head, sequence); scores in shared memory.
+__global__ void attn_decode_f32_kernel(const float* __restrict__ q, const int32_t* positions,
+                                       const float* __restrict__ kc, const float* __restrict__ vc,
+                                       const int32_t* page_table, float* __restrict__ out,
+                                       int n_q, int n_kv, int d, int layer, int page_size,
+                                       int capacity, int batch_cap, int n_pages, int max_pages,
+                                       uint32_t* status) {
+  extern __shared__ float sh[];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int g = h / (n_q / n_kv);
+  const int cap_keys = page_size ? max_pages * page_size : capacity;
+  const int n = decode_keys(positions[b], cap_keys);
+  float* qs = sh;
+  float* sc = sh + d;
+  float* red = sc + cap_keys;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) qs[i] = q[((size_t)b * n_q + h) * d + i];
+  __syncthreads();
+  auto slot = [&](int m) -> long long {
+    if (page_size == 0) return (((long long)layer * batch_cap + b) * n_kv + g) * capacity + m;
+    const int page = page_table[(size_t)b * max_pages + m / page_size];
+    if (page < 0 || page >= n_pages) return -1;
+    return (((long long)layer * n_pages + page) * n_kv + g) * page_size + m % page_size;
+  };
+  const float scale = 1.0f / sqrtf((float)d);
+  for (int m = threadIdx.x; m < n; m += blockDim.x) {
+    const long long sl = slot(m);
+    float s = 0.f;
+    if (sl >= 0) {
+      const float* kr = kc + sl * d;
+      for (int i = 0; i < d; ++i) s = fmaf(qs[i], kr[i], s);
+    } else {
+      flag(status, LLAMA_FLAG_PAGE_RANGE);
+    }
+    sc[m] = s * scale;
+  }
+  __syncthreads();
+  float mx = -INFINITY;
+  for (int m = threadIdx.x; m < n; m += blockDim.x) mx = fmaxf(mx, sc[m]);
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = -INFINITY;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
+  __syncthreads();
+  for (int m = threadIdx.x; m < n; m += blockDim.x) sc[m] = expf(sc[m] - mx);
+  __syncthreads();
+  float sum = 0.f;
+  for (int m = 0; m < n; ++m) sum += sc[m];
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float o = 0.f;
+    for (int m = 0; m < n; ++m) {
+      const long long sl = slot(m);
+      if (sl >= 0) o = fmaf(sc[m], vc[sl * d + i], o);
+    }
+    out[((size_t)b * n_q + h) * d + i] = n > 0 ? o / sum : 0.f;
+  }
+}
+
+// Prefill: one CTA per (row, head, sequence), keys 0..row of its sequence.
+__global__ void attn_prefill_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                                        const float* __restrict__ v, float* __restrict__ out,
+                                        int T, int n_q, int n_kv, int d) {
+  extern __shared__ float sh[];
+  const int t = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (n_q / n_kv);
+  const int n = t + 1;
+  float* qs = sh;
+  float* sc = sh + d;
+  float* red = sc + T;
+  const size_t r = (size_t)b * T + t;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) qs[i] = q[(r * n_q + h) * d + i];
+  __syncthreads();
+  const float scale = 1.0f / sqrtf((float)d);
+  for (int m = threadIdx.x; m < n; m += blockDim.x) {
+    const float* kr = k + (((size_t)b * T + m) * n_kv + g) * d;
+    float s = 0.f;
+    for (int i = 0; i < d; ++i) s = fmaf(qs[i], kr[i], s);
+    sc[m] = s * scale;
+  }
+  __syncthreads();
+  float mx = -INFINITY;
+  for (int m = threadIdx.x; m < n; m += blockDim.x) mx = fmaxf(mx, sc[m]);
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = -INFINITY;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
+  __syncthreads();
+  for (int m = threadIdx.x; m < n; m += blockDim.x) sc[m] = expf(sc[m] - mx);
+  __syncthreads();
+  float sum = 0.f;
+  for (int m = 0; m < n; ++m) sum += sc[m];
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float o = 0.f;
+    for (int m = 0; m < n; ++m) o = fmaf(sc[m], v[(((size_t)b * T + m) * n_kv + g) * d + i], o);
+    out[(r * n_q + h) * d + i] = o / sum;
+  }
+}
+
+// ======================================================================== host side
+static void decode_plan(int B, int n_kv, int max_keys, int sm_count, int& splits, int& kps) {
+  const int slots = std::max(1, sm_count) * 2;
+  const int pairs = std::max(1, B * n_kv);
+  int s = 1;
+  while (pairs * s < 2 * slots && s < 16 && (max_keys + 2 * s - 1) / (2 * s) >= 256) s *= 2;
+  kps = (max_keys + s - 1) / s;
+  kps = std::min(kps, 2048);
+  kps = std::max(DTILE, (kps + DTILE - 1) / DTILE * DTILE);
+  splits = (max_keys + kps - 1) / kps;
+}
+
+size_t attn_decode_partial_bytes(int B, int n_q, int head_dim, int max_keys, int sm_count,
+                                 int n_kv) {
+  int splits, kps;
+  decode_plan(B, n_kv, max_keys, sm_count, splits, kps);
+  if (splits <= 1) return 0;
+  return (size_t)B * n_q * splits * (head_dim + 2) * sizeof(float);
+}
+
+cudaError_t attn_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEC_SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)PRE_SMEM);
+}
+
+cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t st) {
+  int splits, kps;
+  decode_plan(a.B, a.n_kv, a.max_keys, a.sm_count, splits, kps);
+  if (dtype == LLAMA_F32) {
+    const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
+    const size_t sm = (size_t)(a.head_dim + cap_keys + 32) * sizeof(float);
+    if (sm > 200 * 1024) return cudaErrorInvalidValue;
+    if (sm > 48 * 1024)
+      cudaFuncSetAttribute(attn_decode_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sm);
+    attn_decode_f32_kernel<<<dim3(a.n_q, a.B), 128, sm, st>>>(
+        (const float*)a.q, a.positions, (const float*)a.k_cache, (const float*)a.v_cache,
+        a.page_table, (float*)a.out, a.n_q, a.n_kv, a.head_dim, a.layer, a.page_size, a.capacity,
+        a.batch_cap, a.n_pages, a.max_pages, a.status);
+    return cudaGetLastError();
+  }
+  if (a.head_dim != AD) return cudaErrorInvalidValue;
+  if (splits > 1 && (size_t)a.B * a.n_q * splits * (AD + 2) * sizeof(float) > a.partial_bytes) {
+    // workspace sized for fewer splits: one split per sequence
+    splits = 1;
+    kps = std::max(DTILE, (a.max_keys + DTILE - 1) / DTILE * DTILE);
+  }
+  DecParams p;
+  p.q = (const bf16*)a.q;
+  p.positions = a.positions;
+  p.page_table = a.page_table;
+  p.out = (bf16*)a.out;
+  p.part = a.partial;
+  p.status = a.status;
+  p.n_q = a.n_q;
+  p.n_kv = a.n_kv;
+  p.G = a.n_q / a.n_kv;
+  p.layer = a.layer;
+  p.page_size = a.page_size;
+  p.capacity = a.capacity;
+  p.batch_cap = a.batch_cap;
+  p.n_pages = a.n_pages;
+  p.max_pages = a.max_pages;
+  p.splits = splits;
+  p.keys_per_split = kps;
+  p.scale_log2 = kLog2e / sqrtf((float)AD);
+  attn_decode_kernel<<<dim3(splits, a.n_kv, a.B), DEC_THREADS, DEC_SMEM, st>>>(*a.map_k,
+                                                                             *a.map_v, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
+  attn_combine_kernel<<<a.B * a.n_q, AD, 0, st>>>(a.partial, a.positions, a.n_q, splits, kps,
+                                                  cap_keys, AD, a.out, 0);
+  return cudaGetLastError();
+}
+
+int attn_decode_launches(int B, int n_kv, int max_keys, int sm_count, int dtype) {
+  if (dtype == LLAMA_F32) return 1;
+  int splits, kps;
+  decode_plan(B, n_kv, max_keys, sm_count, splits, kps);
+  return splits > 1 ? 2 : 1;
+}
+
+cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_t st) {
+  if (dtype == LLAMA_F32) {
+    const size_t sm = (size_t)(a.head_dim + a.T + 32) * sizeof(float);
+    if (sm > 200 * 1024) return cudaErrorInvalidValue;
+    if (sm > 48 * 1024)
+      cudaFuncSetAttribute(attn_prefill_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sm);
+    attn_prefill_f32_kernel<<<dim3(a.T, a.n_q, a.B), 128, sm, st>>>(
+        (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)a.out, a.T, a.n_q,
+        a.n_kv, a.head_dim);
+    return cudaGetLastError();
+  }
+  if (a.head_dim != AD) return cudaErrorInvalidValue;
+  PreParams p;
+  p.out = (bf16*)a.out;
+  p.status = a.status;
+  p.T = a.T;
+  p.n_q = a.n_q;
+  p.n_kv = a.n_kv;
+  p.G = a.n_q / a.n_kv;
+  p.n_qtiles = (a.T + PQ - 1) / PQ;
+  p.scale_log2 = kLog2e / sqrtf((float)AD);
+  attn_prefill_kernel<<<dim3(p.n_qtiles, a.n_q, a.B), PRE_THREADS, PRE_SMEM, st>>>(
+      *a.map_q, *a.map_k, *a.map_v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace llgb

@@ -1,0 +1,250 @@
+// Row-wise kernels of the decoder forward: embedding gather, RMSNorm, the
+// RoPE table, RoPE + KV-cache append, and the greedy argmax.
+//
+// "Llama2架构与推理全解析": §2.3 (embedding lookup, residual stream),
+// §1.2 (RMSNorm), §1.4 (RoPE), §2.4 (KV cache append), §2.5 (greedy choice).
+#include "common.cuh"
+#include "internal.h"
+
+namespace llgb {
+
+// ------------------------------------------------------------------ embedding
+// out[r, :] = (fp32) table[tokens[r], :]. A token id outside [0, V) sets
+// LLAMA_FLAG_TOKEN_RANGE and yields a zero row.
+template <typename T>
+__global__ void embed_kernel(const int32_t* __restrict__ tokens, const T* __restrict__ table,
+                             int V, int H, float* __restrict__ out, uint32_t* status) {
+  const int r = blockIdx.x;
+  const int tok = tokens[r];
+  const bool ok = tok >= 0 && tok < V;
+  if (!ok && threadIdx.x == 0) flag(status, LLAMA_FLAG_TOKEN_RANGE);
+  const T* src = table + (size_t)(ok ? tok : 0) * H;
+  float* dst = out + (size_t)r * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) dst[i] = ok ? to_f32(src[i]) : 0.f;
+}
+
+// ------------------------------------------------------------------ RMSNorm
+// One CTA per row: y = x / sqrt(mean(x^2) + eps) * gamma; statistics in fp32.
+// Input row r is x + (r * in_stride + in_offset) * H.
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, int in_stride,
+                                                      int in_offset, const T* __restrict__ gamma,
+                                                      int H, float eps, T* __restrict__ out) {
+  __shared__ float red[8];
+  const int r = blockIdx.x;
+  const float* xr = x + ((size_t)r * in_stride + in_offset) * H;
+  T* yr = out + (size_t)r * H;
+  float ss = 0.f;
+  const bool vec = (H % 4) == 0;
+  if (vec) {
+    const float4* x4 = reinterpret_cast<const float4*>(xr);
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
+      float4 v = x4[i];
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+  } else {
+    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
+  }
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = 1.0f / sqrtf(red[0] / (float)H + eps);
+  if (vec) {
+    const float4* x4 = reinterpret_cast<const float4*>(xr);
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
+      float4 v = x4[i];
+      const int c = i * 4;
+      float g0 = to_f32(gamma[c]), g1 = to_f32(gamma[c + 1]), g2 = to_f32(gamma[c + 2]),
+            g3 = to_f32(gamma[c + 3]);
+      yr[c] = from_f32<T>(v.x * inv * g0);
+      yr[c + 1] = from_f32<T>(v.y * inv * g1);
+      yr[c + 2] = from_f32<T>(v.z * inv * g2);
+      yr[c + 3] = from_f32<T>(v.w * inv * g3);
+    }
+  } else {
+    for (int i = threadIdx.x; i < H; i += blockDim.x)
+      yr[i] = from_f32<T>(xr[i] * inv * to_f32(gamma[i]));
+  }
+}
+
+// ------------------------------------------------------------------ RoPE table
+// tab[m * (d/2) + j] = (cos(m * theta_j), sin(m * theta_j)), theta_j =
+// base^(-2j/d), evaluated in fp64 and rounded once to fp32.
+__global__ void rope_table_kernel(float2* __restrict__ tab, int max_seq, int half, double base) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)max_seq * half) return;
+  const int m = (int)(i / half), j = (int)(i % half);
+  const double inv = pow(base, -2.0 * (double)j / (double)(2 * half));
+  double s, c;
+  sincos((double)m * inv, &s, &c);
+  tab[i] = make_float2((float)c, (float)s);
+}
+
+// ------------------------------------------------------------------ RoPE + KV append
+// Row r of qkv (fp32, Q heads | K heads | V heads) belongs to sequence
+// r / rows_per_seq at position positions[r] (or r % rows_per_seq when
+// positions is null). Each thread takes 8 consecutive values (two 128-bit
+// loads), rotates adjacent pairs of Q and K by their position's angles, and
+// writes Q to q_out and K, V into the cache slot (and to k_out / v_out when
+// given). Positions outside the cache, or page ids outside the pool, set a
+// status flag and skip the cache write.
+template <typename T>
+__global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
+  const int r = blockIdx.y;
+  const int b = r / a.rows_per_seq;
+  const int pos = a.positions ? a.positions[r] : (r % a.rows_per_seq);
+  const int d = a.head_dim;
+  const int qw = a.n_q * d, kw = a.n_kv * d;
+  const int width = qw + 2 * kw;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c = i * 8;
+  if (c >= width) return;
+  const float* src = a.qkv + (size_t)r * width + c;
+  float v[8];
+  {
+    float4 lo = *reinterpret_cast<const float4*>(src);
+    float4 hi = *reinterpret_cast<const float4*>(src + 4);
+    v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+    v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+  }
+  const bool is_v = c >= qw + kw;
+  const bool pos_ok = pos >= 0 && pos < a.max_seq;
+  if (!pos_ok && c == 0) flag(a.status, LLAMA_FLAG_POS_RANGE);
+  if (!is_v) {
+    const int dd = (c < qw ? c : c - qw) % d;
+    const float2* tab = a.rope + (size_t)(pos_ok ? pos : 0) * (d / 2) + dd / 2;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 cs = tab[p];
+      const float x0 = v[2 * p], x1 = v[2 * p + 1];
+      v[2 * p] = x0 * cs.x - x1 * cs.y;
+      v[2 * p + 1] = x0 * cs.y + x1 * cs.x;
+    }
+  }
+  T o[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) o[k] = from_f32<T>(v[k]);
+  if (c < qw) {
+    T* dst = reinterpret_cast<T*>(a.q_out) + (size_t)r * qw + c;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = o[k];
+    return;
+  }
+  const int ck = is_v ? c - qw - kw : c - qw;  // column within the K (or V) block
+  const int g = ck / d, dd = ck % d;
+  T* side = reinterpret_cast<T*>(is_v ? a.v_out : a.k_out);
+  if (side) {
+    T* dst = side + (size_t)r * kw + ck;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = o[k];
+  }
+  // cache slot
+  size_t slot;
+  if (a.page_size == 0) {
+    if (!pos_ok || pos >= a.capacity) {
+      if (dd == 0) flag(a.status, LLAMA_FLAG_POS_RANGE);
+      return;
+    }
+    slot = (((size_t)a.layer * a.batch_cap + b) * a.n_kv + g) * a.capacity + pos;
+  } else {
+    const int pi = pos_ok ? pos / a.page_size : -1;
+    if (pi < 0 || pi >= a.max_pages) {
+      if (dd == 0) flag(a.status, LLAMA_FLAG_POS_RANGE);
+      return;
+    }
+    const int page = a.page_table[(size_t)b * a.max_pages + pi];
+    if (page < 0 || page >= a.n_pages) {
+      if (dd == 0) flag(a.status, LLAMA_FLAG_PAGE_RANGE);
+      return;
+    }
+    slot = (((size_t)a.layer * a.n_pages + page) * a.n_kv + g) * a.page_size + pos % a.page_size;
+  }
+  T* cache = reinterpret_cast<T*>(is_v ? a.v_cache : a.k_cache) + slot * d + dd;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) cache[k] = o[k];
+}
+
+// ------------------------------------------------------------------ greedy argmax
+// ids[b] = index of the largest logit of row b; ties go to the lowest index.
+__global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ logits, int V,
+                                                      int32_t* __restrict__ ids) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const float* row = logits + (size_t)blockIdx.x * V;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float x = row[i];
+    if (x > best || (x == best && i < bi)) { best = x; bi = i; }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+  }
+  if ((threadIdx.x & 31) == 0) { sv[threadIdx.x >> 5] = best; si[threadIdx.x >> 5] = bi; }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int nw = blockDim.x >> 5;
+    best = threadIdx.x < nw ? sv[threadIdx.x] : -INFINITY;
+    bi = threadIdx.x < nw ? si[threadIdx.x] : 0x7fffffff;
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+    }
+    if (threadIdx.x == 0) ids[blockIdx.x] = bi == 0x7fffffff ? 0 : bi;
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_embed(int dtype, const int32_t* tokens, const void* table, int V, int H, int n,
+                         float* out, uint32_t* status, cudaStream_t st) {
+  if (dtype == LLAMA_BF16)
+    embed_kernel<bf16><<<n, 256, 0, st>>>(tokens, (const bf16*)table, V, H, out, status);
+  else
+    embed_kernel<float><<<n, 256, 0, st>>>(tokens, (const float*)table, V, H, out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(int dtype, const float* x, int rows, int in_stride, int in_offset,
+                           const void* gamma, int H, float eps, void* out, cudaStream_t st) {
+  if (dtype == LLAMA_BF16)
+    rmsnorm_kernel<bf16><<<rows, 256, 0, st>>>(x, in_stride, in_offset, (const bf16*)gamma, H,
+                                               eps, (bf16*)out);
+  else
+    rmsnorm_kernel<float><<<rows, 256, 0, st>>>(x, in_stride, in_offset, (const float*)gamma, H,
+                                                eps, (float*)out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double theta,
+                              cudaStream_t st) {
+  const long long n = (long long)max_seq * (head_dim / 2);
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(tab, max_seq, head_dim / 2,
+                                                                   theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_append(int dtype, const RopeAppendArgs& a, int rows, cudaStream_t st) {
+  const int width = (a.n_q + 2 * a.n_kv) * a.head_dim;
+  dim3 grid((width / 8 + 255) / 256, rows);
+  if (dtype == LLAMA_BF16)
+    rope_append_kernel<bf16><<<grid, 256, 0, st>>>(a);
+  else
+    rope_append_kernel<float><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st) {
+  argmax_kernel<<<B, 1024, 0, st>>>(logits, V, ids);
+  return cudaGetLastError();
+}
+
+}  // namespace llgb

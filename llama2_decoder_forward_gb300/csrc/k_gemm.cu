@@ -1,0 +1,398 @@
+// Linear layers y = x W^T of the decoder forward with fused epilogues.
+//
+// Every projection of the layer ("Llama2架构与推理全解析" §2.3: Q/K/V, output
+// projection; §1.3: SwiGLU gate/up and down; the LM head) is one GEMM whose
+// A operand is the weight matrix W [M, K] and whose B operand is the
+// activation block x [N, K] (both K-major). The accumulator tile is 128
+// weight rows x n_tile activation rows in tensor memory, so a decode step with
+// 8..64 sequences still fills the 128-row MMA, and the epilogue thread that
+// owns weight row m writes output column m for every activation row: stores
+// are coalesced along m.
+//
+// bf16 path (tcgen05, sm_103a): one CTA per (n tile, m tile, k split);
+// warp 0 issues TMA loads (128-byte swizzle) into a ring of shared-memory
+// stages, warp 1 owns the tensor memory and issues tcgen05.mma (M=128,
+// N=n_tile, K=16) per stage, warps 2..5 read the accumulator with tcgen05.ld
+// and apply the epilogue. SwiGLU runs two MMAs per K step (gate rows and up
+// rows of the same 128 features) into two accumulators, so silu(g)*u is
+// formed in registers. When the grid would leave SMs idle (decode), K is
+// split: each split writes an fp32 partial, the last CTA of a tile to arrive
+// sums the partials in split order (deterministic) and applies the epilogue.
+//
+// fp32 path: plain CUDA-core FMAs in fp32 (no TF32), one thread per output.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace llgb {
+
+constexpr int BM = 128;  // weight rows per tile (MMA M)
+constexpr int BK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int GEMM_THREADS = 192;
+constexpr int kMaxDynSmem = 232448;  // 227 KB per CTA
+
+struct TcParams {
+  int M, N, K;
+  int n_tile, num_kb, splits, n_tiles;
+  int stages;
+  uint32_t tmem_cols;
+  void* out;
+  int ldo;
+  float* partial;
+  int* counters;
+  uint32_t* status;
+};
+
+template <int EPI, typename T>
+__device__ __forceinline__ void epi_apply(void* out, size_t idx, float g, float u) {
+  if (EPI == LLAMA_EPI_STORE_F32) {
+    reinterpret_cast<float*>(out)[idx] = g;
+  } else if (EPI == LLAMA_EPI_RESID_F32) {
+    reinterpret_cast<float*>(out)[idx] += g;
+  } else if (EPI == LLAMA_EPI_STORE_T) {
+    reinterpret_cast<T*>(out)[idx] = from_f32<T>(g);
+  } else {  // SWIGLU: silu(g) * u, silu(z) = z * sigmoid(z)
+    const float s = g / (1.0f + expf(-g));
+    reinterpret_cast<T*>(out)[idx] = from_f32<T>(s * u);
+  }
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
+                   const __grid_constant__ CUtensorMap tmX, TcParams p) {
+  constexpr bool DUAL = EPI == LLAMA_EPI_SWIGLU;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t a_bytes = BM * BK * 2;
+  const uint32_t b_bytes = (uint32_t)p.n_tile * BK * 2;
+  const uint32_t stage_bytes = a_bytes * (DUAL ? 2 : 1) + b_bytes;
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
+  // ctl[0]: TMEM base address, ctl[1]: abort, ctl[2]: this CTA reduces the tile
+  volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(accf + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
+  const int kb0 = (int)(((long long)split * p.num_kb) / p.splits);
+  const int kb1 = (int)(((long long)(split + 1) * p.num_kb) / p.splits);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accf, 1);
+    ctl[1] = 0;
+    ctl[2] = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    if (DUAL) tma_prefetch_desc(&tmU);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc(const_cast<uint32_t*>(ctl), p.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl[0];
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------- TMA producer
+      const uint64_t pol_w = l2_policy_evict_first();  // weights are streamed once
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[s], ph ^ 1, p.status)) {
+          ok = false;
+          ctl[1] = 1;
+          break;
+        }
+        uint8_t* st = smem + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        tma_load_2d_hint(st, &tmW, &full[s], kb * BK, tile_m * BM, pol_w);
+        if (DUAL) tma_load_2d_hint(st + a_bytes, &tmU, &full[s], kb * BK, tile_m * BM, pol_w);
+        tma_load_2d(st + a_bytes * (DUAL ? 2 : 1), &tmX, &full[s], kb * BK, tile_n * p.n_tile);
+        ++issued;
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      if (!ok) {  // let the copies already in flight land before the CTA exits
+        for (int i = 0; i < issued && i < S; ++i) {
+          if (--s < 0) {
+            s = S - 1;
+            ph ^= 1;
+          }
+          mbar_wait(&full[s], ph, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------- MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(BM, p.n_tile);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (ctl[1] || !mbar_wait(&full[s], ph, p.status)) {
+          ctl[1] = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(smem + (size_t)s * stage_bytes);
+        const uint64_t da = smem_desc_sw128(a0);
+        const uint64_t du = smem_desc_sw128(a0 + a_bytes);
+        const uint64_t db = smem_desc_sw128(a0 + a_bytes * (DUAL ? 2 : 1));
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {  // advance 32 bytes (16 bf16) along K
+          const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+          tc_mma_f16(tmem, da + 2 * k, db + 2 * k, idesc, acc);
+          if (DUAL) tc_mma_f16(tmem + p.n_tile, du + 2 * k, db + 2 * k, idesc, acc);
+        }
+        tc_commit(&empty[s]);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      tc_commit(accf);
+      mbar_wait(accf, 0, p.status);  // every MMA retired before teardown
+    }
+  } else {  // ---------------- epilogue warps 2..5
+    const bool ok = mbar_wait(accf, 0, p.status);
+    tc_fence_after();
+    if (ok && !ctl[1]) {
+      const int q = warp & 3;  // TMEM lane quadrant this warp may read
+      const int r = q * 32 + lane;
+      const int gm = tile_m * BM + r;
+      const int n0 = tile_n * p.n_tile;
+      const int nvalid = min(p.n_tile, p.N - n0);
+      const bool row_ok = gm < p.M;
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+      if (p.splits == 1) {
+        for (int c0 = 0; c0 < nvalid; c0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld16(tq + c0, g);
+          if (DUAL) tmem_ld16(tq + p.n_tile + c0, u);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < nvalid)
+                epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm,
+                                     __uint_as_float(g[j]), DUAL ? __uint_as_float(u[j]) : 0.f);
+          }
+        }
+      } else {
+        const int tile = tile_m * p.n_tiles + tile_n;
+        const int width = p.n_tile * (DUAL ? 2 : 1);
+        float* base = p.partial + (size_t)tile * p.splits * width * BM;
+        float* mine = base + (size_t)split * width * BM;
+        for (int c0 = 0; c0 < width; c0 += 16) {
+          uint32_t g[16];
+          tmem_ld16(tq + c0, g);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mine[(size_t)(c0 + j) * BM + r] = __uint_as_float(g[j]);
+        }
+        __threadfence();
+        epi_bar();
+        if (threadIdx.x == 64) {
+          const int old = atomicAdd(&p.counters[tile], 1);
+          ctl[2] = (old == p.splits - 1) ? 1u : 0u;
+        }
+        epi_bar();
+        if (ctl[2]) {  // last split of this tile: reduce in split order, then epilogue
+          __threadfence();
+          for (int c0 = 0; c0 < nvalid; c0 += 16) {
+            float gs[16], us[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) gs[j] = us[j] = 0.f;
+            for (int s2 = 0; s2 < p.splits; ++s2) {
+              const float* ps = base + (size_t)s2 * width * BM;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                gs[j] += __ldcg(ps + (size_t)(c0 + j) * BM + r);
+                if (DUAL) us[j] += __ldcg(ps + (size_t)(p.n_tile + c0 + j) * BM + r);
+              }
+            }
+            if (row_ok) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < nvalid)
+                  epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm, gs[j], us[j]);
+            }
+          }
+          if (threadIdx.x == 64) p.counters[tile] = 0;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------------ fp32 CUDA-core path
+template <int EPI>
+__global__ void gemm_f32_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                const float* __restrict__ wu, int M, int N, int K, void* out,
+                                int ldo) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n = blockIdx.y;
+  if (m >= M || n >= N) return;
+  const float* xr = x + (size_t)n * K;
+  const float* wr = w + (size_t)m * K;
+  float acc = 0.f, accu = 0.f;
+  if (EPI == LLAMA_EPI_SWIGLU) {
+    const float* ur = wu + (size_t)m * K;
+    for (int k = 0; k < K; ++k) {
+      acc = fmaf(xr[k], wr[k], acc);
+      accu = fmaf(xr[k], ur[k], accu);
+    }
+  } else {
+    for (int k = 0; k < K; ++k) acc = fmaf(xr[k], wr[k], acc);
+  }
+  epi_apply<EPI, float>(out, (size_t)n * ldo + m, acc, accu);
+}
+
+// ------------------------------------------------------------------ planning
+struct Plan {
+  int n_tile, stages, splits, m_tiles, n_tiles, num_kb, ctas_per_sm;
+  size_t smem;
+  uint32_t tmem_cols;
+};
+
+int gemm_n_tile(int N) { return N >= 256 ? 256 : std::max(16, (N + 15) / 16 * 16); }
+
+static Plan make_plan(int M, int N, int K, bool dual, int sm_count) {
+  Plan pl{};
+  pl.n_tile = gemm_n_tile(N);
+  const int stage_bytes = BM * BK * 2 * (dual ? 2 : 1) + pl.n_tile * BK * 2;
+  const int budget = pl.n_tile <= 64 ? 112 * 1024 : 224 * 1024;
+  pl.stages = std::max(2, std::min(8, (budget - 2048) / stage_bytes));
+  pl.smem = (size_t)pl.stages * stage_bytes + 1024 + 256;
+  pl.ctas_per_sm = std::max(1, std::min(2, (int)(233472 / (pl.smem + 1024))));
+  const int width = pl.n_tile * (dual ? 2 : 1);
+  pl.tmem_cols = 32;
+  while ((int)pl.tmem_cols < width) pl.tmem_cols <<= 1;
+  pl.m_tiles = (M + BM - 1) / BM;
+  pl.n_tiles = (N + pl.n_tile - 1) / pl.n_tile;
+  pl.num_kb = (K + BK - 1) / BK;
+  const int tiles = pl.m_tiles * pl.n_tiles;
+  const int slots = std::max(1, sm_count) * pl.ctas_per_sm;
+  // choose the split count that minimises (waves x k-blocks per CTA); only a
+  // single activation tile (decode) is split, a prefill grid has tiles enough
+  long best = -1;
+  pl.splits = 1;
+  const int max_split = pl.n_tiles == 1 ? std::min(32, pl.num_kb) : 1;
+  for (int s = 1; s <= max_split; ++s) {
+    const long ctas = (long)tiles * s;
+    const long waves = (ctas + slots - 1) / slots;
+    const long cost = waves * ((pl.num_kb + s - 1) / s) + (s > 1 ? 1 : 0);
+    if (best < 0 || cost < best) {
+      best = cost;
+      pl.splits = s;
+    }
+  }
+  return pl;
+}
+
+size_t gemm_partial_bytes(int M, int N, int K, int dual, int sm_count) {
+  const Plan pl = make_plan(M, N, K, dual != 0, sm_count);
+  if (pl.splits <= 1) return 0;
+  return (size_t)pl.m_tiles * pl.n_tiles * pl.splits * pl.n_tile * (dual ? 2 : 1) * BM *
+         sizeof(float);
+}
+
+template <int EPI>
+static cudaError_t set_attr() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kMaxDynSmem);
+}
+
+cudaError_t gemm_prepare() {
+  cudaError_t e;
+  if ((e = set_attr<LLAMA_EPI_STORE_F32>()) != cudaSuccess) return e;
+  if ((e = set_attr<LLAMA_EPI_RESID_F32>()) != cudaSuccess) return e;
+  if ((e = set_attr<LLAMA_EPI_STORE_T>()) != cudaSuccess) return e;
+  return set_attr<LLAMA_EPI_SWIGLU>();
+}
+
+template <int EPI>
+static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st) {
+  TcParams p;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.n_tile = pl.n_tile;
+  p.num_kb = pl.num_kb;
+  p.splits = pl.splits;
+  p.n_tiles = pl.n_tiles;
+  p.stages = pl.stages;
+  p.tmem_cols = pl.tmem_cols;
+  p.out = g.out;
+  p.ldo = g.ldo;
+  p.partial = g.partial;
+  p.counters = g.counters;
+  p.status = g.status;
+  dim3 grid(pl.n_tiles, pl.m_tiles, pl.splits);
+  const CUtensorMap* up = g.map_up ? g.map_up : g.map_w;
+  gemm_tc_kernel<EPI><<<grid, GEMM_THREADS, pl.smem, st>>>(*g.map_w, *up, *g.map_x, p);
+  return cudaGetLastError();
+}
+
+template <int EPI>
+static cudaError_t launch_f32(const GemmCall& g, cudaStream_t st) {
+  dim3 grid((g.M + 127) / 128, g.N);
+  gemm_f32_kernel<EPI><<<grid, 128, 0, st>>>((const float*)g.x, (const float*)g.w,
+                                             (const float*)g.w_up, g.M, g.N, g.K, g.out, g.ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st) {
+  if (g.dtype == LLAMA_F32) {
+    switch (g.epi) {
+      case LLAMA_EPI_STORE_F32: return launch_f32<LLAMA_EPI_STORE_F32>(g, st);
+      case LLAMA_EPI_RESID_F32: return launch_f32<LLAMA_EPI_RESID_F32>(g, st);
+      case LLAMA_EPI_STORE_T: return launch_f32<LLAMA_EPI_STORE_T>(g, st);
+      default: return launch_f32<LLAMA_EPI_SWIGLU>(g, st);
+    }
+  }
+  const bool dual = g.epi == LLAMA_EPI_SWIGLU;
+  Plan pl = make_plan(g.M, g.N, g.K, dual, g.sm_count);
+  if (pl.n_tile != g.n_tile) return cudaErrorInvalidValue;
+  if (pl.splits > 1) {
+    const size_t need = (size_t)pl.m_tiles * pl.n_tiles * pl.splits * pl.n_tile * (dual ? 2 : 1) *
+                        BM * sizeof(float);
+    if (need > g.partial_bytes || pl.m_tiles * pl.n_tiles > g.n_counters) {
+      // not enough workspace for this split: fall back to fewer splits
+      while (pl.splits > 1) {
+        --pl.splits;
+        const size_t n2 = (size_t)pl.m_tiles * pl.n_tiles * pl.splits * pl.n_tile *
+                          (dual ? 2 : 1) * BM * sizeof(float);
+        if (pl.splits == 1 || (n2 <= g.partial_bytes && pl.m_tiles * pl.n_tiles <= g.n_counters))
+          break;
+      }
+    }
+  }
+  switch (g.epi) {
+    case LLAMA_EPI_STORE_F32: return launch_tc<LLAMA_EPI_STORE_F32>(g, pl, st);
+    case LLAMA_EPI_RESID_F32: return launch_tc<LLAMA_EPI_RESID_F32>(g, pl, st);
+    case LLAMA_EPI_STORE_T: return launch_tc<LLAMA_EPI_STORE_T>(g, pl, st);
+    default: return launch_tc<LLAMA_EPI_SWIGLU>(g, pl, st);
+  }
+}
+
+}  // namespace llgb

@@ -1,0 +1,82 @@
+"""The C ABI library builds, loads without a GPU and exports every entry point
+the header declares; host-side argument checks answer without touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from llama2_decoder_forward_gb300 import binding, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return binding.lib()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(llama_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 20
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert names == set(binding.exported_symbols())
+
+
+def test_strerror(lib):
+    assert lib.llama_strerror(0) == b"ok"
+    assert b"argument" in lib.llama_strerror(1)
+    assert lib.llama_strerror(999) == b"unknown status"
+
+
+def _cfg(**kw):
+    c = binding.make_config(synth.LLAMA2_7B, 32, 4096, 4096)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_workspace_bytes_and_config_checks(lib):
+    n = ctypes.c_size_t()
+    assert lib.llama_workspace_bytes(ctypes.byref(_cfg()), ctypes.byref(n)) == 0
+    assert n.value > 0 and n.value % 256 == 0
+    bad = [dict(n_kv_heads=5), dict(hidden=0), dict(dtype=7), dict(head_dim=64),  # bf16 wants d=128
+           dict(max_batch=0), dict(rms_eps=0.0), dict(hidden=4100)]
+    codes = [1, 1, 1, 2, 1, 1, 2]
+    for kw, code in zip(bad, codes):
+        assert lib.llama_workspace_bytes(ctypes.byref(_cfg(**kw)), ctypes.byref(n)) == code, kw
+    assert lib.llama_workspace_bytes(None, ctypes.byref(n)) == 1
+    tiny = binding.make_config(synth.TINY, 1, 16, 32)
+    assert lib.llama_workspace_bytes(ctypes.byref(tiny), ctypes.byref(n)) == 0
+
+
+def test_null_context_and_arguments_rejected(lib):
+    kv = binding.KV()
+    assert lib.llama_decode_step(None, None, None, 1, ctypes.byref(kv), None, None) == 1
+    assert lib.llama_prefill(None, None, 1, 1, ctypes.byref(kv), None, None) == 1
+    assert lib.llama_sync_status(None) == 1
+    assert lib.llama_free(None) == 1
+    assert lib.llama_launch_count(None) == 0
+    out = ctypes.c_void_p()
+    w = binding.Weights()
+    assert lib.llama_init(ctypes.byref(_cfg()), ctypes.byref(w), None, 0, None, ctypes.byref(out)) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.lib()
