@@ -1,0 +1,386 @@
+"""Benchmark: Llama2-7B decode step (32 layers, batch 32, 1024 cached positions).
+
+One step = one llama_decode_step: embedding, 32 x (RMSNorm, Q/K/V projection,
+RoPE + KV append, GQA flash-decode attention over 1025 keys, output
+projection + residual, RMSNorm, gate/up + SiLU*up, down + residual), final
+RMSNorm, LM head and greedy argmax, for 32 sequences. Weights are random
+N(0, 0.02) bf16 of the 7B architecture, the cache holds N(0, 1) bf16 values at
+positions 0..1023 of every layer, token ids are uniform; all synthetic.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload model|layer]
+  python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of
+the workload on its GPU (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Llama2-7B decode tokens/s (bs32, ctx1024); decode-step HBM GB/s vs peak"
+B, CTX, CAP = 32, 1024, 1040
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"attn_decode": "k_attention.cu", "gemm": "k_gemm.cu"}[kernel]
+    with open(os.path.join(ROOT, "llama2_decoder_forward_gb300", "csrc", src), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == B_WORKLOAD:
+            return float(parts[3]) if parts[2] == h else None
+    return None
+
+
+B_WORKLOAD = "model"
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p:
+            self.p.terminate()
+            try:
+                self.out = self.p.communicate(timeout=5)[0]
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def build_model(workload, device):
+    import torch
+    from llama2_decoder_forward_gb300 import binding, synth
+
+    shape = synth.LLAMA2_7B if workload == "model" else synth.LLAMA2_7B.with_(n_layers=1)
+    seed = 1003
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+
+    def rn(*s, std=0.02, mean=0.0):
+        t = torch.randn(*s, generator=g, device=device, dtype=torch.float32)
+        t.mul_(std).add_(mean)
+        return t.to(torch.bfloat16)
+
+    H, I, V = shape.hidden, shape.intermediate, shape.vocab
+    layers = []
+    for _ in range(shape.n_layers):
+        layers.append({"attn_norm": rn(H, std=0.1, mean=1.0), "wqkv": rn(shape.qkv_rows, H),
+                       "wo": rn(H, H), "ffn_norm": rn(H, std=0.1, mean=1.0), "w_gate": rn(I, H),
+                       "w_up": rn(I, H), "w_down": rn(H, I)})
+    w = {"layers": layers}
+    if workload == "model":
+        w.update(embed=rn(V, H), final_norm=rn(H, std=0.1, mean=1.0), lm_head=rn(V, H))
+    kv = binding.KVCache(shape, batch=B, capacity=CAP)
+    for t in (kv.k, kv.v):
+        t.view(-1, CAP, shape.head_dim)[:, :CTX].normal_(generator=g)
+        t.view(-1, CAP, shape.head_dim)[:, CTX:].zero_()
+    model = binding.Model(shape, w, max_batch=B, max_tokens=B, max_seq=CAP,
+                          has_embed_head=(workload == "model"))
+    return shape, model, kv
+
+
+def run_gpu(args):
+    import torch
+    from llama2_decoder_forward_gb300 import binding
+    import __graft_entry__
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    __graft_entry__.build()
+    shape, model, kv = build_model(args.workload, dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    tokens = torch.randint(0, shape.vocab, (B,), generator=g, device=dev, dtype=torch.int32)
+    positions = torch.full((B,), CTX, dtype=torch.int32, device=dev)
+    logits = torch.empty(B, shape.vocab, device=dev)
+    ids = torch.empty(B, dtype=torch.int32, device=dev)
+    hidden0 = torch.randn(B, shape.hidden, generator=g, device=dev)
+    hidden = hidden0.clone()
+
+    def step():
+        if args.workload == "model":
+            model.decode_step(tokens, positions, kv, logits, ids)
+        else:
+            hidden.copy_(hidden0)
+            model.decode_hidden(hidden, positions, kv)
+
+    for _ in range(args.warmup):
+        step()
+    model.sync()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dominant = "attn_decode"
+    model.profile([dominant, "gemm"])
+    barrier()
+    n0 = model.launch_count()
+    with Clocks(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    launches = model.launch_count() - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    attn_ms, attn_n = model.profile_read(dominant)
+    gemm_ms, gemm_n = model.profile_read("gemm")
+    model.profile([])
+    model.sync()
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the host-buffer entry point (copies inside the timed region)
+    e2e = None
+    if args.workload == "model":
+        th = tokens.cpu().pin_memory()
+        ph = positions.cpu().pin_memory()
+        lh = torch.empty(B, shape.vocab).pin_memory()
+        ih = torch.empty(B, dtype=torch.int32).pin_memory()
+        model.decode_step_host(th, ph, kv, lh, ih)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            model.decode_step_host(th, ph, kv, lh, ih)
+        el = time.perf_counter() - t0
+        e2e = {"value": B * ws * args.steps / el, "unit": "tokens/s",
+               "h2d_bytes_per_step": 2 * B * 4, "d2h_bytes_per_step": B * shape.vocab * 4 + B * 4}
+
+    if rank != 0:
+        return
+    hbm, tflops, peak_kind = _peaks()
+    L = shape.n_layers
+    kv_bytes = B * shape.n_kv_heads * (CTX + 1) * shape.head_dim * 2 * 2  # K and V read per layer
+    attn_avg = attn_ms / max(attn_n, 1)
+    achieved = kv_bytes / (attn_avg * 1e-3) / 1e9
+    wbytes = (shape.qkv_rows + shape.hidden) * shape.hidden * 2 + 3 * shape.hidden * shape.intermediate * 2
+    lm_bytes = shape.vocab * shape.hidden * 2 if args.workload == "model" else 0
+    step_bytes = L * (wbytes + kv_bytes) + lm_bytes
+    line = {
+        "metric": METRIC,
+        "value": B * ws / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (random-init 7B weights N(0,0.02), cache N(0,1), uniform token ids)",
+        "config": {"workload": ("llama2-7b decode step: 32 layers + embedding + LM head + greedy, "
+                                "batch 32, 1024 cached positions, contiguous KV")
+                   if args.workload == "model" else
+                   "one llama2-7b decoder layer, decode step, batch 32, 1024 cached positions",
+                   "batch": B, "context": CTX, "l2": "inputs larger than L2 (%.1f GB per step)" % (step_bytes / 1e9),
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
+        "step_hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm,
+        "roofline": {"kernel": "attn_decode (flash-decode over the KV cache)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": peak_kind, "traffic": _traffic("attn_decode"),
+                     "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": attn_avg,
+                     "launches": attn_n},
+        "kernels": {"attn_decode_ms_per_step": attn_ms / args.steps,
+                    "gemm_ms_per_step": gemm_ms / args.steps,
+                    "gemm_gbs": (L * wbytes + lm_bytes) / (gemm_ms / args.steps * 1e-3) / 1e9
+                    if gemm_ms > 0 else None},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+class OracleSample:
+    """The oracle on a bounded sample: one 7B layer's decode step for the 32
+    sequences over a 1024-position cache (plus the LM head and greedy choice
+    for the full model), scaled to the whole step by the layer count. Inputs
+    are drawn once; only the oracle's arithmetic is timed."""
+
+    def __init__(self, workload):
+        import numpy as np
+        import torch
+        from llama2_decoder_forward_gb300 import synth
+        from oracle import llama_oracle as O
+
+        self.O = O
+        self.shape = shape = synth.LLAMA2_7B.with_(n_layers=1)
+        self.workload = workload
+        self.lw = {k: O.as64(v) for k, v in synth.layer_weights(shape, 1003, 0).items()}
+        self.x = O.as64(synth.hidden_input(B, shape.hidden, 1003))
+        self.K = O.as64(synth.cache_values((B, shape.n_kv_heads, CTX + 1, shape.head_dim), 1003,
+                                           torch.bfloat16, stream=0))
+        self.V = O.as64(synth.cache_values((B, shape.n_kv_heads, CTX + 1, shape.head_dim), 1003,
+                                           torch.bfloat16, stream=1))
+        self.pos = np.full(B, CTX)
+        self.lm = None
+        if workload == "model":
+            g = torch.Generator().manual_seed(5)
+            self.lm = O.as64((torch.randn(shape.vocab, shape.hidden, generator=g) * 0.02).to(torch.bfloat16))
+            self.fn = O.as64(synth.layer_weights(shape, 1004, 0)["attn_norm"])
+        self.n_layers = 32 if workload == "model" else 1
+        self.desc = ("one 7B layer's decode step for 32 sequences over 1024 cached positions in fp64, "
+                     "scaled x%d layers%s" % (self.n_layers, " + the LM head and greedy choice"
+                                              if self.lm is not None else ""))
+
+    def step_seconds(self):
+        O = self.O
+        t0 = time.perf_counter()
+        h = O.layer_decode(self.x, self.lw, self.shape, self.K, self.V, self.pos)
+        t_layer = time.perf_counter() - t0
+        t_head = 0.0
+        if self.lm is not None:
+            t0 = time.perf_counter()
+            O.greedy(O.lm_head(h, self.fn, self.lm, self.shape.rms_eps))
+            t_head = time.perf_counter() - t0
+        return self.n_layers * t_layer + t_head
+
+
+def _cores():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+def cpu_baseline(workload):
+    o = OracleSample(workload)
+    sec = min(o.step_seconds() for _ in range(2))
+    return {"value": B / sec, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": o.desc + " (best of 2)"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    o = OracleSample(args.workload)
+    desc = o.desc
+    for _ in range(args.warmup):
+        o.step_seconds()
+    t0 = time.perf_counter()
+    total = 0.0
+    for _ in range(args.steps):
+        total += o.step_seconds()
+    ms = total / args.steps * 1e3
+    v = B / (ms * 1e-3)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama2-7b decode step, batch 32, 1024 cached positions (CPU oracle)",
+                       "batch": B, "context": CTX},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="model", choices=["model", "layer"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    global B_WORKLOAD
+    B_WORKLOAD = args.workload
+    if args.warmup < 3 and args.impl == "gb300":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

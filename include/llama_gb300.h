@@ -227,7 +227,8 @@ int llama_op_rmsnorm(llama_ctx* ctx, const float* x, int32_t rows, int32_t in_st
                      int32_t in_offset, const void* gamma, void* out);
 
 /* Linear layer y = x W^T (§1.3 notation x W) with a fused epilogue.
- *   x T [n_rows, K]; w T [M, K]; w_up T [M, K] (SWIGLU only).
+ *   x T [n_rows, K] (or the pair layout, LLAMA_EPI_SPLIT_X); w T [M, K];
+ *   w_up T [M, K] (SWIGLU only).
  *   epilogue LLAMA_EPI_STORE_F32 : out fp32 [n_rows, M] = x W^T
  *            LLAMA_EPI_RESID_F32 : out fp32 [n_rows, M] += x W^T (residual add)
  *            LLAMA_EPI_STORE_T   : out T [n_rows, M] = x W^T
@@ -237,6 +238,13 @@ int llama_op_rmsnorm(llama_ctx* ctx, const float* x, int32_t rows, int32_t in_st
 #define LLAMA_EPI_RESID_F32 1
 #define LLAMA_EPI_STORE_T 2
 #define LLAMA_EPI_SWIGLU 3
+/* OR-ed into epilogue (bf16, n_rows <= 128): x carries each row as a pair,
+ * rows [0, n_rows) = bf16(v) and rows [L, L + n_rows) = bf16(v - bf16(v)),
+ * L = n_rows rounded up to a multiple of 16, and the product uses both (about
+ * 16 significant bits of v). STORE_T and SWIGLU outputs are written the same
+ * way: rows [0, n_rows) and [L, L + n_rows) of out. The library's decode path
+ * carries every GEMM operand this way. */
+#define LLAMA_EPI_SPLIT_X 16
 int llama_op_linear(llama_ctx* ctx, const void* x, int32_t n_rows, const void* w,
                     const void* w_up, int32_t M, int32_t K, int32_t epilogue, void* out);
 

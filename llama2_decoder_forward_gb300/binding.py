@@ -17,6 +17,7 @@ c_void_p = ctypes.c_void_p
 
 F32, BF16 = 0, 1
 EPI_STORE_F32, EPI_RESID_F32, EPI_STORE_T, EPI_SWIGLU = 0, 1, 2, 3
+EPI_SPLIT_X = 16  # OR-ed flag: x (and bf16 outputs) in the hi/lo pair layout
 KERNELS = ("rmsnorm", "gemm", "rope_append", "attn_decode", "attn_prefill", "embed", "argmax")
 FLAG_TOKEN_RANGE, FLAG_POS_RANGE, FLAG_PAGE_RANGE, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OUT_OF_RANGE", 4: "CUDA",
@@ -187,6 +188,8 @@ class Model:
         nbytes = workspace_bytes(self.cfg)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         layers = weights["layers"]
+        if len(layers) != shape.n_layers:
+            raise ValueError("shape has %d layers, weights have %d" % (shape.n_layers, len(layers)))
         arr = (LayerWeights * len(layers))()
         for i, lw in enumerate(layers):
             arr[i] = LayerWeights(*[lw[n].data_ptr() for n in

@@ -22,6 +22,12 @@ namespace {
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 constexpr int kMaxCounters = 8192;
+// Up to this many activation rows, bf16 GEMM operands are carried as a pair
+// hi = bf16(v), lo = bf16(v - hi) stacked along N (rows [0,n) and [lo, lo+n),
+// lo = n rounded up to 16): the product keeps ~16 mantissa bits of v. The
+// extra MMA work is free in the bandwidth-bound decode regime.
+constexpr int kSplitMaxRows = 128;
+inline int round16(int v) { return (v + 15) / 16 * 16; }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
@@ -102,14 +108,16 @@ Layout make_layout(const llama_config* c, int sm_count) {
   L.counters = take(sizeof(int) * kMaxCounters);
   L.rope = take((size_t)c->max_seq * (d / 2) * sizeof(float) * 2);
   L.x = take((size_t)R * H * 4);
-  L.u = take((size_t)R * H * es);
+  // GEMM operands: room for the hi/lo pair layout of up to 128 rows (256 rows)
+  const size_t RA = std::max(R, 256);
+  L.u = take(RA * H * es);
   L.qkv = take((size_t)R * qkv_rows * 4);
   L.q = take((size_t)R * nq * d * es);
   L.kside = take((size_t)std::max(c->max_tokens, 1) * nkv * d * es);
   L.vside = take((size_t)std::max(c->max_tokens, 1) * nkv * d * es);
-  L.o = take((size_t)R * nq * d * es);
-  L.a = take((size_t)R * I * es);
-  L.u_last = take((size_t)c->max_batch * H * es);
+  L.o = take(RA * nq * d * es);
+  L.a = take(RA * I * es);
+  L.u_last = take((size_t)std::max(c->max_batch, 256) * H * es);
   L.logits = take((size_t)c->max_batch * std::max<size_t>(V, 1) * 4);
   L.ids = take((size_t)c->max_batch * 4);
   L.tok = take((size_t)c->max_batch * 4);
@@ -117,13 +125,17 @@ Layout make_layout(const llama_config* c, int sm_count) {
   size_t gp = 0;
   if (c->dtype == LLAMA_BF16) {
     const int Ns[2] = {c->max_batch, std::max(c->max_tokens, 1)};
-    for (int N : Ns) {
-      gp = std::max(gp, gemm_partial_bytes((int)qkv_rows, N, (int)H, 0, sm_count));
-      gp = std::max(gp, gemm_partial_bytes((int)H, N, (int)(nq * d), 0, sm_count));
-      gp = std::max(gp, gemm_partial_bytes((int)I, N, (int)H, 1, sm_count));
-      gp = std::max(gp, gemm_partial_bytes((int)H, N, (int)I, 0, sm_count));
-      if (V) gp = std::max(gp, gemm_partial_bytes((int)V, std::min(N, c->max_batch), (int)H, 0, sm_count));
-    }
+    for (int N : Ns)
+      for (int split = 0; split < 2; ++split) {
+        if (split && N > kSplitMaxRows) continue;
+        gp = std::max(gp, gemm_partial_bytes((int)qkv_rows, N, (int)H, 0, split, sm_count));
+        gp = std::max(gp, gemm_partial_bytes((int)H, N, (int)(nq * d), 0, split, sm_count));
+        gp = std::max(gp, gemm_partial_bytes((int)I, N, (int)H, 1, split, sm_count));
+        gp = std::max(gp, gemm_partial_bytes((int)H, N, (int)I, 0, split, sm_count));
+        if (V)
+          gp = std::max(gp, gemm_partial_bytes((int)V, std::min(N, c->max_batch), (int)H, 0, split,
+                                               sm_count));
+      }
   }
   L.gpart_bytes = gp;
   L.gpart = take(std::max<size_t>(gp, 16));
@@ -176,7 +188,6 @@ const CUtensorMap* map2d(llama_ctx* c, const void* ptr, uint64_t rows, uint64_t 
   Key2 k{ptr, 2, rows, cols, box_rows, 0, 0};
   auto it = c->maps.find(k);
   if (it != c->maps.end()) return &it->second;
-  if (c->maps.size() > 4096) c->maps.clear();
   CUtensorMap m;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
@@ -196,7 +207,6 @@ const CUtensorMap* map3d(llama_ctx* c, const void* ptr, uint64_t d0, uint64_t d1
   Key2 k{ptr, 3, d0, d1, d2, b1, b2};
   auto it = c->maps.find(k);
   if (it != c->maps.end()) return &it->second;
-  if (c->maps.size() > 4096) c->maps.clear();
   CUtensorMap m;
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
@@ -211,6 +221,12 @@ const CUtensorMap* map3d(llama_ctx* c, const void* ptr, uint64_t d0, uint64_t d1
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Keep the descriptor cache bounded (callers that keep passing new buffers);
+// the weight descriptors are rebuilt on demand after a trim.
+void trim_maps(llama_ctx* c) {
+  if (c->maps.size() > 4096) c->maps.clear();
+}
 
 // Bracket one kernel class with events when profiling is on.
 struct Prof {
@@ -258,16 +274,20 @@ int check_kv(const llama_ctx* c, const llama_kv* kv, int B) {
 
 // ---------------------------------------------------------------- single steps
 int do_rmsnorm(llama_ctx* c, const float* x, int rows, int stride, int offset, const void* gamma,
-               void* out) {
+               void* out, int lo_rows = 0) {
   Prof pf(c, LLAMA_KERNEL_RMSNORM);
   c->launches++;
   return cuda_rc(launch_rmsnorm(c->cfg.dtype, x, rows, stride, offset, gamma, c->cfg.hidden,
-                                c->cfg.rms_eps, out, c->stream));
+                                c->cfg.rms_eps, out, lo_rows, c->stream));
 }
 
+// split: x holds the hi/lo pair layout of its N rows; out_lo: bf16 outputs also
+// store their remainder out_lo elements further on.
 int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, const void* wu,
-            int M, void* out, int ldo) {
+            int M, void* out, int ldo, int split = 0, size_t out_lo = 0) {
   GemmCall g{};
+  g.split = split;
+  g.out_lo = out_lo;
   g.dtype = c->cfg.dtype;
   g.epi = epi;
   g.M = M;
@@ -286,10 +306,11 @@ int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, c
   g.sm_count = c->sm_count;
   if (c->cfg.dtype == LLAMA_BF16) {
     if (!aligned16(x) || !aligned16(w) || (wu && !aligned16(wu))) return LLAMA_ERR_INVALID_ARG;
-    g.n_tile = gemm_n_tile(N);
+    trim_maps(c);
+    g.n_tile = gemm_n_tile(N, split);
     g.map_w = map2d(c, w, M, K, 128);
     g.map_up = wu ? map2d(c, wu, M, K, 128) : nullptr;
-    g.map_x = map2d(c, x, N, K, g.n_tile);
+    g.map_x = map2d(c, x, split ? g.n_tile : N, K, g.n_tile);
     if (!g.map_w || !g.map_x || (wu && !g.map_up)) return LLAMA_ERR_CUDA;
   }
   Prof pf(c, LLAMA_KERNEL_GEMM);
@@ -328,8 +349,9 @@ int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
 }
 
 int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B, int layer,
-                   const llama_kv* kv, void* out) {
+                   const llama_kv* kv, void* out, size_t out_lo = 0) {
   AttnDecodeArgs a{};
+  a.out_lo = out_lo;
   a.q = q;
   a.positions = positions;
   a.k_cache = kv->k;
@@ -353,6 +375,7 @@ int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B,
   a.max_keys = std::max(1, std::min(cap_keys, c->cfg.max_seq));
   a.sm_count = c->sm_count;
   if (c->cfg.dtype == LLAMA_BF16) {
+    trim_maps(c);
     const uint64_t d = c->cfg.head_dim, nkv = c->cfg.n_kv_heads;
     const uint64_t rows = kv->page_size ? (uint64_t)kv->n_pages * nkv * kv->page_size
                                         : (uint64_t)kv->batch_capacity * nkv * kv->capacity;
@@ -366,8 +389,9 @@ int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B,
 }
 
 int do_attn_prefill(llama_ctx* c, const void* q, const void* k, const void* v, int B, int T,
-                    void* out) {
+                    void* out, size_t out_lo = 0) {
   AttnPrefillArgs a{};
+  a.out_lo = out_lo;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -380,6 +404,7 @@ int do_attn_prefill(llama_ctx* c, const void* q, const void* k, const void* v, i
   a.head_dim = c->cfg.head_dim;
   if (c->cfg.dtype == LLAMA_BF16) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return LLAMA_ERR_INVALID_ARG;
+    trim_maps(c);
     const uint64_t d = c->cfg.head_dim, rows = (uint64_t)B * T;
     a.map_q = map3d(c, q, d, c->cfg.n_q_heads, rows, 1, 64);
     a.map_k = map3d(c, k, d, c->cfg.n_kv_heads, rows, 1, 64);
@@ -410,21 +435,23 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   void* q = c->at<void>(c->L.q);
   void* o = c->at<void>(c->L.o);
   void* a = c->at<void>(c->L.a);
-  TRY(do_rmsnorm(c, x, rows, 1, 0, lw.attn_norm, u));
-  TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows));
+  const int lo = (cf.dtype == LLAMA_BF16 && rows <= kSplitMaxRows) ? round16(rows) : 0;
+  const int sp = lo ? 1 : 0;
+  TRY(do_rmsnorm(c, x, rows, 1, 0, lw.attn_norm, u, lo));
+  TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
   if (prefill) {
     void* ks = c->at<void>(c->L.kside);
     void* vs = c->at<void>(c->L.vside);
     TRY(do_rope_append(c, qkv, rows, T, nullptr, l, kv, q, ks, vs));
-    TRY(do_attn_prefill(c, q, ks, vs, B, T, o));
+    TRY(do_attn_prefill(c, q, ks, vs, B, T, o, (size_t)lo * nq * d));
   } else {
     TRY(do_rope_append(c, qkv, rows, 1, positions, l, kv, q, nullptr, nullptr));
-    TRY(do_attn_decode(c, q, positions, B, l, kv, o));
+    TRY(do_attn_decode(c, q, positions, B, l, kv, o, (size_t)lo * nq * d));
   }
-  TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H));
-  TRY(do_rmsnorm(c, x, rows, 1, 0, lw.ffn_norm, u));
-  TRY(do_gemm(c, LLAMA_EPI_SWIGLU, u, rows, H, lw.w_gate, lw.w_up, I, a, I));
-  TRY(do_gemm(c, LLAMA_EPI_RESID_F32, a, rows, I, lw.w_down, nullptr, H, x, H));
+  TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H, sp));
+  TRY(do_rmsnorm(c, x, rows, 1, 0, lw.ffn_norm, u, lo));
+  TRY(do_gemm(c, LLAMA_EPI_SWIGLU, u, rows, H, lw.w_gate, lw.w_up, I, a, I, sp, (size_t)lo * I));
+  TRY(do_gemm(c, LLAMA_EPI_RESID_F32, a, rows, I, lw.w_down, nullptr, H, x, H, sp));
   return LLAMA_OK;
 }
 
@@ -433,9 +460,10 @@ int run_head(llama_ctx* c, const float* x, int B, int stride, int offset, float*
              int32_t* next_ids) {
   const llama_config& cf = c->cfg;
   void* ul = c->at<void>(c->L.u_last);
-  TRY(do_rmsnorm(c, x, B, stride, offset, c->final_norm, ul));
+  const int lo = (cf.dtype == LLAMA_BF16 && B <= kSplitMaxRows) ? round16(B) : 0;
+  TRY(do_rmsnorm(c, x, B, stride, offset, c->final_norm, ul, lo));
   TRY(do_gemm(c, LLAMA_EPI_STORE_F32, ul, B, cf.hidden, c->lm_head, nullptr, cf.vocab, logits,
-              cf.vocab));
+              cf.vocab, lo ? 1 : 0));
   if (next_ids) {
     Prof pf(c, LLAMA_KERNEL_ARGMAX);
     c->launches++;
@@ -707,12 +735,16 @@ int llama_op_linear(llama_ctx* c, const void* x, int32_t n_rows, const void* w, 
                     int32_t M, int32_t K, int32_t epilogue, void* out) {
   TRY(check_ctx(c));
   if (!x || !w || !out || n_rows < 1 || M < 1 || K < 1) return LLAMA_ERR_INVALID_ARG;
+  const int split = (epilogue & LLAMA_EPI_SPLIT_X) ? 1 : 0;
+  epilogue &= ~LLAMA_EPI_SPLIT_X;
   if (epilogue < LLAMA_EPI_STORE_F32 || epilogue > LLAMA_EPI_SWIGLU) return LLAMA_ERR_INVALID_ARG;
   if (epilogue == LLAMA_EPI_SWIGLU && !w_up) return LLAMA_ERR_INVALID_ARG;
   if (c->cfg.dtype == LLAMA_BF16 && K % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (split && (c->cfg.dtype != LLAMA_BF16 || n_rows > kSplitMaxRows)) return LLAMA_ERR_UNSUPPORTED;
   if (n_rows > std::max(c->cfg.max_batch, c->cfg.max_tokens)) return LLAMA_ERR_OUT_OF_RANGE;
+  const bool t_out = epilogue == LLAMA_EPI_SWIGLU || epilogue == LLAMA_EPI_STORE_T;
   return do_gemm(c, epilogue, x, n_rows, K, w, epilogue == LLAMA_EPI_SWIGLU ? w_up : nullptr, M,
-                 out, M);
+                 out, M, split, (split && t_out) ? (size_t)round16(n_rows) * M : 0);
 }
 
 int llama_op_rope_append(llama_ctx* c, const float* qkv, int32_t rows, int32_t rows_per_seq,

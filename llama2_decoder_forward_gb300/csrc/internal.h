@@ -29,7 +29,8 @@ struct RopeAppendArgs {
 cudaError_t launch_embed(int dtype, const int32_t* tokens, const void* table, int V, int H, int n,
                          float* out, uint32_t* status, cudaStream_t st);
 cudaError_t launch_rmsnorm(int dtype, const float* x, int rows, int in_stride, int in_offset,
-                           const void* gamma, int H, float eps, void* out, cudaStream_t st);
+                           const void* gamma, int H, float eps, void* out, int lo_rows,
+                           cudaStream_t st);
 cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double theta,
                               cudaStream_t st);
 cudaError_t launch_rope_append(int dtype, const RopeAppendArgs& a, int rows, cudaStream_t st);
@@ -48,6 +49,9 @@ struct GemmCall {
   const CUtensorMap* map_up;  // bf16 path, SWIGLU
   const CUtensorMap* map_x;   // bf16 path: activations, box {64, n_tile}
   int n_tile;                 // bf16 path: MMA N (multiple of 16, <= 256); map_x box rows
+  int split;                  // bf16 path: x rows [0,N) hold bf16(v), rows [lo, lo+N) hold
+                              // bf16(v - bf16(v)), lo = round16(N); both are multiplied
+  size_t out_lo;              // bf16 outputs: also store the remainder out_lo elements on
   void* out;
   int ldo;
   float* partial;             // split-K partial sums (workspace)
@@ -57,10 +61,10 @@ struct GemmCall {
   uint32_t* status;
   int sm_count;
 };
-// Tile width the bf16 GEMM uses for N activation rows.
-int gemm_n_tile(int N);
+// Activation rows one bf16 GEMM tile reads (MMA N) for N logical rows.
+int gemm_n_tile(int N, int split);
 // Bytes of split-K partials a call may need (upper bound for the workspace).
-size_t gemm_partial_bytes(int M, int N, int K, int dual, int sm_count);
+size_t gemm_partial_bytes(int M, int N, int K, int dual, int split, int sm_count);
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st);
 cudaError_t gemm_prepare();  // sets kernel attributes once per process
 
@@ -74,6 +78,7 @@ struct AttnDecodeArgs {
   const void* v_cache;
   const int32_t* page_table;
   void* out;                 // [B, n_q d]
+  size_t out_lo;             // >0: also store bf16 remainders out_lo elements further
   float* partial;            // split partials (workspace)
   size_t partial_bytes;
   uint32_t* status;
@@ -96,6 +101,7 @@ struct AttnPrefillArgs {
   const CUtensorMap* map_k;
   const CUtensorMap* map_v;
   void* out;                 // [B*T, n_q d]
+  size_t out_lo;             // >0: also store bf16 remainders out_lo elements further
   uint32_t* status;
   int B, T, n_q, n_kv, head_dim;
 };

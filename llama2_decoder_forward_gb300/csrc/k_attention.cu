@@ -44,6 +44,7 @@ struct DecParams {
   const int32_t* positions;
   const int32_t* page_table;
   bf16* out;
+  size_t out_lo;
   float* part;
   uint32_t* status;
   int n_q, n_kv, G, layer;
@@ -302,7 +303,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     }
     const size_t bh = (size_t)b * p.n_q + (size_t)g * G + r;
     if (p.splits == 1) {
-      p.out[bh * AD + t] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+      const float v = L > 0.f ? O / L : 0.f;
+      const bf16 hi = __float2bfloat16_rn(v);
+      p.out[bh * AD + t] = hi;
+      if (p.out_lo) p.out[bh * AD + t + p.out_lo] = __float2bfloat16_rn(v - __bfloat162float(hi));
     } else {
       float* pp = p.part + (bh * p.splits + split) * (AD + 2);
       pp[t] = O;
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
 __global__ void attn_combine_kernel(const float* __restrict__ part,
                                     const int32_t* __restrict__ positions, int n_q, int splits,
                                     int keys_per_split, int cap_keys, int d, void* out,
-                                    int out_f32) {
+                                    size_t out_lo) {
   const int bh = blockIdx.x;
   const int b = bh / n_q;
   const int n_keys = decode_keys(positions[b], cap_keys);
@@ -338,10 +342,11 @@ __global__ void attn_combine_kernel(const float* __restrict__ part,
       }
     }
     const float v = L > 0.f ? O / L : 0.f;
-    if (out_f32)
-      reinterpret_cast<float*>(out)[(size_t)bh * d + t] = v;
-    else
-      reinterpret_cast<bf16*>(out)[(size_t)bh * d + t] = __float2bfloat16_rn(v);
+    const bf16 hi = __float2bfloat16_rn(v);
+    reinterpret_cast<bf16*>(out)[(size_t)bh * d + t] = hi;
+    if (out_lo)
+      reinterpret_cast<bf16*>(out)[(size_t)bh * d + t + out_lo] =
+          __float2bfloat16_rn(v - __bfloat162float(hi));
   }
 }
 
@@ -356,6 +361,7 @@ constexpr size_t PRE_SMEM = PTILE + PSTAGES * 2 * PTILE + 1024 + 256;
 
 struct PreParams {
   bf16* out;
+  size_t out_lo;
   uint32_t* status;
   int T, n_q, n_kv, G, n_qtiles;
   float scale_log2;
@@ -549,8 +555,14 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
 #pragma unroll
     for (int dn = 0; dn < 16; ++dn) {
       const int col = dn * 8 + 2 * (lane & 3);
-      *reinterpret_cast<uint32_t*>(dst + col) =
-          pack_bf16(oacc[dn][2 * hh] * inv, oacc[dn][2 * hh + 1] * inv);
+      const float v0 = oacc[dn][2 * hh] * inv, v1 = oacc[dn][2 * hh + 1] * inv;
+      const uint32_t hi = pack_bf16(v0, v1);
+      *reinterpret_cast<uint32_t*>(dst + col) = hi;
+      if (p.out_lo) {
+        const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&hi);
+        *reinterpret_cast<uint32_t*>(dst + col + p.out_lo) =
+            pack_bf16(v0 - __low2float(h2), v1 - __high2float(h2));
+      }
     }
   }
 }
@@ -710,6 +722,7 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.positions = a.positions;
   p.page_table = a.page_table;
   p.out = (bf16*)a.out;
+  p.out_lo = a.out_lo;
   p.part = a.partial;
   p.status = a.status;
   p.n_q = a.n_q;
@@ -730,7 +743,7 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   if (e != cudaSuccess || splits == 1) return e;
   const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
   attn_combine_kernel<<<a.B * a.n_q, AD, 0, st>>>(a.partial, a.positions, a.n_q, splits, kps,
-                                                  cap_keys, AD, a.out, 0);
+                                                  cap_keys, AD, a.out, a.out_lo);
   return cudaGetLastError();
 }
 
@@ -756,6 +769,7 @@ cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_
   if (a.head_dim != AD) return cudaErrorInvalidValue;
   PreParams p;
   p.out = (bf16*)a.out;
+  p.out_lo = a.out_lo;
   p.status = a.status;
   p.T = a.T;
   p.n_q = a.n_q;

@@ -25,11 +25,21 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, const T* __rest
 
 // ------------------------------------------------------------------ RMSNorm
 // One CTA per row: y = x / sqrt(mean(x^2) + eps) * gamma; statistics in fp32.
-// Input row r is x + (r * in_stride + in_offset) * H.
+// Input row r is x + (r * in_stride + in_offset) * H. With lo_rows > 0 the bf16
+// remainder y - bf16(y) is also written to row r + lo_rows (hi/lo operand pair).
+template <typename T>
+__device__ __forceinline__ void store_y(T* yr, size_t lo, int i, float v) {
+  const T hi = from_f32<T>(v);
+  yr[i] = hi;
+  if (lo) yr[lo + i] = from_f32<T>(v - to_f32(hi));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, int in_stride,
                                                       int in_offset, const T* __restrict__ gamma,
-                                                      int H, float eps, T* __restrict__ out) {
+                                                      int H, float eps, T* __restrict__ out,
+                                                      int lo_rows) {
+  const size_t lo = (size_t)lo_rows * H;
   __shared__ float red[8];
   const int r = blockIdx.x;
   const float* xr = x + ((size_t)r * in_stride + in_offset) * H;
@@ -62,14 +72,14 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
       const int c = i * 4;
       float g0 = to_f32(gamma[c]), g1 = to_f32(gamma[c + 1]), g2 = to_f32(gamma[c + 2]),
             g3 = to_f32(gamma[c + 3]);
-      yr[c] = from_f32<T>(v.x * inv * g0);
-      yr[c + 1] = from_f32<T>(v.y * inv * g1);
-      yr[c + 2] = from_f32<T>(v.z * inv * g2);
-      yr[c + 3] = from_f32<T>(v.w * inv * g3);
+      store_y(yr, lo, c, v.x * inv * g0);
+      store_y(yr, lo, c + 1, v.y * inv * g1);
+      store_y(yr, lo, c + 2, v.z * inv * g2);
+      store_y(yr, lo, c + 3, v.w * inv * g3);
     }
   } else {
     for (int i = threadIdx.x; i < H; i += blockDim.x)
-      yr[i] = from_f32<T>(xr[i] * inv * to_f32(gamma[i]));
+      store_y(yr, lo, i, xr[i] * inv * to_f32(gamma[i]));
   }
 }
 
@@ -214,13 +224,14 @@ cudaError_t launch_embed(int dtype, const int32_t* tokens, const void* table, in
 }
 
 cudaError_t launch_rmsnorm(int dtype, const float* x, int rows, int in_stride, int in_offset,
-                           const void* gamma, int H, float eps, void* out, cudaStream_t st) {
+                           const void* gamma, int H, float eps, void* out, int lo_rows,
+                           cudaStream_t st) {
   if (dtype == LLAMA_BF16)
     rmsnorm_kernel<bf16><<<rows, 256, 0, st>>>(x, in_stride, in_offset, (const bf16*)gamma, H,
-                                               eps, (bf16*)out);
+                                               eps, (bf16*)out, lo_rows);
   else
     rmsnorm_kernel<float><<<rows, 256, 0, st>>>(x, in_stride, in_offset, (const float*)gamma, H,
-                                                eps, (float*)out);
+                                                eps, (float*)out, 0);
   return cudaGetLastError();
 }
 

@@ -37,6 +37,9 @@ struct TcParams {
   int n_tile, num_kb, splits, n_tiles;
   int stages;
   uint32_t tmem_cols;
+  int lo;      // >0: activation rows [lo, lo + N) hold the bf16 remainders of rows [0, N)
+  int ncol;    // output columns one tile produces (n_tile, or lo in the hi/lo mode)
+  size_t out_lo;  // >0: bf16 outputs also write their remainder out_lo elements further
   void* out;
   int ldo;
   float* partial;
@@ -44,17 +47,21 @@ struct TcParams {
   uint32_t* status;
 };
 
+// Store one output element. For bf16 outputs with out_lo > 0 the value is
+// kept as a pair: hi = bf16(v) at idx and lo = bf16(v - hi) at idx + out_lo.
 template <int EPI, typename T>
-__device__ __forceinline__ void epi_apply(void* out, size_t idx, float g, float u) {
+__device__ __forceinline__ void epi_apply(void* out, size_t idx, float g, float u,
+                                          size_t out_lo = 0) {
   if (EPI == LLAMA_EPI_STORE_F32) {
     reinterpret_cast<float*>(out)[idx] = g;
   } else if (EPI == LLAMA_EPI_RESID_F32) {
     reinterpret_cast<float*>(out)[idx] += g;
-  } else if (EPI == LLAMA_EPI_STORE_T) {
-    reinterpret_cast<T*>(out)[idx] = from_f32<T>(g);
-  } else {  // SWIGLU: silu(g) * u, silu(z) = z * sigmoid(z)
-    const float s = g / (1.0f + expf(-g));
-    reinterpret_cast<T*>(out)[idx] = from_f32<T>(s * u);
+  } else {
+    // STORE_T: g; SWIGLU: silu(g) * u with silu(z) = z * sigmoid(z)
+    const float v = EPI == LLAMA_EPI_STORE_T ? g : g / (1.0f + expf(-g)) * u;
+    const T hi = from_f32<T>(v);
+    reinterpret_cast<T*>(out)[idx] = hi;
+    if (out_lo) reinterpret_cast<T*>(out)[idx + out_lo] = from_f32<T>(v - to_f32(hi));
   }
 }
 
@@ -172,35 +179,49 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int q = warp & 3;  // TMEM lane quadrant this warp may read
       const int r = q * 32 + lane;
       const int gm = tile_m * BM + r;
-      const int n0 = tile_n * p.n_tile;
-      const int nvalid = min(p.n_tile, p.N - n0);
+      const int n0 = tile_n * p.ncol;
+      const int nvalid = min(p.ncol, p.N - n0);
       const bool row_ok = gm < p.M;
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+      const int up = p.n_tile;  // first TMEM column of the up-projection accumulator
+      // 16 output columns starting at c0: sum the hi and lo halves when present
+      auto load16 = [&](int col, float (&v)[16]) {
+        uint32_t a[16], b[16];
+        tmem_ld16(tq + col, a);
+        if (p.lo) tmem_ld16(tq + col + p.lo, b);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j] = p.lo ? __uint_as_float(a[j]) + __uint_as_float(b[j]) : __uint_as_float(a[j]);
+      };
       if (p.splits == 1) {
         for (int c0 = 0; c0 < nvalid; c0 += 16) {
-          uint32_t g[16], u[16];
-          tmem_ld16(tq + c0, g);
-          if (DUAL) tmem_ld16(tq + p.n_tile + c0, u);
-          tmem_ld_wait();
+          float g[16], u[16];
+          load16(c0, g);
+          if (DUAL) load16(up + c0, u);
           if (row_ok) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (c0 + j < nvalid)
-                epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm,
-                                     __uint_as_float(g[j]), DUAL ? __uint_as_float(u[j]) : 0.f);
+                epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm, g[j],
+                                     DUAL ? u[j] : 0.f, p.out_lo);
           }
         }
       } else {
         const int tile = tile_m * p.n_tiles + tile_n;
-        const int width = p.n_tile * (DUAL ? 2 : 1);
+        const int width = p.ncol * (DUAL ? 2 : 1);
         float* base = p.partial + (size_t)tile * p.splits * width * BM;
         float* mine = base + (size_t)split * width * BM;
-        for (int c0 = 0; c0 < width; c0 += 16) {
-          uint32_t g[16];
-          tmem_ld16(tq + c0, g);
-          tmem_ld_wait();
+        for (int c0 = 0; c0 < p.ncol; c0 += 16) {
+          float g[16];
+          load16(c0, g);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) mine[(size_t)(c0 + j) * BM + r] = __uint_as_float(g[j]);
+          for (int j = 0; j < 16; ++j) mine[(size_t)(c0 + j) * BM + r] = g[j];
+          if (DUAL) {
+            load16(up + c0, g);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mine[(size_t)(p.ncol + c0 + j) * BM + r] = g[j];
+          }
         }
         __threadfence();
         epi_bar();
@@ -220,14 +241,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 gs[j] += __ldcg(ps + (size_t)(c0 + j) * BM + r);
-                if (DUAL) us[j] += __ldcg(ps + (size_t)(p.n_tile + c0 + j) * BM + r);
+                if (DUAL) us[j] += __ldcg(ps + (size_t)(p.ncol + c0 + j) * BM + r);
               }
             }
             if (row_ok) {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 if (c0 + j < nvalid)
-                  epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm, gs[j], us[j]);
+                  epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm, gs[j], us[j],
+                                       p.out_lo);
             }
           }
           if (threadIdx.x == 64) p.counters[tile] = 0;
@@ -269,26 +291,35 @@ __global__ void gemm_f32_kernel(const float* __restrict__ x, const float* __rest
 
 // ------------------------------------------------------------------ planning
 struct Plan {
-  int n_tile, stages, splits, m_tiles, n_tiles, num_kb, ctas_per_sm;
+  int n_tile, ncol, lo, stages, splits, m_tiles, n_tiles, num_kb, ctas_per_sm;
   size_t smem;
   uint32_t tmem_cols;
 };
 
-int gemm_n_tile(int N) { return N >= 256 ? 256 : std::max(16, (N + 15) / 16 * 16); }
+static int round16(int v) { return (v + 15) / 16 * 16; }
 
-static Plan make_plan(int M, int N, int K, bool dual, int sm_count) {
+int gemm_n_tile(int N, int split) {
+  if (split) return 2 * round16(N);
+  return N >= 256 ? 256 : std::max(16, round16(N));
+}
+
+static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count) {
   Plan pl{};
-  pl.n_tile = gemm_n_tile(N);
-  const int stage_bytes = BM * BK * 2 * (dual ? 2 : 1) + pl.n_tile * BK * 2;
-  const int budget = pl.n_tile <= 64 ? 112 * 1024 : 224 * 1024;
-  pl.stages = std::max(2, std::min(8, (budget - 2048) / stage_bytes));
-  pl.smem = (size_t)pl.stages * stage_bytes + 1024 + 256;
-  pl.ctas_per_sm = std::max(1, std::min(2, (int)(233472 / (pl.smem + 1024))));
-  const int width = pl.n_tile * (dual ? 2 : 1);
+  pl.n_tile = gemm_n_tile(N, split);
+  pl.lo = split ? pl.n_tile / 2 : 0;
+  pl.ncol = split ? pl.lo : pl.n_tile;
+  const int width = pl.n_tile * (dual ? 2 : 1);  // accumulator columns
   pl.tmem_cols = 32;
   while ((int)pl.tmem_cols < width) pl.tmem_cols <<= 1;
+  const int stage_bytes = BM * BK * 2 * (dual ? 2 : 1) + pl.n_tile * BK * 2;
+  // two CTAs per SM while the tile is narrow and both fit in tensor memory
+  const bool two = pl.n_tile <= 128 && pl.tmem_cols <= 256;
+  const int budget = two ? 112 * 1024 : 224 * 1024;
+  pl.stages = std::max(2, std::min(8, (budget - 2048) / stage_bytes));
+  pl.smem = (size_t)pl.stages * stage_bytes + 1024 + 256;
+  pl.ctas_per_sm = std::max(1, std::min(two ? 2 : 1, (int)(233472 / (pl.smem + 1024))));
   pl.m_tiles = (M + BM - 1) / BM;
-  pl.n_tiles = (N + pl.n_tile - 1) / pl.n_tile;
+  pl.n_tiles = split ? 1 : (N + pl.n_tile - 1) / pl.n_tile;
   pl.num_kb = (K + BK - 1) / BK;
   const int tiles = pl.m_tiles * pl.n_tiles;
   const int slots = std::max(1, sm_count) * pl.ctas_per_sm;
@@ -309,11 +340,14 @@ static Plan make_plan(int M, int N, int K, bool dual, int sm_count) {
   return pl;
 }
 
-size_t gemm_partial_bytes(int M, int N, int K, int dual, int sm_count) {
-  const Plan pl = make_plan(M, N, K, dual != 0, sm_count);
-  if (pl.splits <= 1) return 0;
-  return (size_t)pl.m_tiles * pl.n_tiles * pl.splits * pl.n_tile * (dual ? 2 : 1) * BM *
+static size_t partial_need(const Plan& pl, bool dual) {
+  return (size_t)pl.m_tiles * pl.n_tiles * pl.splits * pl.ncol * (dual ? 2 : 1) * BM *
          sizeof(float);
+}
+
+size_t gemm_partial_bytes(int M, int N, int K, int dual, int split, int sm_count) {
+  const Plan pl = make_plan(M, N, K, dual != 0, split, sm_count);
+  return pl.splits <= 1 ? 0 : partial_need(pl, dual != 0);
 }
 
 template <int EPI>
@@ -342,6 +376,9 @@ static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st)
   p.n_tiles = pl.n_tiles;
   p.stages = pl.stages;
   p.tmem_cols = pl.tmem_cols;
+  p.lo = pl.lo;
+  p.ncol = pl.ncol;
+  p.out_lo = g.out_lo;
   p.out = g.out;
   p.ldo = g.ldo;
   p.partial = g.partial;
@@ -371,22 +408,12 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st) {
     }
   }
   const bool dual = g.epi == LLAMA_EPI_SWIGLU;
-  Plan pl = make_plan(g.M, g.N, g.K, dual, g.sm_count);
+  Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count);
   if (pl.n_tile != g.n_tile) return cudaErrorInvalidValue;
-  if (pl.splits > 1) {
-    const size_t need = (size_t)pl.m_tiles * pl.n_tiles * pl.splits * pl.n_tile * (dual ? 2 : 1) *
-                        BM * sizeof(float);
-    if (need > g.partial_bytes || pl.m_tiles * pl.n_tiles > g.n_counters) {
-      // not enough workspace for this split: fall back to fewer splits
-      while (pl.splits > 1) {
-        --pl.splits;
-        const size_t n2 = (size_t)pl.m_tiles * pl.n_tiles * pl.splits * pl.n_tile *
-                          (dual ? 2 : 1) * BM * sizeof(float);
-        if (pl.splits == 1 || (n2 <= g.partial_bytes && pl.m_tiles * pl.n_tiles <= g.n_counters))
-          break;
-      }
-    }
-  }
+  // fewer splits when the workspace was sized for less
+  while (pl.splits > 1 &&
+         (partial_need(pl, dual) > g.partial_bytes || pl.m_tiles * pl.n_tiles > g.n_counters))
+    --pl.splits;
   switch (g.epi) {
     case LLAMA_EPI_STORE_F32: return launch_tc<LLAMA_EPI_STORE_F32>(g, pl, st);
     case LLAMA_EPI_RESID_F32: return launch_tc<LLAMA_EPI_RESID_F32>(g, pl, st);

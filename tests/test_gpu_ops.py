@@ -20,9 +20,11 @@ GEMM_F32_TOL = (2e-3, 1e-3)
 L7 = synth.LLAMA2_7B.with_(n_layers=1)
 
 
-def ctx_for(shape, max_batch=64, max_tokens=4096, max_seq=4608, embed=False, seed=5):
+def ctx_for(shape, max_batch=64, max_tokens=4096, max_seq=4608, embed=False, seed=5, n_layers=1):
     need_gpu()
-    w = synth.model_weights(shape, seed) if embed else {"layers": [synth.layer_weights(shape, seed, 0)]}
+    shape = shape.with_(n_layers=n_layers)
+    w = synth.model_weights(shape, seed) if embed else \
+        {"layers": [synth.layer_weights(shape, seed, l) for l in range(n_layers)]}
     wd = to_dev(w)
     m = binding.Model(shape, wd, max_batch=max_batch, max_tokens=max_tokens, max_seq=max_seq,
                       has_embed_head=embed)
@@ -109,6 +111,49 @@ def test_linear_bf16(ctx7, M, N, K, epi):
         ctx7.op_linear(xd, wd, out, EPIS[epi], w_up=wud)
         ctx7.sync()
         assert_close(out, ref, tol, "linear %s M=%d N=%d K=%d" % (epi, M, N, K))
+
+
+def _pair(x):
+    """hi/lo bf16 pair layout of fp32 rows: [hi rows, pad, lo rows, pad]."""
+    n, K = x.shape
+    L = (n + 15) // 16 * 16
+    hi = x.to(torch.bfloat16)
+    lo = (x - hi.float()).to(torch.bfloat16)
+    out = torch.zeros(2 * L, K, dtype=torch.bfloat16)
+    out[:n] = hi
+    out[L:L + n] = lo
+    return out, L
+
+
+@pytest.mark.parametrize("M,N,K,epi", [
+    (12288, 32, 4096, "store_f32"),
+    (11008, 32, 4096, "swiglu"),
+    (4096, 100, 11008, "resid"),
+    (32000, 8, 4096, "store_f32"),
+    (1024, 1, 256, "store_t"),
+])
+def test_linear_bf16_pair_operands(ctx7, M, N, K, epi):
+    # fp32 activations carried as bf16 hi + lo: the product tracks the fp32 values
+    x = _randn((N, K), 1.0, torch.float32, 25)
+    w = _randn((M, K), 0.02, torch.bfloat16, 26)
+    wu = _randn((M, K), 0.02, torch.bfloat16, 27) if epi == "swiglu" else None
+    xp, L = _pair(x)
+    ref = O.linear(f64(x), f64(w))
+    if epi == "swiglu":
+        ref = O.silu(ref) * O.linear(f64(x), f64(wu))
+    if epi in ("store_t", "swiglu"):
+        out = torch.zeros(2 * L, M, dtype=torch.bfloat16, device="cuda")
+    else:
+        out = torch.zeros(N, M, dtype=torch.float32, device="cuda")
+    if epi == "resid":
+        base = _randn((N, M), 1.0, torch.float32, 28)
+        out.copy_(base)
+        ref = ref + f64(base)
+    ctx7.op_linear(xp.cuda(), w.cuda(), out, EPIS[epi] | binding.EPI_SPLIT_X,
+                   w_up=wu.cuda() if wu is not None else None)
+    ctx7.sync()
+    got = f64(out[:N]) + f64(out[L:L + N]) if epi in ("store_t", "swiglu") else f64(out)
+    assert_close(got, ref, GEMM_F32_TOL, "pair-operand linear %s" % epi)
 
 
 @pytest.mark.parametrize("epi", list(EPIS))
@@ -220,7 +265,7 @@ def test_attention_decode_many_splits():
 
 def test_attention_decode_f32():
     shape = synth.TINY
-    m, _ = ctx_for(shape, max_batch=3, max_tokens=16, max_seq=64)
+    m, _ = ctx_for(shape, max_batch=3, max_tokens=16, max_seq=64, n_layers=2)
     B, nq, nkv, d = 3, 4, 2, 64
     pos = torch.tensor([0, 17, 40], dtype=torch.int32)
     q = _randn((B, nq, d), 1.0, torch.float32, 54)
