@@ -275,9 +275,12 @@ class Model:
         self._chk(lib().llama_op_rmsnorm(self.ctx, _p(x), rows, stride, offset, _p(gamma), _p(out)),
                   "llama_op_rmsnorm")
 
-    def op_linear(self, x, w, out, epilogue, w_up=None):
+    def op_linear(self, x, w, out, epilogue, w_up=None, n_rows=None):
+        """n_rows: logical activation rows (defaults to x.shape[0]; give it for the
+        hi/lo pair layout, whose tensor has 2 * round16(n_rows) rows)."""
         M, K = w.shape
-        self._chk(lib().llama_op_linear(self.ctx, _p(x), x.shape[0], _p(w), _p(w_up), M, K, epilogue,
+        n = x.shape[0] if n_rows is None else n_rows
+        self._chk(lib().llama_op_linear(self.ctx, _p(x), n, _p(w), _p(w_up), M, K, epilogue,
                                         _p(out)), "llama_op_linear")
 
     def op_rope_append(self, qkv, rows_per_seq, positions, layer, kv: KVCache, q_out, k_out=None,

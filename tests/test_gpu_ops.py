@@ -150,7 +150,7 @@ def test_linear_bf16_pair_operands(ctx7, M, N, K, epi):
         out.copy_(base)
         ref = ref + f64(base)
     ctx7.op_linear(xp.cuda(), w.cuda(), out, EPIS[epi] | binding.EPI_SPLIT_X,
-                   w_up=wu.cuda() if wu is not None else None)
+                   w_up=wu.cuda() if wu is not None else None, n_rows=N)
     ctx7.sync()
     got = f64(out[:N]) + f64(out[L:L + N]) if epi in ("store_t", "swiglu") else f64(out)
     assert_close(got, ref, GEMM_F32_TOL, "pair-operand linear %s" % epi)
