@@ -21,7 +21,6 @@ namespace {
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
-constexpr int kMaxCounters = 8192;
 // Up to this many activation rows, bf16 GEMM operands are carried as a pair
 // hi = bf16(v), lo = bf16(v - hi) stacked along N (rows [0,n) and [lo, lo+n),
 // lo = n rounded up to 16): the product keeps ~16 mantissa bits of v. The
@@ -60,9 +59,9 @@ int sm_count_or_default() {
 
 // Workspace layout (byte offsets from the workspace base).
 struct Layout {
-  size_t status, counters, rope, x, u, qkv, q, kside, vside, o, a, u_last, logits, ids, tok, pos,
-      gpart, apart, total;
-  size_t gpart_bytes, apart_bytes;
+  size_t status, rope, x, u, qkv, q, kside, vside, o, a, u_last, logits, ids, tok, pos, apart,
+      total;
+  size_t apart_bytes;
   int R;
 };
 
@@ -105,7 +104,6 @@ Layout make_layout(const llama_config* c, int sm_count) {
     return o;
   };
   L.status = take(16);
-  L.counters = take(sizeof(int) * kMaxCounters);
   L.rope = take((size_t)c->max_seq * (d / 2) * sizeof(float) * 2);
   L.x = take((size_t)R * H * 4);
   // GEMM operands: room for the hi/lo pair layout of up to 128 rows (256 rows)
@@ -122,23 +120,6 @@ Layout make_layout(const llama_config* c, int sm_count) {
   L.ids = take((size_t)c->max_batch * 4);
   L.tok = take((size_t)c->max_batch * 4);
   L.pos = take((size_t)c->max_batch * 4);
-  size_t gp = 0;
-  if (c->dtype == LLAMA_BF16) {
-    const int Ns[2] = {c->max_batch, std::max(c->max_tokens, 1)};
-    for (int N : Ns)
-      for (int split = 0; split < 2; ++split) {
-        if (split && N > kSplitMaxRows) continue;
-        gp = std::max(gp, gemm_partial_bytes((int)qkv_rows, N, (int)H, 0, split, sm_count));
-        gp = std::max(gp, gemm_partial_bytes((int)H, N, (int)(nq * d), 0, split, sm_count));
-        gp = std::max(gp, gemm_partial_bytes((int)I, N, (int)H, 1, split, sm_count));
-        gp = std::max(gp, gemm_partial_bytes((int)H, N, (int)I, 0, split, sm_count));
-        if (V)
-          gp = std::max(gp, gemm_partial_bytes((int)V, std::min(N, c->max_batch), (int)H, 0, split,
-                                               sm_count));
-      }
-  }
-  L.gpart_bytes = gp;
-  L.gpart = take(std::max<size_t>(gp, 16));
   L.apart_bytes = attn_decode_partial_bytes(c->max_batch, (int)nq, (int)d, c->max_seq, sm_count,
                                             (int)nkv);
   L.apart = take(std::max<size_t>(L.apart_bytes, 16));
@@ -165,7 +146,6 @@ struct llama_ctx {
   char* ws = nullptr;
   Layout L;
   uint32_t* status = nullptr;
-  int* counters = nullptr;
   float2* rope = nullptr;
   std::map<Key2, CUtensorMap> maps;
   uint32_t prof_mask = 0;
@@ -298,10 +278,6 @@ int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, c
   g.w_up = wu;
   g.out = out;
   g.ldo = ldo;
-  g.partial = c->at<float>(c->L.gpart);
-  g.partial_bytes = c->L.gpart_bytes;
-  g.counters = c->counters;
-  g.n_counters = kMaxCounters;
   g.status = c->status;
   g.sm_count = c->sm_count;
   if (c->cfg.dtype == LLAMA_BF16) {
@@ -542,7 +518,6 @@ int llama_init(const llama_config* cfg, const llama_weights* w, void* workspace,
   c->ws = reinterpret_cast<char*>(workspace);
   c->L = L;
   c->status = c->at<uint32_t>(L.status);
-  c->counters = c->at<int>(L.counters);
   c->rope = c->at<float2>(L.rope);
   int rc = LLAMA_OK;
   if (cudaMemsetAsync(c->ws, 0, L.rope, c->stream) != cudaSuccess) rc = LLAMA_ERR_CUDA;

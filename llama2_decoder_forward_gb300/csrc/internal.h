@@ -54,17 +54,11 @@ struct GemmCall {
   size_t out_lo;              // bf16 outputs: also store the remainder out_lo elements on
   void* out;
   int ldo;
-  float* partial;             // split-K partial sums (workspace)
-  size_t partial_bytes;
-  int* counters;              // split-K arrival counters (workspace, zeroed)
-  int n_counters;
   uint32_t* status;
   int sm_count;
 };
 // Activation rows one bf16 GEMM tile reads (MMA N) for N logical rows.
 int gemm_n_tile(int N, int split);
-// Bytes of split-K partials a call may need (upper bound for the workspace).
-size_t gemm_partial_bytes(int M, int N, int K, int dual, int split, int sm_count);
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st);
 cudaError_t gemm_prepare();  // sets kernel attributes once per process
 

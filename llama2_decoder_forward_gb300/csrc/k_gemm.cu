@@ -16,8 +16,10 @@
 // and apply the epilogue. SwiGLU runs two MMAs per K step (gate rows and up
 // rows of the same 128 features) into two accumulators, so silu(g)*u is
 // formed in registers. When the grid would leave SMs idle (decode), K is
-// split: each split writes an fp32 partial, the last CTA of a tile to arrive
-// sums the partials in split order (deterministic) and applies the epilogue.
+// split over up to 8 CTAs that form one thread-block cluster: each stages its
+// fp32 sums in shared memory and the cluster adds them through distributed
+// shared memory in split order (deterministic), each CTA finishing a slice of
+// the tile's columns.
 //
 // fp32 path: plain CUDA-core FMAs in fp32 (no TF32), one thread per output.
 #include <algorithm>
@@ -42,8 +44,6 @@ struct TcParams {
   size_t out_lo;  // >0: bf16 outputs also write their remainder out_lo elements further
   void* out;
   int ldo;
-  float* partial;
-  int* counters;
   uint32_t* status;
 };
 
@@ -65,7 +65,18 @@ __device__ __forceinline__ void epi_apply(void* out, size_t idx, float g, float 
   }
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// 16 accumulator columns starting at col for this thread's TMEM lane; in the
+// hi/lo operand mode the column col + lo holds the product with the
+// remainders and is added.
+__device__ __forceinline__ void load_acc16(uint32_t tq, int col, int lo, float (&v)[16]) {
+  uint32_t a[16], b[16];
+  tmem_ld16(tq + col, a);
+  if (lo) tmem_ld16(tq + col + lo, b);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    v[j] = lo ? __uint_as_float(a[j]) + __uint_as_float(b[j]) : __uint_as_float(a[j]);
+}
 
 template <int EPI>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
@@ -178,28 +189,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (ok && !ctl[1]) {
       const int q = warp & 3;  // TMEM lane quadrant this warp may read
       const int r = q * 32 + lane;
-      const int gm = tile_m * BM + r;
-      const int n0 = tile_n * p.ncol;
-      const int nvalid = min(p.ncol, p.N - n0);
-      const bool row_ok = gm < p.M;
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
       const int up = p.n_tile;  // first TMEM column of the up-projection accumulator
-      // 16 output columns starting at c0: sum the hi and lo halves when present
-      auto load16 = [&](int col, float (&v)[16]) {
-        uint32_t a[16], b[16];
-        tmem_ld16(tq + col, a);
-        if (p.lo) tmem_ld16(tq + col + p.lo, b);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          v[j] = p.lo ? __uint_as_float(a[j]) + __uint_as_float(b[j]) : __uint_as_float(a[j]);
-      };
       if (p.splits == 1) {
+        const int gm = tile_m * BM + r;
+        const int n0 = tile_n * p.ncol;
+        const int nvalid = min(p.ncol, p.N - n0);
         for (int c0 = 0; c0 < nvalid; c0 += 16) {
           float g[16], u[16];
-          load16(c0, g);
-          if (DUAL) load16(up + c0, u);
-          if (row_ok) {
+          load_acc16(tq, c0, p.lo, g);
+          if (DUAL) load_acc16(tq, up + c0, p.lo, u);
+          if (gm < p.M) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (c0 + j < nvalid)
@@ -208,54 +208,50 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       } else {
-        const int tile = tile_m * p.n_tiles + tile_n;
-        const int width = p.ncol * (DUAL ? 2 : 1);
-        float* base = p.partial + (size_t)tile * p.splits * width * BM;
-        float* mine = base + (size_t)split * width * BM;
+        // this split's sums -> shared memory, column-major [col][128 rows]
+        float* red = reinterpret_cast<float*>(smem);
         for (int c0 = 0; c0 < p.ncol; c0 += 16) {
           float g[16];
-          load16(c0, g);
+          load_acc16(tq, c0, p.lo, g);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) mine[(size_t)(c0 + j) * BM + r] = g[j];
+          for (int j = 0; j < 16; ++j) red[(c0 + j) * BM + r] = g[j];
           if (DUAL) {
-            load16(up + c0, g);
+            load_acc16(tq, up + c0, p.lo, g);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) mine[(size_t)(p.ncol + c0 + j) * BM + r] = g[j];
+            for (int j = 0; j < 16; ++j) red[(p.ncol + c0 + j) * BM + r] = g[j];
           }
-        }
-        __threadfence();
-        epi_bar();
-        if (threadIdx.x == 64) {
-          const int old = atomicAdd(&p.counters[tile], 1);
-          ctl[2] = (old == p.splits - 1) ? 1u : 0u;
-        }
-        epi_bar();
-        if (ctl[2]) {  // last split of this tile: reduce in split order, then epilogue
-          __threadfence();
-          for (int c0 = 0; c0 < nvalid; c0 += 16) {
-            float gs[16], us[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) gs[j] = us[j] = 0.f;
-            for (int s2 = 0; s2 < p.splits; ++s2) {
-              const float* ps = base + (size_t)s2 * width * BM;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                gs[j] += __ldcg(ps + (size_t)(c0 + j) * BM + r);
-                if (DUAL) us[j] += __ldcg(ps + (size_t)(p.ncol + c0 + j) * BM + r);
-              }
-            }
-            if (row_ok) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (c0 + j < nvalid)
-                  epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm, gs[j], us[j],
-                                       p.out_lo);
-            }
-          }
-          if (threadIdx.x == 64) p.counters[tile] = 0;
         }
       }
     }
+  }
+  if (p.splits > 1) {
+    // The splits of this tile form one cluster: after every CTA has staged its
+    // sums, CTA k adds column slice k of all splits in split order (the same
+    // order on every run) and applies the epilogue.
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2 && !ctl[1]) {
+      const int r = (warp & 3) * 32 + lane;
+      const int gm = tile_m * BM + r;
+      const int S = p.splits;
+      const int k = (int)cluster_ctarank();
+      const int c_beg = (k * p.ncol) / S, c_end = ((k + 1) * p.ncol) / S;
+      const int nvalid = min(p.ncol, p.N);
+      const uint32_t red0 = smem_u32(smem);
+      for (int c = c_beg; c < c_end; ++c) {
+        if (c >= nvalid) break;
+        float g = 0.f, u = 0.f;
+        const uint32_t og = (uint32_t)(c * BM + r) * 4u;
+        const uint32_t ou = (uint32_t)((p.ncol + c) * BM + r) * 4u;
+        for (int s2 = 0; s2 < S; ++s2) {
+          g += dsmem_ld(dsmem_addr(red0 + og, s2));
+          if (DUAL) u += dsmem_ld(dsmem_addr(red0 + ou, s2));
+        }
+        if (gm < p.M) epi_apply<EPI, bf16>(p.out, (size_t)c * p.ldo + gm, g, u, p.out_lo);
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();  // no CTA leaves while another still reads its shared memory
   }
   tc_fence_before();
   __syncthreads();
@@ -323,31 +319,26 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count) {
   pl.num_kb = (K + BK - 1) / BK;
   const int tiles = pl.m_tiles * pl.n_tiles;
   const int slots = std::max(1, sm_count) * pl.ctas_per_sm;
-  // choose the split count that minimises (waves x k-blocks per CTA); only a
-  // single activation tile (decode) is split, a prefill grid has tiles enough
+  // Split K only for a single activation tile (decode) whose split sums fit
+  // in the stage buffers; choose the count minimising waves x (k-blocks per
+  // CTA + a fixed cost of about kFixedKb k-blocks for launch, first-load
+  // latency and the cluster reduction).
+  constexpr int kFixedKb = 4;
+  const size_t red_bytes = (size_t)pl.ncol * (dual ? 2 : 1) * BM * sizeof(float);
+  const bool can_split = pl.n_tiles == 1 && red_bytes <= (size_t)pl.stages * stage_bytes;
+  const int max_split = can_split ? std::min(8, pl.num_kb) : 1;
   long best = -1;
   pl.splits = 1;
-  const int max_split = pl.n_tiles == 1 ? std::min(32, pl.num_kb) : 1;
   for (int s = 1; s <= max_split; ++s) {
     const long ctas = (long)tiles * s;
     const long waves = (ctas + slots - 1) / slots;
-    const long cost = waves * ((pl.num_kb + s - 1) / s) + (s > 1 ? 1 : 0);
+    const long cost = waves * ((pl.num_kb + s - 1) / s + kFixedKb);
     if (best < 0 || cost < best) {
       best = cost;
       pl.splits = s;
     }
   }
   return pl;
-}
-
-static size_t partial_need(const Plan& pl, bool dual) {
-  return (size_t)pl.m_tiles * pl.n_tiles * pl.splits * pl.ncol * (dual ? 2 : 1) * BM *
-         sizeof(float);
-}
-
-size_t gemm_partial_bytes(int M, int N, int K, int dual, int split, int sm_count) {
-  const Plan pl = make_plan(M, N, K, dual != 0, split, sm_count);
-  return pl.splits <= 1 ? 0 : partial_need(pl, dual != 0);
 }
 
 template <int EPI>
@@ -381,13 +372,21 @@ static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st)
   p.out_lo = g.out_lo;
   p.out = g.out;
   p.ldo = g.ldo;
-  p.partial = g.partial;
-  p.counters = g.counters;
   p.status = g.status;
-  dim3 grid(pl.n_tiles, pl.m_tiles, pl.splits);
   const CUtensorMap* up = g.map_up ? g.map_up : g.map_w;
-  gemm_tc_kernel<EPI><<<grid, GEMM_THREADS, pl.smem, st>>>(*g.map_w, *up, *g.map_x, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.n_tiles, pl.m_tiles, pl.splits);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = pl.splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, *g.map_w, *up, *g.map_x, p);
 }
 
 template <int EPI>
@@ -408,12 +407,8 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st) {
     }
   }
   const bool dual = g.epi == LLAMA_EPI_SWIGLU;
-  Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count);
+  const Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count);
   if (pl.n_tile != g.n_tile) return cudaErrorInvalidValue;
-  // fewer splits when the workspace was sized for less
-  while (pl.splits > 1 &&
-         (partial_need(pl, dual) > g.partial_bytes || pl.m_tiles * pl.n_tiles > g.n_counters))
-    --pl.splits;
   switch (g.epi) {
     case LLAMA_EPI_STORE_F32: return launch_tc<LLAMA_EPI_STORE_F32>(g, pl, st);
     case LLAMA_EPI_RESID_F32: return launch_tc<LLAMA_EPI_RESID_F32>(g, pl, st);
