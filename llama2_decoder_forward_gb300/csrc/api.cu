@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -499,6 +500,9 @@ int llama_init(const llama_config* cfg, const llama_weights* w, void* workspace,
     return LLAMA_ERR_CUDA;
   }
   if (!load_encode()) return LLAMA_ERR_CUDA;
+  // LLAMA_GB300_PDL=0: launch in plain stream order (no programmatic overlap)
+  const char* pdl = getenv("LLAMA_GB300_PDL");
+  set_pdl(!(pdl && pdl[0] == '0'));
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return LLAMA_ERR_CUDA;

@@ -10,6 +10,42 @@
 
 namespace llgb {
 
+// ------------------------------------------------------------------ launching
+// Every kernel is launched with programmatic stream serialization: it may
+// start while the previous kernel on the stream drains, runs its prologue
+// (barriers, descriptors, weight prefetch) and then waits in-kernel
+// (griddepcontrol.wait) before touching activations. set_pdl(false) turns
+// this off (plain stream order).
+void set_pdl(bool on);
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, int cluster_z, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_z > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = cluster_z;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------------ RoPE + append
 struct RopeAppendArgs {
   const float* qkv;          // [rows, (n_q + 2 n_kv) d] fp32

@@ -89,10 +89,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
+  // positions and the page table are caller inputs, complete before the step
   const int n_keys = decode_keys(p.positions[b], cap_keys);
   const int kbeg = split * p.keys_per_split;
   const int kend = min(n_keys, kbeg + p.keys_per_split);
-  if (kbeg >= kend) return;  // this split has no keys (the combine skips it)
+  if (kbeg >= kend) {  // this split has no keys (the merge skips it)
+    grid_dep_wait();
+    return;
+  }
   const int n_sub = (kend - kbeg + SUBK - 1) / SUBK;
   const int n_tiles = (n_sub + 3) / 4;
 
@@ -111,10 +115,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
       int issued = 0;
-      bool ok = true;
+      bool ok = true, waited = false;
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t % DSTAGES;
         const uint32_t ph = (t / DSTAGES) & 1;
+        // Keys below the new token were cached by earlier steps and can be
+        // fetched while the previous kernel finishes; the tile holding the
+        // new token's K/V (written by the RoPE/append kernel) waits for it.
+        if (!waited && kbeg + (t + 1) * DTILE >= n_keys) {
+          grid_dep_wait();
+          grid_dep_launch();
+          waited = true;
+        }
         if (!mbar_wait(&empty[s], ph ^ 1, p.status)) {
           ok = false;
           *abort_flag = 1;
@@ -143,6 +155,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   }
 
   // ---------------------------------------------------------------- consumers
+  grid_dep_wait();  // q comes from the RoPE/append kernel
+  grid_dep_launch();
   const int G = p.G;
   const int r0 = lane >> 2;
   uint32_t qa[8][4];
@@ -324,6 +338,8 @@ __global__ void attn_combine_kernel(const float* __restrict__ part,
                                     const int32_t* __restrict__ positions, int n_q, int splits,
                                     int keys_per_split, int cap_keys, int d, void* out,
                                     size_t out_lo) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int bh = blockIdx.x;
   const int b = bh / n_q;
   const int n_keys = decode_keys(positions[b], cap_keys);
@@ -381,6 +397,8 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
   uint64_t* empty = full + PSTAGES;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + PSTAGES);
 
+  grid_dep_wait();  // q, k, v come from the RoPE/append kernel
+  grid_dep_launch();
   const int qt = p.n_qtiles - 1 - (int)blockIdx.x;  // longest rows first
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / p.G;
@@ -575,6 +593,8 @@ __global__ void attn_decode_f32_kernel(const float* __restrict__ q, const int32_
                                        int n_q, int n_kv, int d, int layer, int page_size,
                                        int capacity, int batch_cap, int n_pages, int max_pages,
                                        uint32_t* status) {
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ float sh[];
   const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / (n_q / n_kv);
@@ -630,6 +650,8 @@ __global__ void attn_decode_f32_kernel(const float* __restrict__ q, const int32_
 __global__ void attn_prefill_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                                         const float* __restrict__ v, float* __restrict__ out,
                                         int T, int n_q, int n_kv, int d) {
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ float sh[];
   const int t = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = h / (n_q / n_kv);
@@ -705,11 +727,11 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
     if (sm > 48 * 1024)
       cudaFuncSetAttribute(attn_decode_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sm);
-    attn_decode_f32_kernel<<<dim3(a.n_q, a.B), 128, sm, st>>>(
-        (const float*)a.q, a.positions, (const float*)a.k_cache, (const float*)a.v_cache,
-        a.page_table, (float*)a.out, a.n_q, a.n_kv, a.head_dim, a.layer, a.page_size, a.capacity,
-        a.batch_cap, a.n_pages, a.max_pages, a.status);
-    return cudaGetLastError();
+    return launch_k(attn_decode_f32_kernel, dim3(a.n_q, a.B), dim3(128), sm, st, 0,
+                    (const float*)a.q, a.positions, (const float*)a.k_cache,
+                    (const float*)a.v_cache, a.page_table, (float*)a.out, a.n_q, a.n_kv,
+                    a.head_dim, a.layer, a.page_size, a.capacity, a.batch_cap, a.n_pages,
+                    a.max_pages, a.status);
   }
   if (a.head_dim != AD) return cudaErrorInvalidValue;
   if (splits > 1 && (size_t)a.B * a.n_q * splits * (AD + 2) * sizeof(float) > a.partial_bytes) {
@@ -737,14 +759,13 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.splits = splits;
   p.keys_per_split = kps;
   p.scale_log2 = kLog2e / sqrtf((float)AD);
-  attn_decode_kernel<<<dim3(splits, a.n_kv, a.B), DEC_THREADS, DEC_SMEM, st>>>(*a.map_k,
-                                                                             *a.map_v, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(attn_decode_kernel, dim3(splits, a.n_kv, a.B), dim3(DEC_THREADS),
+                           DEC_SMEM, st, 0, *a.map_k, *a.map_v, p);
   if (e != cudaSuccess || splits == 1) return e;
   const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
-  attn_combine_kernel<<<a.B * a.n_q, AD, 0, st>>>(a.partial, a.positions, a.n_q, splits, kps,
-                                                  cap_keys, AD, a.out, a.out_lo);
-  return cudaGetLastError();
+  return launch_k(attn_combine_kernel, dim3(a.B * a.n_q), dim3(AD), 0, st, 0,
+                  (const float*)a.partial, a.positions, a.n_q, splits, kps, cap_keys, AD, a.out,
+                  a.out_lo);
 }
 
 int attn_decode_launches(int B, int n_kv, int max_keys, int sm_count, int dtype) {
@@ -761,10 +782,9 @@ cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_
     if (sm > 48 * 1024)
       cudaFuncSetAttribute(attn_prefill_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sm);
-    attn_prefill_f32_kernel<<<dim3(a.T, a.n_q, a.B), 128, sm, st>>>(
-        (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)a.out, a.T, a.n_q,
-        a.n_kv, a.head_dim);
-    return cudaGetLastError();
+    return launch_k(attn_prefill_f32_kernel, dim3(a.T, a.n_q, a.B), dim3(128), sm, st, 0,
+                    (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)a.out, a.T,
+                    a.n_q, a.n_kv, a.head_dim);
   }
   if (a.head_dim != AD) return cudaErrorInvalidValue;
   PreParams p;
@@ -777,9 +797,8 @@ cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_
   p.G = a.n_q / a.n_kv;
   p.n_qtiles = (a.T + PQ - 1) / PQ;
   p.scale_log2 = kLog2e / sqrtf((float)AD);
-  attn_prefill_kernel<<<dim3(p.n_qtiles, a.n_q, a.B), PRE_THREADS, PRE_SMEM, st>>>(
-      *a.map_q, *a.map_k, *a.map_v, p);
-  return cudaGetLastError();
+  return launch_k(attn_prefill_kernel, dim3(p.n_qtiles, a.n_q, a.B), dim3(PRE_THREADS), PRE_SMEM,
+                  st, 0, *a.map_q, *a.map_k, *a.map_v, p);
 }
 
 }  // namespace llgb

@@ -14,6 +14,8 @@ namespace llgb {
 template <typename T>
 __global__ void embed_kernel(const int32_t* __restrict__ tokens, const T* __restrict__ table,
                              int V, int H, float* __restrict__ out, uint32_t* status) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int r = blockIdx.x;
   const int tok = tokens[r];
   const bool ok = tok >= 0 && tok < V;
@@ -39,6 +41,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       int in_offset, const T* __restrict__ gamma,
                                                       int H, float eps, T* __restrict__ out,
                                                       int lo_rows) {
+  grid_dep_wait();
+  grid_dep_launch();
   const size_t lo = (size_t)lo_rows * H;
   __shared__ float red[8];
   const int r = blockIdx.x;
@@ -87,6 +91,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
 // tab[m * (d/2) + j] = (cos(m * theta_j), sin(m * theta_j)), theta_j =
 // base^(-2j/d), evaluated in fp64 and rounded once to fp32.
 __global__ void rope_table_kernel(float2* __restrict__ tab, int max_seq, int half, double base) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)max_seq * half) return;
   const int m = (int)(i / half), j = (int)(i % half);
@@ -106,6 +112,8 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int max_seq, int hal
 // status flag and skip the cache write.
 template <typename T>
 __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int r = blockIdx.y;
   const int b = r / a.rows_per_seq;
   const int pos = a.positions ? a.positions[r] : (r % a.rows_per_seq);
@@ -184,6 +192,8 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
 // ids[b] = index of the largest logit of row b; ties go to the lowest index.
 __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ logits, int V,
                                                       int32_t* __restrict__ ids) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float sv[32];
   __shared__ int si[32];
   const float* row = logits + (size_t)blockIdx.x * V;
@@ -214,48 +224,45 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ 
 }
 
 // ------------------------------------------------------------------ launchers
+static bool g_pdl = true;
+void set_pdl(bool on) { g_pdl = on; }
+bool pdl_enabled() { return g_pdl; }
+
 cudaError_t launch_embed(int dtype, const int32_t* tokens, const void* table, int V, int H, int n,
                          float* out, uint32_t* status, cudaStream_t st) {
   if (dtype == LLAMA_BF16)
-    embed_kernel<bf16><<<n, 256, 0, st>>>(tokens, (const bf16*)table, V, H, out, status);
-  else
-    embed_kernel<float><<<n, 256, 0, st>>>(tokens, (const float*)table, V, H, out, status);
-  return cudaGetLastError();
+    return launch_k(embed_kernel<bf16>, dim3(n), dim3(256), 0, st, 0, tokens, (const bf16*)table, V,
+                    H, out, status);
+  return launch_k(embed_kernel<float>, dim3(n), dim3(256), 0, st, 0, tokens, (const float*)table,
+                  V, H, out, status);
 }
 
 cudaError_t launch_rmsnorm(int dtype, const float* x, int rows, int in_stride, int in_offset,
                            const void* gamma, int H, float eps, void* out, int lo_rows,
                            cudaStream_t st) {
   if (dtype == LLAMA_BF16)
-    rmsnorm_kernel<bf16><<<rows, 256, 0, st>>>(x, in_stride, in_offset, (const bf16*)gamma, H,
-                                               eps, (bf16*)out, lo_rows);
-  else
-    rmsnorm_kernel<float><<<rows, 256, 0, st>>>(x, in_stride, in_offset, (const float*)gamma, H,
-                                                eps, (float*)out, 0);
-  return cudaGetLastError();
+    return launch_k(rmsnorm_kernel<bf16>, dim3(rows), dim3(256), 0, st, 0, x, in_stride, in_offset,
+                    (const bf16*)gamma, H, eps, (bf16*)out, lo_rows);
+  return launch_k(rmsnorm_kernel<float>, dim3(rows), dim3(256), 0, st, 0, x, in_stride, in_offset,
+                  (const float*)gamma, H, eps, (float*)out, 0);
 }
 
 cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double theta,
                               cudaStream_t st) {
   const long long n = (long long)max_seq * (head_dim / 2);
-  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(tab, max_seq, head_dim / 2,
-                                                                   theta);
-  return cudaGetLastError();
+  return launch_k(rope_table_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, 0, tab,
+                  max_seq, head_dim / 2, theta);
 }
 
 cudaError_t launch_rope_append(int dtype, const RopeAppendArgs& a, int rows, cudaStream_t st) {
   const int width = (a.n_q + 2 * a.n_kv) * a.head_dim;
   dim3 grid((width / 8 + 255) / 256, rows);
-  if (dtype == LLAMA_BF16)
-    rope_append_kernel<bf16><<<grid, 256, 0, st>>>(a);
-  else
-    rope_append_kernel<float><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  if (dtype == LLAMA_BF16) return launch_k(rope_append_kernel<bf16>, grid, dim3(256), 0, st, 0, a);
+  return launch_k(rope_append_kernel<float>, grid, dim3(256), 0, st, 0, a);
 }
 
 cudaError_t launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st) {
-  argmax_kernel<<<B, 1024, 0, st>>>(logits, V, ids);
-  return cudaGetLastError();
+  return launch_k(argmax_kernel, dim3(B), dim3(1024), 0, st, 0, logits, V, ids);
 }
 
 }  // namespace llgb

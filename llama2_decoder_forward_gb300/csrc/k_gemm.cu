@@ -123,10 +123,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {  // ---------------- TMA producer
       const uint64_t pol_w = l2_policy_evict_first();  // weights are streamed once
-      int s = 0, issued = 0;
-      uint32_t ph = 0;
+      const uint32_t b_off = a_bytes * (DUAL ? 2 : 1);
+      // The weights do not depend on the previous kernel: fill the first
+      // stages with them before waiting, then add the activation tiles.
+      const int npre = min(S, kb1 - kb0);
+      for (int i = 0; i < npre; ++i) {
+        uint8_t* st = smem + (size_t)i * stage_bytes;
+        mbar_arrive_expect_tx(&full[i], stage_bytes);
+        tma_load_2d_hint(st, &tmW, &full[i], (kb0 + i) * BK, tile_m * BM, pol_w);
+        if (DUAL) tma_load_2d_hint(st + a_bytes, &tmU, &full[i], (kb0 + i) * BK, tile_m * BM, pol_w);
+      }
+      grid_dep_wait();
+      grid_dep_launch();
+      for (int i = 0; i < npre; ++i)
+        tma_load_2d(smem + (size_t)i * stage_bytes + b_off, &tmX, &full[i], (kb0 + i) * BK,
+                    tile_n * p.n_tile);
+      int s = npre % S, issued = npre;
+      uint32_t ph = npre == S ? 1u : 0u;
       bool ok = true;
-      for (int kb = kb0; kb < kb1; ++kb) {
+      for (int kb = kb0 + npre; kb < kb1; ++kb) {
         if (!mbar_wait(&empty[s], ph ^ 1, p.status)) {
           ok = false;
           ctl[1] = 1;
@@ -136,7 +151,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         mbar_arrive_expect_tx(&full[s], stage_bytes);
         tma_load_2d_hint(st, &tmW, &full[s], kb * BK, tile_m * BM, pol_w);
         if (DUAL) tma_load_2d_hint(st + a_bytes, &tmU, &full[s], kb * BK, tile_m * BM, pol_w);
-        tma_load_2d(st + a_bytes * (DUAL ? 2 : 1), &tmX, &full[s], kb * BK, tile_n * p.n_tile);
+        tma_load_2d(st + b_off, &tmX, &full[s], kb * BK, tile_n * p.n_tile);
         ++issued;
         if (++s == S) {
           s = 0;
@@ -184,6 +199,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_wait(accf, 0, p.status);  // every MMA retired before teardown
     }
   } else {  // ---------------- epilogue warps 2..5
+    grid_dep_wait();  // the residual and the outputs belong to the previous kernels' order
+    grid_dep_launch();
     const bool ok = mbar_wait(accf, 0, p.status);
     tc_fence_after();
     if (ok && !ctl[1]) {
@@ -227,27 +244,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (p.splits > 1) {
     // The splits of this tile form one cluster: after every CTA has staged its
     // sums, CTA k adds column slice k of all splits in split order (the same
-    // order on every run) and applies the epilogue.
+    // order on every run) and applies the epilogue. One work item is 4
+    // consecutive rows of one column (a 16-byte remote load per split).
     __syncwarp();
     cluster_sync_all();
     if (warp >= 2 && !ctl[1]) {
-      const int r = (warp & 3) * 32 + lane;
-      const int gm = tile_m * BM + r;
+      const int t = threadIdx.x - 64;
       const int S = p.splits;
       const int k = (int)cluster_ctarank();
-      const int c_beg = (k * p.ncol) / S, c_end = ((k + 1) * p.ncol) / S;
-      const int nvalid = min(p.ncol, p.N);
+      const int c_beg = (k * p.ncol) / S;
+      const int c_end = min(((k + 1) * p.ncol) / S, min(p.ncol, p.N));
+      const int items = max(0, c_end - c_beg) * (BM / 4);
       const uint32_t red0 = smem_u32(smem);
-      for (int c = c_beg; c < c_end; ++c) {
-        if (c >= nvalid) break;
-        float g = 0.f, u = 0.f;
-        const uint32_t og = (uint32_t)(c * BM + r) * 4u;
-        const uint32_t ou = (uint32_t)((p.ncol + c) * BM + r) * 4u;
-        for (int s2 = 0; s2 < S; ++s2) {
-          g += dsmem_ld(dsmem_addr(red0 + og, s2));
-          if (DUAL) u += dsmem_ld(dsmem_addr(red0 + ou, s2));
-        }
-        if (gm < p.M) epi_apply<EPI, bf16>(p.out, (size_t)c * p.ldo + gm, g, u, p.out_lo);
+      for (int it = t; it < items; it += 128) {
+        const int c = c_beg + it / (BM / 4), rq = (it % (BM / 4)) * 4;
+        const uint32_t og = red0 + (uint32_t)(c * BM + rq) * 4u;
+        const uint32_t ou = red0 + (uint32_t)((p.ncol + c) * BM + rq) * 4u;
+        float4 gv[8], uv[8];
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2)
+          if (s2 < S) {
+            gv[s2] = dsmem_ld4(dsmem_addr(og, s2));
+            if (DUAL) uv[s2] = dsmem_ld4(dsmem_addr(ou, s2));
+          }
+        float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2)
+          if (s2 < S) {
+            g[0] += gv[s2].x; g[1] += gv[s2].y; g[2] += gv[s2].z; g[3] += gv[s2].w;
+            if (DUAL) { u[0] += uv[s2].x; u[1] += uv[s2].y; u[2] += uv[s2].z; u[3] += uv[s2].w; }
+          }
+        const int gm0 = tile_m * BM + rq;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (gm0 + e < p.M)
+            epi_apply<EPI, bf16>(p.out, (size_t)c * p.ldo + gm0 + e, g[e], u[e], p.out_lo);
       }
     }
     __syncwarp();
@@ -267,6 +298,8 @@ template <int EPI>
 __global__ void gemm_f32_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                 const float* __restrict__ wu, int M, int N, int K, void* out,
                                 int ldo) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   const int n = blockIdx.y;
   if (m >= M || n >= N) return;
@@ -374,27 +407,15 @@ static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st)
   p.ldo = g.ldo;
   p.status = g.status;
   const CUtensorMap* up = g.map_up ? g.map_up : g.map_w;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.n_tiles, pl.m_tiles, pl.splits);
-  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = pl.smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = pl.splits;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, *g.map_w, *up, *g.map_x, p);
+  return launch_k(gemm_tc_kernel<EPI>, dim3(pl.n_tiles, pl.m_tiles, pl.splits),
+                  dim3(GEMM_THREADS), pl.smem, st, pl.splits, *g.map_w, *up, *g.map_x, p);
 }
 
 template <int EPI>
 static cudaError_t launch_f32(const GemmCall& g, cudaStream_t st) {
   dim3 grid((g.M + 127) / 128, g.N);
-  gemm_f32_kernel<EPI><<<grid, 128, 0, st>>>((const float*)g.x, (const float*)g.w,
-                                             (const float*)g.w_up, g.M, g.N, g.K, g.out, g.ldo);
-  return cudaGetLastError();
+  return launch_k(gemm_f32_kernel<EPI>, grid, dim3(128), 0, st, 0, (const float*)g.x,
+                  (const float*)g.w, (const float*)g.w_up, g.M, g.N, g.K, g.out, g.ldo);
 }
 
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st) {
