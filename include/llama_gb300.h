@@ -262,6 +262,28 @@ int llama_op_rope_append(llama_ctx* ctx, const float* qkv, int32_t rows, int32_t
 int llama_op_attention_decode(llama_ctx* ctx, const void* q, const int32_t* positions,
                               int32_t B, int32_t layer, const llama_kv* kv, void* out);
 
+/* Decode attention that allocates nothing. The pages have no counterpart to
+ * this entry point: it exists for callers that cannot allocate device memory
+ * at the moment they need attention, such as a framework that owns all device
+ * memory through its own pool (and forbids other allocators), a plugin loaded
+ * into such a framework, or code running while a stream is captured into a
+ * CUDA graph (an allocation would break the capture).
+ * Same computation and argument meaning as llama_op_attention_decode, but it
+ * takes the model config instead of a context, plus a cudaStream_t (NULL =
+ * legacy default stream); q, positions, out and kv are the caller's. The
+ * key-split partial sums live in an 8 MiB array inside the library's device
+ * image: one per GPU that loads the library, held until the process exits.
+ * The first call on a device (with that device current) looks up the array's
+ * address and sets kernel attributes; make that first call before any stream
+ * capture. Calls share the array: calls that overlap on the GPU race and must
+ * be serialised by the caller. Shapes whose partial sums would exceed 8 MiB
+ * return LLAMA_ERR_OUT_OF_RANGE and enqueue nothing. bf16 and head_dim 128
+ * only. Range problems in positions or the page table are still skipped on
+ * the device but are not reported (there is no status word). */
+int llama_attention_decode_noalloc(const llama_config* cfg, const void* q,
+                                   const int32_t* positions, int32_t B, int32_t layer,
+                                   const llama_kv* kv, void* out, void* stream);
+
 /* Causal prefill attention (§2.1, §2.3) of fresh prompts: q T [B*T, n_q, d],
  * k, v T [B*T, n_kv, d] (k rotated); row t attends keys 0..t of its own
  * sequence; out T [B*T, n_q d]. */

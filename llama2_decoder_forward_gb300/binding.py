@@ -76,6 +76,8 @@ _SIGS = {
                                        ctypes.POINTER(KV), c_void_p, c_void_p, c_void_p]),
     "llama_op_attention_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32,
                                             ctypes.POINTER(KV), c_void_p]),
+    "llama_attention_decode_noalloc": (c_int32, [ctypes.POINTER(LlamaConfig), c_void_p, c_void_p, c_int32,
+                                                 c_int32, ctypes.POINTER(KV), c_void_p, c_void_p]),
     "llama_op_attention_prefill": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
                                              c_void_p]),
     "llama_op_embed": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p]),
