@@ -282,6 +282,75 @@ def run_gpu(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args):
+    """Prefill of 8 sequences x 512 random ids on the full 7B model (the
+    prefill half of the full-model workload): prefill tokens/s and the tensor
+    throughput of the GEMMs (the dense contraction that bounds prefill)."""
+    import torch
+    import __graft_entry__
+    from llama2_decoder_forward_gb300 import binding, synth
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    __graft_entry__.build()
+    Bp, Tp, cap = 8, 512, 768
+    shape = synth.LLAMA2_7B
+    g = torch.Generator(device=dev)
+    g.manual_seed(1004)
+
+    def rn(*s, std=0.02, mean=0.0):
+        t = torch.randn(*s, generator=g, device=dev, dtype=torch.float32)
+        return t.mul_(std).add_(mean).to(torch.bfloat16)
+
+    H, I, V = shape.hidden, shape.intermediate, shape.vocab
+    w = {"layers": [{"attn_norm": rn(H, std=0.1, mean=1.0), "wqkv": rn(shape.qkv_rows, H), "wo": rn(H, H),
+                     "ffn_norm": rn(H, std=0.1, mean=1.0), "w_gate": rn(I, H), "w_up": rn(I, H),
+                     "w_down": rn(H, I)} for _ in range(shape.n_layers)],
+         "embed": rn(V, H), "final_norm": rn(H, std=0.1, mean=1.0), "lm_head": rn(V, H)}
+    model = binding.Model(shape, w, max_batch=Bp, max_tokens=Bp * Tp, max_seq=cap)
+    kv = binding.KVCache(shape, batch=Bp, capacity=cap)
+    tokens = torch.randint(0, V, (Bp, Tp), generator=g, device=dev, dtype=torch.int32)
+    logits = torch.empty(Bp, V, device=dev)
+    ids = torch.empty(Bp, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        model.prefill(tokens, kv, logits, ids)
+    model.sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(0) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            model.prefill(tokens, kv, logits, ids)
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    model.profile(["gemm", "attn_prefill"])
+    for _ in range(args.steps):
+        model.prefill(tokens, kv, logits, ids)
+    gemm_ms, gemm_n = model.profile_read("gemm")
+    att_ms, att_n = model.profile_read("attn_prefill")
+    model.profile([])
+    model.sync()
+    rows = Bp * Tp
+    layer_params = shape.qkv_rows * H + H * H + 3 * H * I
+    gemm_flops = 2.0 * rows * layer_params * shape.n_layers + 2.0 * Bp * V * H
+    att_flops = 4.0 * shape.n_q_heads * shape.head_dim * (Tp * (Tp + 1) / 2) * Bp * shape.n_layers
+    hbm, tflops, peak_kind = _peaks()
+    g_tf = gemm_flops / (gemm_ms / args.steps * 1e-3) / 1e12
+    line = {"metric": "Llama2-7B prefill tokens/s (bs8, 512 tokens)", "value": rows / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (random-init 7B weights, uniform ids)",
+            "config": {"workload": "llama2-7b prefill, 8 sequences x 512 tokens, 32 layers + LM head on last rows"},
+            "roofline": {"kernel": "gemm_tc_kernel (all prefill projections)", "bound": "tensor",
+                         "achieved": g_tf, "peak": tflops, "unit": "TFLOP/s", "frac": g_tf / tflops,
+                         "peak_source": peak_kind, "traffic": None,
+                         "algorithmic_flops_per_step": gemm_flops, "launches_per_step": gemm_n / args.steps},
+            "kernels": {"gemm_ms_per_step": gemm_ms / args.steps, "attn_prefill_ms_per_step": att_ms / args.steps,
+                        "attn_prefill_tflops": att_flops / (att_ms / args.steps * 1e-3) / 1e12 if att_ms else None},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 class OracleSample:
     """The oracle on a bounded sample: one 7B layer's decode step for the 32
@@ -374,7 +443,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="model", choices=["model", "layer"])
+    ap.add_argument("--workload", default="model", choices=["model", "layer", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     global B_WORKLOAD
@@ -383,6 +452,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_gpu(args)
 
