@@ -30,6 +30,12 @@ design notes):
   * GQA: query head h reads K/V head floor(h / G), G = n_q / n_kv (§1.5).
   * No biases anywhere; embedding and LM head are separate matrices (§2.3).
   * Greedy choice: argmax, lowest index on ties (§2.5).
+  * The KV cache holds K and V in the model's storage type: the pages keep the
+    cache in half precision to halve its memory ("Llama2架构全景解析" §2.1),
+    so a bf16 model's cache stores each value rounded to bf16 (nearest, ties
+    to even) and an fp32 model's cache rounds to fp32; attention reads the
+    stored values. This is the only rounding in the oracle (cache_dtype="f64"
+    turns it off).
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py
 (closed forms, invariants, library routines, brute force); the end-to-end
@@ -57,6 +63,21 @@ def as64(t) -> np.ndarray:
 # --------------------------------------------------------------------------
 # Layer operations
 # --------------------------------------------------------------------------
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 value (8 significant bits), ties to even: with
+    x = m * 2^e, m in [0.5, 1), keep rint(m * 256) / 256 * 2^e."""
+    m, e = np.frexp(np.asarray(x, dtype=f64))
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
+def cache_store(values: np.ndarray, cache_dtype: str) -> np.ndarray:
+    """Values as a KV cache of the given storage type holds them."""
+    if cache_dtype == "bf16":
+        return round_to_bf16(values)
+    if cache_dtype == "f32":
+        return np.asarray(values, dtype=np.float32).astype(f64)
+    return np.asarray(values, dtype=f64)
 
 def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     """RMSNorm over the last axis, each token on its own
@@ -144,14 +165,16 @@ def _split_qkv(qkv, n_q, n_kv, d):
     return q, k, v
 
 
-def layer_decode(x, lw, shape, K, V, positions):
+def layer_decode(x, lw, shape, K, V, positions, cache_dtype=None):
     """Decode step of one layer (§2.3 main computation, §2.4 KV cache).
 
     x: [B, H] hidden input. lw: dict of float64 weights. K, V: per-sequence
-    caches [B, n_kv, S_cap, d] (float64, updated in place: the new token's
-    rotated K and its V are written at slot positions[b]). Returns the
-    layer output [B, H].
+    caches [B, n_kv, S_cap, d] (float64 arrays, updated in place: the new
+    token's rotated K and its V are stored at slot positions[b], as the
+    cache's storage type holds them; cache_dtype defaults to the model's).
+    Returns the layer output [B, H].
     """
+    cdt = shape.dtype if cache_dtype is None else cache_dtype
     n_q, n_kv, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
     pos = np.asarray(positions, dtype=np.int64)
     u = rmsnorm(x, lw["attn_norm"], shape.rms_eps)
@@ -162,22 +185,24 @@ def layer_decode(x, lw, shape, K, V, positions):
     o = np.empty((B, n_q, d), dtype=f64)
     for b in range(B):
         m = int(pos[b])
-        K[b, :, m] = k[b]
-        V[b, :, m] = v[b]
+        K[b, :, m] = cache_store(k[b], cdt)
+        V[b, :, m] = cache_store(v[b], cdt)
         o[b] = gqa_attention(q[b], K[b], V[b], m + 1)
     h = x + linear(o.reshape(B, n_q * d), lw["wo"])
     u2 = rmsnorm(h, lw["ffn_norm"], shape.rms_eps)
     return h + swiglu_ffn(u2, lw["w_gate"], lw["w_up"], lw["w_down"])
 
 
-def layer_prefill(x, lw, shape, K, V, rows=None):
+def layer_prefill(x, lw, shape, K, V, rows=None, cache_dtype=None):
     """Prefill of one layer for a fresh prompt (§2.1): x [B, T, H], token t at
     position t. Writes rotated K and V of every prompt token into K, V
     ([B, n_kv, S_cap, d], in place) and returns the output rows.
 
     rows: optional list of token indices whose outputs are wanted (all by
     default); K/V of every token are still computed, since later rows read them.
+    The cache stores K/V in cache_dtype (default: the model's storage type).
     """
+    cdt = shape.dtype if cache_dtype is None else cache_dtype
     n_q, n_kv, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
     B, T, H = x.shape
     rows = list(range(T)) if rows is None else list(rows)
@@ -192,8 +217,8 @@ def layer_prefill(x, lw, shape, K, V, rows=None):
         k = kv[:, : n_kv * d].reshape(T, n_kv, d)
         v = kv[:, n_kv * d:].reshape(T, n_kv, d)
         k = rope(k, pos_all, shape.rope_theta)
-        K[b, :, :T] = np.transpose(k, (1, 0, 2))
-        V[b, :, :T] = np.transpose(v, (1, 0, 2))
+        K[b, :, :T] = cache_store(np.transpose(k, (1, 0, 2)), cdt)
+        V[b, :, :T] = cache_store(np.transpose(v, (1, 0, 2)), cdt)
         q = linear(u[q_rows], wq).reshape(len(rows), n_q, d)
         q = rope(q, q_rows, shape.rope_theta)
         o = np.empty((len(rows), n_q, d), dtype=f64)
@@ -227,8 +252,9 @@ def greedy(logits: np.ndarray) -> np.ndarray:
 class Model:
     """fp64 copy of a model's weights plus per-sequence caches."""
 
-    def __init__(self, shape, weights: dict, batch: int, capacity: int):
+    def __init__(self, shape, weights: dict, batch: int, capacity: int, cache_dtype=None):
         self.shape = shape
+        self.cache_dtype = cache_dtype
         self.embed_t = as64(weights["embed"]) if weights.get("embed") is not None else None
         self.final_norm = as64(weights["final_norm"]) if weights.get("final_norm") is not None else None
         self.lm = as64(weights["lm_head"]) if weights.get("lm_head") is not None else None
@@ -242,14 +268,15 @@ class Model:
         [B, T, V] (the API keeps only the last row; the oracle keeps all)."""
         h = embed(self.embed_t, tokens)
         for l, lw in enumerate(self.layers):
-            h = layer_prefill(h, lw, self.shape, self.K[l], self.V[l])
+            h = layer_prefill(h, lw, self.shape, self.K[l], self.V[l], cache_dtype=self.cache_dtype)
         return lm_head(h, self.final_norm, self.lm, self.shape.rms_eps)
 
     def decode(self, tokens, positions):
         """One token per sequence at its position; returns logits [B, V]."""
         h = embed(self.embed_t, tokens)
         for l, lw in enumerate(self.layers):
-            h = layer_decode(h, lw, self.shape, self.K[l], self.V[l], positions)
+            h = layer_decode(h, lw, self.shape, self.K[l], self.V[l], positions,
+                             cache_dtype=self.cache_dtype)
         return lm_head(h, self.final_norm, self.lm, self.shape.rms_eps)
 
 
@@ -286,7 +313,7 @@ def gather_paged(pool: np.ndarray, table_row, n_tokens: int, page_size: int) -> 
     return out
 
 
-def layer_decode_paged(x, lw, shape, Kpool, Vpool, table, positions, page_size):
+def layer_decode_paged(x, lw, shape, Kpool, Vpool, table, positions, page_size, cache_dtype=None):
     """Decode step of one layer over a paged cache: gather each sequence's
     pages into a logical contiguous cache, run layer_decode, and write the
     new token's K/V back into its page slot."""
@@ -300,7 +327,7 @@ def layer_decode_paged(x, lw, shape, Kpool, Vpool, table, positions, page_size):
         n = int(pos[b])
         K[b, :, :n] = gather_paged(Kpool, table[b], n, page_size)
         V[b, :, :n] = gather_paged(Vpool, table[b], n, page_size)
-    out = layer_decode(x, lw, shape, K, V, pos)
+    out = layer_decode(x, lw, shape, K, V, pos, cache_dtype=cache_dtype)
     for b in range(B):
         m = int(pos[b])
         page = int(table[b][m // page_size])

@@ -225,7 +225,7 @@ def test_layer_matches_library_composition(nq, nkv):
     x = rng.standard_normal((1, 9, 48))
     K = np.zeros((1, nkv, 16, 8))
     V = np.zeros((1, nkv, 16, 8))
-    ours = O.layer_prefill(x, w, shape, K, V)[0]
+    ours = O.layer_prefill(x, w, shape, K, V, cache_dtype="f64")[0]
     np.testing.assert_allclose(ours, _torch_layer_prefill(x[0], w, shape), rtol=1e-11, atol=1e-12)
 
 
@@ -264,6 +264,9 @@ def test_paged_equals_contiguous():
             Vp[table[b, m // P], :, m % P] = Vc[b, :, m]
     contig = O.layer_decode(x, lw, shape, Kc.copy(), Vc.copy(), lens)
     paged = O.layer_decode_paged(x, lw, shape, Kp, Vp, table, lens, P)
+    np.testing.assert_allclose(paged, contig, rtol=1e-13)
+    contig = O.layer_decode(x, lw, shape, Kc.copy(), Vc.copy(), lens, cache_dtype="f64")
+    paged = O.layer_decode_paged(x, lw, shape, Kp, Vp, table, lens, P, cache_dtype="f64")
     np.testing.assert_allclose(paged, contig, rtol=1e-13)
     for b in range(B):   # new token landed in its page slot
         m = lens[b]
@@ -352,3 +355,35 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant, pin):
         monkeypatch.setattr(O, "rmsnorm", lambda x, g, eps: x / (np.sqrt(np.mean(x * x, -1, keepdims=True)) + eps) * g)
     with pytest.raises(AssertionError):
         globals()[pin]()
+
+
+# ---------------------------------------------------------------- KV cache storage type
+
+def test_round_to_bf16_hand_values_and_library_cast():
+    # ties go to the even significand
+    assert O.round_to_bf16(np.array(1 + 2 ** -8)) == 1.0
+    assert O.round_to_bf16(np.array(1 + 3 * 2 ** -8)) == 1 + 2 ** -6
+    assert O.round_to_bf16(np.array(-(1 + 2 ** -7))) == -(1 + 2 ** -7)   # representable: unchanged
+    assert O.round_to_bf16(np.array(0.0)) == 0.0
+    x = (rng.standard_normal(100000) * 3).astype(np.float32).astype(np.float64)  # exact in fp32
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(O.round_to_bf16(x), ref)
+
+
+def test_cache_holds_storage_type_and_decode_still_equals_prefill():
+    shape = synth.Shape(1, 32, 4, 2, 8, 24, 16, dtype="bf16")
+    lw = {k: O.as64(v) for k, v in synth.layer_weights(shape, 8, 0, std=0.3).items()}
+    x = rng.standard_normal((1, 6, 32))
+    K = np.zeros((1, 2, 8, 8)); V = np.zeros_like(K)
+    full = O.layer_prefill(x, lw, shape, K, V)[0]
+    assert np.array_equal(K[:, :, :6], O.round_to_bf16(K[:, :, :6]))      # bf16 values only
+    assert np.array_equal(V[:, :, :6], O.round_to_bf16(V[:, :, :6]))
+    K2 = np.zeros_like(K); V2 = np.zeros_like(K)
+    O.layer_prefill(x[:, :5], lw, shape, K2, V2)
+    step = O.layer_decode(x[:, 5], lw, shape, K2, V2, [5])
+    np.testing.assert_allclose(step[0], full[5], rtol=1e-12, atol=1e-12)
+    # with fp64 storage the cache keeps the exact projections
+    K3 = np.zeros_like(K); V3 = np.zeros_like(K)
+    O.layer_prefill(x, lw, shape, K3, V3, cache_dtype="f64")
+    assert not np.array_equal(K3[:, :, :6], O.round_to_bf16(K3[:, :, :6]))
+    np.testing.assert_allclose(K[:, :, :6], K3[:, :, :6], rtol=2 ** -8)
