@@ -22,11 +22,11 @@ namespace {
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
-// Up to this many activation rows, bf16 GEMM operands are carried as a pair
-// hi = bf16(v), lo = bf16(v - hi) stacked along N (rows [0,n) and [lo, lo+n),
-// lo = n rounded up to 16): the product keeps ~16 mantissa bits of v. The
-// extra MMA work is free in the bandwidth-bound decode regime.
-constexpr int kSplitMaxRows = 128;
+// bf16 GEMM and attention operands are carried as a pair hi = bf16(v),
+// lo = bf16(v - hi): rows [0, n) and [L, L + n) of the buffer, L = n rounded
+// up to 16. Products use both, keeping about 16 significant bits of v; only
+// the KV cache holds single bf16 values. (The extra MMA work is free while
+// decode is bound by weight bytes; it doubles the prefill's tensor work.)
 inline int round16(int v) { return (v + 15) / 16 * 16; }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -107,16 +107,16 @@ Layout make_layout(const llama_config* c, int sm_count) {
   L.status = take(16);
   L.rope = take((size_t)c->max_seq * (d / 2) * sizeof(float) * 2);
   L.x = take((size_t)R * H * 4);
-  // GEMM operands: room for the hi/lo pair layout of up to 128 rows (256 rows)
-  const size_t RA = std::max(R, 256);
+  // GEMM operands in the hi/lo pair layout: rows [0, R) and [round16(R), ..+R)
+  const size_t RA = 2 * (size_t)round16(std::max(R, 1));
   L.u = take(RA * H * es);
   L.qkv = take((size_t)R * qkv_rows * 4);
-  L.q = take((size_t)R * nq * d * es);
+  L.q = take(RA * nq * d * es);
   L.kside = take((size_t)std::max(c->max_tokens, 1) * nkv * d * es);
   L.vside = take((size_t)std::max(c->max_tokens, 1) * nkv * d * es);
   L.o = take(RA * nq * d * es);
   L.a = take(RA * I * es);
-  L.u_last = take((size_t)std::max(c->max_batch, 256) * H * es);
+  L.u_last = take(2 * (size_t)round16(c->max_batch) * H * es);
   L.logits = take((size_t)c->max_batch * std::max<size_t>(V, 1) * 4);
   L.ids = take((size_t)c->max_batch * 4);
   L.tok = take((size_t)c->max_batch * 4);
@@ -287,7 +287,8 @@ int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, c
     g.n_tile = gemm_n_tile(N, split);
     g.map_w = map2d(c, w, M, K, 128);
     g.map_up = wu ? map2d(c, wu, M, K, 128) : nullptr;
-    g.map_x = map2d(c, x, split ? g.n_tile : N, K, g.n_tile);
+    g.map_x = map2d(c, x, split ? (uint64_t)round16(N) + N : (uint64_t)N, K,
+                    gemm_box_rows(N, split));
     if (!g.map_w || !g.map_x || (wu && !g.map_up)) return LLAMA_ERR_CUDA;
   }
   Prof pf(c, LLAMA_KERNEL_GEMM);
@@ -297,8 +298,9 @@ int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, c
 
 int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
                    const int32_t* positions, int layer, const llama_kv* kv, void* q_out,
-                   void* k_out, void* v_out) {
+                   void* k_out, void* v_out, size_t q_lo = 0) {
   RopeAppendArgs a{};
+  a.q_lo = q_lo;
   a.qkv = qkv;
   a.positions = positions;
   a.rope = c->rope;
@@ -326,9 +328,10 @@ int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
 }
 
 int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B, int layer,
-                   const llama_kv* kv, void* out, size_t out_lo = 0) {
+                   const llama_kv* kv, void* out, size_t out_lo = 0, size_t q_lo = 0) {
   AttnDecodeArgs a{};
   a.out_lo = out_lo;
+  a.q_lo = q_lo;
   a.q = q;
   a.positions = positions;
   a.k_cache = kv->k;
@@ -366,9 +369,10 @@ int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B,
 }
 
 int do_attn_prefill(llama_ctx* c, const void* q, const void* k, const void* v, int B, int T,
-                    void* out, size_t out_lo = 0) {
+                    void* out, size_t out_lo = 0, int q_lo_rows = 0) {
   AttnPrefillArgs a{};
   a.out_lo = out_lo;
+  a.q_lo_rows = q_lo_rows;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -383,7 +387,7 @@ int do_attn_prefill(llama_ctx* c, const void* q, const void* k, const void* v, i
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return LLAMA_ERR_INVALID_ARG;
     trim_maps(c);
     const uint64_t d = c->cfg.head_dim, rows = (uint64_t)B * T;
-    a.map_q = map3d(c, q, d, c->cfg.n_q_heads, rows, 1, 64);
+    a.map_q = map3d(c, q, d, c->cfg.n_q_heads, rows + (uint64_t)q_lo_rows, 1, 64);
     a.map_k = map3d(c, k, d, c->cfg.n_kv_heads, rows, 1, 64);
     a.map_v = map3d(c, v, d, c->cfg.n_kv_heads, rows, 1, 64);
     if (!a.map_q || !a.map_k || !a.map_v) return LLAMA_ERR_CUDA;
@@ -412,18 +416,19 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   void* q = c->at<void>(c->L.q);
   void* o = c->at<void>(c->L.o);
   void* a = c->at<void>(c->L.a);
-  const int lo = (cf.dtype == LLAMA_BF16 && rows <= kSplitMaxRows) ? round16(rows) : 0;
+  const int lo = cf.dtype == LLAMA_BF16 ? round16(rows) : 0;
   const int sp = lo ? 1 : 0;
   TRY(do_rmsnorm(c, x, rows, 1, 0, lw.attn_norm, u, lo));
   TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
   if (prefill) {
     void* ks = c->at<void>(c->L.kside);
     void* vs = c->at<void>(c->L.vside);
-    TRY(do_rope_append(c, qkv, rows, T, nullptr, l, kv, q, ks, vs));
-    TRY(do_attn_prefill(c, q, ks, vs, B, T, o, (size_t)lo * nq * d));
+    TRY(do_rope_append(c, qkv, rows, T, nullptr, l, kv, q, ks, vs, (size_t)lo * nq * d));
+    TRY(do_attn_prefill(c, q, ks, vs, B, T, o, (size_t)lo * nq * d, lo));
   } else {
-    TRY(do_rope_append(c, qkv, rows, 1, positions, l, kv, q, nullptr, nullptr));
-    TRY(do_attn_decode(c, q, positions, B, l, kv, o, (size_t)lo * nq * d));
+    TRY(do_rope_append(c, qkv, rows, 1, positions, l, kv, q, nullptr, nullptr,
+                       (size_t)lo * nq * d));
+    TRY(do_attn_decode(c, q, positions, B, l, kv, o, (size_t)lo * nq * d, (size_t)lo * nq * d));
   }
   TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H, sp));
   TRY(do_rmsnorm(c, x, rows, 1, 0, lw.ffn_norm, u, lo));
@@ -437,7 +442,7 @@ int run_head(llama_ctx* c, const float* x, int B, int stride, int offset, float*
              int32_t* next_ids) {
   const llama_config& cf = c->cfg;
   void* ul = c->at<void>(c->L.u_last);
-  const int lo = (cf.dtype == LLAMA_BF16 && B <= kSplitMaxRows) ? round16(B) : 0;
+  const int lo = cf.dtype == LLAMA_BF16 ? round16(B) : 0;
   TRY(do_rmsnorm(c, x, B, stride, offset, c->final_norm, ul, lo));
   TRY(do_gemm(c, LLAMA_EPI_STORE_F32, ul, B, cf.hidden, c->lm_head, nullptr, cf.vocab, logits,
               cf.vocab, lo ? 1 : 0));
@@ -719,7 +724,7 @@ int llama_op_linear(llama_ctx* c, const void* x, int32_t n_rows, const void* w, 
   if (epilogue < LLAMA_EPI_STORE_F32 || epilogue > LLAMA_EPI_SWIGLU) return LLAMA_ERR_INVALID_ARG;
   if (epilogue == LLAMA_EPI_SWIGLU && !w_up) return LLAMA_ERR_INVALID_ARG;
   if (c->cfg.dtype == LLAMA_BF16 && K % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
-  if (split && (c->cfg.dtype != LLAMA_BF16 || n_rows > kSplitMaxRows)) return LLAMA_ERR_UNSUPPORTED;
+  if (split && c->cfg.dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
   if (n_rows > std::max(c->cfg.max_batch, c->cfg.max_tokens)) return LLAMA_ERR_OUT_OF_RANGE;
   const bool t_out = epilogue == LLAMA_EPI_SWIGLU || epilogue == LLAMA_EPI_STORE_T;
   return do_gemm(c, epilogue, x, n_rows, K, w, epilogue == LLAMA_EPI_SWIGLU ? w_up : nullptr, M,

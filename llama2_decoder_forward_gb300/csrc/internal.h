@@ -52,6 +52,7 @@ struct RopeAppendArgs {
   const int32_t* positions;  // [rows] or null (position = r % rows_per_seq)
   const float2* rope;        // [max_seq, d/2] (cos, sin)
   void* q_out;               // [rows, n_q d]
+  size_t q_lo;               // >0: also store bf16(q - bf16(q)) q_lo elements further
   void* k_out;               // [rows, n_kv d] or null
   void* v_out;               // [rows, n_kv d] or null
   void* k_cache;
@@ -84,23 +85,28 @@ struct GemmCall {
   const CUtensorMap* map_w;   // bf16 path: weights, box {64, 128}, SWIZZLE_128B
   const CUtensorMap* map_up;  // bf16 path, SWIGLU
   const CUtensorMap* map_x;   // bf16 path: activations, box {64, n_tile}
-  int n_tile;                 // bf16 path: MMA N (multiple of 16, <= 256); map_x box rows
-  int split;                  // bf16 path: x rows [0,N) hold bf16(v), rows [lo, lo+N) hold
-                              // bf16(v - bf16(v)), lo = round16(N); both are multiplied
+  int n_tile;                 // bf16 path: MMA N (multiple of 16, <= 256)
+  int split;                  // bf16 path: x rows [0,N) hold bf16(v), rows [L, L+N) hold
+                              // bf16(v - bf16(v)), L = round16(N); both are multiplied
   size_t out_lo;              // bf16 outputs: also store the remainder out_lo elements on
   void* out;
   int ldo;
   uint32_t* status;
   int sm_count;
 };
-// Activation rows one bf16 GEMM tile reads (MMA N) for N logical rows.
+// Activation rows one bf16 GEMM tile reads (MMA N) for N logical rows; the
+// activation descriptor's box holds gemm_box_rows of them.
 int gemm_n_tile(int N, int split);
+inline int gemm_box_rows(int N, int split) {
+  return split ? gemm_n_tile(N, split) / 2 : gemm_n_tile(N, split);
+}
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st);
 cudaError_t gemm_prepare();  // sets kernel attributes once per process
 
 // ------------------------------------------------------------------ attention
 struct AttnDecodeArgs {
   const void* q;             // [B, n_q, d]
+  size_t q_lo;               // >0: q + q_lo holds the bf16 remainders of q (pair operand)
   const int32_t* positions;  // [B]
   const CUtensorMap* map_k;  // bf16: 3D {d, rows per layer, layers}, box {64, 16, 1}, SW128
   const CUtensorMap* map_v;
@@ -125,6 +131,7 @@ int attn_decode_launches(int B, int n_kv, int max_keys, int sm_count, int dtype)
 
 struct AttnPrefillArgs {
   const void* q;             // [B*T, n_q, d]
+  int q_lo_rows;             // >0: row q_lo_rows + r holds the bf16 remainder of q row r
   const void* k;             // [B*T, n_kv, d]
   const void* v;
   const CUtensorMap* map_q;  // bf16: 3D {d, heads, rows}, box {64, 1, 64}, SW128

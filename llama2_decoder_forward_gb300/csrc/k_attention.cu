@@ -41,6 +41,7 @@ constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 256;
 
 struct DecParams {
   const bf16* q;
+  size_t q_lo;
   const int32_t* positions;
   const int32_t* page_table;
   bf16* out;
@@ -159,17 +160,23 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   grid_dep_launch();
   const int G = p.G;
   const int r0 = lane >> 2;
-  uint32_t qa[8][4];
+  // Q fragments (the G heads of the group as rows 0..G-1 of a 16-row tile);
+  // with a pair operand the remainder fragments ride along (two MMAs each)
+  uint32_t qa[8][4], ql[8][4];
   {
     const bf16* qb = p.q + ((size_t)b * p.n_q + (size_t)g * G) * AD;
+    const bf16* qr = qb + p.q_lo;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int col = kk * 16 + 2 * (lane & 3);
-      qa[kk][0] = r0 < G ? *reinterpret_cast<const uint32_t*>(qb + r0 * AD + col) : 0u;
-      qa[kk][1] = r0 + 8 < G ? *reinterpret_cast<const uint32_t*>(qb + (r0 + 8) * AD + col) : 0u;
-      qa[kk][2] = r0 < G ? *reinterpret_cast<const uint32_t*>(qb + r0 * AD + col + 8) : 0u;
-      qa[kk][3] =
-          r0 + 8 < G ? *reinterpret_cast<const uint32_t*>(qb + (r0 + 8) * AD + col + 8) : 0u;
+      const int offs[4] = {r0 * AD + col, (r0 + 8) * AD + col, r0 * AD + col + 8,
+                           (r0 + 8) * AD + col + 8};
+      const bool ok[4] = {r0 < G, r0 + 8 < G, r0 < G, r0 + 8 < G};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qa[kk][i] = ok[i] ? *reinterpret_cast<const uint32_t*>(qb + offs[i]) : 0u;
+        ql[kk][i] = (ok[i] && p.q_lo) ? *reinterpret_cast<const uint32_t*>(qr + offs[i]) : 0u;
+      }
     }
   }
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
@@ -217,6 +224,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         ldsm_x4(kbase + half * HALF_BYTES + swz128(row, chunk), b0, b1, b2, b3);
         mma_bf16_16816(sc[0], qa[kk], b0, b1);
         mma_bf16_16816(sc[1], qa[kk], b2, b3);
+        if (p.q_lo) {
+          mma_bf16_16816(sc[0], ql[kk], b0, b1);
+          mma_bf16_16816(sc[1], ql[kk], b2, b3);
+        }
       }
       // online softmax in base 2
       float mx[2] = {-INFINITY, -INFINITY};
@@ -257,9 +268,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         oacc[dn][2] *= corr[1];
         oacc[dn][3] *= corr[1];
       }
-      uint32_t pa[4] = {pack_bf16(sc[0][0], sc[0][1]), pack_bf16(sc[0][2], sc[0][3]),
-                        pack_bf16(sc[1][0], sc[1][1]), pack_bf16(sc[1][2], sc[1][3])};
-      // O += P V
+      // P as a bf16 pair: hi = bf16(p), lo = bf16(p - hi); O += P_hi V + P_lo V
+      uint32_t pa[4], pl[4];
+      split_pack(sc[0][0], sc[0][1], pa[0], pl[0]);
+      split_pack(sc[0][2], sc[0][3], pa[1], pl[1]);
+      split_pack(sc[1][0], sc[1][1], pa[2], pl[2]);
+      split_pack(sc[1][2], sc[1][3], pa[3], pl[3]);
 #pragma unroll
       for (int dp = 0; dp < 8; ++dp) {
         const int c16 = dp * 2 + (mi >> 1);
@@ -268,6 +282,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         ldsm_x4_t(vbase + (c16 >> 3) * HALF_BYTES + swz128(row, c16 & 7), b0, b1, b2, b3);
         mma_bf16_16816(oacc[2 * dp], pa, b0, b1);
         mma_bf16_16816(oacc[2 * dp + 1], pa, b2, b3);
+        mma_bf16_16816(oacc[2 * dp], pl, b0, b1);
+        mma_bf16_16816(oacc[2 * dp + 1], pl, b2, b3);
       }
     }
     __syncwarp();
@@ -373,9 +389,10 @@ constexpr int PSTAGES = 2;
 constexpr int PRE_THREADS = 160;
 constexpr uint32_t PHALF = PK * 128;       // 64 rows x 64 dims bf16 = 8 KB
 constexpr uint32_t PTILE = 2 * PHALF;      // 64 x 128 = 16 KB
-constexpr size_t PRE_SMEM = PTILE + PSTAGES * 2 * PTILE + 1024 + 256;
+constexpr size_t PRE_SMEM = 2 * PTILE + PSTAGES * 2 * PTILE + 1024 + 256;
 
 struct PreParams {
+  int q_lo_rows;
   bf16* out;
   size_t out_lo;
   uint32_t* status;
@@ -390,9 +407,9 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* qs = smem;
-  uint8_t* kvs = smem + PTILE;  // stage s: K at s*2*PTILE, V at s*2*PTILE + PTILE
-  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + PTILE + PSTAGES * 2 * PTILE);
+  uint8_t* qs = smem;           // Q tile; its bf16 remainders follow at qs + PTILE
+  uint8_t* kvs = smem + 2 * PTILE;  // stage s: K at s*2*PTILE, V at s*2*PTILE + PTILE
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + 2 * PTILE + PSTAGES * 2 * PTILE);
   uint64_t* full = qfull + 1;
   uint64_t* empty = full + PSTAGES;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + PSTAGES);
@@ -423,9 +440,13 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
       tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
-      mbar_arrive_expect_tx(qfull, PTILE);
+      mbar_arrive_expect_tx(qfull, p.q_lo_rows ? 2 * PTILE : PTILE);
       tma_load_3d(qs, &mapQ, qfull, 0, h, rowbase + q0);
       tma_load_3d(qs + PHALF, &mapQ, qfull, 64, h, rowbase + q0);
+      if (p.q_lo_rows) {
+        tma_load_3d(qs + PTILE, &mapQ, qfull, 0, h, p.q_lo_rows + rowbase + q0);
+        tma_load_3d(qs + PTILE + PHALF, &mapQ, qfull, 64, h, p.q_lo_rows + rowbase + q0);
+      }
       int issued = 0;
       bool ok = true;
       for (int kt = 0; kt < n_kt; ++kt) {
@@ -459,15 +480,13 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
   const int myrow0 = q0 + warp * 16 + r0;  // rows myrow0 and myrow0 + 8
   if (!mbar_wait(qfull, 0, p.status)) *abort_flag = 1;
   uint32_t qa[8][4];
-  {
-    const uint32_t qb = smem_u32(qs);
+  const uint32_t qb = smem_u32(qs);
+  const int q_row = warp * 16 + ((mi & 1) << 3) + rr;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int row = warp * 16 + ((mi & 1) << 3) + rr;
-      const int chunk = (kk & 3) * 2 + (mi >> 1);
-      ldsm_x4(qb + (kk >> 2) * PHALF + swz128(row, chunk), qa[kk][0], qa[kk][1], qa[kk][2],
-              qa[kk][3]);
-    }
+  for (int kk = 0; kk < 8; ++kk) {
+    const int chunk = (kk & 3) * 2 + (mi >> 1);
+    ldsm_x4(qb + (kk >> 2) * PHALF + swz128(q_row, chunk), qa[kk][0], qa[kk][1], qa[kk][2],
+            qa[kk][3]);
   }
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   float oacc[16][4];
@@ -489,6 +508,10 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
     for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
+      uint32_t ql[4];  // remainder fragment of Q, read again from shared memory
+      if (p.q_lo_rows)
+        ldsm_x4(qb + PTILE + (kk >> 2) * PHALF + swz128(q_row, (kk & 3) * 2 + (mi >> 1)), ql[0],
+                ql[1], ql[2], ql[3]);
 #pragma unroll
       for (int np = 0; np < 4; ++np) {
         const int row = np * 16 + ((mi >> 1) << 3) + rr;
@@ -497,6 +520,10 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
         ldsm_x4(kb + (kk >> 2) * PHALF + swz128(row, chunk), b0, b1, b2, b3);
         mma_bf16_16816(sc[2 * np], qa[kk], b0, b1);
         mma_bf16_16816(sc[2 * np + 1], qa[kk], b2, b3);
+        if (p.q_lo_rows) {
+          mma_bf16_16816(sc[2 * np], ql, b0, b1);
+          mma_bf16_16816(sc[2 * np + 1], ql, b2, b3);
+        }
       }
     }
     float mx[2] = {-INFINITY, -INFINITY};
@@ -540,10 +567,12 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
     }
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
-      uint32_t pa[4] = {pack_bf16(sc[2 * ks][0], sc[2 * ks][1]),
-                        pack_bf16(sc[2 * ks][2], sc[2 * ks][3]),
-                        pack_bf16(sc[2 * ks + 1][0], sc[2 * ks + 1][1]),
-                        pack_bf16(sc[2 * ks + 1][2], sc[2 * ks + 1][3])};
+      // P as a bf16 pair: O += P_hi V + P_lo V
+      uint32_t pa[4], pl[4];
+      split_pack(sc[2 * ks][0], sc[2 * ks][1], pa[0], pl[0]);
+      split_pack(sc[2 * ks][2], sc[2 * ks][3], pa[1], pl[1]);
+      split_pack(sc[2 * ks + 1][0], sc[2 * ks + 1][1], pa[2], pl[2]);
+      split_pack(sc[2 * ks + 1][2], sc[2 * ks + 1][3], pa[3], pl[3]);
 #pragma unroll
       for (int dp = 0; dp < 8; ++dp) {
         const int c16 = dp * 2 + (mi >> 1);
@@ -552,6 +581,8 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
         ldsm_x4_t(vb + (c16 >> 3) * PHALF + swz128(row, c16 & 7), b0, b1, b2, b3);
         mma_bf16_16816(oacc[2 * dp], pa, b0, b1);
         mma_bf16_16816(oacc[2 * dp + 1], pa, b2, b3);
+        mma_bf16_16816(oacc[2 * dp], pl, b0, b1);
+        mma_bf16_16816(oacc[2 * dp + 1], pl, b2, b3);
       }
     }
     __syncwarp();
@@ -741,6 +772,7 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   }
   DecParams p;
   p.q = (const bf16*)a.q;
+  p.q_lo = a.q_lo;
   p.positions = a.positions;
   p.page_table = a.page_table;
   p.out = (bf16*)a.out;
@@ -788,6 +820,7 @@ cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_
   }
   if (a.head_dim != AD) return cudaErrorInvalidValue;
   PreParams p;
+  p.q_lo_rows = a.q_lo_rows;
   p.out = (bf16*)a.out;
   p.out_lo = a.out_lo;
   p.status = a.status;

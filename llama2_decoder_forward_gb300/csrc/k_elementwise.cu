@@ -152,6 +152,10 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
     T* dst = reinterpret_cast<T*>(a.q_out) + (size_t)r * qw + c;
 #pragma unroll
     for (int k = 0; k < 8; ++k) dst[k] = o[k];
+    if (a.q_lo) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dst[a.q_lo + k] = from_f32<T>(v[k] - to_f32(o[k]));
+    }
     return;
   }
   const int ck = is_v ? c - qw - kw : c - qw;  // column within the K (or V) block

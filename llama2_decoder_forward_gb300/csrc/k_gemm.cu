@@ -39,8 +39,9 @@ struct TcParams {
   int n_tile, num_kb, splits, n_tiles;
   int stages;
   uint32_t tmem_cols;
-  int lo;      // >0: activation rows [lo, lo + N) hold the bf16 remainders of rows [0, N)
-  int ncol;    // output columns one tile produces (n_tile, or lo in the hi/lo mode)
+  int lo;      // >0 (hi/lo mode): TMEM column offset of the remainder product (= ncol)
+  int lo_rows; // hi/lo mode: activation row r's remainder is row lo_rows + r
+  int ncol;    // output columns one tile produces (n_tile, or n_tile / 2 in the hi/lo mode)
   size_t out_lo;  // >0: bf16 outputs also write their remainder out_lo elements further
   void* out;
   int ldo;
@@ -133,11 +134,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tma_load_2d_hint(st, &tmW, &full[i], (kb0 + i) * BK, tile_m * BM, pol_w);
         if (DUAL) tma_load_2d_hint(st + a_bytes, &tmU, &full[i], (kb0 + i) * BK, tile_m * BM, pol_w);
       }
+      // activation tile: one box of n_tile rows, or in the hi/lo mode the hi
+      // rows and the remainder rows of the same ncol activations back to back
+      auto load_x = [&](uint8_t* dst, uint64_t* bar, int kb) {
+        if (p.lo) {
+          tma_load_2d(dst, &tmX, bar, kb * BK, tile_n * p.ncol);
+          tma_load_2d(dst + (uint32_t)p.ncol * BK * 2, &tmX, bar, kb * BK,
+                      p.lo_rows + tile_n * p.ncol);
+        } else {
+          tma_load_2d(dst, &tmX, bar, kb * BK, tile_n * p.n_tile);
+        }
+      };
       grid_dep_wait();
       grid_dep_launch();
       for (int i = 0; i < npre; ++i)
-        tma_load_2d(smem + (size_t)i * stage_bytes + b_off, &tmX, &full[i], (kb0 + i) * BK,
-                    tile_n * p.n_tile);
+        load_x(smem + (size_t)i * stage_bytes + b_off, &full[i], kb0 + i);
       int s = npre % S, issued = npre;
       uint32_t ph = npre == S ? 1u : 0u;
       bool ok = true;
@@ -151,7 +162,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         mbar_arrive_expect_tx(&full[s], stage_bytes);
         tma_load_2d_hint(st, &tmW, &full[s], kb * BK, tile_m * BM, pol_w);
         if (DUAL) tma_load_2d_hint(st + a_bytes, &tmU, &full[s], kb * BK, tile_m * BM, pol_w);
-        tma_load_2d(st + b_off, &tmX, &full[s], kb * BK, tile_n * p.n_tile);
+        load_x(st + b_off, &full[s], kb);
         ++issued;
         if (++s == S) {
           s = 0;
@@ -320,7 +331,7 @@ __global__ void gemm_f32_kernel(const float* __restrict__ x, const float* __rest
 
 // ------------------------------------------------------------------ planning
 struct Plan {
-  int n_tile, ncol, lo, stages, splits, m_tiles, n_tiles, num_kb, ctas_per_sm;
+  int n_tile, ncol, lo, lo_rows, stages, splits, m_tiles, n_tiles, num_kb, ctas_per_sm;
   size_t smem;
   uint32_t tmem_cols;
 };
@@ -328,7 +339,7 @@ struct Plan {
 static int round16(int v) { return (v + 15) / 16 * 16; }
 
 int gemm_n_tile(int N, int split) {
-  if (split) return 2 * round16(N);
+  if (split) return 2 * std::min(128, round16(N));
   return N >= 256 ? 256 : std::max(16, round16(N));
 }
 
@@ -337,6 +348,7 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count) {
   pl.n_tile = gemm_n_tile(N, split);
   pl.lo = split ? pl.n_tile / 2 : 0;
   pl.ncol = split ? pl.lo : pl.n_tile;
+  pl.lo_rows = split ? round16(N) : 0;
   const int width = pl.n_tile * (dual ? 2 : 1);  // accumulator columns
   pl.tmem_cols = 32;
   while ((int)pl.tmem_cols < width) pl.tmem_cols <<= 1;
@@ -348,7 +360,7 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count) {
   pl.smem = (size_t)pl.stages * stage_bytes + 1024 + 256;
   pl.ctas_per_sm = std::max(1, std::min(two ? 2 : 1, (int)(233472 / (pl.smem + 1024))));
   pl.m_tiles = (M + BM - 1) / BM;
-  pl.n_tiles = split ? 1 : (N + pl.n_tile - 1) / pl.n_tile;
+  pl.n_tiles = (N + pl.ncol - 1) / pl.ncol;
   pl.num_kb = (K + BK - 1) / BK;
   const int tiles = pl.m_tiles * pl.n_tiles;
   const int slots = std::max(1, sm_count) * pl.ctas_per_sm;
@@ -401,6 +413,7 @@ static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st)
   p.stages = pl.stages;
   p.tmem_cols = pl.tmem_cols;
   p.lo = pl.lo;
+  p.lo_rows = pl.lo_rows;
   p.ncol = pl.ncol;
   p.out_lo = g.out_lo;
   p.out = g.out;
