@@ -37,7 +37,7 @@ constexpr int DEC_THREADS = 160;                       // 4 consumer warps + pro
 constexpr uint32_t HALF_BYTES = SUBK * 128;            // 16 rows x 64 dims x bf16
 constexpr uint32_t SUB_BYTES = 2 * HALF_BYTES;         // 16 rows x 128 dims
 constexpr uint32_t DSTAGE_BYTES = 4 * SUB_BYTES * 2;   // 4 sub-tiles, K and V: 32 KB
-constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 256;
+constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 64 + 2 * 128 * 4;  // + barriers, Q (fp32)
 
 struct DecParams {
   const bf16* q;
@@ -77,87 +77,14 @@ __device__ __forceinline__ int kv_row(const DecParams& p, int b, int g, int k0) 
 
 __device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-__global__ void __launch_bounds__(DEC_THREADS, 2)
-    attn_decode_kernel(const __grid_constant__ CUtensorMap mapK,
-                       const __grid_constant__ CUtensorMap mapV, DecParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + DSTAGES * DSTAGE_BYTES);
-  uint64_t* empty = full + DSTAGES;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + DSTAGES);
-
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
-  // positions and the page table are caller inputs, complete before the step
-  const int n_keys = decode_keys(p.positions[b], cap_keys);
-  const int kbeg = split * p.keys_per_split;
-  const int kend = min(n_keys, kbeg + p.keys_per_split);
-  if (kbeg >= kend) {  // this split has no keys (the merge skips it)
-    grid_dep_wait();
-    return;
-  }
-  const int n_sub = (kend - kbeg + SUBK - 1) / SUBK;
-  const int n_tiles = (n_sub + 3) / 4;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < DSTAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == 4) {  // ------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&mapK);
-      tma_prefetch_desc(&mapV);
-      int issued = 0;
-      bool ok = true, waited = false;
-      for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % DSTAGES;
-        const uint32_t ph = (t / DSTAGES) & 1;
-        // Keys below the new token were cached by earlier steps and can be
-        // fetched while the previous kernel finishes; the tile holding the
-        // new token's K/V (written by the RoPE/append kernel) waits for it.
-        if (!waited && kbeg + (t + 1) * DTILE >= n_keys) {
-          grid_dep_wait();
-          grid_dep_launch();
-          waited = true;
-        }
-        if (!mbar_wait(&empty[s], ph ^ 1, p.status)) {
-          ok = false;
-          *abort_flag = 1;
-          break;
-        }
-        const int nsub = min(4, n_sub - 4 * t);
-        uint8_t* st = smem + s * DSTAGE_BYTES;
-        mbar_arrive_expect_tx(&full[s], nsub * SUB_BYTES * 2);
-        for (int j = 0; j < nsub; ++j) {
-          const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
-          uint8_t* kd = st + j * SUB_BYTES;
-          uint8_t* vd = st + 4 * SUB_BYTES + j * SUB_BYTES;
-          tma_load_3d(kd, &mapK, &full[s], 0, row, p.layer);
-          tma_load_3d(kd + HALF_BYTES, &mapK, &full[s], 64, row, p.layer);
-          tma_load_3d(vd, &mapV, &full[s], 0, row, p.layer);
-          tma_load_3d(vd + HALF_BYTES, &mapV, &full[s], 64, row, p.layer);
-        }
-        ++issued;
-      }
-      if (!ok) {
-        for (int t = issued - 1; t >= 0 && t >= issued - DSTAGES; --t)
-          mbar_wait(&full[t % DSTAGES], (t / DSTAGES) & 1, p.status);
-      }
-    }
-    return;
-  }
-
-  // ---------------------------------------------------------------- consumers
-  grid_dep_wait();  // q comes from the RoPE/append kernel
-  grid_dep_launch();
+// Consumer warps, tensor-core variant: the G query heads of the group are the
+// M rows of mma.sync (zero-padded to 16); Q and P are carried as bf16 pairs.
+// Leaves this warp's running max, sum and O in shared memory for the merge.
+__device__ __forceinline__ void decode_consume_mma(const DecParams& p, uint8_t* smem,
+                                                   uint64_t* full, uint64_t* empty,
+                                                   volatile uint32_t* abort_flag, int b, int g,
+                                                   int kbeg, int kend, int n_sub, int n_tiles,
+                                                   int warp, int lane) {
   const int G = p.G;
   const int r0 = lane >> 2;
   // Q fragments (the G heads of the group as rows 0..G-1 of a 16-row tile);
@@ -290,7 +217,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     if (lane == 0) mbar_arrive(&empty[s]);
   }
 
-  // ---------------------------------------------------------------- merge the 4 warps
+  // ---- this warp's (max, sum, O) to shared memory for the 4-warp merge
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
@@ -314,6 +241,244 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     sl[warp * 16 + r0] = lrow[0];
     sl[warp * 16 + r0 + 8] = lrow[1];
   }
+}
+
+// Consumer warps, CUDA-core variant for groups of at most kSimtMaxG query
+// heads (MHA): everything in fp32 (Q is the sum of its bf16 pair). Lane
+// (key = lane & 15, half = lane >> 4) takes the dot product of one key with
+// 64 dims of Q; lane l then owns output dims 4l..4l+3 for P V. Same shared
+// memory output as the tensor-core variant.
+constexpr int kSimtMaxG = 2;
+__device__ __forceinline__ void decode_consume_simt(const DecParams& p, uint8_t* smem,
+                                                    uint64_t* full, uint64_t* empty,
+                                                    volatile uint32_t* abort_flag, int b, int g,
+                                                    int kbeg, int kend, int n_sub, int n_tiles,
+                                                    int warp, int lane) {
+  const int G = p.G;
+  float* qsm = reinterpret_cast<float*>(smem + DSTAGES * DSTAGE_BYTES + 64);  // [G][128]
+  {
+    const bf16* qb = p.q + ((size_t)b * p.n_q + (size_t)g * G) * AD;
+    for (int i = threadIdx.x; i < G * AD; i += 128)
+      qsm[i] = __bfloat162float(qb[i]) + (p.q_lo ? __bfloat162float(qb[i + p.q_lo]) : 0.f);
+  }
+  cons_bar();
+  const int key = lane & 15, half = lane >> 4;
+  float m_run[kSimtMaxG], l_run[kSimtMaxG], o[kSimtMaxG][4];
+#pragma unroll
+  for (int r = 0; r < kSimtMaxG; ++r) {
+    m_run[r] = -INFINITY;
+    l_run[r] = 0.f;
+    o[r][0] = o[r][1] = o[r][2] = o[r][3] = 0.f;
+  }
+  for (int t = 0; t < n_tiles; ++t) {
+    const int s = t % DSTAGES;
+    const uint32_t ph = (t / DSTAGES) & 1;
+    if (*abort_flag) break;
+    if (!mbar_wait(&full[s], ph, p.status)) {
+      *abort_flag = 1;
+      break;
+    }
+    const int sub = 4 * t + warp;
+    if (sub < n_sub) {
+      const uint8_t* st = smem + s * DSTAGE_BYTES;
+      const int k0 = kbeg + sub * SUBK;
+      const int nvalid = min(SUBK, kend - k0);
+      // s_r = q_r . k over this lane's 64 dims, then the other half's
+      const uint8_t* krow = st + warp * SUB_BYTES + half * HALF_BYTES;
+      float sc[kSimtMaxG] = {0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(krow + swz128(key, c));
+        const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+        float kf[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          kf[2 * i] = __uint_as_float(w[i] << 16);
+          kf[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+#pragma unroll
+        for (int r = 0; r < kSimtMaxG; ++r) {
+          if (r < G) {
+            const float* qv = qsm + r * AD + half * 64 + c * 8;
+            const float4 qa = *reinterpret_cast<const float4*>(qv);
+            const float4 qc = *reinterpret_cast<const float4*>(qv + 4);
+            sc[r] = fmaf(qa.x, kf[0], sc[r]);
+            sc[r] = fmaf(qa.y, kf[1], sc[r]);
+            sc[r] = fmaf(qa.z, kf[2], sc[r]);
+            sc[r] = fmaf(qa.w, kf[3], sc[r]);
+            sc[r] = fmaf(qc.x, kf[4], sc[r]);
+            sc[r] = fmaf(qc.y, kf[5], sc[r]);
+            sc[r] = fmaf(qc.z, kf[6], sc[r]);
+            sc[r] = fmaf(qc.w, kf[7], sc[r]);
+          }
+        }
+      }
+      float pk[kSimtMaxG];
+#pragma unroll
+      for (int r = 0; r < kSimtMaxG; ++r) {
+        if (r < G) {
+          float v = sc[r] + __shfl_xor_sync(0xffffffffu, sc[r], 16);
+          v = key < nvalid ? v * p.scale_log2 : -INFINITY;
+          float mx = v;
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          const float mnew = fmaxf(m_run[r], mx);
+          const float corr = mnew == -INFINITY ? 1.f : exp2f(m_run[r] - mnew);
+          m_run[r] = mnew;
+          pk[r] = mnew == -INFINITY ? 0.f : exp2f(v - mnew);
+          l_run[r] = l_run[r] * corr + (half == 0 ? pk[r] : 0.f);
+          o[r][0] *= corr;
+          o[r][1] *= corr;
+          o[r][2] *= corr;
+          o[r][3] *= corr;
+        } else {
+          pk[r] = 0.f;
+        }
+      }
+      // O += P V: lane owns dims 4*lane .. 4*lane+3 (box lane >> 4)
+      const uint8_t* vbox = st + 4 * SUB_BYTES + warp * SUB_BYTES + (lane >> 4) * HALF_BYTES;
+      const uint32_t vchunk = (lane & 15) >> 1, vbyte = (lane & 1) * 8;
+      for (int j = 0; j < nvalid; ++j) {
+        const uint2 vv = *reinterpret_cast<const uint2*>(vbox + swz128(j, vchunk) + vbyte);
+        const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xffff0000u);
+        const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xffff0000u);
+#pragma unroll
+        for (int r = 0; r < kSimtMaxG; ++r) {
+          if (r < G) {
+            const float pj = __shfl_sync(0xffffffffu, pk[r], j);
+            o[r][0] = fmaf(pj, v0, o[r][0]);
+            o[r][1] = fmaf(pj, v1, o[r][1]);
+            o[r][2] = fmaf(pj, v2, o[r][2]);
+            o[r][3] = fmaf(pj, v3, o[r][3]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  // ---- this warp's (max, sum, O) to shared memory for the 4-warp merge
+  float* so = reinterpret_cast<float*>(smem);  // [4][16][128]
+  float* sm = so + 4 * 16 * AD;                // [4][16]
+  float* sl = sm + 64;                         // [4][16]
+#pragma unroll
+  for (int r = 0; r < kSimtMaxG; ++r) {
+    float l = l_run[r];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    l_run[r] = l;
+  }
+  cons_bar();  // every consumer is done with the stage buffers
+#pragma unroll
+  for (int r = 0; r < kSimtMaxG; ++r) {
+    if (r < G) {
+      *reinterpret_cast<float4*>(so + (warp * 16 + r) * AD + 4 * lane) =
+          make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
+      if (lane == 0) {
+        sm[warp * 16 + r] = m_run[r];
+        sl[warp * 16 + r] = l_run[r];
+      }
+    }
+  }
+}
+
+template <bool SIMT>
+__global__ void __launch_bounds__(DEC_THREADS, 2)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap mapK,
+                       const __grid_constant__ CUtensorMap mapV, DecParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + DSTAGES * DSTAGE_BYTES);
+  uint64_t* empty = full + DSTAGES;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + DSTAGES);
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
+  // positions and the page table are caller inputs, complete before the step
+  const int n_keys = decode_keys(p.positions[b], cap_keys);
+  const int kbeg = split * p.keys_per_split;
+  const int kend = min(n_keys, kbeg + p.keys_per_split);
+  if (kbeg >= kend) {  // this split has no keys (the merge skips it)
+    grid_dep_wait();
+    return;
+  }
+  const int n_sub = (kend - kbeg + SUBK - 1) / SUBK;
+  const int n_tiles = (n_sub + 3) / 4;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < DSTAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 4) {  // ------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      int issued = 0;
+      bool ok = true, waited = false;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % DSTAGES;
+        const uint32_t ph = (t / DSTAGES) & 1;
+        // Keys below the new token were cached by earlier steps and can be
+        // fetched while the previous kernel finishes; the tile holding the
+        // new token's K/V (written by the RoPE/append kernel) waits for it.
+        if (!waited && kbeg + (t + 1) * DTILE >= n_keys) {
+          grid_dep_wait();
+          grid_dep_launch();
+          waited = true;
+        }
+        if (!mbar_wait(&empty[s], ph ^ 1, p.status)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        const int nsub = min(4, n_sub - 4 * t);
+        uint8_t* st = smem + s * DSTAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], nsub * SUB_BYTES * 2);
+        for (int j = 0; j < nsub; ++j) {
+          const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
+          uint8_t* kd = st + j * SUB_BYTES;
+          uint8_t* vd = st + 4 * SUB_BYTES + j * SUB_BYTES;
+          tma_load_3d(kd, &mapK, &full[s], 0, row, p.layer);
+          tma_load_3d(kd + HALF_BYTES, &mapK, &full[s], 64, row, p.layer);
+          tma_load_3d(vd, &mapV, &full[s], 0, row, p.layer);
+          tma_load_3d(vd + HALF_BYTES, &mapV, &full[s], 64, row, p.layer);
+        }
+        ++issued;
+      }
+      if (!ok) {
+        for (int t = issued - 1; t >= 0 && t >= issued - DSTAGES; --t)
+          mbar_wait(&full[t % DSTAGES], (t / DSTAGES) & 1, p.status);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  grid_dep_wait();  // q comes from the RoPE/append kernel
+  grid_dep_launch();
+  if (SIMT)
+    decode_consume_simt(p, smem, full, empty, abort_flag, b, g, kbeg, kend, n_sub, n_tiles, warp,
+                        lane);
+  else
+    decode_consume_mma(p, smem, full, empty, abort_flag, b, g, kbeg, kend, n_sub, n_tiles, warp,
+                       lane);
+  const int G = p.G;
+  float* so = reinterpret_cast<float*>(smem);  // [4][16][128]
+  float* sm = so + 4 * 16 * AD;                // [4][16]
+  float* sl = sm + 64;                         // [4][16]
   cons_bar();
   if (*abort_flag) return;
   const int t = threadIdx.x;  // output dim
@@ -741,8 +906,11 @@ size_t attn_decode_partial_bytes(int B, int n_q, int head_dim, int max_keys, int
 }
 
 cudaError_t attn_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel,
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEC_SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)DEC_SMEM);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)PRE_SMEM);
@@ -791,8 +959,11 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.splits = splits;
   p.keys_per_split = kps;
   p.scale_log2 = kLog2e / sqrtf((float)AD);
-  cudaError_t e = launch_k(attn_decode_kernel, dim3(splits, a.n_kv, a.B), dim3(DEC_THREADS),
-                           DEC_SMEM, st, 0, *a.map_k, *a.map_v, p);
+  const bool simt = p.G <= kSimtMaxG;
+  cudaError_t e = simt ? launch_k(attn_decode_kernel<true>, dim3(splits, a.n_kv, a.B),
+                                  dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, p)
+                       : launch_k(attn_decode_kernel<false>, dim3(splits, a.n_kv, a.B),
+                                  dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, p);
   if (e != cudaSuccess || splits == 1) return e;
   const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
   return launch_k(attn_combine_kernel, dim3(a.B * a.n_q), dim3(AD), 0, st, 0,

@@ -246,7 +246,7 @@ def _decode_case(nq, nkv, positions, paged, seed, cap=None):
         assert_close(out[b].view(nq, d), ref, BF16_TOL, "decode attention b=%d n=%d" % (b, n))
 
 
-@pytest.mark.parametrize("nq,nkv", [(32, 32), (32, 8), (16, 4)])
+@pytest.mark.parametrize("nq,nkv", [(32, 32), (32, 8), (16, 4), (16, 8)])
 @pytest.mark.parametrize("paged", [False, True])
 def test_attention_decode_bf16(nq, nkv, paged):
     positions = [0, 14, 15, 16, 17, 63, 64, 65, 1024, 2047, 4095, 333]
