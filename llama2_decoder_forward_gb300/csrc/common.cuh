@@ -188,6 +188,13 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// Transpose an 8x8 b16 matrix held one 32-bit register per thread in the
+// MMA fragment layout (thread l: row l/4, columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
 // Two floats as a bf16 pair each: hi = bf16(v), rem = bf16(v - hi), packed
 // two lanes per 32-bit register (the MMA A-fragment layout).
 __device__ __forceinline__ void split_pack(float v0, float v1, uint32_t& hi, uint32_t& rem) {

@@ -37,7 +37,7 @@ constexpr int DEC_THREADS = 160;                       // 4 consumer warps + pro
 constexpr uint32_t HALF_BYTES = SUBK * 128;            // 16 rows x 64 dims x bf16
 constexpr uint32_t SUB_BYTES = 2 * HALF_BYTES;         // 16 rows x 128 dims
 constexpr uint32_t DSTAGE_BYTES = 4 * SUB_BYTES * 2;   // 4 sub-tiles, K and V: 32 KB
-constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 64 + 2 * 128 * 4;  // + barriers, Q (fp32)
+constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 256;
 
 struct DecParams {
   const bf16* q;
@@ -243,33 +243,40 @@ __device__ __forceinline__ void decode_consume_mma(const DecParams& p, uint8_t* 
   }
 }
 
-// Consumer warps, CUDA-core variant for groups of at most kSimtMaxG query
-// heads (MHA): everything in fp32 (Q is the sum of its bf16 pair). Lane
-// (key = lane & 15, half = lane >> 4) takes the dot product of one key with
-// 64 dims of Q; lane l then owns output dims 4l..4l+3 for P V. Same shared
-// memory output as the tensor-core variant.
-constexpr int kSimtMaxG = 2;
-__device__ __forceinline__ void decode_consume_simt(const DecParams& p, uint8_t* smem,
-                                                    uint64_t* full, uint64_t* empty,
-                                                    volatile uint32_t* abort_flag, int b, int g,
-                                                    int kbeg, int kend, int n_sub, int n_tiles,
-                                                    int warp, int lane) {
+// Consumer warps, key-major tensor-core variant for groups of at most 8 query
+// heads: S^T = K Q^T puts the 16 keys of a sub-tile on the M rows and the
+// group's heads on N = 8, and O^T = V^T P^T puts 16 head dims on M, so MHA
+// wastes no MMA rows. Q and P are bf16 pairs (two MMAs each); P^T reaches
+// operand layout through movmatrix transposes. Lane l tracks heads 2(l%4) and
+// 2(l%4)+1. Same shared-memory output as the other variant.
+constexpr int kKeyMajorMaxG = 8;
+__device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint8_t* smem,
+                                                        uint64_t* full, uint64_t* empty,
+                                                        volatile uint32_t* abort_flag, int b,
+                                                        int g, int kbeg, int kend, int n_sub,
+                                                        int n_tiles, int warp, int lane) {
   const int G = p.G;
-  float* qsm = reinterpret_cast<float*>(smem + DSTAGES * DSTAGE_BYTES + 64);  // [G][128]
+  const int hq = lane >> 2;             // head of this lane's Q^T columns (B operand)
+  const int hc = 2 * (lane & 3);        // first of the two heads this lane accumulates
+  // Q^T fragments: b0/b1 = Q[head lane/4][16 kk + 2(l%4) + {0,1} (+8)]
+  uint32_t qh[8][2], ql[8][2];
   {
-    const bf16* qb = p.q + ((size_t)b * p.n_q + (size_t)g * G) * AD;
-    for (int i = threadIdx.x; i < G * AD; i += 128)
-      qsm[i] = __bfloat162float(qb[i]) + (p.q_lo ? __bfloat162float(qb[i + p.q_lo]) : 0.f);
-  }
-  cons_bar();
-  const int key = lane & 15, half = lane >> 4;
-  float m_run[kSimtMaxG], l_run[kSimtMaxG], o[kSimtMaxG][4];
+    const bf16* qb = p.q + ((size_t)b * p.n_q + (size_t)g * G + hq) * AD;
 #pragma unroll
-  for (int r = 0; r < kSimtMaxG; ++r) {
-    m_run[r] = -INFINITY;
-    l_run[r] = 0.f;
-    o[r][0] = o[r][1] = o[r][2] = o[r][3] = 0.f;
+    for (int kk = 0; kk < 8; ++kk) {
+      const int col = kk * 16 + 2 * (lane & 3);
+      const bool ok = hq < G;
+      qh[kk][0] = ok ? *reinterpret_cast<const uint32_t*>(qb + col) : 0u;
+      qh[kk][1] = ok ? *reinterpret_cast<const uint32_t*>(qb + col + 8) : 0u;
+      ql[kk][0] = (ok && p.q_lo) ? *reinterpret_cast<const uint32_t*>(qb + p.q_lo + col) : 0u;
+      ql[kk][1] = (ok && p.q_lo) ? *reinterpret_cast<const uint32_t*>(qb + p.q_lo + col + 8) : 0u;
+    }
   }
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float oacc[8][4];  // O^T tile dt: rows d = 16 dt + l/4 (+8), columns heads hc, hc+1
+#pragma unroll
+  for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  const int mi = lane >> 3, rr = lane & 7;
   for (int t = 0; t < n_tiles; ++t) {
     const int s = t % DSTAGES;
     const uint32_t ph = (t / DSTAGES) & 1;
@@ -280,114 +287,117 @@ __device__ __forceinline__ void decode_consume_simt(const DecParams& p, uint8_t*
     }
     const int sub = 4 * t + warp;
     if (sub < n_sub) {
-      const uint8_t* st = smem + s * DSTAGE_BYTES;
+      uint8_t* st = smem + s * DSTAGE_BYTES;
       const int k0 = kbeg + sub * SUBK;
       const int nvalid = min(SUBK, kend - k0);
-      // s_r = q_r . k over this lane's 64 dims, then the other half's
-      const uint8_t* krow = st + warp * SUB_BYTES + half * HALF_BYTES;
-      float sc[kSimtMaxG] = {0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 kv = *reinterpret_cast<const uint4*>(krow + swz128(key, c));
-        const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
-        float kf[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          kf[2 * i] = __uint_as_float(w[i] << 16);
-          kf[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      const uint32_t kbase = smem_u32(st + warp * SUB_BYTES);
+      uint8_t* vptr = st + 4 * SUB_BYTES + warp * SUB_BYTES;
+      if (nvalid < SUBK) {  // rows past the last key may hold anything: zero them
+        const int nz = (SUBK - nvalid) * 16;
+        for (int i = lane; i < nz; i += 32) {
+          const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
+          *reinterpret_cast<uint4*>(vptr + half * HALF_BYTES + row * 128 + chunk * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
         }
-#pragma unroll
-        for (int r = 0; r < kSimtMaxG; ++r) {
-          if (r < G) {
-            const float* qv = qsm + r * AD + half * 64 + c * 8;
-            const float4 qa = *reinterpret_cast<const float4*>(qv);
-            const float4 qc = *reinterpret_cast<const float4*>(qv + 4);
-            sc[r] = fmaf(qa.x, kf[0], sc[r]);
-            sc[r] = fmaf(qa.y, kf[1], sc[r]);
-            sc[r] = fmaf(qa.z, kf[2], sc[r]);
-            sc[r] = fmaf(qa.w, kf[3], sc[r]);
-            sc[r] = fmaf(qc.x, kf[4], sc[r]);
-            sc[r] = fmaf(qc.y, kf[5], sc[r]);
-            sc[r] = fmaf(qc.z, kf[6], sc[r]);
-            sc[r] = fmaf(qc.w, kf[7], sc[r]);
-          }
-        }
+        fence_proxy_async_smem();
+        __syncwarp();
       }
-      float pk[kSimtMaxG];
+      const uint32_t vbase = smem_u32(vptr);
+      // S^T (16 keys x 8 heads): hi and lo parts of Q in separate chains
+      float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int r = 0; r < kSimtMaxG; ++r) {
-        if (r < G) {
-          float v = sc[r] + __shfl_xor_sync(0xffffffffu, sc[r], 16);
-          v = key < nvalid ? v * p.scale_log2 : -INFINITY;
-          float mx = v;
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          const float mnew = fmaxf(m_run[r], mx);
-          const float corr = mnew == -INFINITY ? 1.f : exp2f(m_run[r] - mnew);
-          m_run[r] = mnew;
-          pk[r] = mnew == -INFINITY ? 0.f : exp2f(v - mnew);
-          l_run[r] = l_run[r] * corr + (half == 0 ? pk[r] : 0.f);
-          o[r][0] *= corr;
-          o[r][1] *= corr;
-          o[r][2] *= corr;
-          o[r][3] *= corr;
-        } else {
-          pk[r] = 0.f;
-        }
+      for (int kk = 0; kk < 8; ++kk) {
+        // A = K[16 keys][16 dims]: matrices (keys 0-7, c), (keys 8-15, c), (0-7, c+1), (8-15, c+1)
+        const int row = ((mi & 1) << 3) + rr;
+        const int chunk = (kk & 3) * 2 + (mi >> 1);
+        uint32_t a[4];
+        ldsm_x4(kbase + (kk >> 2) * HALF_BYTES + swz128(row, chunk), a[0], a[1], a[2], a[3]);
+        mma_bf16_16816(sh, a, qh[kk][0], qh[kk][1]);
+        if (p.q_lo) mma_bf16_16816(sl, a, ql[kk][0], ql[kk][1]);
       }
-      // O += P V: lane owns dims 4*lane .. 4*lane+3 (box lane >> 4)
-      const uint8_t* vbox = st + 4 * SUB_BYTES + warp * SUB_BYTES + (lane >> 4) * HALF_BYTES;
-      const uint32_t vchunk = (lane & 15) >> 1, vbyte = (lane & 1) * 8;
-      for (int j = 0; j < nvalid; ++j) {
-        const uint2 vv = *reinterpret_cast<const uint2*>(vbox + swz128(j, vchunk) + vbyte);
-        const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xffff0000u);
-        const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xffff0000u);
+      // lane holds S^T[key l/4 (+8)][heads hc, hc+1]; online softmax per head
+      float sv[4];
 #pragma unroll
-        for (int r = 0; r < kSimtMaxG; ++r) {
-          if (r < G) {
-            const float pj = __shfl_sync(0xffffffffu, pk[r], j);
-            o[r][0] = fmaf(pj, v0, o[r][0]);
-            o[r][1] = fmaf(pj, v1, o[r][1]);
-            o[r][2] = fmaf(pj, v2, o[r][2]);
-            o[r][3] = fmaf(pj, v3, o[r][3]);
-          }
-        }
+      for (int i = 0; i < 4; ++i) {
+        const int key = (lane >> 2) + (i >= 2 ? 8 : 0);
+        sv[i] = key < nvalid ? (sh[i] + sl[i]) * p.scale_log2 : -INFINITY;
+      }
+      float corr[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(sv[j], sv[j + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(m_run[j], mx);
+        corr[j] = mnew == -INFINITY ? 1.f : exp2f(m_run[j] - mnew);
+        m_run[j] = mnew;
+      }
+      float pv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = i & 1;
+        pv[i] = m_run[j] == -INFINITY ? 0.f : exp2f(sv[i] - m_run[j]);
+      }
+      l_run[0] = l_run[0] * corr[0] + pv[0] + pv[2];
+      l_run[1] = l_run[1] * corr[1] + pv[1] + pv[3];
+#pragma unroll
+      for (int dt = 0; dt < 8; ++dt) {
+        oacc[dt][0] *= corr[0];
+        oacc[dt][1] *= corr[1];
+        oacc[dt][2] *= corr[0];
+        oacc[dt][3] *= corr[1];
+      }
+      // P^T as the B operand (16 keys x 8 heads): transpose the two 8x8 halves
+      uint32_t p0h, p0l, p1h, p1l;
+      split_pack(pv[0], pv[1], p0h, p0l);  // keys 0-7
+      split_pack(pv[2], pv[3], p1h, p1l);  // keys 8-15
+      const uint32_t bh0 = movmatrix_t(p0h), bh1 = movmatrix_t(p1h);
+      const uint32_t bl0 = movmatrix_t(p0l), bl1 = movmatrix_t(p1l);
+      // O^T += V^T P^T: A = V^T[16 dims][16 keys] from V[key][dim] by transposed loads
+#pragma unroll
+      for (int dt = 0; dt < 8; ++dt) {
+        const int c16 = dt * 2 + (mi & 1);
+        const int row = ((mi >> 1) << 3) + rr;
+        uint32_t a[4];
+        ldsm_x4_t(vbase + (c16 >> 3) * HALF_BYTES + swz128(row, c16 & 7), a[0], a[1], a[2], a[3]);
+        mma_bf16_16816(oacc[dt], a, bh0, bh1);
+        mma_bf16_16816(oacc[dt], a, bl0, bl1);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
   // ---- this warp's (max, sum, O) to shared memory for the 4-warp merge
-  float* so = reinterpret_cast<float*>(smem);  // [4][16][128]
-  float* sm = so + 4 * 16 * AD;                // [4][16]
-  float* sl = sm + 64;                         // [4][16]
 #pragma unroll
-  for (int r = 0; r < kSimtMaxG; ++r) {
-    float l = l_run[r];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
-    l_run[r] = l;
+  for (int j = 0; j < 2; ++j) {
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
   }
+  float* so = reinterpret_cast<float*>(smem);  // [4][16][128]
+  float* smx = so + 4 * 16 * AD;               // [4][16]
+  float* ssum = smx + 64;                      // [4][16]
   cons_bar();  // every consumer is done with the stage buffers
 #pragma unroll
-  for (int r = 0; r < kSimtMaxG; ++r) {
-    if (r < G) {
-      *reinterpret_cast<float4*>(so + (warp * 16 + r) * AD + 4 * lane) =
-          make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
-      if (lane == 0) {
-        sm[warp * 16 + r] = m_run[r];
-        sl[warp * 16 + r] = l_run[r];
-      }
+  for (int dt = 0; dt < 8; ++dt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int head = hc + (i & 1);
+      const int d = dt * 16 + (lane >> 2) + (i >= 2 ? 8 : 0);
+      if (head < G) so[(warp * 16 + head) * AD + d] = oacc[dt][i];
     }
+  if (lane < 4) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (hc + j < G) {
+        smx[warp * 16 + hc + j] = m_run[j];
+        ssum[warp * 16 + hc + j] = l_run[j];
+      }
   }
 }
 
-template <bool SIMT>
+template <bool KEYMAJOR>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
     attn_decode_kernel(const __grid_constant__ CUtensorMap mapK,
                        const __grid_constant__ CUtensorMap mapV, DecParams p) {
@@ -469,9 +479,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   // ---------------------------------------------------------------- consumers
   grid_dep_wait();  // q comes from the RoPE/append kernel
   grid_dep_launch();
-  if (SIMT)
-    decode_consume_simt(p, smem, full, empty, abort_flag, b, g, kbeg, kend, n_sub, n_tiles, warp,
-                        lane);
+  if (KEYMAJOR)
+    decode_consume_keymajor(p, smem, full, empty, abort_flag, b, g, kbeg, kend, n_sub, n_tiles,
+                            warp, lane);
   else
     decode_consume_mma(p, smem, full, empty, abort_flag, b, g, kbeg, kend, n_sub, n_tiles, warp,
                        lane);
@@ -959,8 +969,8 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.splits = splits;
   p.keys_per_split = kps;
   p.scale_log2 = kLog2e / sqrtf((float)AD);
-  const bool simt = p.G <= kSimtMaxG;
-  cudaError_t e = simt ? launch_k(attn_decode_kernel<true>, dim3(splits, a.n_kv, a.B),
+  const bool keymajor = p.G <= kKeyMajorMaxG;
+  cudaError_t e = keymajor ? launch_k(attn_decode_kernel<true>, dim3(splits, a.n_kv, a.B),
                                   dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, p)
                        : launch_k(attn_decode_kernel<false>, dim3(splits, a.n_kv, a.B),
                                   dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, p);
