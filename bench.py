@@ -116,6 +116,20 @@ def _dist():
     return ws, rank, local
 
 
+def replica_result(ms_per_step, tokens_per_step, device=None):
+    """Combine the replicas of a multi-GPU run: the slowest rank's step time
+    (max over ranks) and the whole job's tokens per second (every rank decodes
+    its own batch; no data crosses ranks). Single process: unchanged."""
+    import torch
+    import torch.distributed as dist
+    ws = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    if ws > 1:
+        t = torch.tensor([float(ms_per_step)], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    return ms_per_step, tokens_per_step * ws / (ms_per_step * 1e-3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def build_model(workload, device):
     import torch
@@ -211,11 +225,7 @@ def run_gpu(args):
     gemm_ms, gemm_n = model.profile_read("gemm")
     model.profile([])
     model.sync()
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, value = replica_result(ms, B, dev)
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = None
@@ -245,7 +255,7 @@ def run_gpu(args):
     step_bytes = L * (wbytes + kv_bytes) + lm_bytes
     line = {
         "metric": METRIC,
-        "value": B * ws / (ms * 1e-3),
+        "value": value,
         "unit": "tokens/s",
         "n_gpus": ws,
         "steps": args.steps,
