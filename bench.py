@@ -176,6 +176,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
     __graft_entry__.build()
     shape, model, kv = build_model(args.workload, dev)
+    torch.cuda.synchronize()  # inputs are drawn on the default stream; the model runs on its own
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     tokens = torch.randint(0, shape.vocab, (B,), generator=g, device=dev, dtype=torch.int32)
@@ -185,12 +186,24 @@ def run_gpu(args):
     hidden0 = torch.randn(B, shape.hidden, generator=g, device=dev)
     hidden = hidden0.clone()
 
+    stream = torch.cuda.Stream(device=dev)
+    model.set_stream(stream)
+    use_graph = args.workload == "model" and not args.no_graph
+
     def step():
         if args.workload == "model":
-            model.decode_step(tokens, positions, kv, logits, ids)
+            if use_graph:
+                model.graph_launch()
+            else:
+                model.decode_step(tokens, positions, kv, logits, ids)
         else:
-            hidden.copy_(hidden0)
+            with torch.cuda.stream(stream):
+                hidden.copy_(hidden0)
             model.decode_hidden(hidden, positions, kv)
+
+    torch.cuda.synchronize()
+    if use_graph:  # the whole decode step as one CUDA graph (positions stay at 1024)
+        model.capture_decode(tokens, positions, kv, logits, ids, advance=False)
 
     for _ in range(args.warmup):
         step()
@@ -202,7 +215,6 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     n0 = model.launch_count()
@@ -215,12 +227,16 @@ def run_gpu(args):
     launches = model.launch_count() - n0
     ms = e0.elapsed_time(e1) / args.steps
     model.sync()
-    # per-kernel device time: a second pass over the same steps with the
-    # library's event hooks around every launch of the two big kernel classes
+    # per-kernel device time: a second pass over the same steps (direct
+    # launches) with the library's event hooks around every launch of the two
+    # big kernel classes
     dominant = "attn_decode"
     model.profile([dominant, "gemm"])
     for _ in range(args.steps):
-        step()
+        if args.workload == "model":
+            model.decode_step(tokens, positions, kv, logits, ids)
+        else:
+            step()
     attn_ms, attn_n = model.profile_read(dominant)
     gemm_ms, gemm_n = model.profile_read("gemm")
     model.profile([])
@@ -271,7 +287,8 @@ def run_gpu(args):
                    if args.workload == "model" else
                    "one llama2-7b decoder layer, decode step, batch 32, 1024 cached positions",
                    "batch": B, "context": CTX, "l2": "inputs larger than L2 (%.1f GB per step)" % (step_bytes / 1e9),
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "launch": "cuda graph of the step" if use_graph else "direct launches"},
         "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
         "step_hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm,
         "roofline": {"kernel": "attn_decode (flash-decode over the KV cache)", "bound": "hbm",
@@ -455,6 +472,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="model", choices=["model", "layer", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels directly")
     args = ap.parse_args()
     global B_WORKLOAD
     B_WORKLOAD = args.workload

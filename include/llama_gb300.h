@@ -185,6 +185,21 @@ int llama_prefill_hidden(llama_ctx* ctx, float* hidden, int32_t B, int32_t T,
 int llama_decode_hidden(llama_ctx* ctx, float* hidden, const int32_t* positions, int32_t B,
                         const llama_kv* kv);
 
+/* Capture one decode step into a CUDA graph owned by the context (the launch
+ * overhead of a step's ~9 kernels per layer goes away on replay). The device
+ * buffers are fixed at capture: tokens [B], positions [B], kv, logits [B, V],
+ * next_ids [B] (may be NULL). With advance = 1 the graph ends by adding 1 to
+ * every position, so passing next_ids as tokens makes each replay one step
+ * of the greedy generation loop ("Llama2架构与推理全解析" §3.4). The context's
+ * stream must not be the legacy default stream. A new capture replaces the
+ * previous graph. Device-side flags are reported by llama_sync_status as for
+ * direct calls. */
+int llama_graph_capture_decode(llama_ctx* ctx, const int32_t* tokens, int32_t* positions,
+                               int32_t B, const llama_kv* kv, float* logits, int32_t* next_ids,
+                               int32_t advance);
+/* Replay the captured step on the context's stream. */
+int llama_graph_launch(llama_ctx* ctx);
+
 /* Synchronise the stream, then read and clear the device status word.
  * Returns LLAMA_OK, LLAMA_ERR_CUDA or LLAMA_ERR_DEVICE_CHECK. */
 int llama_sync_status(llama_ctx* ctx);

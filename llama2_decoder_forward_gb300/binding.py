@@ -61,6 +61,9 @@ _SIGS = {
                                          c_void_p, c_void_p]),
     "llama_prefill_hidden": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, ctypes.POINTER(KV)]),
     "llama_decode_hidden": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(KV)]),
+    "llama_graph_capture_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(KV),
+                                             c_void_p, c_void_p, c_int32]),
+    "llama_graph_launch": (c_int32, [c_void_p]),
     "llama_sync_status": (c_int32, [c_void_p]),
     "llama_last_device_flags": (ctypes.c_uint32, [c_void_p]),
     "llama_strerror": (ctypes.c_char_p, [c_int32]),
@@ -235,6 +238,19 @@ class Model:
                                           ctypes.byref(kv.struct()), _p(logits), _p(next_ids))
         if rc:
             raise LlamaError(rc, "llama_decode_step_host", lib().llama_last_device_flags(self.ctx))
+
+    def capture_decode(self, tokens, positions, kv: KVCache, logits, next_ids=None, advance=False):
+        """Capture one decode step into a CUDA graph (the context's stream must be a
+        non-default stream, see set_stream). Keep the buffers alive while replaying."""
+        self._graph_args = (tokens, positions, kv, logits, next_ids)
+        self._graph_kv = kv.struct()
+        self._chk(lib().llama_graph_capture_decode(self.ctx, _p(tokens), _p(positions), tokens.shape[0],
+                                                   ctypes.byref(self._graph_kv), _p(logits),
+                                                   _p(next_ids), 1 if advance else 0),
+                  "llama_graph_capture_decode")
+
+    def graph_launch(self):
+        self._chk(lib().llama_graph_launch(self.ctx), "llama_graph_launch")
 
     def prefill_hidden(self, hidden, B, T, kv: KVCache):
         self._chk(lib().llama_prefill_hidden(self.ctx, _p(hidden), B, T, ctypes.byref(kv.struct())),

@@ -154,6 +154,9 @@ struct llama_ctx {
   size_t ev_used[LLAMA_KERNEL_COUNT] = {};
   int64_t launches = 0;
   uint32_t last_flags = 0;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t graph_exec = nullptr;
+  int64_t graph_launches = 0;  // kernels in one replay of the captured step
 
   template <typename T>
   T* at(size_t off) const {
@@ -562,6 +565,8 @@ int llama_set_stream(llama_ctx* c, void* stream) {
 
 int llama_free(llama_ctx* c) {
   if (!c) return LLAMA_ERR_INVALID_ARG;
+  if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+  if (c->graph) cudaGraphDestroy(c->graph);
   for (auto& v : c->ev)
     for (auto& pr : v) {
       cudaEventDestroy(pr.first);
@@ -660,6 +665,59 @@ int llama_decode_hidden(llama_ctx* c, float* hidden, const int32_t* positions, i
   TRY(check_kv(c, kv, B));
   for (int l = 0; l < c->cfg.n_layers; ++l)
     TRY(run_layer(c, l, hidden, B, B, 1, positions, kv, false));
+  return LLAMA_OK;
+}
+
+int llama_graph_capture_decode(llama_ctx* c, const int32_t* tokens, int32_t* positions, int32_t B,
+                               const llama_kv* kv, float* logits, int32_t* next_ids,
+                               int32_t advance) {
+  TRY(check_ctx(c));
+  if (!c->stream) return LLAMA_ERR_UNSUPPORTED;  // the legacy stream cannot be captured
+  if (!tokens || !positions || !logits || B < 1) return LLAMA_ERR_INVALID_ARG;
+  if (advance != 0 && advance != 1) return LLAMA_ERR_INVALID_ARG;
+  if (c->graph_exec) {
+    cudaGraphExecDestroy(c->graph_exec);
+    c->graph_exec = nullptr;
+  }
+  if (c->graph) {
+    cudaGraphDestroy(c->graph);
+    c->graph = nullptr;
+  }
+  const uint32_t prof = c->prof_mask;
+  c->prof_mask = 0;  // no timing events inside the graph
+  if (cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    c->prof_mask = prof;
+    return LLAMA_ERR_CUDA;
+  }
+  const int64_t n0 = c->launches;
+  int rc = llama_decode_step(c, tokens, positions, B, kv, logits, next_ids);
+  if (rc == LLAMA_OK && advance) {
+    rc = cuda_rc(launch_advance_positions(positions, B, c->stream));
+    c->launches++;
+  }
+  cudaGraph_t g = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(c->stream, &g);
+  c->prof_mask = prof;
+  c->graph_launches = c->launches - n0;
+  c->launches = n0;
+  if (rc != LLAMA_OK || ec != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return rc != LLAMA_OK ? rc : LLAMA_ERR_CUDA;
+  }
+  if (cudaGraphInstantiate(&c->graph_exec, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return LLAMA_ERR_CUDA;
+  }
+  c->graph = g;
+  return LLAMA_OK;
+}
+
+int llama_graph_launch(llama_ctx* c) {
+  TRY(check_ctx(c));
+  if (!c->graph_exec) return LLAMA_ERR_INVALID_ARG;
+  if (cudaGraphLaunch(c->graph_exec, c->stream) != cudaSuccess) return LLAMA_ERR_CUDA;
+  c->launches += c->graph_launches;
   return LLAMA_OK;
 }
 

@@ -72,6 +72,7 @@ cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double the
                               cudaStream_t st);
 cudaError_t launch_rope_append(int dtype, const RopeAppendArgs& a, int rows, cudaStream_t st);
 cudaError_t launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st);
+cudaError_t launch_advance_positions(int32_t* positions, int B, cudaStream_t st);
 
 // ------------------------------------------------------------------ GEMM
 // y[n, m] (epilogue) sum_k x[n, k] * w[m, k]; x has N rows, w has M rows.

@@ -227,6 +227,16 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const float* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------ positions += 1
+// Advances every sequence by one position (used at the end of a captured
+// decode step so that graph replays walk through the sequence).
+__global__ void advance_positions_kernel(int32_t* __restrict__ positions, int B) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) positions[b] += 1;
+}
+
 // ------------------------------------------------------------------ launchers
 static bool g_pdl = true;
 void set_pdl(bool on) { g_pdl = on; }
@@ -269,4 +279,10 @@ cudaError_t launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaS
   return launch_k(argmax_kernel, dim3(B), dim3(1024), 0, st, 0, logits, V, ids);
 }
 
+}  // namespace llgb
+
+namespace llgb {
+cudaError_t launch_advance_positions(int32_t* positions, int B, cudaStream_t st) {
+  return launch_k(advance_positions_kernel, dim3((B + 127) / 128), dim3(128), 0, st, 0, positions, B);
+}
 }  // namespace llgb

@@ -253,3 +253,44 @@ def test_host_checks_reject_bad_sizes():
         m.decode_step(torch.zeros(2, dtype=torch.int32, device="cuda"),
                       torch.zeros(2, dtype=torch.int32, device="cuda"), bad, lg)
     assert e.value.rc == 1
+
+
+# --------------------------------------------------------------------------- CUDA graph replay
+def test_graph_replay_matches_direct_steps_and_runs_the_greedy_loop():
+    need_gpu()
+    shape = _small_bf16()
+    B, T, cap, steps = 3, 12, 48, 6
+    w = to_dev(synth.model_weights(shape, 13))
+    stream = torch.cuda.Stream()
+    m = binding.Model(shape, w, max_batch=B, max_tokens=B * T, max_seq=cap, stream=stream)
+    toks = synth.token_ids(B, T, shape.vocab, 13).cuda()
+    with torch.cuda.stream(stream):
+        # direct greedy loop
+        kv_d = binding.KVCache(shape, batch=B, capacity=cap)
+        lg = torch.empty(B, shape.vocab, device="cuda")
+        ids = torch.empty(B, dtype=torch.int32, device="cuda")
+        m.prefill(toks, kv_d, lg, ids)
+        direct_ids, direct_lg = [ids.clone()], [lg.clone()]
+        for s in range(steps):
+            pos = torch.full((B,), T + s, dtype=torch.int32, device="cuda")
+            m.decode_step(ids.clone(), pos, kv_d, lg, ids)
+            direct_ids.append(ids.clone())
+            direct_lg.append(lg.clone())
+        # the same loop as graph replays: tokens are the previous step's choices
+        kv_g = binding.KVCache(shape, batch=B, capacity=cap)
+        lg_g = torch.empty(B, shape.vocab, device="cuda")
+        ids_g = torch.empty(B, dtype=torch.int32, device="cuda")
+        m.prefill(toks, kv_g, lg_g, ids_g)
+        pos_g = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        m.capture_decode(ids_g, pos_g, kv_g, lg_g, ids_g, advance=True)
+        graph_ids, graph_lg = [ids_g.clone()], [lg_g.clone()]
+        for s in range(steps):
+            m.graph_launch()
+            graph_ids.append(ids_g.clone())
+            graph_lg.append(lg_g.clone())
+    m.sync()
+    for a, b in zip(direct_ids, graph_ids):
+        np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
+    for a, b in zip(direct_lg, graph_lg):
+        np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
+    assert int(pos_g[0]) == T + steps
