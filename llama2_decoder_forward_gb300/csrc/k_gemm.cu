@@ -228,11 +228,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           load_acc16(tq, c0, p.lo, g);
           if (DUAL) load_acc16(tq, up + c0, p.lo, u);
           if (gm < p.M) {
+            if (EPI == LLAMA_EPI_RESID_F32) {
+              // read the 16 residual values before writing any (one round trip)
+              float* o = reinterpret_cast<float*>(p.out);
+              float res[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < nvalid)
-                epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm, g[j],
-                                     DUAL ? u[j] : 0.f, p.out_lo);
+              for (int j = 0; j < 16; ++j)
+                res[j] = c0 + j < nvalid ? o[(size_t)(n0 + c0 + j) * p.ldo + gm] : 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < nvalid) o[(size_t)(n0 + c0 + j) * p.ldo + gm] = res[j] + g[j];
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < nvalid)
+                  epi_apply<EPI, bf16>(p.out, (size_t)(n0 + c0 + j) * p.ldo + gm, g[j],
+                                       DUAL ? u[j] : 0.f, p.out_lo);
+            }
           }
         }
       } else {
@@ -286,10 +298,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (DUAL) { u[0] += uv[s2].x; u[1] += uv[s2].y; u[2] += uv[s2].z; u[3] += uv[s2].w; }
           }
         const int gm0 = tile_m * BM + rq;
+        if (EPI == LLAMA_EPI_RESID_F32) {
+          float* o = reinterpret_cast<float*>(p.out) + (size_t)c * p.ldo + gm0;
+          float res[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (gm0 + e < p.M)
-            epi_apply<EPI, bf16>(p.out, (size_t)c * p.ldo + gm0 + e, g[e], u[e], p.out_lo);
+          for (int e = 0; e < 4; ++e) res[e] = gm0 + e < p.M ? o[e] : 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (gm0 + e < p.M) o[e] = res[e] + g[e];
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (gm0 + e < p.M)
+              epi_apply<EPI, bf16>(p.out, (size_t)c * p.ldo + gm0 + e, g[e], u[e], p.out_lo);
+        }
       }
     }
     __syncwarp();
