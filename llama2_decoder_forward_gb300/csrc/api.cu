@@ -110,6 +110,7 @@ Layout make_layout(const llama_config* c, int sm_count) {
   // GEMM operands in the hi/lo pair layout: rows [0, R) and [round16(R), ..+R)
   const size_t RA = 2 * (size_t)round16(std::max(R, 1));
   L.u = take(RA * H * es);
+  // fp32 Q/K/V rows between the projection and RoPE (bf16 decode applies RoPE in the GEMM epilogue)
   L.qkv = take((size_t)R * qkv_rows * 4);
   L.q = take(RA * nq * d * es);
   L.kside = take((size_t)std::max(c->max_tokens, 1) * nkv * d * es);
@@ -267,9 +268,12 @@ int do_rmsnorm(llama_ctx* c, const float* x, int rows, int stride, int offset, c
 
 // split: x holds the hi/lo pair layout of its N rows; out_lo: bf16 outputs also
 // store their remainder out_lo elements further on.
+// rope: the Q/K/V projection's RoPE + cache-append epilogue (bf16 only).
 int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, const void* wu,
-            int M, void* out, int ldo, int split = 0, size_t out_lo = 0) {
+            int M, void* out, int ldo, int split = 0, size_t out_lo = 0,
+            const RopeAppendArgs* rope = nullptr) {
   GemmCall g{};
+  g.rope = rope;
   g.split = split;
   g.out_lo = out_lo;
   g.dtype = c->cfg.dtype;
@@ -299,9 +303,9 @@ int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, c
   return cuda_rc(launch_gemm(g, c->stream));
 }
 
-int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
-                   const int32_t* positions, int layer, const llama_kv* kv, void* q_out,
-                   void* k_out, void* v_out, size_t q_lo = 0) {
+RopeAppendArgs rope_args(const llama_ctx* c, const float* qkv, int rows_per_seq,
+                         const int32_t* positions, int layer, const llama_kv* kv, void* q_out,
+                         void* k_out, void* v_out, size_t q_lo) {
   RopeAppendArgs a{};
   a.q_lo = q_lo;
   a.qkv = qkv;
@@ -325,6 +329,14 @@ int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
   a.batch_cap = kv->batch_capacity;
   a.n_pages = kv->n_pages;
   a.max_pages = kv->max_pages_per_seq;
+  return a;
+}
+
+int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
+                   const int32_t* positions, int layer, const llama_kv* kv, void* q_out,
+                   void* k_out, void* v_out, size_t q_lo = 0) {
+  const RopeAppendArgs a =
+      rope_args(c, qkv, rows_per_seq, positions, layer, kv, q_out, k_out, v_out, q_lo);
   Prof pf(c, LLAMA_KERNEL_ROPE_APPEND);
   c->launches++;
   return cuda_rc(launch_rope_append(c->cfg.dtype, a, rows, c->stream));
@@ -422,17 +434,27 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   const int lo = cf.dtype == LLAMA_BF16 ? round16(rows) : 0;
   const int sp = lo ? 1 : 0;
   TRY(do_rmsnorm(c, x, rows, 1, 0, lw.attn_norm, u, lo));
-  TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
-  if (prefill) {
-    void* ks = c->at<void>(c->L.kside);
-    void* vs = c->at<void>(c->L.vside);
-    TRY(do_rope_append(c, qkv, rows, T, nullptr, l, kv, q, ks, vs, (size_t)lo * nq * d));
-    TRY(do_attn_prefill(c, q, ks, vs, B, T, o, (size_t)lo * nq * d, lo));
+  void* ks = prefill ? c->at<void>(c->L.kside) : nullptr;
+  void* vs = prefill ? c->at<void>(c->L.vside) : nullptr;
+  const int rps = prefill ? T : 1;
+  const int32_t* pos = prefill ? nullptr : positions;
+  const size_t q_lo = (size_t)lo * nq * d;
+  if (cf.dtype == LLAMA_BF16 && !prefill) {
+    // Q/K/V projection with RoPE and the cache append in its epilogue. Prefill
+    // keeps them in a separate kernel: its GEMM runs one CTA per SM with the
+    // epilogue after the K loop, where the per-element work would stall the
+    // tensor pipe for longer than the separate pass over the fp32 rows takes.
+    const RopeAppendArgs ra = rope_args(c, nullptr, rps, pos, l, kv, q, ks, vs, q_lo);
+    TRY(do_gemm(c, kEpiRope, u, rows, H, lw.wqkv, nullptr, qkv_rows, nullptr, qkv_rows, sp, 0,
+                &ra));
   } else {
-    TRY(do_rope_append(c, qkv, rows, 1, positions, l, kv, q, nullptr, nullptr,
-                       (size_t)lo * nq * d));
-    TRY(do_attn_decode(c, q, positions, B, l, kv, o, (size_t)lo * nq * d, (size_t)lo * nq * d));
+    TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
+    TRY(do_rope_append(c, qkv, rows, rps, pos, l, kv, q, ks, vs, q_lo));
   }
+  if (prefill)
+    TRY(do_attn_prefill(c, q, ks, vs, B, T, o, q_lo, lo));
+  else
+    TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
   TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H, sp));
   TRY(do_rmsnorm(c, x, rows, 1, 0, lw.ffn_norm, u, lo));
   TRY(do_gemm(c, LLAMA_EPI_SWIGLU, u, rows, H, lw.w_gate, lw.w_up, I, a, I, sp, (size_t)lo * I));

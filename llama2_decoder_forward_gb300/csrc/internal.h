@@ -76,6 +76,10 @@ cudaError_t launch_advance_positions(int32_t* positions, int B, cudaStream_t st)
 
 // ------------------------------------------------------------------ GEMM
 // y[n, m] (epilogue) sum_k x[n, k] * w[m, k]; x has N rows, w has M rows.
+// Internal epilogue of the Q/K/V projection: RoPE on Q and K, Q to its pair
+// buffer, K and V into the cache (the work of the RoPE/append kernel).
+constexpr int kEpiRope = 4;
+
 struct GemmCall {
   int dtype;
   int epi;                    // LLAMA_EPI_*
@@ -90,6 +94,7 @@ struct GemmCall {
   int split;                  // bf16 path: x rows [0,N) hold bf16(v), rows [L, L+N) hold
                               // bf16(v - bf16(v)), L = round16(N); both are multiplied
   size_t out_lo;              // bf16 outputs: also store the remainder out_lo elements on
+  const RopeAppendArgs* rope; // kEpiRope: where the rotated Q and the K/V rows go
   void* out;
   int ldo;
   uint32_t* status;

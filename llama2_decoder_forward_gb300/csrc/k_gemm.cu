@@ -35,6 +35,7 @@ constexpr int GEMM_THREADS = 192;
 constexpr int kMaxDynSmem = 232448;  // 227 KB per CTA
 
 struct TcParams {
+  RopeAppendArgs rope;  // kEpiRope only
   int M, N, K;
   int n_tile, num_kb, splits, n_tiles;
   int stages;
@@ -66,6 +67,110 @@ __device__ __forceinline__ void epi_apply(void* out, size_t idx, float g, float 
   }
 }
 
+// Q/K/V projection epilogue. A RopeFeat describes output feature m (Q heads,
+// then K heads, then V heads; features 2j and 2j+1 of a head form a RoPE
+// pair); rope_emit stores that feature of token row r given its own sum and
+// its pair partner's. Q and K are rotated by the token's angle; Q goes to its
+// bf16 pair buffer, K and V to the cache slot (and to the prefill side
+// buffers when given). Positions outside the RoPE table or the cache and page
+// ids outside the pool are flagged and their cache writes skipped.
+struct RopeFeat {
+  int kind;   // 0 = Q, 1 = K, 2 = V
+  int col;    // column within the Q, K or V block
+  int g, dd;  // head and dimension within it
+  bool odd;
+};
+
+__device__ __forceinline__ RopeFeat rope_feat(const RopeAppendArgs& a, int m) {
+  const int d = a.head_dim, qw = a.n_q * d, kw = a.n_kv * d;
+  RopeFeat f;
+  f.kind = m < qw ? 0 : (m < qw + kw ? 1 : 2);
+  f.col = f.kind == 0 ? m : (f.kind == 1 ? m - qw : m - qw - kw);
+  f.g = f.col / d;
+  f.dd = f.col - f.g * d;
+  f.odd = f.dd & 1;
+  return f;
+}
+
+// Per-token part of the Q/K/V epilogue, computed once per tile token before
+// the accumulator is ready: the RoPE position (-1 when outside the table; Q
+// then keeps the angles of position 0) and the cache slot of the token for KV
+// head 0 (head g adds g * capacity, or g * page_size when paged; -1: no cache
+// write). Out-of-range positions and page ids are flagged here.
+struct TokInfo {
+  long long kv;
+  int pos;
+  int pad;
+};
+
+__device__ __forceinline__ TokInfo rope_token(const RopeAppendArgs& a, int r) {
+  TokInfo t{-1, -1, 0};
+  const int pos = a.positions ? a.positions[r] : r % a.rows_per_seq;
+  if (pos < 0 || pos >= a.max_seq) {
+    flag(a.status, LLAMA_FLAG_POS_RANGE);
+    return t;
+  }
+  t.pos = pos;
+  const int b = r / a.rows_per_seq;
+  if (a.page_size == 0) {
+    if (pos >= a.capacity) {
+      flag(a.status, LLAMA_FLAG_POS_RANGE);
+      return t;
+    }
+    t.kv = ((long long)a.layer * a.batch_cap + b) * a.n_kv * a.capacity + pos;
+  } else {
+    const int pi = pos / a.page_size;
+    if (pi >= a.max_pages) {
+      flag(a.status, LLAMA_FLAG_POS_RANGE);
+      return t;
+    }
+    const int page = a.page_table[(size_t)b * a.max_pages + pi];
+    if (page < 0 || page >= a.n_pages) {
+      flag(a.status, LLAMA_FLAG_PAGE_RANGE);
+      return t;
+    }
+    t.kv = ((long long)a.layer * a.n_pages + page) * a.n_kv * a.page_size + pos % a.page_size;
+  }
+  return t;
+}
+
+// (cos, sin) of feature f's pair at position pos (identity for V and for
+// positions outside the table); rope_cs2 also returns the next pair's (f.dd
+// a multiple of 4: one 16-byte load).
+__device__ __forceinline__ float2 rope_cs(const RopeAppendArgs& a, const RopeFeat& f, int pos) {
+  if (f.kind == 2 || pos < 0) return make_float2(1.f, 0.f);
+  return __ldg(a.rope + (size_t)pos * (a.head_dim / 2) + (f.dd >> 1));
+}
+__device__ __forceinline__ float4 rope_cs2(const RopeAppendArgs& a, const RopeFeat& f, int pos) {
+  if (f.kind == 2 || pos < 0) return make_float4(1.f, 0.f, 1.f, 0.f);
+  return __ldg(reinterpret_cast<const float4*>(a.rope + (size_t)pos * (a.head_dim / 2) +
+                                               (f.dd >> 1)));
+}
+
+// Stores feature f of token row r: own is its sum, partner the other member
+// of its RoPE pair, cs the pair's angle.
+__device__ __forceinline__ void rope_emit(const RopeAppendArgs& a, const RopeFeat& f, int r,
+                                          const TokInfo& t, float2 cs, float own, float partner) {
+  const int d = a.head_dim;
+  const float v = f.kind == 2 ? own
+                  : f.odd     ? own * cs.x + partner * cs.y
+                              : own * cs.x - partner * cs.y;
+  const bf16 hi = __float2bfloat16_rn(v);
+  if (f.kind == 0) {
+    bf16* q = reinterpret_cast<bf16*>(a.q_out) + (size_t)r * a.n_q * d + f.col;
+    q[0] = hi;
+    if (a.q_lo) q[a.q_lo] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    return;
+  }
+  const bool is_v = f.kind == 2;
+  bf16* side = reinterpret_cast<bf16*>(is_v ? a.v_out : a.k_out);
+  if (side) side[(size_t)r * a.n_kv * d + f.col] = hi;
+  if (t.kv >= 0) {
+    const long long slot = t.kv + (long long)f.g * (a.page_size ? a.page_size : a.capacity);
+    reinterpret_cast<bf16*>(is_v ? a.v_cache : a.k_cache)[slot * d + f.dd] = hi;
+  }
+}
+
 // 16 accumulator columns starting at col for this thread's TMEM lane; in the
 // hi/lo operand mode the column col + lo holds the product with the
 // remainders and is added.
@@ -79,8 +184,23 @@ __device__ __forceinline__ void load_acc16(uint32_t tq, int col, int lo, float (
     v[j] = lo ? __uint_as_float(a[j]) + __uint_as_float(b[j]) : __uint_as_float(a[j]);
 }
 
+// Split-K cluster reduction: CTA k of the cluster finishes columns
+// [c_beg, c_end) of the tile; a work item is 4 consecutive rows of one column.
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+struct RedSlice {
+  int c_beg, items;
+};
+__device__ __forceinline__ RedSlice red_slice(const TcParams& p, int k) {
+  RedSlice r;
+  r.c_beg = (k * p.ncol) / p.splits;
+  const int c_end = min(((k + 1) * p.ncol) / p.splits, min(p.ncol, p.N));
+  r.items = max(0, c_end - r.c_beg) * (BM / 4);
+  return r;
+}
+
 template <int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(GEMM_THREADS, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
                    const __grid_constant__ CUtensorMap tmX, TcParams p) {
   constexpr bool DUAL = EPI == LLAMA_EPI_SWIGLU;
@@ -96,9 +216,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* accf = empty + S;
   // ctl[0]: TMEM base address, ctl[1]: abort, ctl[2]: this CTA reduces the tile
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(accf + 1);
+  // kEpiRope: the tile's tokens (ncol entries after the 256-byte barrier block)
+  TokInfo* tok = reinterpret_cast<TokInfo*>(smem + (size_t)S * stage_bytes + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
+
   const int kb0 = (int)(((long long)split * p.num_kb) / p.splits);
   const int kb1 = (int)(((long long)(split + 1) * p.num_kb) / p.splits);
 
@@ -212,6 +335,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else {  // ---------------- epilogue warps 2..5
     grid_dep_wait();  // the residual and the outputs belong to the previous kernels' order
     grid_dep_launch();
+    if (EPI == kEpiRope) {  // token table, filled while the MMAs run
+      for (int i = threadIdx.x - 64; i < p.ncol; i += 128) {
+        const int r = tile_n * p.ncol + i;
+        tok[i] = r < p.N ? rope_token(p.rope, r) : TokInfo{-1, -1, 0};
+      }
+      epi_bar();
+    }
     const bool ok = mbar_wait(accf, 0, p.status);
     tc_fence_after();
     if (ok && !ctl[1]) {
@@ -223,11 +353,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int gm = tile_m * BM + r;
         const int n0 = tile_n * p.ncol;
         const int nvalid = min(p.ncol, p.N - n0);
+        const RopeFeat rf = EPI == kEpiRope ? rope_feat(p.rope, min(gm, p.M - 1)) : RopeFeat{};
         for (int c0 = 0; c0 < nvalid; c0 += 16) {
           float g[16], u[16];
           load_acc16(tq, c0, p.lo, g);
           if (DUAL) load_acc16(tq, up + c0, p.lo, u);
-          if (gm < p.M) {
+          if (EPI == kEpiRope) {
+            float partner[16];  // the RoPE partner feature sits in the neighbouring lane
+#pragma unroll
+            for (int j = 0; j < 16; ++j) partner[j] = __shfl_xor_sync(0xffffffffu, g[j], 1);
+            // the chunk's angles: all loads issued before any store
+            float2 cs[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) cs[j] = rope_cs(p.rope, rf, tok[c0 + j].pos);
+            if (gm < p.M) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < nvalid)
+                  rope_emit(p.rope, rf, n0 + c0 + j, tok[c0 + j], cs[j], g[j], partner[j]);
+            }
+          } else if (gm < p.M) {
             if (EPI == LLAMA_EPI_RESID_F32) {
               // read the 16 residual values before writing any (one round trip)
               float* o = reinterpret_cast<float*>(p.out);
@@ -274,13 +419,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (warp >= 2 && !ctl[1]) {
       const int t = threadIdx.x - 64;
       const int S = p.splits;
-      const int k = (int)cluster_ctarank();
-      const int c_beg = (k * p.ncol) / S;
-      const int c_end = min(((k + 1) * p.ncol) / S, min(p.ncol, p.N));
-      const int items = max(0, c_end - c_beg) * (BM / 4);
+      const RedSlice sl = red_slice(p, (int)cluster_ctarank());
       const uint32_t red0 = smem_u32(smem);
-      for (int it = t; it < items; it += 128) {
-        const int c = c_beg + it / (BM / 4), rq = (it % (BM / 4)) * 4;
+      for (int it = t; it < sl.items; it += 128) {
+        const int c = sl.c_beg + it / (BM / 4), rq = (it % (BM / 4)) * 4;
         const uint32_t og = red0 + (uint32_t)(c * BM + rq) * 4u;
         const uint32_t ou = red0 + (uint32_t)((p.ncol + c) * BM + rq) * 4u;
         float4 gv[8], uv[8];
@@ -298,7 +440,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (DUAL) { u[0] += uv[s2].x; u[1] += uv[s2].y; u[2] += uv[s2].z; u[3] += uv[s2].w; }
           }
         const int gm0 = tile_m * BM + rq;
-        if (EPI == LLAMA_EPI_RESID_F32) {
+        if (EPI == kEpiRope) {  // rows gm0..gm0+3: two complete RoPE pairs
+          const TokInfo ti = tok[c];
+          const RopeFeat f0 = rope_feat(p.rope, gm0);
+          const float4 cs = rope_cs2(p.rope, f0, ti.pos);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            RopeFeat f = f0;
+            f.col += e;
+            f.dd += e;
+            f.odd = e & 1;
+            if (gm0 + e < p.M)
+              rope_emit(p.rope, f, c, ti, e < 2 ? make_float2(cs.x, cs.y) : make_float2(cs.z, cs.w),
+                        g[e], g[e ^ 1]);
+          }
+        } else if (EPI == LLAMA_EPI_RESID_F32) {
           float* o = reinterpret_cast<float*>(p.out) + (size_t)c * p.ldo + gm0;
           float res[4];
 #pragma unroll
@@ -365,7 +521,9 @@ int gemm_n_tile(int N, int split) {
   return N >= 256 ? 256 : std::max(16, round16(N));
 }
 
-static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count) {
+// rope: the Q/K/V epilogue's token table (16 bytes per tile column) follows
+// the barrier block.
+static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, bool rope) {
   Plan pl{};
   pl.n_tile = gemm_n_tile(N, split);
   pl.lo = split ? pl.n_tile / 2 : 0;
@@ -378,8 +536,9 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count) {
   // two CTAs per SM while the tile is narrow and both fit in tensor memory
   const bool two = pl.n_tile <= 128 && pl.tmem_cols <= 256;
   const int budget = two ? 112 * 1024 : 224 * 1024;
-  pl.stages = std::max(2, std::min(8, (budget - 2048) / stage_bytes));
-  pl.smem = (size_t)pl.stages * stage_bytes + 1024 + 256;
+  const int extra = rope ? 16 * pl.ncol : 0;
+  pl.stages = std::max(2, std::min(8, (budget - 2048 - extra) / stage_bytes));
+  pl.smem = (size_t)pl.stages * stage_bytes + 1024 + 256 + extra;
   pl.ctas_per_sm = std::max(1, std::min(two ? 2 : 1, (int)(233472 / (pl.smem + 1024))));
   pl.m_tiles = (M + BM - 1) / BM;
   pl.n_tiles = (N + pl.ncol - 1) / pl.ncol;
@@ -419,12 +578,14 @@ cudaError_t gemm_prepare() {
   if ((e = set_attr<LLAMA_EPI_STORE_F32>()) != cudaSuccess) return e;
   if ((e = set_attr<LLAMA_EPI_RESID_F32>()) != cudaSuccess) return e;
   if ((e = set_attr<LLAMA_EPI_STORE_T>()) != cudaSuccess) return e;
+  if ((e = set_attr<kEpiRope>()) != cudaSuccess) return e;
   return set_attr<LLAMA_EPI_SWIGLU>();
 }
 
 template <int EPI>
 static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st) {
   TcParams p;
+  if (g.rope) p.rope = *g.rope;
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
@@ -463,12 +624,13 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st) {
     }
   }
   const bool dual = g.epi == LLAMA_EPI_SWIGLU;
-  const Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count);
+  const Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count, g.epi == kEpiRope);
   if (pl.n_tile != g.n_tile) return cudaErrorInvalidValue;
   switch (g.epi) {
     case LLAMA_EPI_STORE_F32: return launch_tc<LLAMA_EPI_STORE_F32>(g, pl, st);
     case LLAMA_EPI_RESID_F32: return launch_tc<LLAMA_EPI_RESID_F32>(g, pl, st);
     case LLAMA_EPI_STORE_T: return launch_tc<LLAMA_EPI_STORE_T>(g, pl, st);
+    case kEpiRope: return g.rope ? launch_tc<kEpiRope>(g, pl, st) : cudaErrorInvalidValue;
     default: return launch_tc<LLAMA_EPI_SWIGLU>(g, pl, st);
   }
 }

@@ -115,6 +115,18 @@ def test_ragged_paged_decode_7b_layer(n_kv):
                        paged_lengths=lengths.tolist(), n_kv_variant=n_kv)
 
 
+def test_layer_7b_decode_bs160_two_activation_tiles():
+    # 160 sequences span two 128-row activation tiles (the last one ragged), so
+    # the Q/K/V projection takes its unsplit path with RoPE in the epilogue
+    _layer_decode_case(synth.LLAMA2_7B.with_(n_layers=1), 0.02, 160, 64, 1005)
+
+
+def test_ragged_paged_gqa_decode_bs160():
+    lengths = synth.ragged_lengths(160, 1, 300, 1006)
+    _layer_decode_case(synth.LLAMA2_7B.with_(n_layers=1), 0.02, 160, None, 1006,
+                       paged_lengths=lengths.tolist(), n_kv_variant=8)
+
+
 def test_layer_70b_prefill_4096_sampled_rows():
     need_gpu()
     shape = synth.LLAMA2_70B.with_(n_layers=1)
