@@ -374,8 +374,9 @@ int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B,
     const uint64_t d = c->cfg.head_dim, nkv = c->cfg.n_kv_heads;
     const uint64_t rows = kv->page_size ? (uint64_t)kv->n_pages * nkv * kv->page_size
                                         : (uint64_t)kv->batch_capacity * nkv * kv->capacity;
-    a.map_k = map3d(c, kv->k, d, rows, c->cfg.n_layers, 16, 1);
-    a.map_v = map3d(c, kv->v, d, rows, c->cfg.n_layers, 16, 1);
+    a.box_rows = attn_decode_box_rows(kv->page_size);
+    a.map_k = map3d(c, kv->k, d, rows, c->cfg.n_layers, a.box_rows, 1);
+    a.map_v = map3d(c, kv->v, d, rows, c->cfg.n_layers, a.box_rows, 1);
     if (!a.map_k || !a.map_v) return LLAMA_ERR_CUDA;
   }
   Prof pf(c, LLAMA_KERNEL_ATTN_DECODE);

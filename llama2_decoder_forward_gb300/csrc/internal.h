@@ -114,8 +114,9 @@ struct AttnDecodeArgs {
   const void* q;             // [B, n_q, d]
   size_t q_lo;               // >0: q + q_lo holds the bf16 remainders of q (pair operand)
   const int32_t* positions;  // [B]
-  const CUtensorMap* map_k;  // bf16: 3D {d, rows per layer, layers}, box {64, 16, 1}, SW128
+  const CUtensorMap* map_k;  // bf16: 3D {d, rows per layer, layers}, box {64, box_rows, 1}, SW128
   const CUtensorMap* map_v;
+  int box_rows;              // 64 (one box per half of a 64-key tile) or 16 (one per 16 keys)
   const void* k_cache;       // fp32 path
   const void* v_cache;
   const int32_t* page_table;
@@ -132,6 +133,9 @@ struct AttnDecodeArgs {
 size_t attn_decode_partial_bytes(int B, int n_q, int head_dim, int max_keys, int sm_count,
                                  int n_kv);
 cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t st);
+// Rows of the K/V cache boxes: 64 when every 64-key tile is contiguous in
+// the cache (no paging, or pages of a multiple of 64 keys), else 16.
+inline int attn_decode_box_rows(int page_size) { return page_size % 64 == 0 ? 64 : 16; }
 // Kernel launches one decode-attention call makes (1, or 2 with a split merge).
 int attn_decode_launches(int B, int n_kv, int max_keys, int sm_count, int dtype);
 

@@ -36,7 +36,10 @@ constexpr int DSTAGES = 3;
 constexpr int DEC_THREADS = 160;                       // 4 consumer warps + producer warp
 constexpr uint32_t HALF_BYTES = SUBK * 128;            // 16 rows x 64 dims x bf16
 constexpr uint32_t SUB_BYTES = 2 * HALF_BYTES;         // 16 rows x 128 dims
-constexpr uint32_t DSTAGE_BYTES = 4 * SUB_BYTES * 2;   // 4 sub-tiles, K and V: 32 KB
+constexpr uint32_t TILE_HALF = DTILE * 128;            // 64 keys x 64 dims x bf16: 8 KB
+constexpr uint32_t DSTAGE_BYTES = 4 * TILE_HALF;       // K and V, two dim halves each: 32 KB
+// Stage layout: K dims 0-63 [64 keys][128 B], K dims 64-127, V dims 0-63,
+// V dims 64-127; 16-key sub-tile j of a half starts at j * HALF_BYTES.
 constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 256;
 
 struct DecParams {
@@ -51,6 +54,7 @@ struct DecParams {
   int n_q, n_kv, G, layer;
   int page_size, capacity, batch_cap, n_pages, max_pages;
   int splits, keys_per_split;
+  int box_rows;  // 64: one TMA box per K/V half of a tile; 16: one per sub-tile
   float scale_log2;
 };
 
@@ -125,13 +129,13 @@ __device__ __forceinline__ void decode_consume_mma(const DecParams& p, uint8_t* 
       uint8_t* st = smem + s * DSTAGE_BYTES;
       const int k0 = kbeg + sub * SUBK;
       const int nvalid = min(SUBK, kend - k0);
-      const uint32_t kbase = smem_u32(st + warp * SUB_BYTES);
-      uint8_t* vptr = st + 4 * SUB_BYTES + warp * SUB_BYTES;
+      const uint32_t kbase = smem_u32(st + warp * HALF_BYTES);
+      uint8_t* vptr = st + 2 * TILE_HALF + warp * HALF_BYTES;
       if (nvalid < SUBK) {  // rows past the last key may hold anything: zero them
         const int nz = (SUBK - nvalid) * 16;
         for (int i = lane; i < nz; i += 32) {
           const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
-          *reinterpret_cast<uint4*>(vptr + half * HALF_BYTES + row * 128 + chunk * 16) =
+          *reinterpret_cast<uint4*>(vptr + half * TILE_HALF + row * 128 + chunk * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
@@ -148,7 +152,7 @@ __device__ __forceinline__ void decode_consume_mma(const DecParams& p, uint8_t* 
         const int chunk = (kk & 3) * 2 + (mi & 1);
         const int row = ((mi >> 1) << 3) + rr;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + half * HALF_BYTES + swz128(row, chunk), b0, b1, b2, b3);
+        ldsm_x4(kbase + half * TILE_HALF + swz128(row, chunk), b0, b1, b2, b3);
         mma_bf16_16816(sc[0], qa[kk], b0, b1);
         mma_bf16_16816(sc[1], qa[kk], b2, b3);
         if (p.q_lo) {
@@ -206,7 +210,7 @@ __device__ __forceinline__ void decode_consume_mma(const DecParams& p, uint8_t* 
         const int c16 = dp * 2 + (mi >> 1);
         const int row = ((mi & 1) << 3) + rr;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vbase + (c16 >> 3) * HALF_BYTES + swz128(row, c16 & 7), b0, b1, b2, b3);
+        ldsm_x4_t(vbase + (c16 >> 3) * TILE_HALF + swz128(row, c16 & 7), b0, b1, b2, b3);
         mma_bf16_16816(oacc[2 * dp], pa, b0, b1);
         mma_bf16_16816(oacc[2 * dp + 1], pa, b2, b3);
         mma_bf16_16816(oacc[2 * dp], pl, b0, b1);
@@ -290,13 +294,13 @@ __device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint
       uint8_t* st = smem + s * DSTAGE_BYTES;
       const int k0 = kbeg + sub * SUBK;
       const int nvalid = min(SUBK, kend - k0);
-      const uint32_t kbase = smem_u32(st + warp * SUB_BYTES);
-      uint8_t* vptr = st + 4 * SUB_BYTES + warp * SUB_BYTES;
+      const uint32_t kbase = smem_u32(st + warp * HALF_BYTES);
+      uint8_t* vptr = st + 2 * TILE_HALF + warp * HALF_BYTES;
       if (nvalid < SUBK) {  // rows past the last key may hold anything: zero them
         const int nz = (SUBK - nvalid) * 16;
         for (int i = lane; i < nz; i += 32) {
           const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
-          *reinterpret_cast<uint4*>(vptr + half * HALF_BYTES + row * 128 + chunk * 16) =
+          *reinterpret_cast<uint4*>(vptr + half * TILE_HALF + row * 128 + chunk * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
@@ -311,7 +315,7 @@ __device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint
         const int row = ((mi & 1) << 3) + rr;
         const int chunk = (kk & 3) * 2 + (mi >> 1);
         uint32_t a[4];
-        ldsm_x4(kbase + (kk >> 2) * HALF_BYTES + swz128(row, chunk), a[0], a[1], a[2], a[3]);
+        ldsm_x4(kbase + (kk >> 2) * TILE_HALF + swz128(row, chunk), a[0], a[1], a[2], a[3]);
         mma_bf16_16816(sh, a, qh[kk][0], qh[kk][1]);
         if (p.q_lo) mma_bf16_16816(sl, a, ql[kk][0], ql[kk][1]);
       }
@@ -360,7 +364,7 @@ __device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint
         const int c16 = dt * 2 + (mi & 1);
         const int row = ((mi >> 1) << 3) + rr;
         uint32_t a[4];
-        ldsm_x4_t(vbase + (c16 >> 3) * HALF_BYTES + swz128(row, c16 & 7), a[0], a[1], a[2], a[3]);
+        ldsm_x4_t(vbase + (c16 >> 3) * TILE_HALF + swz128(row, c16 & 7), a[0], a[1], a[2], a[3]);
         mma_bf16_16816(oacc[dt], a, bh0, bh1);
         mma_bf16_16816(oacc[dt], a, bl0, bl1);
       }
@@ -456,15 +460,24 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         }
         const int nsub = min(4, n_sub - 4 * t);
         uint8_t* st = smem + s * DSTAGE_BYTES;
-        mbar_arrive_expect_tx(&full[s], nsub * SUB_BYTES * 2);
-        for (int j = 0; j < nsub; ++j) {
-          const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
-          uint8_t* kd = st + j * SUB_BYTES;
-          uint8_t* vd = st + 4 * SUB_BYTES + j * SUB_BYTES;
-          tma_load_3d(kd, &mapK, &full[s], 0, row, p.layer);
-          tma_load_3d(kd + HALF_BYTES, &mapK, &full[s], 64, row, p.layer);
-          tma_load_3d(vd, &mapV, &full[s], 0, row, p.layer);
-          tma_load_3d(vd + HALF_BYTES, &mapV, &full[s], 64, row, p.layer);
+        if (p.box_rows == DTILE) {  // the tile's 64 keys are contiguous: one box per half
+          const int row = kv_row(p, b, g, kbeg + t * DTILE);
+          mbar_arrive_expect_tx(&full[s], DSTAGE_BYTES);
+          tma_load_3d(st, &mapK, &full[s], 0, row, p.layer);
+          tma_load_3d(st + TILE_HALF, &mapK, &full[s], 64, row, p.layer);
+          tma_load_3d(st + 2 * TILE_HALF, &mapV, &full[s], 0, row, p.layer);
+          tma_load_3d(st + 3 * TILE_HALF, &mapV, &full[s], 64, row, p.layer);
+        } else {
+          mbar_arrive_expect_tx(&full[s], nsub * SUB_BYTES * 2);
+          for (int j = 0; j < nsub; ++j) {
+            const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
+            uint8_t* kd = st + j * HALF_BYTES;
+            uint8_t* vd = st + 2 * TILE_HALF + j * HALF_BYTES;
+            tma_load_3d(kd, &mapK, &full[s], 0, row, p.layer);
+            tma_load_3d(kd + TILE_HALF, &mapK, &full[s], 64, row, p.layer);
+            tma_load_3d(vd, &mapV, &full[s], 0, row, p.layer);
+            tma_load_3d(vd + TILE_HALF, &mapV, &full[s], 64, row, p.layer);
+          }
         }
         ++issued;
       }
@@ -968,6 +981,7 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.max_pages = a.max_pages;
   p.splits = splits;
   p.keys_per_split = kps;
+  p.box_rows = a.box_rows == DTILE ? DTILE : SUBK;
   p.scale_log2 = kLog2e / sqrtf((float)AD);
   const bool keymajor = p.G <= kKeyMajorMaxG;
   cudaError_t e = keymajor ? launch_k(attn_decode_kernel<true>, dim3(splits, a.n_kv, a.B),

@@ -64,10 +64,11 @@ int setup_device(int dev, void** scratch) {
   return LLAMA_OK;
 }
 
-bool encode_cache_map(CUtensorMap* m, void* base, uint64_t d, uint64_t rows, uint64_t layers) {
+bool encode_cache_map(CUtensorMap* m, void* base, uint64_t d, uint64_t rows, uint64_t layers,
+                      uint32_t box_rows) {
   cuuint64_t dims[3] = {d, rows, layers};
   cuuint64_t strides[2] = {d * 2, d * rows * 2};
-  cuuint32_t box[3] = {64, 16, 1};
+  cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode_fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -121,14 +122,16 @@ extern "C" int llama_attention_decode_noalloc(const llama_config* cfg, const voi
   if (need > kNoAllocScratchBytes) return LLAMA_ERR_OUT_OF_RANGE;
 
   CUtensorMap mk, mv;
-  if (!encode_cache_map(&mk, kv->k, d, rows, cfg->n_layers) ||
-      !encode_cache_map(&mv, kv->v, d, rows, cfg->n_layers))
+  const int box_rows = llgb::attn_decode_box_rows(kv->page_size);
+  if (!encode_cache_map(&mk, kv->k, d, rows, cfg->n_layers, box_rows) ||
+      !encode_cache_map(&mv, kv->v, d, rows, cfg->n_layers, box_rows))
     return LLAMA_ERR_CUDA;
   llgb::AttnDecodeArgs a{};
   a.q = q;
   a.positions = positions;
   a.map_k = &mk;
   a.map_v = &mv;
+  a.box_rows = box_rows;
   a.k_cache = kv->k;
   a.v_cache = kv->v;
   a.page_table = kv->page_table;

@@ -216,19 +216,21 @@ def test_rope_append_bf16(ctx7, paged):
 
 # --------------------------------------------------------------------------- decode attention
 def _decode_case(nq, nkv, positions, paged, seed, cap=None):
+    """paged: False (contiguous cache) or the page size in keys."""
     shape = L7.with_(n_q_heads=nq, n_kv_heads=nkv)
     m, _ = ctx_for(shape, max_batch=len(positions), max_tokens=0, max_seq=4608)
     B, d = len(positions), shape.head_dim
     pos = torch.tensor(positions, dtype=torch.int32)
     q = _randn((B, nq, d), 1.0, torch.bfloat16, seed)
     if paged:
-        table, total = _paged_setup(positions, nkv, d, 16, seed, torch.bfloat16)
-        k = synth.cache_values((1, total, nkv, 16, d), seed, torch.bfloat16, stream=0)
-        v = synth.cache_values((1, total, nkv, 16, d), seed, torch.bfloat16, stream=1)
-        kv = binding.KVCache(shape, n_pages=total, page_size=16, page_table=table.cuda(),
+        ps = int(paged)
+        table, total = _paged_setup(positions, nkv, d, ps, seed, torch.bfloat16)
+        k = synth.cache_values((1, total, nkv, ps, d), seed, torch.bfloat16, stream=0)
+        v = synth.cache_values((1, total, nkv, ps, d), seed, torch.bfloat16, stream=1)
+        kv = binding.KVCache(shape, n_pages=total, page_size=ps, page_table=table.cuda(),
                              k=k.cuda(), v=v.cuda())
         Kf, Vf = f64(k)[0], f64(v)[0]
-        logical = lambda pool, b, n: O.gather_paged(pool, table[b].numpy(), n, 16)
+        logical = lambda pool, b, n: O.gather_paged(pool, table[b].numpy(), n, ps)
     else:
         cap = cap or (max(positions) + 1 + 15) // 16 * 16
         k = synth.cache_values((1, B, nkv, cap, d), seed, torch.bfloat16, stream=0)
@@ -247,7 +249,7 @@ def _decode_case(nq, nkv, positions, paged, seed, cap=None):
 
 
 @pytest.mark.parametrize("nq,nkv", [(32, 32), (32, 8), (16, 4), (16, 8)])
-@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("paged", [False, 16, 64])
 def test_attention_decode_bf16(nq, nkv, paged):
     positions = [0, 14, 15, 16, 17, 63, 64, 65, 1024, 2047, 4095, 333]
     _decode_case(nq, nkv, positions, paged, 51)
