@@ -377,7 +377,9 @@ int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B,
     a.box_rows = attn_decode_box_rows(kv->page_size);
     a.map_k = map3d(c, kv->k, d, rows, c->cfg.n_layers, a.box_rows, 1);
     a.map_v = map3d(c, kv->v, d, rows, c->cfg.n_layers, a.box_rows, 1);
-    if (!a.map_k || !a.map_v) return LLAMA_ERR_CUDA;
+    a.map_k16 = map3d(c, kv->k, d, rows, c->cfg.n_layers, 16, 1);
+    a.map_v16 = map3d(c, kv->v, d, rows, c->cfg.n_layers, 16, 1);
+    if (!a.map_k || !a.map_v || !a.map_k16 || !a.map_v16) return LLAMA_ERR_CUDA;
   }
   Prof pf(c, LLAMA_KERNEL_ATTN_DECODE);
   c->launches += attn_decode_launches(B, a.n_kv, a.max_keys, c->sm_count, c->cfg.dtype);

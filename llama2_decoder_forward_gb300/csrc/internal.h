@@ -116,7 +116,9 @@ struct AttnDecodeArgs {
   const int32_t* positions;  // [B]
   const CUtensorMap* map_k;  // bf16: 3D {d, rows per layer, layers}, box {64, box_rows, 1}, SW128
   const CUtensorMap* map_v;
-  int box_rows;              // 64 (one box per half of a 64-key tile) or 16 (one per 16 keys)
+  const CUtensorMap* map_k16;  // the same views with box {64, 16, 1} (partial tiles, 16-key pages)
+  const CUtensorMap* map_v16;
+  int box_rows;              // 64 (one box per half of a full 64-key tile) or 16 (one per 16 keys)
   const void* k_cache;       // fp32 path
   const void* v_cache;
   const int32_t* page_table;

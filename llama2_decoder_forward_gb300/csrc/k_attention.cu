@@ -404,7 +404,9 @@ __device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint
 template <bool KEYMAJOR>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
     attn_decode_kernel(const __grid_constant__ CUtensorMap mapK,
-                       const __grid_constant__ CUtensorMap mapV, DecParams p) {
+                       const __grid_constant__ CUtensorMap mapV,
+                       const __grid_constant__ CUtensorMap mapK16,
+                       const __grid_constant__ CUtensorMap mapV16, DecParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -440,6 +442,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     if (lane == 0) {
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
+      tma_prefetch_desc(&mapK16);
+      tma_prefetch_desc(&mapV16);
       int issued = 0;
       bool ok = true, waited = false;
       for (int t = 0; t < n_tiles; ++t) {
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         }
         const int nsub = min(4, n_sub - 4 * t);
         uint8_t* st = smem + s * DSTAGE_BYTES;
-        if (p.box_rows == DTILE) {  // the tile's 64 keys are contiguous: one box per half
+        if (p.box_rows == DTILE && nsub == 4) {  // 64 contiguous keys: one box per half
           const int row = kv_row(p, b, g, kbeg + t * DTILE);
           mbar_arrive_expect_tx(&full[s], DSTAGE_BYTES);
           tma_load_3d(st, &mapK, &full[s], 0, row, p.layer);
@@ -473,10 +477,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
             const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
             uint8_t* kd = st + j * HALF_BYTES;
             uint8_t* vd = st + 2 * TILE_HALF + j * HALF_BYTES;
-            tma_load_3d(kd, &mapK, &full[s], 0, row, p.layer);
-            tma_load_3d(kd + TILE_HALF, &mapK, &full[s], 64, row, p.layer);
-            tma_load_3d(vd, &mapV, &full[s], 0, row, p.layer);
-            tma_load_3d(vd + TILE_HALF, &mapV, &full[s], 64, row, p.layer);
+            tma_load_3d(kd, &mapK16, &full[s], 0, row, p.layer);
+            tma_load_3d(kd + TILE_HALF, &mapK16, &full[s], 64, row, p.layer);
+            tma_load_3d(vd, &mapV16, &full[s], 0, row, p.layer);
+            tma_load_3d(vd + TILE_HALF, &mapV16, &full[s], 64, row, p.layer);
           }
         }
         ++issued;
@@ -985,9 +989,11 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.scale_log2 = kLog2e / sqrtf((float)AD);
   const bool keymajor = p.G <= kKeyMajorMaxG;
   cudaError_t e = keymajor ? launch_k(attn_decode_kernel<true>, dim3(splits, a.n_kv, a.B),
-                                  dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, p)
+                                  dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, *a.map_k16,
+                                  *a.map_v16, p)
                        : launch_k(attn_decode_kernel<false>, dim3(splits, a.n_kv, a.B),
-                                  dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, p);
+                                  dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, *a.map_k16,
+                                  *a.map_v16, p);
   if (e != cudaSuccess || splits == 1) return e;
   const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
   return launch_k(attn_combine_kernel, dim3(a.B * a.n_q), dim3(AD), 0, st, 0,

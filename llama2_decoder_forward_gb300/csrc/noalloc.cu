@@ -121,16 +121,20 @@ extern "C" int llama_attention_decode_noalloc(const llama_config* cfg, const voi
                                                       max_keys < 1 ? 1 : max_keys, sms, (int)nkv);
   if (need > kNoAllocScratchBytes) return LLAMA_ERR_OUT_OF_RANGE;
 
-  CUtensorMap mk, mv;
+  CUtensorMap mk, mv, mk16, mv16;
   const int box_rows = llgb::attn_decode_box_rows(kv->page_size);
   if (!encode_cache_map(&mk, kv->k, d, rows, cfg->n_layers, box_rows) ||
-      !encode_cache_map(&mv, kv->v, d, rows, cfg->n_layers, box_rows))
+      !encode_cache_map(&mv, kv->v, d, rows, cfg->n_layers, box_rows) ||
+      !encode_cache_map(&mk16, kv->k, d, rows, cfg->n_layers, 16) ||
+      !encode_cache_map(&mv16, kv->v, d, rows, cfg->n_layers, 16))
     return LLAMA_ERR_CUDA;
   llgb::AttnDecodeArgs a{};
   a.q = q;
   a.positions = positions;
   a.map_k = &mk;
   a.map_v = &mv;
+  a.map_k16 = &mk16;
+  a.map_v16 = &mv16;
   a.box_rows = box_rows;
   a.k_cache = kv->k;
   a.v_cache = kv->v;
