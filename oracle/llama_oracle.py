@@ -249,6 +249,73 @@ def greedy(logits: np.ndarray) -> np.ndarray:
     return np.argmax(logits, axis=-1).astype(np.int32)
 
 
+def sample_detail(logits, history, temperature: float, top_k: int, top_p: float,
+                  repetition_penalty: float, u: float) -> dict:
+    """Sampling of one next token from one row of logits ("Llama2架构与推理全解析"
+    §2.5 from logits to sampling, §3.3 sampling parameters; "Llama2 模型推理
+    全流程" generation step 3: probs = softmax(logits / T), then a draw).
+
+    Steps, in this order (the pages name the parts; their order and the
+    penalty's form are the readings listed in the design notes):
+      1. repetition penalty r: each distinct token id of `history` has its
+         logit divided by r when positive, multiplied by r otherwise
+         (§2.5: "press down the probability of tokens already seen");
+      2. temperature T: s = logit / T; T == 0 is the greedy limit (argmax,
+         lowest index on ties);
+      3. top-k: keep the k largest s (ties broken by the lower index);
+      4. softmax over the kept tokens;
+      5. top-p: in the same order keep the smallest prefix whose cumulative
+         probability reaches p (§2.5, nucleus sampling);
+      6. renormalise and draw with the uniform u in [0, 1): the first token,
+         in ascending vocabulary order, whose cumulative probability exceeds
+         u (the last kept token if rounding leaves none).
+    top_k <= 0 or >= V and top_p >= 1 switch steps 3 and 5 off.
+
+    Returns {"token", "kept" (ids, ascending), "q" (their probabilities),
+    "cdf_lo", "cdf_hi" (each kept token's interval of u), "z" (penalised
+    logits), "s_sorted" (kept s, descending), "cum_sorted" (step-5
+    cumulative probabilities in that order)}.
+    """
+    z = np.array(logits, dtype=f64)
+    V = z.shape[0]
+    if repetition_penalty != 1.0 and history is not None:
+        seen = np.unique(np.asarray([t for t in np.asarray(history).ravel() if 0 <= t < V],
+                                    dtype=np.int64))
+        zs = z[seen]
+        z[seen] = np.where(zs > 0, zs / repetition_penalty, zs * repetition_penalty)
+    if temperature == 0:
+        t = int(np.argmax(z))
+        return {"token": t, "kept": np.array([t]), "q": np.array([1.0]),
+                "cdf_lo": np.array([0.0]), "cdf_hi": np.array([1.0]), "z": z,
+                "s_sorted": np.array([z[t]]), "cum_sorted": np.array([1.0])}
+    s = z / temperature
+    order = np.lexsort((np.arange(V), -s))  # s descending, lower index first on ties
+    if 0 < top_k < V:
+        order = order[:top_k]
+    e = np.exp(s[order] - s[order[0]])
+    cum = np.cumsum(e / e.sum())
+    if top_p < 1.0:
+        n = int(np.argmax(cum >= top_p)) + 1 if np.any(cum >= top_p) else len(order)
+        order, e = order[:n], e[:n]
+    q_sorted = e / e.sum()
+    asc = np.argsort(order)
+    kept, q = order[asc], q_sorted[asc]
+    hi = np.cumsum(q)
+    lo = hi - q
+    pick = np.nonzero(hi > u)[0]
+    token = int(kept[pick[0]]) if len(pick) else int(kept[-1])
+    return {"token": token, "kept": kept, "q": q, "cdf_lo": lo, "cdf_hi": hi, "z": z,
+            "s_sorted": s[order], "cum_sorted": cum}
+
+
+def sample(logits, histories, temperature, top_k, top_p, repetition_penalty, uniforms):
+    """sample_detail for each row of logits [B, V]; returns the token ids."""
+    return np.array([sample_detail(logits[b], None if histories is None else histories[b],
+                                   temperature, top_k, top_p, repetition_penalty,
+                                   float(uniforms[b]))["token"]
+                     for b in range(len(logits))], dtype=np.int32)
+
+
 class Model:
     """fp64 copy of a model's weights plus per-sequence caches."""
 

@@ -387,3 +387,67 @@ def test_cache_holds_storage_type_and_decode_still_equals_prefill():
     O.layer_prefill(x, lw, shape, K3, V3, cache_dtype="f64")
     assert not np.array_equal(K3[:, :, :6], O.round_to_bf16(K3[:, :, :6]))
     np.testing.assert_allclose(K[:, :, :6], K3[:, :, :6], rtol=2 ** -8)
+
+
+# ---------------------------------------------------------------- sampling (§2.5, §3.3)
+
+def test_sample_temperature_zero_is_greedy():
+    rng = np.random.default_rng(21)
+    z = rng.standard_normal(50)
+    z[[3, 17]] = z.max() + 1.0  # a tie: the lower index wins
+    for u in (0.0, 0.5, 0.999):
+        assert O.sample_detail(z, None, 0.0, 0, 1.0, 1.0, u)["token"] == 3
+
+
+def test_sample_top_k_one_is_argmax():
+    rng = np.random.default_rng(22)
+    z = rng.standard_normal(40)
+    for T in (0.3, 1.0, 2.5):
+        for u in (0.01, 0.6, 0.99):
+            assert O.sample_detail(z, None, T, 1, 1.0, 1.0, u)["token"] == int(np.argmax(z))
+
+
+def test_sample_draws_follow_the_library_softmax():
+    # inverse-CDF draws over a uniform grid of u reproduce softmax(z / T)
+    rng = np.random.default_rng(23)
+    z = rng.standard_normal(7) * 2
+    T, N = 0.8, 20000
+    counts = np.zeros(7)
+    for i in range(N):
+        counts[O.sample_detail(z, None, T, 0, 1.0, 1.0, (i + 0.5) / N)["token"]] += 1
+    np.testing.assert_allclose(counts / N, scipy.special.softmax(z / T), atol=1.5 / N)
+
+
+def test_sample_top_k_keeps_the_k_largest_by_brute_force():
+    rng = np.random.default_rng(24)
+    z = np.round(rng.standard_normal(30), 1)  # rounding makes ties
+    for k in (1, 3, 7, 29):
+        ranked = sorted(range(30), key=lambda i: (-z[i], i))
+        kept = O.sample_detail(z, None, 1.3, k, 1.0, 1.0, 0.5)["kept"]
+        assert sorted(kept.tolist()) == sorted(ranked[:k])
+
+
+def test_sample_top_p_hand_example():
+    z = np.log(np.array([0.05, 0.5, 0.15, 0.3]))  # probabilities at T = 1
+    cases = {0.45: [1], 0.7: [1, 3], 0.9: [1, 2, 3], 0.99: [0, 1, 2, 3]}
+    for p, want in cases.items():
+        d = O.sample_detail(z, None, 1.0, 0, p, 1.0, 0.3)
+        assert d["kept"].tolist() == want, p
+        np.testing.assert_allclose(d["q"].sum(), 1.0, rtol=1e-14)
+    d = O.sample_detail(z, None, 1.0, 0, 0.7, 1.0, 0.3)
+    np.testing.assert_allclose(d["q"], [0.5 / 0.8, 0.3 / 0.8], rtol=1e-12)
+
+
+def test_sample_repetition_penalty_hand_example():
+    z = np.array([2.0, -1.0, 0.5, 3.0, 1.0])
+    d = O.sample_detail(z, [0, 1, 1, 3, 7, -2], 0.0, 0, 1.0, 2.0, 0.5)  # 7, -2: outside V
+    np.testing.assert_array_equal(d["z"], [1.0, -2.0, 0.5, 1.5, 1.0])
+    assert d["token"] == 3
+    z2 = np.array([2.0, 1.9, 0.0])
+    assert O.sample_detail(z2, [0], 0.0, 0, 1.0, 1.5, 0.5)["token"] == 1
+
+
+def test_sample_draw_walks_the_vocabulary_in_ascending_order():
+    z = np.log(np.array([0.2, 0.5, 0.3]))
+    for u, want in ((0.1, 0), (0.19, 0), (0.3, 1), (0.69, 1), (0.75, 2), (0.999, 2)):
+        assert O.sample_detail(z, None, 1.0, 0, 1.0, 1.0, u)["token"] == want, u
