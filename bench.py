@@ -241,6 +241,27 @@ def run_gpu(args):
     gemm_ms, gemm_n = model.profile_read("gemm")
     model.profile([])
     model.sync()
+    sample_ms = None
+    if args.workload == "model":
+        # the sampler on this step's logits (not part of the greedy step timed
+        # above): T 0.7, top-k 50, top-p 0.9, repetition penalty 1.1 over a
+        # 1024-token history per sequence
+        hist = torch.randint(0, shape.vocab, (B, CTX), generator=g, device=dev, dtype=torch.int32)
+        hlen = torch.full((B,), CTX, dtype=torch.int32, device=dev)
+        uni = torch.rand(B, generator=g, device=dev)
+        sids = torch.empty(B, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+        kw = dict(temperature=0.7, top_k=50, top_p=0.9, repetition_penalty=1.1, history=hist,
+                  history_len=hlen)
+        for _ in range(3):
+            model.sample(logits, uni, sids, **kw)
+        model.profile(["sample"])
+        for _ in range(20):
+            model.sample(logits, uni, sids, **kw)
+        s_ms, s_n = model.profile_read("sample")
+        model.profile([])
+        model.sync()
+        sample_ms = s_ms / max(s_n, 1)
     ms, value = replica_result(ms, B, dev)
 
     # end to end through the host-buffer entry point (copies inside the timed region)
@@ -299,7 +320,8 @@ def run_gpu(args):
         "kernels": {"attn_decode_ms_per_step": attn_ms / args.steps,
                     "gemm_ms_per_step": gemm_ms / args.steps,
                     "gemm_gbs": (L * wbytes + lm_bytes) / (gemm_ms / args.steps * 1e-3) / 1e9
-                    if gemm_ms > 0 else None},
+                    if gemm_ms > 0 else None,
+                    "sample_ms": sample_ms},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "e2e": e2e,

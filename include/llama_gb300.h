@@ -224,7 +224,8 @@ int llama_free(llama_ctx* ctx);
 #define LLAMA_KERNEL_ATTN_PREFILL 4
 #define LLAMA_KERNEL_EMBED 5
 #define LLAMA_KERNEL_ARGMAX 6
-#define LLAMA_KERNEL_COUNT 7
+#define LLAMA_KERNEL_SAMPLE 7
+#define LLAMA_KERNEL_COUNT 8
 int llama_profile_enable(llama_ctx* ctx, uint32_t kind_mask);
 int llama_profile_read(llama_ctx* ctx, int32_t kind, double* total_ms, int64_t* launches);
 /* Launches of this library's kernels enqueued since context creation. */
@@ -310,6 +311,42 @@ int llama_op_embed(llama_ctx* ctx, const int32_t* tokens, int32_t n, void* out);
 
 /* Greedy choice (§2.5): ids[b] = argmax_v logits[b, v], lowest index on ties. */
 int llama_op_argmax(llama_ctx* ctx, const float* logits, int32_t B, int32_t V, int32_t* ids);
+
+/* ---- Sampling of the next token ("Llama2架构与推理全解析" §2.5 from logits to
+ * sampling, §3.3 sampling parameters; "Llama2 模型推理全流程" generation step 3:
+ * probs = softmax(logits / T), then a draw). Per row b of logits, in order:
+ *   1. repetition penalty r: every distinct id among history[b][0 .. history_len[b])
+ *      has its logit divided by r if positive, multiplied by r otherwise;
+ *   2. temperature T: s = logit / T; T == 0 gives the greedy choice (argmax,
+ *      lowest index on ties) and ignores the rest;
+ *   3. top-k: keep the k largest s (ties to the lower index);
+ *   4. softmax over the kept ids;
+ *   5. top-p: keep the smallest prefix of that order whose probability
+ *      reaches p;
+ *   6. renormalise and draw with uniforms[b] in [0, 1): the first kept id, in
+ *      ascending id order, whose cumulative probability exceeds the uniform
+ *      (the last kept id if rounding leaves none).
+ * The draw is deterministic given the inputs. Random numbers are the caller's:
+ * uniforms[b] is drawn by the caller (any generator). */
+typedef struct {
+  float temperature;        /* >= 0; 0: greedy */
+  int32_t top_k;            /* <= 0 or >= V: off */
+  float top_p;              /* (0, 1]; 1: off */
+  float repetition_penalty; /* > 0; 1: off */
+} llama_sampling;
+
+/* logits: [B, V] fp32 device rows (contiguous), V <= 32768;
+ * history: [B, history_stride] int32 device ids or NULL (then no penalty),
+ * history_len: [B] int32 device counts (may be NULL when history is NULL);
+ * uniforms: [B] fp32 device; next_ids: [B] int32 device output. All pointers
+ * stay the caller's. Returns INVALID_ARG for NULL buffers or parameters out of
+ * range, UNSUPPORTED for V above 32768. History ids outside [0, V)
+ * are skipped and set LLAMA_FLAG_TOKEN_RANGE. Asynchronous on the context's
+ * stream; one kernel launch. */
+int llama_sample(llama_ctx* ctx, const float* logits, int32_t B, int32_t V,
+                 const llama_sampling* params,
+                 const int32_t* history, const int32_t* history_len, int32_t history_stride,
+                 const float* uniforms, int32_t* next_ids);
 
 #ifdef __cplusplus
 }

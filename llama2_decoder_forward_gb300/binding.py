@@ -18,7 +18,8 @@ c_void_p = ctypes.c_void_p
 F32, BF16 = 0, 1
 EPI_STORE_F32, EPI_RESID_F32, EPI_STORE_T, EPI_SWIGLU = 0, 1, 2, 3
 EPI_SPLIT_X = 16  # OR-ed flag: x (and bf16 outputs) in the hi/lo pair layout
-KERNELS = ("rmsnorm", "gemm", "rope_append", "attn_decode", "attn_prefill", "embed", "argmax")
+KERNELS = ("rmsnorm", "gemm", "rope_append", "attn_decode", "attn_prefill", "embed", "argmax",
+           "sample")
 FLAG_TOKEN_RANGE, FLAG_POS_RANGE, FLAG_PAGE_RANGE, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OUT_OF_RANGE", 4: "CUDA",
           5: "DEVICE_CHECK", 6: "WORKSPACE"}
@@ -40,6 +41,13 @@ class LayerWeights(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("embed", c_void_p), ("final_norm", c_void_p), ("lm_head", c_void_p),
                 ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class Sampling(ctypes.Structure):
+    """llama_sampling: temperature (0 = greedy), top_k (<= 0 off), top_p (1 = off),
+    repetition_penalty (1 = off)."""
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", c_int32), ("top_p", ctypes.c_float),
+                ("repetition_penalty", ctypes.c_float)]
 
 
 class KV(ctypes.Structure):
@@ -85,6 +93,8 @@ _SIGS = {
                                              c_void_p]),
     "llama_op_embed": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p]),
     "llama_op_argmax": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p]),
+    "llama_sample": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, ctypes.POINTER(Sampling), c_void_p,
+                               c_void_p, c_int32, c_void_p, c_void_p]),
 }
 
 _lib = None
@@ -322,3 +332,14 @@ class Model:
     def op_argmax(self, logits, ids):
         B, V = logits.shape
         self._chk(lib().llama_op_argmax(self.ctx, _p(logits), B, V, _p(ids)), "llama_op_argmax")
+
+    def sample(self, logits, uniforms, next_ids, *, temperature=1.0, top_k=0, top_p=1.0,
+               repetition_penalty=1.0, history=None, history_len=None):
+        """Draw next_ids[b] from logits[b] (see llama_sample). history: [B, S] int32
+        device ids and history_len: [B] int32 counts, or None."""
+        sp = Sampling(temperature, top_k, top_p, repetition_penalty)
+        stride = history.shape[1] if history is not None else 0
+        self._chk(lib().llama_sample(self.ctx, _p(logits), logits.shape[0], logits.shape[1],
+                                     ctypes.byref(sp),
+                                     _p(history), _p(history_len), stride, _p(uniforms),
+                                     _p(next_ids)), "llama_sample")

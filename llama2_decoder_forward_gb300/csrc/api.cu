@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -43,6 +44,7 @@ bool load_encode() {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     g_prep_err = gemm_prepare();
     if (g_prep_err == cudaSuccess) g_prep_err = attn_prepare();
+    if (g_prep_err == cudaSuccess) g_prep_err = sample_prepare();
   });
   return g_encode != nullptr && g_prep_err == cudaSuccess;
 }
@@ -851,6 +853,38 @@ int llama_op_embed(llama_ctx* c, const int32_t* tokens, int32_t n, void* out) {
   c->launches++;
   return cuda_rc(launch_embed(c->cfg.dtype, tokens, c->embed, c->cfg.vocab, c->cfg.hidden, n,
                               reinterpret_cast<float*>(out), c->status, c->stream));
+}
+
+int llama_sample(llama_ctx* c, const float* logits, int32_t B, int32_t V, const llama_sampling* sp,
+                 const int32_t* history, const int32_t* history_len, int32_t history_stride,
+                 const float* uniforms, int32_t* next_ids) {
+  TRY(check_ctx(c));
+  if (!logits || !sp || !uniforms || !next_ids || B < 1) return LLAMA_ERR_INVALID_ARG;
+  if (!(sp->temperature >= 0.f) || !(sp->top_p > 0.f && sp->top_p <= 1.f) ||
+      !(sp->repetition_penalty > 0.f) || !std::isfinite(sp->temperature) ||
+      !std::isfinite(sp->repetition_penalty))
+    return LLAMA_ERR_INVALID_ARG;
+  if (history && (!history_len || history_stride < 0)) return LLAMA_ERR_INVALID_ARG;
+  if (V < 1) return LLAMA_ERR_INVALID_ARG;
+  if (V > kSampleMaxVocab) return LLAMA_ERR_UNSUPPORTED;
+  SampleCall sc{};
+  sc.logits = logits;
+  sc.B = B;
+  sc.V = V;
+  sc.ldl = V;
+  sc.temperature = sp->temperature;
+  sc.top_k = sp->top_k;
+  sc.top_p = sp->top_p;
+  sc.penalty = sp->repetition_penalty;
+  sc.history = history;
+  sc.history_len = history_len;
+  sc.history_stride = history_stride;
+  sc.uniforms = uniforms;
+  sc.next_ids = next_ids;
+  sc.status = c->status;
+  Prof pf(c, LLAMA_KERNEL_SAMPLE);
+  c->launches++;
+  return cuda_rc(launch_sample(sc, c->stream));
 }
 
 int llama_op_argmax(llama_ctx* c, const float* logits, int32_t B, int32_t V, int32_t* ids) {

@@ -157,4 +157,25 @@ struct AttnPrefillArgs {
 cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_t st);
 cudaError_t attn_prepare();
 
+// ---- token sampling (k_sample.cu)
+struct SampleCall {
+  const float* logits;  // [B, ldl] fp32, V used per row
+  int B, V, ldl;
+  float temperature;    // 0: greedy
+  int top_k;            // <= 0 or >= V: off
+  float top_p;          // >= 1: off
+  float penalty;        // 1: off
+  const int32_t* history;      // [B, history_stride] ids (penalty only)
+  const int32_t* history_len;  // [B]
+  int history_stride;
+  const float* uniforms;       // [B] in [0, 1)
+  int32_t* next_ids;           // [B]
+  uint32_t* status;
+};
+constexpr int kSampleMaxVocab = 32768;  // 64 entries per thread of one 512-thread CTA
+int sample_chunk(int V);
+size_t sample_smem_bytes(int V);
+cudaError_t sample_prepare();
+cudaError_t launch_sample(const SampleCall& c, cudaStream_t st);
+
 }  // namespace llgb

@@ -70,6 +70,8 @@ def test_null_context_and_arguments_rejected(lib):
     assert lib.llama_sync_status(None) == 1
     assert lib.llama_free(None) == 1
     assert lib.llama_launch_count(None) == 0
+    sp = binding.Sampling(1.0, 0, 1.0, 1.0)
+    assert lib.llama_sample(None, None, 1, 8, ctypes.byref(sp), None, None, 0, None, None) == 1
     out = ctypes.c_void_p()
     w = binding.Weights()
     assert lib.llama_init(ctypes.byref(_cfg()), ctypes.byref(w), None, 0, None, ctypes.byref(out)) == 1
