@@ -258,8 +258,8 @@ def sample_detail(logits, history, temperature: float, top_k: int, top_p: float,
     Steps, in this order (the pages name the parts; their order and the
     penalty's form are the readings listed in the design notes):
       1. repetition penalty r: each distinct token id of `history` has its
-         logit divided by r when positive, multiplied by r otherwise
-         (§2.5: "press down the probability of tokens already seen");
+         logit divided by r when positive, multiplied by r otherwise (§2.5
+         asks for a lower probability for ids already produced);
       2. temperature T: s = logit / T; T == 0 is the greedy limit (argmax,
          lowest index on ties);
       3. top-k: keep the k largest s (ties broken by the lower index);
