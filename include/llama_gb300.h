@@ -313,7 +313,7 @@ int llama_op_embed(llama_ctx* ctx, const int32_t* tokens, int32_t n, void* out);
 int llama_op_argmax(llama_ctx* ctx, const float* logits, int32_t B, int32_t V, int32_t* ids);
 
 /* ---- Sampling of the next token ("Llama2架构与推理全解析" §2.5 from logits to
- * sampling, §3.3 sampling parameters; "Llama2 模型推理全流程" generation step 3:
+ * sampling, §3.3 sampling parameters; "Llama2架构全景解析" §2.2 step 3:
  * probs = softmax(logits / T), then a draw). Per row b of logits, in order:
  *   1. repetition penalty r: every distinct id among history[b][0 .. history_len[b])
  *      has its logit divided by r if positive, multiplied by r otherwise;

@@ -1,6 +1,6 @@
 // Token sampling from the LM head's logits ("Llama2架构与推理全解析" §2.5 from
-// logits to sampling, §3.3 sampling parameters; "Llama2 模型推理全流程"
-// generation step 3, probs = softmax(logits / T) and a draw).
+// logits to sampling, §3.3 sampling parameters; "Llama2架构全景解析"
+// §2.2 step 3, probs = softmax(logits / T) and a draw).
 //
 // One CTA of 512 threads per sequence. Thread t owns the CH consecutive
 // vocabulary entries [t*CH, t*CH + CH): their scaled logits s live in its

@@ -230,6 +230,39 @@ def layer_prefill(x, lw, shape, K, V, rows=None, cache_dtype=None):
     return out
 
 
+def layer_extend(x, lw, shape, K, V, seq_of_row, positions, cache_dtype=None):
+    """One layer over a batch of new tokens of several sequences at once: the
+    continuous-batching step ("Llama2架构全景解析" §3.1 and "基于LLAMA2与PyTorch的高效推理框架实践指南"
+    §三.2 name continuous batching; §2.1's
+    prefill and §2.4's decode are its two special cases). Row r is the token of
+    sequence seq_of_row[r] at position positions[r]; any mix of whole prompts,
+    prompt pieces after earlier pieces, and single decode tokens.
+
+    Every row's rotated K and its V go into K, V ([B_cap, n_kv, S_cap, d], in
+    place, in the cache's storage type) first; then row r attends over keys
+    0 .. positions[r] of its sequence (the causal mask of §2.3: earlier rows
+    of the same piece and everything cached before it). Returns [rows, H].
+    """
+    cdt = shape.dtype if cache_dtype is None else cache_dtype
+    n_q, n_kv, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    seq = np.asarray(seq_of_row, dtype=np.int64)
+    pos = np.asarray(positions, dtype=np.int64)
+    R = x.shape[0]
+    u = rmsnorm(x, lw["attn_norm"], shape.rms_eps)
+    q, k, v = _split_qkv(linear(u, lw["wqkv"]), n_q, n_kv, d)
+    q = rope(q, pos, shape.rope_theta)
+    k = rope(k, pos, shape.rope_theta)
+    for r in range(R):
+        K[seq[r], :, pos[r]] = cache_store(k[r], cdt)
+        V[seq[r], :, pos[r]] = cache_store(v[r], cdt)
+    o = np.empty((R, n_q, d), dtype=f64)
+    for r in range(R):
+        o[r] = gqa_attention(q[r], K[seq[r]], V[seq[r]], int(pos[r]) + 1)
+    h = x + linear(o.reshape(R, n_q * d), lw["wo"])
+    u2 = rmsnorm(h, lw["ffn_norm"], shape.rms_eps)
+    return h + swiglu_ffn(u2, lw["w_gate"], lw["w_up"], lw["w_down"])
+
+
 # --------------------------------------------------------------------------
 # Whole model
 # --------------------------------------------------------------------------
@@ -252,8 +285,8 @@ def greedy(logits: np.ndarray) -> np.ndarray:
 def sample_detail(logits, history, temperature: float, top_k: int, top_p: float,
                   repetition_penalty: float, u: float) -> dict:
     """Sampling of one next token from one row of logits ("Llama2架构与推理全解析"
-    §2.5 from logits to sampling, §3.3 sampling parameters; "Llama2 模型推理
-    全流程" generation step 3: probs = softmax(logits / T), then a draw).
+    §2.5 from logits to sampling, §3.3 sampling parameters; "Llama2架构全景解析"
+    §2.2 step 3: probs = softmax(logits / T), then a draw).
 
     Steps, in this order (the pages name the parts; their order and the
     penalty's form are the readings listed in the design notes):
@@ -336,6 +369,14 @@ class Model:
         h = embed(self.embed_t, tokens)
         for l, lw in enumerate(self.layers):
             h = layer_prefill(h, lw, self.shape, self.K[l], self.V[l], cache_dtype=self.cache_dtype)
+        return lm_head(h, self.final_norm, self.lm, self.shape.rms_eps)
+
+    def extend(self, tokens, seq_of_row, positions):
+        """New tokens of several sequences (layer_extend); logits of every row."""
+        h = embed(self.embed_t, tokens)
+        for l, lw in enumerate(self.layers):
+            h = layer_extend(h, lw, self.shape, self.K[l], self.V[l], seq_of_row, positions,
+                             cache_dtype=self.cache_dtype)
         return lm_head(h, self.final_norm, self.lm, self.shape.rms_eps)
 
     def decode(self, tokens, positions):

@@ -451,3 +451,48 @@ def test_sample_draw_walks_the_vocabulary_in_ascending_order():
     z = np.log(np.array([0.2, 0.5, 0.3]))
     for u, want in ((0.1, 0), (0.19, 0), (0.3, 1), (0.69, 1), (0.75, 2), (0.999, 2)):
         assert O.sample_detail(z, None, 1.0, 0, 1.0, 1.0, u)["token"] == want, u
+
+
+# ---------------------------------------------------------------- continuous batching (extend)
+
+def test_extend_covers_prefill_decode_chunks_and_mixed_batches():
+    # One extend step of rows (sequence, position) reproduces: a whole-prompt
+    # prefill; a prompt fed in two pieces; ragged prompts in one batch; and a
+    # decode token of one sequence next to a prompt piece of another.
+    shape = synth.TINY
+    w = synth.model_weights(shape, 1002)
+    toks = synth.token_ids(2, 12, shape.vocab, 1002).numpy()
+    full = O.Model(shape, w, 2, 16).prefill(toks)           # [2, 12, V]
+
+    m = O.Model(shape, w, 2, 16)                              # whole prompts as one extend
+    seq = np.repeat([0, 1], 12)
+    pos = np.tile(np.arange(12), 2)
+    lg = m.extend(toks.reshape(-1), seq, pos)
+    np.testing.assert_allclose(lg.reshape(2, 12, -1), full, rtol=1e-10, atol=1e-12)
+
+    m = O.Model(shape, w, 2, 16)                              # ragged: 5 and 9 tokens, then the rest
+    seq = np.array([0] * 5 + [1] * 9)
+    pos = np.concatenate([np.arange(5), np.arange(9)])
+    lg = m.extend(np.concatenate([toks[0, :5], toks[1, :9]]), seq, pos)
+    np.testing.assert_allclose(lg[:5], full[0, :5], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lg[5:], full[1, :9], rtol=1e-10, atol=1e-12)
+    # mixed: sequence 1 decodes token 9 while sequence 0 feeds its prompt piece 5..11
+    seq = np.array([0] * 7 + [1])
+    pos = np.concatenate([np.arange(5, 12), [9]])
+    lg = m.extend(np.concatenate([toks[0, 5:], toks[1, 9:10]]), seq, pos)
+    np.testing.assert_allclose(lg[:7], full[0, 5:], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lg[7], full[1, 9], rtol=1e-10, atol=1e-12)
+    lg = m.extend(toks[1, 10:11], np.array([1]), np.array([10]))  # sequence 1 alone continues
+    np.testing.assert_allclose(lg[0], full[1, 10], rtol=1e-10, atol=1e-12)
+
+
+def test_extend_of_one_token_per_sequence_is_decode():
+    shape = synth.TINY
+    w = synth.model_weights(shape, 1003)
+    toks = synth.token_ids(3, 6, shape.vocab, 1003).numpy()
+    a, b = O.Model(shape, w, 3, 8), O.Model(shape, w, 3, 8)
+    a.prefill(toks[:, :5])
+    b.prefill(toks[:, :5])
+    want = a.decode(toks[:, 5], np.full(3, 5))
+    got = b.extend(toks[:, 5], np.arange(3), np.full(3, 5))
+    np.testing.assert_array_equal(got, want)
