@@ -185,6 +185,37 @@ int llama_prefill_hidden(llama_ctx* ctx, float* hidden, int32_t B, int32_t T,
 int llama_decode_hidden(llama_ctx* ctx, float* hidden, const int32_t* positions, int32_t B,
                         const llama_kv* kv);
 
+/* Extend step of continuous batching ("Llama2架构全景解析" §3.1 and
+ * "基于LLAMA2与PyTorch的高效推理框架实践指南" §三.2 name continuous batching;
+ * prefill, §2.1 of "Llama2架构与推理全解析", and decode, §2.4, are its two
+ * special cases): one call feeds new tokens of B sequences, each any number of
+ * rows at any position — whole prompts of different lengths, a piece of a
+ * prompt whose earlier pieces are already cached, or single decode tokens,
+ * mixed in one batch. Rows are packed: sequence b owns rows cu_rows[b] ..
+ * cu_rows[b+1] - 1 (cu_rows[0] = 0, cu_rows[B] = n_rows, non-decreasing), the
+ * first at position start_pos[b] and the rest at consecutive positions; the
+ * cache slots of sequence b are those of batch index (or page-table row) b.
+ * Every row's rotated K and its V are appended first; row i of sequence b
+ * then attends over keys 0 .. start_pos[b] + i of b (its cached keys, the
+ * earlier rows of its piece and itself).
+ *   tokens   : DEVICE int32 [n_rows]
+ *   cu_rows  : DEVICE int32 [B + 1];  start_pos: DEVICE int32 [B]
+ *   max_rows : host int, the largest cu_rows[b+1] - cu_rows[b] (sizes the grid)
+ *   logits   : DEVICE fp32 [B, V] for the last row of each sequence; next_ids
+ *              [B] the greedy ids (or NULL)
+ * n_rows <= max(max_batch, max_tokens), B <= max_batch; bf16 models only
+ * (UNSUPPORTED otherwise). Positions past the cache, page ids outside the pool
+ * and a last row outside [0, n_rows) set device flags (llama_sync_status);
+ * malformed cu_rows are the caller's error. Asynchronous. */
+int llama_extend(llama_ctx* ctx, const int32_t* tokens, int32_t n_rows, const int32_t* cu_rows,
+                 const int32_t* start_pos, int32_t B, int32_t max_rows, const llama_kv* kv,
+                 float* logits, int32_t* next_ids);
+/* The layer stack of llama_extend on a hidden state: hidden [n_rows, H] fp32,
+ * updated in place (for models without embedding and LM head). */
+int llama_extend_hidden(llama_ctx* ctx, float* hidden, int32_t n_rows, const int32_t* cu_rows,
+                        const int32_t* start_pos, int32_t B, int32_t max_rows,
+                        const llama_kv* kv);
+
 /* Capture one decode step into a CUDA graph owned by the context (the launch
  * overhead of a step's ~9 kernels per layer goes away on replay). The device
  * buffers are fixed at capture: tokens [B], positions [B], kv, logits [B, V],

@@ -69,6 +69,10 @@ _SIGS = {
                                          c_void_p, c_void_p]),
     "llama_prefill_hidden": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, ctypes.POINTER(KV)]),
     "llama_decode_hidden": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(KV)]),
+    "llama_extend": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_int32,
+                               ctypes.POINTER(KV), c_void_p, c_void_p]),
+    "llama_extend_hidden": (c_int32, [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32,
+                                      c_int32, ctypes.POINTER(KV)]),
     "llama_graph_capture_decode": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, ctypes.POINTER(KV),
                                              c_void_p, c_void_p, c_int32]),
     "llama_graph_launch": (c_int32, [c_void_p]),
@@ -237,6 +241,25 @@ class Model:
         B, T = tokens.shape
         self._chk(lib().llama_prefill(self.ctx, _p(tokens), B, T, ctypes.byref(kv.struct()),
                                       _p(logits), _p(next_ids)), "llama_prefill")
+
+    def extend(self, tokens, cu_rows, start_pos, kv: KVCache, logits, next_ids=None,
+               max_rows=None):
+        """Continuous-batching step (llama_extend): tokens [n_rows] packed by
+        cu_rows [B+1] (device int32), sequence b's first row at start_pos[b]."""
+        B = start_pos.shape[0]
+        if max_rows is None:
+            max_rows = int((cu_rows[1:] - cu_rows[:-1]).max())
+        self._chk(lib().llama_extend(self.ctx, _p(tokens), tokens.shape[0], _p(cu_rows),
+                                     _p(start_pos), B, max_rows, ctypes.byref(kv.struct()),
+                                     _p(logits), _p(next_ids)), "llama_extend")
+
+    def extend_hidden(self, hidden, cu_rows, start_pos, kv: KVCache, max_rows=None):
+        B = start_pos.shape[0]
+        if max_rows is None:
+            max_rows = int((cu_rows[1:] - cu_rows[:-1]).max())
+        self._chk(lib().llama_extend_hidden(self.ctx, _p(hidden), hidden.shape[0], _p(cu_rows),
+                                            _p(start_pos), B, max_rows,
+                                            ctypes.byref(kv.struct())), "llama_extend_hidden")
 
     def decode_step(self, tokens, positions, kv: KVCache, logits, next_ids=None):
         self._chk(lib().llama_decode_step(self.ctx, _p(tokens), _p(positions), tokens.shape[0],

@@ -261,11 +261,12 @@ int check_kv(const llama_ctx* c, const llama_kv* kv, int B) {
 
 // ---------------------------------------------------------------- single steps
 int do_rmsnorm(llama_ctx* c, const float* x, int rows, int stride, int offset, const void* gamma,
-               void* out, int lo_rows = 0) {
+               void* out, int lo_rows = 0, const int32_t* row_end = nullptr, int n_in = 0) {
   Prof pf(c, LLAMA_KERNEL_RMSNORM);
   c->launches++;
   return cuda_rc(launch_rmsnorm(c->cfg.dtype, x, rows, stride, offset, gamma, c->cfg.hidden,
-                                c->cfg.rms_eps, out, lo_rows, c->stream));
+                                c->cfg.rms_eps, out, lo_rows, c->stream, row_end, n_in,
+                                c->status));
 }
 
 // split: x holds the hi/lo pair layout of its N rows; out_lo: bf16 outputs also
@@ -334,11 +335,25 @@ RopeAppendArgs rope_args(const llama_ctx* c, const float* qkv, int rows_per_seq,
   return a;
 }
 
+// Packed sequences of an extend step: sequence b owns rows cu_rows[b] ..
+// cu_rows[b+1]-1, the first at position start_pos[b]; max_rows bounds the
+// rows of one sequence.
+struct RowMap {
+  const int32_t* cu_rows;
+  const int32_t* start_pos;
+  int B, max_rows;
+};
+
 int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
                    const int32_t* positions, int layer, const llama_kv* kv, void* q_out,
-                   void* k_out, void* v_out, size_t q_lo = 0) {
-  const RopeAppendArgs a =
+                   void* k_out, void* v_out, size_t q_lo = 0, const RowMap* rm = nullptr) {
+  RopeAppendArgs a =
       rope_args(c, qkv, rows_per_seq, positions, layer, kv, q_out, k_out, v_out, q_lo);
+  if (rm) {
+    a.cu_rows = rm->cu_rows;
+    a.start_pos = rm->start_pos;
+    a.n_seq = rm->B;
+  }
   Prof pf(c, LLAMA_KERNEL_ROPE_APPEND);
   c->launches++;
   return cuda_rc(launch_rope_append(c->cfg.dtype, a, rows, c->stream));
@@ -417,6 +432,50 @@ int do_attn_prefill(llama_ctx* c, const void* q, const void* k, const void* v, i
   return cuda_rc(launch_attn_prefill(c->cfg.dtype, a, c->stream));
 }
 
+// Attention of an extend step: every packed row over keys 0 .. its position
+// of its sequence, read from the cache (the rows' own K/V already appended).
+int do_attn_extend(llama_ctx* c, const void* q, int n_rows, const RowMap& rm, int layer,
+                   const llama_kv* kv, void* out, size_t out_lo, int q_lo_rows) {
+  if (c->cfg.dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
+  if (!aligned16(q)) return LLAMA_ERR_INVALID_ARG;
+  AttnPrefillArgs a{};
+  a.out_lo = out_lo;
+  a.q_lo_rows = q_lo_rows;
+  a.q = q;
+  a.out = out;
+  a.status = c->status;
+  a.B = rm.B;
+  a.T = rm.max_rows;
+  a.n_q = c->cfg.n_q_heads;
+  a.n_kv = c->cfg.n_kv_heads;
+  a.head_dim = c->cfg.head_dim;
+  a.cu_rows = rm.cu_rows;
+  a.start_pos = rm.start_pos;
+  a.n_rows = n_rows;
+  a.from_cache = 1;
+  a.box_rows = attn_decode_box_rows(kv->page_size);
+  a.layer = layer;
+  a.page_size = kv->page_size;
+  a.capacity = kv->capacity;
+  a.batch_cap = kv->batch_capacity;
+  a.n_pages = kv->n_pages;
+  a.max_pages = kv->max_pages_per_seq;
+  a.page_table = kv->page_table;
+  trim_maps(c);
+  const uint64_t d = c->cfg.head_dim, nkv = c->cfg.n_kv_heads;
+  const uint64_t crow = kv->page_size ? (uint64_t)kv->n_pages * nkv * kv->page_size
+                                      : (uint64_t)kv->batch_capacity * nkv * kv->capacity;
+  a.map_q = map3d(c, q, d, c->cfg.n_q_heads, (uint64_t)n_rows + (uint64_t)q_lo_rows, 1, 64);
+  a.map_k = map3d(c, kv->k, d, crow, c->cfg.n_layers, a.box_rows, 1);
+  a.map_v = map3d(c, kv->v, d, crow, c->cfg.n_layers, a.box_rows, 1);
+  a.map_k16 = map3d(c, kv->k, d, crow, c->cfg.n_layers, 16, 1);
+  a.map_v16 = map3d(c, kv->v, d, crow, c->cfg.n_layers, 16, 1);
+  if (!a.map_q || !a.map_k || !a.map_v || !a.map_k16 || !a.map_v16) return LLAMA_ERR_CUDA;
+  Prof pf(c, LLAMA_KERNEL_ATTN_PREFILL);
+  c->launches++;
+  return cuda_rc(launch_attn_prefill(c->cfg.dtype, a, c->stream));
+}
+
 #define TRY(expr)                   \
   do {                              \
     const int _rc = (expr);         \
@@ -424,8 +483,10 @@ int do_attn_prefill(llama_ctx* c, const void* q, const void* k, const void* v, i
   } while (0)
 
 // One decoder layer on rows x[0..rows): h = h + attn(rmsnorm(h)); h = h + ffn(rmsnorm(h)).
+// rm: an extend step (packed rows of several sequences at any positions);
+// B, T, positions and prefill are then unused.
 int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32_t* positions,
-              const llama_kv* kv, bool prefill) {
+              const llama_kv* kv, bool prefill, const RowMap* rm = nullptr) {
   const llama_config& cf = c->cfg;
   const llama_layer_weights& lw = c->layers[l];
   const int H = cf.hidden, d = cf.head_dim, nq = cf.n_q_heads, nkv = cf.n_kv_heads,
@@ -444,7 +505,11 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   const int rps = prefill ? T : 1;
   const int32_t* pos = prefill ? nullptr : positions;
   const size_t q_lo = (size_t)lo * nq * d;
-  if (cf.dtype == LLAMA_BF16 && !prefill) {
+  if (rm) {  // extend: RoPE/append, then attention over the cache
+    TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
+    TRY(do_rope_append(c, qkv, rows, 1, nullptr, l, kv, q, nullptr, nullptr, q_lo, rm));
+    TRY(do_attn_extend(c, q, rows, *rm, l, kv, o, q_lo, lo));
+  } else if (cf.dtype == LLAMA_BF16 && !prefill) {
     // Q/K/V projection with RoPE and the cache append in its epilogue. Prefill
     // keeps them in a separate kernel: its GEMM runs one CTA per SM with the
     // epilogue after the K loop, where the per-element work would stall the
@@ -452,14 +517,15 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
     const RopeAppendArgs ra = rope_args(c, nullptr, rps, pos, l, kv, q, ks, vs, q_lo);
     TRY(do_gemm(c, kEpiRope, u, rows, H, lw.wqkv, nullptr, qkv_rows, nullptr, qkv_rows, sp, 0,
                 &ra));
+    TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
   } else {
     TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
     TRY(do_rope_append(c, qkv, rows, rps, pos, l, kv, q, ks, vs, q_lo));
+    if (prefill)
+      TRY(do_attn_prefill(c, q, ks, vs, B, T, o, q_lo, lo));
+    else
+      TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
   }
-  if (prefill)
-    TRY(do_attn_prefill(c, q, ks, vs, B, T, o, q_lo, lo));
-  else
-    TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
   TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H, sp));
   TRY(do_rmsnorm(c, x, rows, 1, 0, lw.ffn_norm, u, lo));
   TRY(do_gemm(c, LLAMA_EPI_SWIGLU, u, rows, H, lw.w_gate, lw.w_up, I, a, I, sp, (size_t)lo * I));
@@ -468,12 +534,13 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
 }
 
 // Final RMSNorm + LM head (+ greedy choice) on rows stride*b + offset of x.
+// row_end (extend): sequence b's last row is row_end[b] - 1 of the n_in rows.
 int run_head(llama_ctx* c, const float* x, int B, int stride, int offset, float* logits,
-             int32_t* next_ids) {
+             int32_t* next_ids, const int32_t* row_end = nullptr, int n_in = 0) {
   const llama_config& cf = c->cfg;
   void* ul = c->at<void>(c->L.u_last);
   const int lo = cf.dtype == LLAMA_BF16 ? round16(B) : 0;
-  TRY(do_rmsnorm(c, x, B, stride, offset, c->final_norm, ul, lo));
+  TRY(do_rmsnorm(c, x, B, stride, offset, c->final_norm, ul, lo, row_end, n_in));
   TRY(do_gemm(c, LLAMA_EPI_STORE_F32, ul, B, cf.hidden, c->lm_head, nullptr, cf.vocab, logits,
               cf.vocab, lo ? 1 : 0));
   if (next_ids) {
@@ -624,6 +691,52 @@ int llama_prefill(llama_ctx* c, const int32_t* tokens, int32_t B, int32_t T, con
   }
   for (int l = 0; l < cf.n_layers; ++l) TRY(run_layer(c, l, x, rows, B, T, nullptr, kv, true));
   return run_head(c, x, B, T, T - 1, logits, next_ids);
+}
+
+namespace {
+int check_extend(const llama_ctx* c, int32_t n_rows, const int32_t* cu_rows,
+                 const int32_t* start_pos, int32_t B, int32_t max_rows, const llama_kv* kv) {
+  const llama_config& cf = c->cfg;
+  if (!cu_rows || !start_pos || B < 1 || n_rows < 1 || max_rows < 1 || max_rows > n_rows)
+    return LLAMA_ERR_INVALID_ARG;
+  if (cf.dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
+  if (B > cf.max_batch || n_rows > std::max(cf.max_batch, cf.max_tokens))
+    return LLAMA_ERR_OUT_OF_RANGE;
+  return check_kv(c, kv, B);
+}
+}  // namespace
+
+int llama_extend(llama_ctx* c, const int32_t* tokens, int32_t n_rows, const int32_t* cu_rows,
+                 const int32_t* start_pos, int32_t B, int32_t max_rows, const llama_kv* kv,
+                 float* logits, int32_t* next_ids) {
+  TRY(check_ctx(c));
+  const llama_config& cf = c->cfg;
+  if (!cf.has_embed_head) return LLAMA_ERR_UNSUPPORTED;
+  if (!tokens || !logits) return LLAMA_ERR_INVALID_ARG;
+  TRY(check_extend(c, n_rows, cu_rows, start_pos, B, max_rows, kv));
+  float* x = c->at<float>(c->L.x);
+  {
+    Prof pf(c, LLAMA_KERNEL_EMBED);
+    c->launches++;
+    TRY(cuda_rc(launch_embed(cf.dtype, tokens, c->embed, cf.vocab, cf.hidden, n_rows, x, c->status,
+                             c->stream)));
+  }
+  const RowMap rm{cu_rows, start_pos, B, max_rows};
+  for (int l = 0; l < cf.n_layers; ++l)
+    TRY(run_layer(c, l, x, n_rows, B, 0, nullptr, kv, false, &rm));
+  return run_head(c, x, B, 0, 0, logits, next_ids, cu_rows + 1, n_rows);
+}
+
+int llama_extend_hidden(llama_ctx* c, float* hidden, int32_t n_rows, const int32_t* cu_rows,
+                        const int32_t* start_pos, int32_t B, int32_t max_rows,
+                        const llama_kv* kv) {
+  TRY(check_ctx(c));
+  if (!hidden) return LLAMA_ERR_INVALID_ARG;
+  TRY(check_extend(c, n_rows, cu_rows, start_pos, B, max_rows, kv));
+  const RowMap rm{cu_rows, start_pos, B, max_rows};
+  for (int l = 0; l < c->cfg.n_layers; ++l)
+    TRY(run_layer(c, l, hidden, n_rows, B, 0, nullptr, kv, false, &rm));
+  return LLAMA_OK;
 }
 
 int llama_decode_step(llama_ctx* c, const int32_t* tokens, const int32_t* positions, int32_t B,

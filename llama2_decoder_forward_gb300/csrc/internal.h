@@ -50,6 +50,11 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 struct RopeAppendArgs {
   const float* qkv;          // [rows, (n_q + 2 n_kv) d] fp32
   const int32_t* positions;  // [rows] or null (position = r % rows_per_seq)
+  // extend steps (separate RoPE kernel only): row r belongs to the sequence b
+  // with cu_rows[b] <= r < cu_rows[b + 1] and sits at start_pos[b] + r - cu_rows[b]
+  const int32_t* cu_rows;    // [n_seq + 1] or null
+  const int32_t* start_pos;  // [n_seq]
+  int n_seq;
   const float2* rope;        // [max_seq, d/2] (cos, sin)
   void* q_out;               // [rows, n_q d]
   size_t q_lo;               // >0: also store bf16(q - bf16(q)) q_lo elements further
@@ -65,9 +70,13 @@ struct RopeAppendArgs {
 
 cudaError_t launch_embed(int dtype, const int32_t* tokens, const void* table, int V, int H, int n,
                          float* out, uint32_t* status, cudaStream_t st);
+// row_end: optional [rows] — output row r normalises input row row_end[r] - 1
+// (the last row of sequence r in a packed batch; in_stride/in_offset unused),
+// rows outside [0, n_in) flag LLAMA_FLAG_TOKEN_RANGE and give zeros.
 cudaError_t launch_rmsnorm(int dtype, const float* x, int rows, int in_stride, int in_offset,
                            const void* gamma, int H, float eps, void* out, int lo_rows,
-                           cudaStream_t st);
+                           cudaStream_t st, const int32_t* row_end = nullptr, int n_in = 0,
+                           uint32_t* status = nullptr);
 cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double theta,
                               cudaStream_t st);
 cudaError_t launch_rope_append(int dtype, const RopeAppendArgs& a, int rows, cudaStream_t st);
@@ -153,6 +162,19 @@ struct AttnPrefillArgs {
   size_t out_lo;             // >0: also store bf16 remainders out_lo elements further
   uint32_t* status;
   int B, T, n_q, n_kv, head_dim;
+  // Extend (bf16 only): packed sequences and K/V read from the cache.
+  // cu_rows [B+1] / start_pos [B] on the device; T is then the longest
+  // sequence's row count and n_rows the packed total. The maps are the
+  // cache's 3D views {d, rows per layer, layers} with box {64, box_rows, 1}
+  // (map_k, map_v) and box {64, 16, 1} (map_k16, map_v16).
+  const int32_t* cu_rows = nullptr;
+  const int32_t* start_pos = nullptr;
+  int n_rows = 0;
+  int from_cache = 0, box_rows = 16, layer = 0;
+  int page_size = 0, capacity = 0, batch_cap = 0, n_pages = 0, max_pages = 0;
+  const int32_t* page_table = nullptr;
+  const CUtensorMap* map_k16 = nullptr;
+  const CUtensorMap* map_v16 = nullptr;
 };
 cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_t st);
 cudaError_t attn_prepare();

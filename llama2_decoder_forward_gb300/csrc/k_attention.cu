@@ -590,12 +590,38 @@ struct PreParams {
   uint32_t* status;
   int T, n_q, n_kv, G, n_qtiles;
   float scale_log2;
+  // Packed sequences (extend): sequence b owns rows cu_rows[b] .. cu_rows[b+1]-1
+  // at positions start_pos[b], start_pos[b] + 1, ...; null: T rows per
+  // sequence at positions 0 .. T-1.
+  const int32_t* cu_rows;
+  const int32_t* start_pos;
+  int n_rows;  // rows of Q and of the output
+  // K/V source: 0 = per-row buffers [rows, n_kv, d]; 1 = the KV cache (all
+  // keys 0 .. position of the row, earlier pieces included)
+  int from_cache, box_rows, layer, page_size, capacity, batch_cap, n_pages, max_pages;
+  const int32_t* page_table;
 };
+
+// Cache row of the keys starting at k0 (a multiple of 16) of sequence b, K/V
+// head g; a page id outside the pool is flagged and mapped to rows TMA fills
+// with zeros.
+__device__ __forceinline__ int pre_kv_row(const PreParams& p, int b, int g, int k0) {
+  if (p.page_size == 0) return (b * p.n_kv + g) * p.capacity + k0;
+  const int pi = k0 / p.page_size;
+  const int page = pi < p.max_pages ? p.page_table[(size_t)b * p.max_pages + pi] : -1;
+  if (page < 0 || page >= p.n_pages) {
+    flag(p.status, LLAMA_FLAG_PAGE_RANGE);
+    return -4 * SUBK;
+  }
+  return (page * p.n_kv + g) * p.page_size + (k0 % p.page_size);
+}
 
 __global__ void __launch_bounds__(PRE_THREADS, 2)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap mapQ,
                         const __grid_constant__ CUtensorMap mapK,
-                        const __grid_constant__ CUtensorMap mapV, PreParams p) {
+                        const __grid_constant__ CUtensorMap mapV,
+                        const __grid_constant__ CUtensorMap mapK16,
+                        const __grid_constant__ CUtensorMap mapV16, PreParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -612,9 +638,20 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / p.G;
   const int q0 = qt * PQ;
-  const int n_kt = min(qt + 1, (p.T + PK - 1) / PK);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rowbase = b * p.T;
+  const int rowbase = p.cu_rows ? p.cu_rows[b] : b * p.T;
+  const int n_b = p.cu_rows ? p.cu_rows[b + 1] - rowbase : p.T;  // this sequence's rows
+  const int start = p.start_pos ? p.start_pos[b] : 0;             // position of its first row
+  if (q0 >= n_b) return;
+  if (p.from_cache) {  // the sequence's keys must fit its cache slots
+    const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
+    if (start < 0 || start > cap_keys - n_b) {
+      if (threadIdx.x == 0) flag(p.status, LLAMA_FLAG_POS_RANGE);
+      return;
+    }
+  }
+  const int n_keys = start + n_b;  // keys 0 .. n_keys - 1 exist once the rows are appended
+  const int n_kt = (start + min(q0 + PQ, n_b) - 1) / PK + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
@@ -632,6 +669,10 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
       tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
+      if (p.from_cache) {
+        tma_prefetch_desc(&mapK16);
+        tma_prefetch_desc(&mapV16);
+      }
       mbar_arrive_expect_tx(qfull, p.q_lo_rows ? 2 * PTILE : PTILE);
       tma_load_3d(qs, &mapQ, qfull, 0, h, rowbase + q0);
       tma_load_3d(qs + PHALF, &mapQ, qfull, 64, h, rowbase + q0);
@@ -650,11 +691,32 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
           break;
         }
         uint8_t* ks = kvs + s * 2 * PTILE;
-        mbar_arrive_expect_tx(&full[s], 2 * PTILE);
-        tma_load_3d(ks, &mapK, &full[s], 0, g, rowbase + kt * PK);
-        tma_load_3d(ks + PHALF, &mapK, &full[s], 64, g, rowbase + kt * PK);
-        tma_load_3d(ks + PTILE, &mapV, &full[s], 0, g, rowbase + kt * PK);
-        tma_load_3d(ks + PTILE + PHALF, &mapV, &full[s], 64, g, rowbase + kt * PK);
+        const int k0 = kt * PK, nvalid = min(PK, n_keys - k0);
+        if (!p.from_cache) {
+          mbar_arrive_expect_tx(&full[s], 2 * PTILE);
+          tma_load_3d(ks, &mapK, &full[s], 0, g, rowbase + k0);
+          tma_load_3d(ks + PHALF, &mapK, &full[s], 64, g, rowbase + k0);
+          tma_load_3d(ks + PTILE, &mapV, &full[s], 0, g, rowbase + k0);
+          tma_load_3d(ks + PTILE + PHALF, &mapV, &full[s], 64, g, rowbase + k0);
+        } else if (p.box_rows == PK && nvalid == PK) {  // 64 contiguous keys: one box per half
+          const int row = pre_kv_row(p, b, g, k0);
+          mbar_arrive_expect_tx(&full[s], 2 * PTILE);
+          tma_load_3d(ks, &mapK, &full[s], 0, row, p.layer);
+          tma_load_3d(ks + PHALF, &mapK, &full[s], 64, row, p.layer);
+          tma_load_3d(ks + PTILE, &mapV, &full[s], 0, row, p.layer);
+          tma_load_3d(ks + PTILE + PHALF, &mapV, &full[s], 64, row, p.layer);
+        } else {  // 16-key boxes, only those holding keys of this sequence
+          const int nsub = (nvalid + SUBK - 1) / SUBK;
+          mbar_arrive_expect_tx(&full[s], nsub * 4 * HALF_BYTES);
+          for (int j = 0; j < nsub; ++j) {
+            const int row = pre_kv_row(p, b, g, k0 + j * SUBK);
+            uint8_t* kd = ks + j * HALF_BYTES;
+            tma_load_3d(kd, &mapK16, &full[s], 0, row, p.layer);
+            tma_load_3d(kd + PHALF, &mapK16, &full[s], 64, row, p.layer);
+            tma_load_3d(kd + PTILE, &mapV16, &full[s], 0, row, p.layer);
+            tma_load_3d(kd + PTILE + PHALF, &mapV16, &full[s], 64, row, p.layer);
+          }
+        }
         ++issued;
       }
       mbar_wait(qfull, 0, p.status);
@@ -693,6 +755,21 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
       *abort_flag = 1;
       break;
     }
+    const int nvalid = min(PK, n_keys - kt * PK);
+    if (nvalid < PK) {
+      // V rows past the last key may hold anything (P is 0 there, but 0 * NaN
+      // is not): every warp zeroes all of them itself, so no warp waits for
+      // another (they all store the same zeros)
+      uint8_t* vt = kvs + s * 2 * PTILE + PTILE;
+      const int nz = (PK - nvalid) * 16;
+      for (int i = lane; i < nz; i += 32) {
+        const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
+        *reinterpret_cast<uint4*>(vt + half * PHALF + row * 128 + chunk * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
     const uint32_t kb = smem_u32(kvs + s * 2 * PTILE);
     const uint32_t vb = kb + PTILE;
     float sc[8][4];
@@ -724,8 +801,8 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int key = kt * PK + nb * 8 + 2 * (lane & 3) + (i & 1);
-        const int row = myrow0 + (i >= 2 ? 8 : 0);
-        const float v = (key <= row && key < p.T) ? sc[nb][i] * p.scale_log2 : -INFINITY;
+        const int qpos = start + myrow0 + (i >= 2 ? 8 : 0);
+        const float v = (key <= qpos && key < n_keys) ? sc[nb][i] * p.scale_log2 : -INFINITY;
         sc[nb][i] = v;
         mx[i >> 1] = fmaxf(mx[i >> 1], v);
       }
@@ -790,7 +867,7 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const int row = myrow0 + hh * 8;
-    if (row >= p.T) continue;
+    if (row >= n_b || rowbase + row >= p.n_rows) continue;
     const float inv = lrow[hh] > 0.f ? 1.f / lrow[hh] : 0.f;
     bf16* dst = p.out + (size_t)(rowbase + row) * ld + (size_t)h * AD;
 #pragma unroll
@@ -1031,8 +1108,23 @@ cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_
   p.G = a.n_q / a.n_kv;
   p.n_qtiles = (a.T + PQ - 1) / PQ;
   p.scale_log2 = kLog2e / sqrtf((float)AD);
+  p.cu_rows = a.cu_rows;
+  p.start_pos = a.start_pos;
+  p.n_rows = a.cu_rows ? a.n_rows : a.B * a.T;
+  p.from_cache = a.from_cache;
+  p.box_rows = a.box_rows == PK ? PK : SUBK;
+  p.layer = a.layer;
+  p.page_size = a.page_size;
+  p.capacity = a.capacity;
+  p.batch_cap = a.batch_cap;
+  p.n_pages = a.n_pages;
+  p.max_pages = a.max_pages;
+  p.page_table = a.page_table;
+  if (a.from_cache && (!a.map_k16 || !a.map_v16)) return cudaErrorInvalidValue;
+  const CUtensorMap* k16 = a.from_cache ? a.map_k16 : a.map_k;
+  const CUtensorMap* v16 = a.from_cache ? a.map_v16 : a.map_v;
   return launch_k(attn_prefill_kernel, dim3(p.n_qtiles, a.n_q, a.B), dim3(PRE_THREADS), PRE_SMEM,
-                  st, 0, *a.map_q, *a.map_k, *a.map_v, p);
+                  st, 0, *a.map_q, *a.map_k, *a.map_v, *k16, *v16, p);
 }
 
 }  // namespace llgb

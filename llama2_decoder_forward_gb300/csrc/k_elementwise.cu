@@ -40,7 +40,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, int in_stride,
                                                       int in_offset, const T* __restrict__ gamma,
                                                       int H, float eps, T* __restrict__ out,
-                                                      int lo_rows) {
+                                                      int lo_rows, const int32_t* row_end,
+                                                      int n_in, uint32_t* status) {
   grid_dep_wait();
   grid_dep_launch();
   const size_t lo = (size_t)lo_rows * H;
@@ -48,6 +49,15 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
   const int r = blockIdx.x;
   const float* xr = x + ((size_t)r * in_stride + in_offset) * H;
   T* yr = out + (size_t)r * H;
+  if (row_end) {  // the last row of packed sequence r
+    const int src = row_end[r] - 1;
+    if (src < 0 || src >= n_in) {
+      if (threadIdx.x == 0) flag(status, LLAMA_FLAG_TOKEN_RANGE);
+      for (int i = threadIdx.x; i < H; i += blockDim.x) store_y(yr, lo, i, 0.f);
+      return;
+    }
+    xr = x + (size_t)src * H;
+  }
   float ss = 0.f;
   const bool vec = (H % 4) == 0;
   if (vec) {
@@ -115,8 +125,19 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
   grid_dep_wait();
   grid_dep_launch();
   const int r = blockIdx.y;
-  const int b = r / a.rows_per_seq;
-  const int pos = a.positions ? a.positions[r] : (r % a.rows_per_seq);
+  int b, pos;
+  if (a.cu_rows) {  // packed rows of several sequences: find r's sequence
+    int lo = 0, hi = a.n_seq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.cu_rows[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    pos = a.start_pos[b] + r - a.cu_rows[b];
+  } else {
+    b = r / a.rows_per_seq;
+    pos = a.positions ? a.positions[r] : (r % a.rows_per_seq);
+  }
   const int d = a.head_dim;
   const int qw = a.n_q * d, kw = a.n_kv * d;
   const int width = qw + 2 * kw;
@@ -253,12 +274,12 @@ cudaError_t launch_embed(int dtype, const int32_t* tokens, const void* table, in
 
 cudaError_t launch_rmsnorm(int dtype, const float* x, int rows, int in_stride, int in_offset,
                            const void* gamma, int H, float eps, void* out, int lo_rows,
-                           cudaStream_t st) {
+                           cudaStream_t st, const int32_t* row_end, int n_in, uint32_t* status) {
   if (dtype == LLAMA_BF16)
     return launch_k(rmsnorm_kernel<bf16>, dim3(rows), dim3(256), 0, st, 0, x, in_stride, in_offset,
-                    (const bf16*)gamma, H, eps, (bf16*)out, lo_rows);
+                    (const bf16*)gamma, H, eps, (bf16*)out, lo_rows, row_end, n_in, status);
   return launch_k(rmsnorm_kernel<float>, dim3(rows), dim3(256), 0, st, 0, x, in_stride, in_offset,
-                  (const float*)gamma, H, eps, (float*)out, 0);
+                  (const float*)gamma, H, eps, (float*)out, 0, row_end, n_in, status);
 }
 
 cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double theta,
