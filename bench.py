@@ -7,7 +7,7 @@ RMSNorm, LM head and greedy argmax, for 32 sequences. Weights are random
 N(0, 0.02) bf16 of the 7B architecture, the cache holds N(0, 1) bf16 values at
 positions 0..1023 of every layer, token ids are uniform; all synthetic.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload model|layer]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload model|layer|prefill|extend]
   python bench.py --impl reference ...   (the CPU oracle on a bounded sample)
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own replica of
@@ -400,6 +400,94 @@ def run_prefill(args):
     print(json.dumps(line), flush=True)
 
 
+def run_extend(args):
+    """One continuous-batching step on the full 7B model: 28 sequences decode
+    one token at position 1024 while 4 others feed a 256-token prompt piece
+    at positions 512..767, all in one llama_extend call (1052 rows)."""
+    import torch
+    import __graft_entry__
+    from llama2_decoder_forward_gb300 import binding, synth
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    __graft_entry__.build()
+    n_dec, n_pre, piece, ctx, pstart, cap = 28, 4, 256, 1024, 512, 1040
+    B = n_dec + n_pre
+    shape = synth.LLAMA2_7B
+    g = torch.Generator(device=dev)
+    g.manual_seed(1005)
+
+    def rn(*s, std=0.02, mean=0.0):
+        t = torch.randn(*s, generator=g, device=dev, dtype=torch.float32)
+        return t.mul_(std).add_(mean).to(torch.bfloat16)
+
+    H, I, V = shape.hidden, shape.intermediate, shape.vocab
+    w = {"layers": [{"attn_norm": rn(H, std=0.1, mean=1.0), "wqkv": rn(shape.qkv_rows, H), "wo": rn(H, H),
+                     "ffn_norm": rn(H, std=0.1, mean=1.0), "w_gate": rn(I, H), "w_up": rn(I, H),
+                     "w_down": rn(H, I)} for _ in range(shape.n_layers)],
+         "embed": rn(V, H), "final_norm": rn(H, std=0.1, mean=1.0), "lm_head": rn(V, H)}
+    counts = [1] * n_dec + [piece] * n_pre
+    starts = [ctx] * n_dec + [pstart] * n_pre
+    rows = sum(counts)
+    model = binding.Model(shape, w, max_batch=B, max_tokens=rows, max_seq=cap)
+    kv = binding.KVCache(shape, batch=B, capacity=cap)
+    kv.k.normal_(generator=g)
+    kv.v.normal_(generator=g)
+    tokens = torch.randint(0, V, (rows,), generator=g, device=dev, dtype=torch.int32)
+    cu = torch.tensor([0] + [sum(counts[:i + 1]) for i in range(B)], dtype=torch.int32, device=dev)
+    st = torch.tensor(starts, dtype=torch.int32, device=dev)
+    logits = torch.empty(B, V, device=dev)
+    ids = torch.empty(B, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        model.extend(tokens, cu, st, kv, logits, ids, max_rows=piece)
+
+    for _ in range(args.warmup):
+        step()
+    model.sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(0) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    model.profile(["gemm", "attn_prefill", "attn_decode"])
+    for _ in range(args.steps):
+        step()
+    gemm_ms, gemm_n = model.profile_read("gemm")
+    att_ms, att_n = model.profile_read("attn_prefill")
+    dec_ms, dec_n = model.profile_read("attn_decode")
+    model.profile([])
+    model.sync()
+    layer_params = shape.qkv_rows * H + H * H + 3 * H * I
+    gemm_flops = 2.0 * rows * layer_params * shape.n_layers + 2.0 * B * V * H
+    keys = n_pre * sum(pstart + i + 1 for i in range(piece))  # rows of the prompt pieces
+    att_bytes = n_dec * (ctx + 1) * shape.n_kv_heads * shape.head_dim * 4 * shape.n_layers
+    hbm, tflops, peak_kind = _peaks()
+    g_tf = gemm_flops / (gemm_ms / args.steps * 1e-3) / 1e12
+    line = {"metric": "Llama2-7B continuous-batching step tokens/s (28 decode + 4 x 256-token prompt pieces)",
+            "value": rows / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init 7B weights, uniform ids, N(0,1) cache)",
+            "config": {"workload": "llama2-7b extend step: 28 sequences decode at position 1024, 4 feed "
+                                   "256-token prompt pieces at positions 512..767; one call, 1052 rows"},
+            "roofline": {"kernel": "gemm_tc_kernel (all projections of the 1052 rows)", "bound": "tensor",
+                         "achieved": g_tf, "peak": tflops, "unit": "TFLOP/s", "frac": g_tf / tflops,
+                         "peak_source": peak_kind, "traffic": None,
+                         "algorithmic_flops_per_step": gemm_flops, "launches_per_step": gemm_n / args.steps},
+            "kernels": {"gemm_ms_per_step": gemm_ms / args.steps,
+                        "piece_attn_ms_per_step": att_ms / args.steps,
+                        "piece_attn_tflops": 4.0 * shape.n_q_heads * shape.head_dim * keys * shape.n_layers
+                        / (att_ms / args.steps * 1e-3) / 1e12 if att_ms else None,
+                        "decode_attn_ms_per_step": dec_ms / args.steps,
+                        "decode_attn_gbs": att_bytes / (dec_ms / args.steps * 1e-3) / 1e9 if dec_ms else None},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 class OracleSample:
     """The oracle on a bounded sample: one 7B layer's decode step for the 32
@@ -492,7 +580,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="model", choices=["model", "layer", "prefill"])
+    ap.add_argument("--workload", default="model", choices=["model", "layer", "prefill", "extend"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels directly")
     args = ap.parse_args()
@@ -504,6 +592,8 @@ def main():
         run_reference(args)
     elif args.workload == "prefill":
         run_prefill(args)
+    elif args.workload == "extend":
+        run_extend(args)
     else:
         run_gpu(args)
 

@@ -360,8 +360,10 @@ int do_rope_append(llama_ctx* c, const float* qkv, int rows, int rows_per_seq,
 }
 
 int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B, int layer,
-                   const llama_kv* kv, void* out, size_t out_lo = 0, size_t q_lo = 0) {
+                   const llama_kv* kv, void* out, size_t out_lo = 0, size_t q_lo = 0,
+                   const int32_t* cu_rows = nullptr) {
   AttnDecodeArgs a{};
+  a.cu_rows = cu_rows;
   a.out_lo = out_lo;
   a.q_lo = q_lo;
   a.q = q;
@@ -508,7 +510,8 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   if (rm) {  // extend: RoPE/append, then attention over the cache
     TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
     TRY(do_rope_append(c, qkv, rows, 1, nullptr, l, kv, q, nullptr, nullptr, q_lo, rm));
-    TRY(do_attn_extend(c, q, rows, *rm, l, kv, o, q_lo, lo));
+    TRY(do_attn_extend(c, q, rows, *rm, l, kv, o, q_lo, lo));  // pieces of 2+ rows
+    TRY(do_attn_decode(c, q, rm->start_pos, rm->B, l, kv, o, q_lo, q_lo, rm->cu_rows));  // 1 row
   } else if (cf.dtype == LLAMA_BF16 && !prefill) {
     // Q/K/V projection with RoPE and the cache append in its epilogue. Prefill
     // keeps them in a separate kernel: its GEMM runs one CTA per SM with the

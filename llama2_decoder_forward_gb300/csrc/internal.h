@@ -139,6 +139,9 @@ struct AttnDecodeArgs {
   int B, n_q, n_kv, head_dim, layer;
   int page_size, capacity, batch_cap, n_pages, max_pages;
   int max_keys;              // upper bound of positions[b] + 1 (sizes the split count)
+  // extend steps: only sequences with one new row (cu_rows[b+1] - cu_rows[b]
+  // == 1) are handled, their q / output row being cu_rows[b]; null: row b
+  const int32_t* cu_rows = nullptr;
   int sm_count;
 };
 size_t attn_decode_partial_bytes(int B, int n_q, int head_dim, int max_keys, int sm_count,

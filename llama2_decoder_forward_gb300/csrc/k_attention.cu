@@ -56,6 +56,9 @@ struct DecParams {
   int splits, keys_per_split;
   int box_rows;  // 64: one TMA box per K/V half of a tile; 16: one per sub-tile
   float scale_log2;
+  // extend steps: sequence b is handled only when it has exactly one new row,
+  // which is row cu_rows[b] of q and of the output (null: row b)
+  const int32_t* cu_rows;
 };
 
 // Number of keys sequence b attends (positions[b] + 1), clamped to the cache;
@@ -417,6 +420,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
+  int qrow = b;  // row of q and of the output
+  if (p.cu_rows) {
+    qrow = p.cu_rows[b];
+    if (p.cu_rows[b + 1] - qrow != 1) {  // longer pieces go to the prefill-style kernel
+      grid_dep_wait();
+      return;
+    }
+  }
   // positions and the page table are caller inputs, complete before the step
   const int n_keys = decode_keys(p.positions[b], cap_keys);
   const int kbeg = split * p.keys_per_split;
@@ -497,10 +508,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   grid_dep_wait();  // q comes from the RoPE/append kernel
   grid_dep_launch();
   if (KEYMAJOR)
-    decode_consume_keymajor(p, smem, full, empty, abort_flag, b, g, kbeg, kend, n_sub, n_tiles,
+    decode_consume_keymajor(p, smem, full, empty, abort_flag, qrow, g, kbeg, kend, n_sub, n_tiles,
                             warp, lane);
   else
-    decode_consume_mma(p, smem, full, empty, abort_flag, b, g, kbeg, kend, n_sub, n_tiles, warp,
+    decode_consume_mma(p, smem, full, empty, abort_flag, qrow, g, kbeg, kend, n_sub, n_tiles, warp,
                        lane);
   const int G = p.G;
   float* so = reinterpret_cast<float*>(smem);  // [4][16][128]
@@ -525,10 +536,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     }
     const size_t bh = (size_t)b * p.n_q + (size_t)g * G + r;
     if (p.splits == 1) {
+      const size_t oh = (size_t)qrow * p.n_q + (size_t)g * G + r;
       const float v = L > 0.f ? O / L : 0.f;
       const bf16 hi = __float2bfloat16_rn(v);
-      p.out[bh * AD + t] = hi;
-      if (p.out_lo) p.out[bh * AD + t + p.out_lo] = __float2bfloat16_rn(v - __bfloat162float(hi));
+      p.out[oh * AD + t] = hi;
+      if (p.out_lo) p.out[oh * AD + t + p.out_lo] = __float2bfloat16_rn(v - __bfloat162float(hi));
     } else {
       float* pp = p.part + (bh * p.splits + split) * (AD + 2);
       pp[t] = O;
@@ -545,11 +557,16 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
 __global__ void attn_combine_kernel(const float* __restrict__ part,
                                     const int32_t* __restrict__ positions, int n_q, int splits,
                                     int keys_per_split, int cap_keys, int d, void* out,
-                                    size_t out_lo) {
+                                    size_t out_lo, const int32_t* cu_rows) {
   grid_dep_wait();
   grid_dep_launch();
   const int bh = blockIdx.x;
   const int b = bh / n_q;
+  size_t oh = bh;  // output row-head
+  if (cu_rows) {
+    if (cu_rows[b + 1] - cu_rows[b] != 1) return;
+    oh = (size_t)cu_rows[b] * n_q + (bh - (size_t)b * n_q);
+  }
   const int n_keys = decode_keys(positions[b], cap_keys);
   const int used = min(splits, (n_keys + keys_per_split - 1) / keys_per_split);
   const float* pp = part + (size_t)bh * splits * (d + 2);
@@ -567,9 +584,9 @@ __global__ void attn_combine_kernel(const float* __restrict__ part,
     }
     const float v = L > 0.f ? O / L : 0.f;
     const bf16 hi = __float2bfloat16_rn(v);
-    reinterpret_cast<bf16*>(out)[(size_t)bh * d + t] = hi;
+    reinterpret_cast<bf16*>(out)[oh * d + t] = hi;
     if (out_lo)
-      reinterpret_cast<bf16*>(out)[(size_t)bh * d + t + out_lo] =
+      reinterpret_cast<bf16*>(out)[oh * d + t + out_lo] =
           __float2bfloat16_rn(v - __bfloat162float(hi));
   }
 }
@@ -643,6 +660,7 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
   const int n_b = p.cu_rows ? p.cu_rows[b + 1] - rowbase : p.T;  // this sequence's rows
   const int start = p.start_pos ? p.start_pos[b] : 0;             // position of its first row
   if (q0 >= n_b) return;
+  if (p.cu_rows && p.from_cache && n_b == 1) return;  // single new rows: the decode kernel's
   if (p.from_cache) {  // the sequence's keys must fit its cache slots
     const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
     if (start < 0 || start > cap_keys - n_b) {
@@ -1063,6 +1081,7 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.splits = splits;
   p.keys_per_split = kps;
   p.box_rows = a.box_rows == DTILE ? DTILE : SUBK;
+  p.cu_rows = a.cu_rows;
   p.scale_log2 = kLog2e / sqrtf((float)AD);
   const bool keymajor = p.G <= kKeyMajorMaxG;
   cudaError_t e = keymajor ? launch_k(attn_decode_kernel<true>, dim3(splits, a.n_kv, a.B),
@@ -1075,7 +1094,7 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
   return launch_k(attn_combine_kernel, dim3(a.B * a.n_q), dim3(AD), 0, st, 0,
                   (const float*)a.partial, a.positions, a.n_q, splits, kps, cap_keys, AD, a.out,
-                  a.out_lo);
+                  a.out_lo, a.cu_rows);
 }
 
 int attn_decode_launches(int B, int n_kv, int max_keys, int sm_count, int dtype) {
