@@ -71,13 +71,40 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     return np.ldexp(np.rint(m * 256.0) / 256.0, e)
 
 
-def cache_store(values: np.ndarray, cache_dtype: str) -> np.ndarray:
-    """Values as a KV cache of the given storage type holds them."""
+E4M3_MAX = 448.0  # largest finite FP8 E4M3 value (1.75 * 2^8)
+
+
+def round_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Nearest FP8 E4M3 value, ties to even, saturating at +-448: 3 fraction
+    bits, exponent bias 7, smallest normal 2^-6, subnormal spacing 2^-9. With
+    |x| = m * 2^e, m in [0.5, 1), the spacing is 2^(max(e - 1, -6) - 3)."""
+    x = np.asarray(x, dtype=f64)
+    a = np.abs(x)
+    _, e = np.frexp(a)
+    step = np.maximum(e - 1, -6) - 3
+    q = np.ldexp(np.rint(np.ldexp(a, -step)), step)
+    return np.sign(x) * np.minimum(q, E4M3_MAX)
+
+
+def cache_store(values: np.ndarray, cache_dtype: str, scale: float = 1.0) -> np.ndarray:
+    """Values as a KV cache of the given storage type holds them. "e4m3"
+    stores e4m3(v / scale) and reads it back times scale (the FP8 cache of
+    "Llama2架构全景解析" §3.2, reading R28)."""
     if cache_dtype == "bf16":
         return round_to_bf16(values)
     if cache_dtype == "f32":
         return np.asarray(values, dtype=np.float32).astype(f64)
+    if cache_dtype == "e4m3":
+        return round_to_e4m3(np.asarray(values, dtype=f64) / scale) * scale
     return np.asarray(values, dtype=f64)
+
+
+def _kv_store(cdt, k, v):
+    """K and V as stored: cdt is a storage type, or ("e4m3", k_scale, v_scale)."""
+    if isinstance(cdt, tuple):
+        name, ks, vs = cdt
+        return cache_store(k, name, ks), cache_store(v, name, vs)
+    return cache_store(k, cdt), cache_store(v, cdt)
 
 def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     """RMSNorm over the last axis, each token on its own
@@ -185,8 +212,7 @@ def layer_decode(x, lw, shape, K, V, positions, cache_dtype=None):
     o = np.empty((B, n_q, d), dtype=f64)
     for b in range(B):
         m = int(pos[b])
-        K[b, :, m] = cache_store(k[b], cdt)
-        V[b, :, m] = cache_store(v[b], cdt)
+        K[b, :, m], V[b, :, m] = _kv_store(cdt, k[b], v[b])
         o[b] = gqa_attention(q[b], K[b], V[b], m + 1)
     h = x + linear(o.reshape(B, n_q * d), lw["wo"])
     u2 = rmsnorm(h, lw["ffn_norm"], shape.rms_eps)
@@ -217,8 +243,8 @@ def layer_prefill(x, lw, shape, K, V, rows=None, cache_dtype=None):
         k = kv[:, : n_kv * d].reshape(T, n_kv, d)
         v = kv[:, n_kv * d:].reshape(T, n_kv, d)
         k = rope(k, pos_all, shape.rope_theta)
-        K[b, :, :T] = cache_store(np.transpose(k, (1, 0, 2)), cdt)
-        V[b, :, :T] = cache_store(np.transpose(v, (1, 0, 2)), cdt)
+        K[b, :, :T], V[b, :, :T] = _kv_store(cdt, np.transpose(k, (1, 0, 2)),
+                                             np.transpose(v, (1, 0, 2)))
         q = linear(u[q_rows], wq).reshape(len(rows), n_q, d)
         q = rope(q, q_rows, shape.rope_theta)
         o = np.empty((len(rows), n_q, d), dtype=f64)
@@ -253,8 +279,7 @@ def layer_extend(x, lw, shape, K, V, seq_of_row, positions, cache_dtype=None):
     q = rope(q, pos, shape.rope_theta)
     k = rope(k, pos, shape.rope_theta)
     for r in range(R):
-        K[seq[r], :, pos[r]] = cache_store(k[r], cdt)
-        V[seq[r], :, pos[r]] = cache_store(v[r], cdt)
+        K[seq[r], :, pos[r]], V[seq[r], :, pos[r]] = _kv_store(cdt, k[r], v[r])
     o = np.empty((R, n_q, d), dtype=f64)
     for r in range(R):
         o[r] = gqa_attention(q[r], K[seq[r]], V[seq[r]], int(pos[r]) + 1)

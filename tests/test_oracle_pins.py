@@ -496,3 +496,37 @@ def test_extend_of_one_token_per_sequence_is_decode():
     want = a.decode(toks[:, 5], np.full(3, 5))
     got = b.extend(toks[:, 5], np.arange(3), np.full(3, 5))
     np.testing.assert_array_equal(got, want)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) cache storage
+
+def test_round_to_e4m3_hand_values():
+    x = np.array([0.0, 1.0625, 1.1875, 17.0, 19.0, 2.0**-9, 2.0**-10, 3 * 2.0**-11, 2.0**-6,
+                  448.0, 464.0, 500.0, -500.0, -0.3])
+    want = np.array([0.0, 1.0, 1.25, 16.0, 20.0, 2.0**-9, 0.0, 2.0**-9, 2.0**-6,
+                     448.0, 448.0, 448.0, -448.0, -0.3125])
+    np.testing.assert_array_equal(O.round_to_e4m3(x), want)
+
+
+def test_round_to_e4m3_matches_library_cast():
+    rng = np.random.default_rng(31)
+    x = np.concatenate([rng.standard_normal(50000) * 40, rng.standard_normal(50000) * 0.01])
+    x = np.clip(x, -448, 448).astype(np.float32)
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_to_e4m3(x.astype(np.float64)), lib)
+
+
+def test_e4m3_cache_stores_scaled_values_and_decode_still_equals_prefill():
+    shape = synth.TINY
+    w = synth.model_weights(shape, 1004)
+    toks = synth.token_ids(2, 9, shape.vocab, 1004).numpy()
+    cdt = ("e4m3", 0.05, 0.03)
+    full = O.Model(shape, w, 2, 12, cache_dtype=cdt).prefill(toks)
+    m = O.Model(shape, w, 2, 12, cache_dtype=cdt)
+    m.prefill(toks[:, :6])
+    for t in range(6, 9):
+        np.testing.assert_allclose(m.decode(toks[:, t], np.full(2, t)), full[:, t], rtol=1e-10,
+                                   atol=1e-12)
+    k = m.K[0][:, :, :9] / 0.05  # every stored K is an E4M3 value times the scale
+    np.testing.assert_allclose(O.round_to_e4m3(k), k, rtol=1e-14, atol=0)
+    assert len(np.unique(np.round(np.abs(k[k != 0]), 9))) < 250  # at most 2 x 126 finite magnitudes
