@@ -131,7 +131,7 @@ def replica_result(ms_per_step, tokens_per_step, device=None):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def build_model(workload, device):
+def build_model(workload, device, kv_e4m3=False):
     import torch
     from llama2_decoder_forward_gb300 import binding, synth
 
@@ -154,10 +154,20 @@ def build_model(workload, device):
     w = {"layers": layers}
     if workload == "model":
         w.update(embed=rn(V, H), final_norm=rn(H, std=0.1, mean=1.0), lm_head=rn(V, H))
-    kv = binding.KVCache(shape, batch=B, capacity=CAP)
-    for t in (kv.k, kv.v):
-        t.view(-1, CAP, shape.head_dim)[:, :CTX].normal_(generator=g)
-        t.view(-1, CAP, shape.head_dim)[:, CTX:].zero_()
+    if kv_e4m3:  # one byte per value: N(0, 1) / scale rounded to E4M3
+        kv = binding.KVCache(shape, batch=B, capacity=CAP, e4m3=(1.0 / 64, 1.0 / 64))
+        for t in (kv.k, kv.v):
+            f = torch.randn(t.numel() // (CAP * shape.head_dim), CTX, shape.head_dim,
+                            generator=g, device=device) * 64
+            t.view(-1, CAP, shape.head_dim)[:, :CTX] = f.clamp_(-448, 448).to(
+                torch.float8_e4m3fn).view(torch.uint8)
+            t.view(-1, CAP, shape.head_dim)[:, CTX:].zero_()
+            del f
+    else:
+        kv = binding.KVCache(shape, batch=B, capacity=CAP)
+        for t in (kv.k, kv.v):
+            t.view(-1, CAP, shape.head_dim)[:, :CTX].normal_(generator=g)
+            t.view(-1, CAP, shape.head_dim)[:, CTX:].zero_()
     model = binding.Model(shape, w, max_batch=B, max_tokens=B, max_seq=CAP,
                           has_embed_head=(workload == "model"))
     return shape, model, kv
@@ -175,7 +185,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     __graft_entry__.build()
-    shape, model, kv = build_model(args.workload, dev)
+    shape, model, kv = build_model(args.workload, dev, kv_e4m3=args.kv == "e4m3")
     torch.cuda.synchronize()  # inputs are drawn on the default stream; the model runs on its own
     g = torch.Generator(device=dev)
     g.manual_seed(7)
@@ -284,7 +294,8 @@ def run_gpu(args):
         return
     hbm, tflops, peak_kind = _peaks()
     L = shape.n_layers
-    kv_bytes = B * shape.n_kv_heads * (CTX + 1) * shape.head_dim * 2 * 2  # K and V read per layer
+    kv_elem = 1 if args.kv == "e4m3" else 2
+    kv_bytes = B * shape.n_kv_heads * (CTX + 1) * shape.head_dim * 2 * kv_elem  # K and V per layer
     attn_avg = attn_ms / max(attn_n, 1)
     achieved = kv_bytes / (attn_avg * 1e-3) / 1e9
     wbytes = (shape.qkv_rows + shape.hidden) * shape.hidden * 2 + 3 * shape.hidden * shape.intermediate * 2
@@ -301,20 +312,21 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if args.kv == "bf16" else "bf16 (KV cache e4m3)",
         "data": "synthetic (random-init 7B weights N(0,0.02), cache N(0,1), uniform token ids)",
         "config": {"workload": ("llama2-7b decode step: 32 layers + embedding + LM head + greedy, "
                                 "batch 32, 1024 cached positions, contiguous KV")
                    if args.workload == "model" else
                    "one llama2-7b decoder layer, decode step, batch 32, 1024 cached positions",
-                   "batch": B, "context": CTX, "l2": "inputs larger than L2 (%.1f GB per step)" % (step_bytes / 1e9),
+                   "batch": B, "context": CTX, "kv_cache": args.kv, "l2": "inputs larger than L2 (%.1f GB per step)" % (step_bytes / 1e9),
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "launch": "cuda graph of the step" if use_graph else "direct launches"},
         "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
         "step_hbm_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm,
         "roofline": {"kernel": "attn_decode (flash-decode over the KV cache)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": peak_kind, "traffic": _traffic("attn_decode"),
+                     "peak_source": peak_kind,
+                     "traffic": _traffic("attn_decode") if args.kv == "bf16" else None,
                      "algorithmic_bytes_per_launch": kv_bytes, "avg_launch_ms": attn_avg,
                      "launches": attn_n},
         "kernels": {"attn_decode_ms_per_step": attn_ms / args.steps,
@@ -583,6 +595,8 @@ def main():
     ap.add_argument("--workload", default="model", choices=["model", "layer", "prefill", "extend"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels directly")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
+                    help="KV-cache storage (e4m3: the FP8 cache; not the headline configuration)")
     args = ap.parse_args()
     global B_WORKLOAD
     B_WORKLOAD = args.workload

@@ -121,7 +121,16 @@ typedef struct llama_weights {
  *   page_table : DEVICE int32 [batch][max_pages_per_seq]; token m of sequence
  *                b lives in page page_table[b][m / page_size], slot
  *                m % page_size.
- * The cache stores the RoPE-rotated K and the plain V. */
+ * The cache stores the RoPE-rotated K and the plain V.
+ * Element type (kv_dtype): LLAMA_KV_MODEL (0) — the config's dtype; or
+ * LLAMA_KV_E4M3 (1) — one FP8 E4M3 byte per value (bf16 models only, head_dim
+ * 128): a stored byte q means e4m3(q) * k_scale for K, * v_scale for V; values
+ * are written as e4m3(x / scale), nearest with ties to even, saturating at
+ * +-448 (the FP8 option of "Llama2架构全景解析" §3.2; half the bytes the decode
+ * attention streams). An E4M3 cache serves prefill and decode; llama_extend and
+ * llama_attention_decode_noalloc answer UNSUPPORTED for it. */
+#define LLAMA_KV_MODEL 0
+#define LLAMA_KV_E4M3 1
 typedef struct llama_kv {
   void* k;
   void* v;
@@ -131,6 +140,9 @@ typedef struct llama_kv {
   int32_t n_pages;
   const int32_t* page_table;
   int32_t max_pages_per_seq;
+  int32_t kv_dtype;  /* LLAMA_KV_MODEL or LLAMA_KV_E4M3 */
+  float k_scale;     /* E4M3 only, > 0 */
+  float v_scale;     /* E4M3 only, > 0 */
 } llama_kv;
 
 typedef struct llama_ctx llama_ctx;

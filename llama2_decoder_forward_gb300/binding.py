@@ -50,10 +50,14 @@ class Sampling(ctypes.Structure):
                 ("repetition_penalty", ctypes.c_float)]
 
 
+KV_MODEL, KV_E4M3 = 0, 1
+
+
 class KV(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("page_size", c_int32), ("capacity", c_int32),
                 ("batch_capacity", c_int32), ("n_pages", c_int32), ("page_table", c_void_p),
-                ("max_pages_per_seq", c_int32)]
+                ("max_pages_per_seq", c_int32), ("kv_dtype", c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
 
 
 _SIGS = {
@@ -164,12 +168,16 @@ class KVCache:
 
     contiguous: k, v [n_layers, batch, n_kv, capacity, d]
     paged     : k, v [n_layers, n_pages, n_kv, page_size, d] + page_table [B, max_pages] int32
+    e4m3=(k_scale, v_scale): one FP8 E4M3 byte per value (uint8 tensors), read
+    back as e4m3 * scale.
     """
 
     def __init__(self, shape, *, batch=None, capacity=None, n_pages=None, page_size=0,
-                 page_table=None, dtype=None, device="cuda", k=None, v=None):
+                 page_table=None, dtype=None, device="cuda", k=None, v=None, e4m3=None):
         import torch
-        dt = dtype or shape.torch_dtype
+        self.kv_dtype = KV_E4M3 if e4m3 else KV_MODEL
+        self.k_scale, self.v_scale = e4m3 if e4m3 else (1.0, 1.0)
+        dt = torch.uint8 if e4m3 else (dtype or shape.torch_dtype)
         L, nkv, d = shape.n_layers, shape.n_kv_heads, shape.head_dim
         self.page_size = page_size
         self.page_table = page_table
@@ -187,7 +195,7 @@ class KVCache:
     def struct(self) -> KV:
         return KV(self.k.data_ptr(), self.v.data_ptr(), self.page_size, self.capacity, self.batch,
                   self.n_pages, None if self.page_table is None else self.page_table.data_ptr(),
-                  self.max_pages)
+                  self.max_pages, self.kv_dtype, self.k_scale, self.v_scale)
 
 
 class Model:

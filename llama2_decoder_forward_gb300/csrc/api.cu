@@ -189,6 +189,26 @@ const CUtensorMap* map2d(llama_ctx* c, const void* ptr, uint64_t rows, uint64_t 
 }
 
 // 3D [d2][d1][d0] bf16 tensor (d0 innermost), box {64, b1, b2}, 128-byte swizzle.
+// 3D [d2][d1][d0] byte tensor (the FP8 cache, d0 = 128), box {128, b1, b2},
+// 128-byte swizzle.
+const CUtensorMap* map3d_u8(llama_ctx* c, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                            uint32_t b1, uint32_t b2) {
+  Key2 k{ptr, 4, d0, d1, d2, b1, b2};
+  auto it = c->maps.find(k);
+  if (it != c->maps.end()) return &it->second;
+  CUtensorMap m;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0, d0 * d1};
+  cuuint32_t box[3] = {128, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return nullptr;
+  return &c->maps.emplace(k, m).first->second;
+}
+
 const CUtensorMap* map3d(llama_ctx* c, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
                          uint32_t b1, uint32_t b2) {
   Key2 k{ptr, 3, d0, d1, d2, b1, b2};
@@ -244,6 +264,15 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA
 int check_kv(const llama_ctx* c, const llama_kv* kv, int B) {
   if (!kv || !kv->k || !kv->v) return LLAMA_ERR_INVALID_ARG;
   if (!aligned16(kv->k) || !aligned16(kv->v)) return LLAMA_ERR_INVALID_ARG;
+  if (kv->kv_dtype != LLAMA_KV_MODEL && kv->kv_dtype != LLAMA_KV_E4M3) return LLAMA_ERR_INVALID_ARG;
+  if (kv->kv_dtype == LLAMA_KV_E4M3) {
+    if (c->cfg.dtype != LLAMA_BF16 || c->cfg.head_dim != 128 ||
+        c->cfg.n_q_heads / c->cfg.n_kv_heads > 8)
+      return LLAMA_ERR_UNSUPPORTED;
+    if (!(kv->k_scale > 0.f) || !(kv->v_scale > 0.f) || !std::isfinite(kv->k_scale) ||
+        !std::isfinite(kv->v_scale))
+      return LLAMA_ERR_INVALID_ARG;
+  }
   const uint64_t nkv = c->cfg.n_kv_heads;
   uint64_t rows;
   if (kv->page_size == 0) {
@@ -332,6 +361,9 @@ RopeAppendArgs rope_args(const llama_ctx* c, const float* qkv, int rows_per_seq,
   a.batch_cap = kv->batch_capacity;
   a.n_pages = kv->n_pages;
   a.max_pages = kv->max_pages_per_seq;
+  a.kv_fp8 = kv->kv_dtype == LLAMA_KV_E4M3;
+  a.k_scale = kv->k_scale;
+  a.v_scale = kv->v_scale;
   return a;
 }
 
@@ -388,7 +420,21 @@ int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B,
   const int cap_keys = kv->page_size ? kv->max_pages_per_seq * kv->page_size : kv->capacity;
   a.max_keys = std::max(1, std::min(cap_keys, c->cfg.max_seq));
   a.sm_count = c->sm_count;
-  if (c->cfg.dtype == LLAMA_BF16) {
+  a.kv_fp8 = kv->kv_dtype == LLAMA_KV_E4M3;
+  a.k_scale = kv->k_scale;
+  a.v_scale = kv->v_scale;
+  if (a.kv_fp8) {  // byte views of the cache
+    trim_maps(c);
+    const uint64_t d = c->cfg.head_dim, nkv = c->cfg.n_kv_heads;
+    const uint64_t rows = kv->page_size ? (uint64_t)kv->n_pages * nkv * kv->page_size
+                                        : (uint64_t)kv->batch_capacity * nkv * kv->capacity;
+    a.box_rows = attn_decode_box_rows(kv->page_size);
+    a.map_k = map3d_u8(c, kv->k, d, rows, c->cfg.n_layers, a.box_rows, 1);
+    a.map_v = map3d_u8(c, kv->v, d, rows, c->cfg.n_layers, a.box_rows, 1);
+    a.map_k16 = map3d_u8(c, kv->k, d, rows, c->cfg.n_layers, 16, 1);
+    a.map_v16 = map3d_u8(c, kv->v, d, rows, c->cfg.n_layers, 16, 1);
+    if (!a.map_k || !a.map_v || !a.map_k16 || !a.map_v16) return LLAMA_ERR_CUDA;
+  } else if (c->cfg.dtype == LLAMA_BF16) {
     trim_maps(c);
     const uint64_t d = c->cfg.head_dim, nkv = c->cfg.n_kv_heads;
     const uint64_t rows = kv->page_size ? (uint64_t)kv->n_pages * nkv * kv->page_size
@@ -406,8 +452,11 @@ int do_attn_decode(llama_ctx* c, const void* q, const int32_t* positions, int B,
 }
 
 int do_attn_prefill(llama_ctx* c, const void* q, const void* k, const void* v, int B, int T,
-                    void* out, size_t out_lo = 0, int q_lo_rows = 0) {
+                    void* out, size_t out_lo = 0, int q_lo_rows = 0, float k_scale = 1.f,
+                    float v_scale = 1.f) {
   AttnPrefillArgs a{};
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.out_lo = out_lo;
   a.q_lo_rows = q_lo_rows;
   a.q = q;
@@ -524,8 +573,10 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   } else {
     TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
     TRY(do_rope_append(c, qkv, rows, rps, pos, l, kv, q, ks, vs, q_lo));
+    const bool f8 = kv->kv_dtype == LLAMA_KV_E4M3;  // side buffers hold unscaled E4M3 values
     if (prefill)
-      TRY(do_attn_prefill(c, q, ks, vs, B, T, o, q_lo, lo));
+      TRY(do_attn_prefill(c, q, ks, vs, B, T, o, q_lo, lo, f8 ? kv->k_scale : 1.f,
+                          f8 ? kv->v_scale : 1.f));
     else
       TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
   }
@@ -705,7 +756,8 @@ int check_extend(const llama_ctx* c, int32_t n_rows, const int32_t* cu_rows,
   if (cf.dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
   if (B > cf.max_batch || n_rows > std::max(cf.max_batch, cf.max_tokens))
     return LLAMA_ERR_OUT_OF_RANGE;
-  return check_kv(c, kv, B);
+  TRY(check_kv(c, kv, B));
+  return kv->kv_dtype == LLAMA_KV_MODEL ? LLAMA_OK : LLAMA_ERR_UNSUPPORTED;
 }
 }  // namespace
 

@@ -4,6 +4,8 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,6 +25,20 @@ template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __f
 // ------------------------------------------------------------------ status word
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
+}
+
+// FP8 E4M3 cache values: nearest with ties to even, saturating at +-448, and
+// back (exact in f16 / fp32).
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)q, __NV_E4M3)));
+}
+// Two E4M3 bytes (low byte first) as an f16x2 register (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t q2) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(q2 & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -196,6 +212,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 // Transpose an 8x8 b16 matrix held one 32-bit register per thread in the
 // MMA fragment layout (thread l: row l/4, columns 2(l%4), 2(l%4)+1).
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
@@ -208,6 +232,13 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
 __device__ __forceinline__ void split_pack(float v0, float v1, uint32_t& hi, uint32_t& rem) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
   const __nv_bfloat162 r = __floats2bfloat162_rn(v0 - __low2float(h), v1 - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  rem = *reinterpret_cast<const uint32_t*>(&r);
+}
+// The same as an f16 pair (hi = f16(v), rem = f16(v - hi)).
+__device__ __forceinline__ void split_pack_f16(float v0, float v1, uint32_t& hi, uint32_t& rem) {
+  const __half2 h = __floats2half2_rn(v0, v1);
+  const __half2 r = __floats2half2_rn(v0 - __low2float(h), v1 - __high2float(h));
   hi = *reinterpret_cast<const uint32_t*>(&h);
   rem = *reinterpret_cast<const uint32_t*>(&r);
 }

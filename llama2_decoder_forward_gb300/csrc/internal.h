@@ -55,6 +55,10 @@ struct RopeAppendArgs {
   const int32_t* cu_rows;    // [n_seq + 1] or null
   const int32_t* start_pos;  // [n_seq]
   int n_seq;
+  // FP8 E4M3 cache: byte = e4m3(x / scale); the K/V side buffers then hold the
+  // unscaled e4m3 values (exact in bf16)
+  int kv_fp8;
+  float k_scale, v_scale;
   const float2* rope;        // [max_seq, d/2] (cos, sin)
   void* q_out;               // [rows, n_q d]
   size_t q_lo;               // >0: also store bf16(q - bf16(q)) q_lo elements further
@@ -142,6 +146,9 @@ struct AttnDecodeArgs {
   // extend steps: only sequences with one new row (cu_rows[b+1] - cu_rows[b]
   // == 1) are handled, their q / output row being cu_rows[b]; null: row b
   const int32_t* cu_rows = nullptr;
+  // FP8 E4M3 cache (key-major groups only): maps over bytes, box {128, rows, 1}
+  int kv_fp8 = 0;
+  float k_scale = 1.f, v_scale = 1.f;
   int sm_count;
 };
 size_t attn_decode_partial_bytes(int B, int n_q, int head_dim, int max_keys, int sm_count,
@@ -178,6 +185,8 @@ struct AttnPrefillArgs {
   const int32_t* page_table = nullptr;
   const CUtensorMap* map_k16 = nullptr;
   const CUtensorMap* map_v16 = nullptr;
+  // K/V read as stored values times these (the FP8 cache's unscaled values)
+  float k_scale = 1.f, v_scale = 1.f;
 };
 cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_t st);
 cudaError_t attn_prepare();

@@ -41,6 +41,13 @@ constexpr uint32_t DSTAGE_BYTES = 4 * TILE_HALF;       // K and V, two dim halve
 // Stage layout: K dims 0-63 [64 keys][128 B], K dims 64-127, V dims 0-63,
 // V dims 64-127; 16-key sub-tile j of a half starts at j * HALF_BYTES.
 constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 256;
+// FP8 E4M3 cache: one byte per value, so a 64-key tile of K (or V) is one
+// 128-byte-swizzled box of 64 rows x 128 bytes; three CTAs per SM.
+constexpr int F8_STAGES = 4;
+constexpr uint32_t F8_TILE = DTILE * 128;  // K (or V) of 64 keys: 8 KB
+constexpr uint32_t F8_SUB = SUBK * 128;    // 16 keys: 2 KB
+constexpr uint32_t F8_STAGE = 2 * F8_TILE;
+constexpr size_t DEC_SMEM_F8 = F8_STAGES * F8_STAGE + 1024 + 256;
 
 struct DecParams {
   const bf16* q;
@@ -59,6 +66,7 @@ struct DecParams {
   // extend steps: sequence b is handled only when it has exactly one new row,
   // which is row cu_rows[b] of q and of the output (null: row b)
   const int32_t* cu_rows;
+  float v_scale;  // FP8 cache: V bytes are e4m3 * v_scale (1 otherwise; K's scale is in scale_log2)
 };
 
 // Number of keys sequence b attends (positions[b] + 1), clamped to the cache;
@@ -404,8 +412,194 @@ __device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint
   }
 }
 
-template <bool KEYMAJOR>
-__global__ void __launch_bounds__(DEC_THREADS, 2)
+// Consumer warps for an FP8 E4M3 cache (groups of at most 8 query heads),
+// key-major like decode_consume_keymajor but on f16 tensor-core MMAs: E4M3
+// values are exact in f16, so K and V enter the MMA unrounded; Q and P are
+// single f16 values (11 significant bits, against the 4 of every cached value:
+// a second, remainder MMA would buy nothing here). The stage holds K
+// [64 keys][128 bytes] then V the same.
+//  * S^T = K Q^T: ldmatrix on the byte rows gives each lane 4 consecutive
+//    dims of a key; their two f16 pairs serve as the fragment's k-columns
+//    (2t, 2t+1) and (2t+8, 2t+9). The head dims are thus taken in a permuted
+//    order, and Q's fragments use the same order, so the dot products are
+//    unchanged.
+//  * O^T += V^T P^T: the A fragment needs one dim of two keys per register,
+//    so each lane loads 4-byte words (4 dims) of its 4 keys and pairs bytes
+//    of two keys with a byte permute. The output dims come out permuted:
+//    row r of m-tile mt is dim 64*(mt/4) + 4*r + mt%4, undone when O is
+//    written. K's scale is in scale_log2, V's is applied at the output.
+__device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* smem,
+                                                   uint64_t* full, uint64_t* empty,
+                                                   volatile uint32_t* abort_flag, int b, int g,
+                                                   int kbeg, int kend, int n_sub, int n_tiles,
+                                                   int warp, int lane) {
+  const int G = p.G;
+  const int hq = lane >> 2;   // head of this lane's Q^T column (B operand), also its row group
+  const int t4 = lane & 3;
+  const int hc = 2 * t4;      // first of the two heads this lane accumulates
+  // Q^T fragments (f16), dims in the permuted order: chunk kk of 16 dims;
+  // register 0 holds dims 4t, 4t+1 and register 1 dims 4t+2, 4t+3
+  uint32_t qh[8][2];
+  {
+    const bf16* qb = p.q + ((size_t)b * p.n_q + (size_t)g * G + hq) * AD;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = kk * 16 + 4 * t4 + 2 * j;
+        float v0 = 0.f, v1 = 0.f;
+        if (hq < G) {
+          v0 = __bfloat162float(qb[col]) + (p.q_lo ? __bfloat162float(qb[p.q_lo + col]) : 0.f);
+          v1 = __bfloat162float(qb[col + 1]) +
+               (p.q_lo ? __bfloat162float(qb[p.q_lo + col + 1]) : 0.f);
+        }
+        const __half2 h2 = __floats2half2_rn(v0, v1);
+        qh[kk][j] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+  }
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float oacc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  const int mi = lane >> 3, rr = lane & 7;
+  for (int t = 0; t < n_tiles; ++t) {
+    const int s = t % F8_STAGES;
+    const uint32_t ph = (t / F8_STAGES) & 1;
+    if (*abort_flag) break;
+    if (!mbar_wait(&full[s], ph, p.status)) {
+      *abort_flag = 1;
+      break;
+    }
+    const int sub = 4 * t + warp;
+    if (sub < n_sub) {
+      uint8_t* st = smem + s * F8_STAGE;
+      const int k0 = kbeg + sub * SUBK;
+      const int nvalid = min(SUBK, kend - k0);
+      const uint32_t kbase = smem_u32(st + warp * F8_SUB);
+      const uint8_t* vsub = st + F8_TILE + warp * F8_SUB;
+      if (nvalid < SUBK) {  // V rows past the last key may hold anything: zero them
+        const int nz = (SUBK - nvalid) * 8;
+        for (int i = lane; i < nz; i += 32)
+          *reinterpret_cast<uint4*>(const_cast<uint8_t*>(vsub) + (nvalid + (i >> 3)) * 128 +
+                                    (i & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // S^T (16 keys x 8 heads), even and odd k-steps in separate chains
+      float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kp = 0; kp < 4; ++kp) {  // dims 32kp .. 32kp + 31: two k-steps
+        const int row = ((mi & 1) << 3) + rr;
+        const int chunk = kp * 2 + (mi >> 1);
+        uint32_t r[4];
+        ldsm_x4(kbase + swz128(row, chunk), r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t lo_r = r[2 * h], hi_r = r[2 * h + 1];  // key rows g and g + 8
+          const uint32_t a[4] = {e4m3x2_to_f16x2(lo_r), e4m3x2_to_f16x2(hi_r),
+                                 e4m3x2_to_f16x2(lo_r >> 16), e4m3x2_to_f16x2(hi_r >> 16)};
+          const int kk = 2 * kp + h;
+          mma_f16_16816(h ? sl : sh, a, qh[kk][0], qh[kk][1]);
+        }
+      }
+      // lane holds S^T[key l/4 (+8)][heads hc, hc+1]; online softmax per head
+      float sv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int key = (lane >> 2) + (i >= 2 ? 8 : 0);
+        sv[i] = key < nvalid ? (sh[i] + sl[i]) * p.scale_log2 : -INFINITY;
+      }
+      float corr[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(sv[j], sv[j + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(m_run[j], mx);
+        corr[j] = mnew == -INFINITY ? 1.f : exp2f(m_run[j] - mnew);
+        m_run[j] = mnew;
+      }
+      float pv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = i & 1;
+        pv[i] = m_run[j] == -INFINITY ? 0.f : exp2f(sv[i] - m_run[j]);
+      }
+      l_run[0] = l_run[0] * corr[0] + pv[0] + pv[2];
+      l_run[1] = l_run[1] * corr[1] + pv[1] + pv[3];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        oacc[mt][0] *= corr[0];
+        oacc[mt][1] *= corr[1];
+        oacc[mt][2] *= corr[0];
+        oacc[mt][3] *= corr[1];
+      }
+      // P^T as the B operand (16 keys x 8 heads), f16
+      const __half2 p0 = __floats2half2_rn(pv[0], pv[1]);  // keys 0-7
+      const __half2 p1 = __floats2half2_rn(pv[2], pv[3]);  // keys 8-15
+      const uint32_t bh0 = movmatrix_t(*reinterpret_cast<const uint32_t*>(&p0));
+      const uint32_t bh1 = movmatrix_t(*reinterpret_cast<const uint32_t*>(&p1));
+      // V words: keys 2t, 2t+1, 2t+8, 2t+9; dims 64h + 32e + 4(l/4) .. +3
+      uint32_t w[4][2][2];
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int key = (kq & 1) + 2 * t4 + (kq >> 1) * 8;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int off = 64 * h + 32 * e + 4 * hq;
+            w[kq][h][e] = *reinterpret_cast<const uint32_t*>(
+                vsub + key * 128 + ((((off >> 4) ^ (key & 7))) << 4) + (off & 15));
+          }
+      }
+      // O^T += V^T P^T over 8 m-tiles of permuted dims
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int h = mt >> 2, j = mt & 3;
+        const uint32_t sel = (uint32_t)j | ((uint32_t)(4 + j) << 4);
+        const uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(w[0][h][0], w[1][h][0], sel)),
+                               e4m3x2_to_f16x2(__byte_perm(w[0][h][1], w[1][h][1], sel)),
+                               e4m3x2_to_f16x2(__byte_perm(w[2][h][0], w[3][h][0], sel)),
+                               e4m3x2_to_f16x2(__byte_perm(w[2][h][1], w[3][h][1], sel))};
+        mma_f16_16816(oacc[mt], a, bh0, bh1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  // ---- this warp's (max, sum, O) to shared memory for the 4-warp merge
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+    l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+  }
+  float* so = reinterpret_cast<float*>(smem);  // [4][16][128]
+  float* smx = so + 4 * 16 * AD;               // [4][16]
+  float* ssum = smx + 64;                      // [4][16]
+  cons_bar();  // every consumer is done with the stage buffers
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int head = hc + (i & 1);
+      const int d = 64 * (mt >> 2) + 4 * ((lane >> 2) + (i >= 2 ? 8 : 0)) + (mt & 3);
+      if (head < G) so[(warp * 16 + head) * AD + d] = oacc[mt][i];
+    }
+  if (lane < 4) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (hc + j < G) {
+        smx[warp * 16 + hc + j] = m_run[j];
+        ssum[warp * 16 + hc + j] = l_run[j];
+      }
+  }
+}
+
+template <bool KEYMAJOR, bool FP8>
+__global__ void __launch_bounds__(DEC_THREADS, FP8 ? 3 : 2)
     attn_decode_kernel(const __grid_constant__ CUtensorMap mapK,
                        const __grid_constant__ CUtensorMap mapV,
                        const __grid_constant__ CUtensorMap mapK16,
@@ -413,9 +607,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + DSTAGES * DSTAGE_BYTES);
-  uint64_t* empty = full + DSTAGES;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + DSTAGES);
+  constexpr int NS = FP8 ? F8_STAGES : DSTAGES;
+  constexpr uint32_t SB = FP8 ? F8_STAGE : DSTAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * SB);
+  uint64_t* empty = full + NS;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + NS);
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -440,7 +636,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   const int n_tiles = (n_sub + 3) / 4;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < DSTAGES; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 4);
     }
@@ -458,8 +654,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
       int issued = 0;
       bool ok = true, waited = false;
       for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % DSTAGES;
-        const uint32_t ph = (t / DSTAGES) & 1;
+        const int s = t % NS;
+        const uint32_t ph = (t / NS) & 1;
         // Keys below the new token were cached by earlier steps and can be
         // fetched while the previous kernel finishes; the tile holding the
         // new token's K/V (written by the RoPE/append kernel) waits for it.
@@ -474,8 +670,22 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
           break;
         }
         const int nsub = min(4, n_sub - 4 * t);
-        uint8_t* st = smem + s * DSTAGE_BYTES;
-        if (p.box_rows == DTILE && nsub == 4) {  // 64 contiguous keys: one box per half
+        uint8_t* st = smem + s * SB;
+        if (FP8) {  // K tile at st, V tile at st + F8_TILE, [keys][128 bytes] each
+          if (p.box_rows == DTILE && nsub == 4) {
+            const int row = kv_row(p, b, g, kbeg + t * DTILE);
+            mbar_arrive_expect_tx(&full[s], F8_STAGE);
+            tma_load_3d(st, &mapK, &full[s], 0, row, p.layer);
+            tma_load_3d(st + F8_TILE, &mapV, &full[s], 0, row, p.layer);
+          } else {
+            mbar_arrive_expect_tx(&full[s], nsub * 2 * F8_SUB);
+            for (int j = 0; j < nsub; ++j) {
+              const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
+              tma_load_3d(st + j * F8_SUB, &mapK16, &full[s], 0, row, p.layer);
+              tma_load_3d(st + F8_TILE + j * F8_SUB, &mapV16, &full[s], 0, row, p.layer);
+            }
+          }
+        } else if (p.box_rows == DTILE && nsub == 4) {  // 64 contiguous keys: one box per half
           const int row = kv_row(p, b, g, kbeg + t * DTILE);
           mbar_arrive_expect_tx(&full[s], DSTAGE_BYTES);
           tma_load_3d(st, &mapK, &full[s], 0, row, p.layer);
@@ -497,8 +707,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         ++issued;
       }
       if (!ok) {
-        for (int t = issued - 1; t >= 0 && t >= issued - DSTAGES; --t)
-          mbar_wait(&full[t % DSTAGES], (t / DSTAGES) & 1, p.status);
+        for (int t = issued - 1; t >= 0 && t >= issued - NS; --t)
+          mbar_wait(&full[t % NS], (t / NS) & 1, p.status);
       }
     }
     return;
@@ -507,7 +717,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
   // ---------------------------------------------------------------- consumers
   grid_dep_wait();  // q comes from the RoPE/append kernel
   grid_dep_launch();
-  if (KEYMAJOR)
+  if (FP8)
+    decode_consume_fp8(p, smem, full, empty, abort_flag, qrow, g, kbeg, kend, n_sub, n_tiles, warp,
+                       lane);
+  else if (KEYMAJOR)
     decode_consume_keymajor(p, smem, full, empty, abort_flag, qrow, g, kbeg, kend, n_sub, n_tiles,
                             warp, lane);
   else
@@ -537,7 +750,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     const size_t bh = (size_t)b * p.n_q + (size_t)g * G + r;
     if (p.splits == 1) {
       const size_t oh = (size_t)qrow * p.n_q + (size_t)g * G + r;
-      const float v = L > 0.f ? O / L : 0.f;
+      const float v = L > 0.f ? O / L * p.v_scale : 0.f;
       const bf16 hi = __float2bfloat16_rn(v);
       p.out[oh * AD + t] = hi;
       if (p.out_lo) p.out[oh * AD + t + p.out_lo] = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -557,7 +770,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
 __global__ void attn_combine_kernel(const float* __restrict__ part,
                                     const int32_t* __restrict__ positions, int n_q, int splits,
                                     int keys_per_split, int cap_keys, int d, void* out,
-                                    size_t out_lo, const int32_t* cu_rows) {
+                                    size_t out_lo, const int32_t* cu_rows, float v_scale) {
   grid_dep_wait();
   grid_dep_launch();
   const int bh = blockIdx.x;
@@ -582,7 +795,7 @@ __global__ void attn_combine_kernel(const float* __restrict__ part,
         O += ps[t] * f;
       }
     }
-    const float v = L > 0.f ? O / L : 0.f;
+    const float v = L > 0.f ? O / L * v_scale : 0.f;
     const bf16 hi = __float2bfloat16_rn(v);
     reinterpret_cast<bf16*>(out)[oh * d + t] = hi;
     if (out_lo)
@@ -617,6 +830,7 @@ struct PreParams {
   // keys 0 .. position of the row, earlier pieces included)
   int from_cache, box_rows, layer, page_size, capacity, batch_cap, n_pages, max_pages;
   const int32_t* page_table;
+  float v_scale;  // V values are the stored ones times this (K's scale is in scale_log2)
 };
 
 // Cache row of the keys starting at k0 (a multiple of 16) of sequence b, K/V
@@ -886,7 +1100,7 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
   for (int hh = 0; hh < 2; ++hh) {
     const int row = myrow0 + hh * 8;
     if (row >= n_b || rowbase + row >= p.n_rows) continue;
-    const float inv = lrow[hh] > 0.f ? 1.f / lrow[hh] : 0.f;
+    const float inv = lrow[hh] > 0.f ? p.v_scale / lrow[hh] : 0.f;
     bf16* dst = p.out + (size_t)(rowbase + row) * ld + (size_t)h * AD;
 #pragma unroll
     for (int dn = 0; dn < 16; ++dn) {
@@ -1028,11 +1242,14 @@ size_t attn_decode_partial_bytes(int B, int n_q, int head_dim, int max_keys, int
 }
 
 cudaError_t attn_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<false>,
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEC_SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)DEC_SMEM);
+  e = cudaFuncSetAttribute(attn_decode_kernel<true, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEC_SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_decode_kernel<true, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEC_SMEM_F8);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)PRE_SMEM);
@@ -1082,19 +1299,23 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.keys_per_split = kps;
   p.box_rows = a.box_rows == DTILE ? DTILE : SUBK;
   p.cu_rows = a.cu_rows;
-  p.scale_log2 = kLog2e / sqrtf((float)AD);
+  p.scale_log2 = kLog2e / sqrtf((float)AD) * (a.kv_fp8 ? a.k_scale : 1.f);
+  p.v_scale = a.kv_fp8 ? a.v_scale : 1.f;
   const bool keymajor = p.G <= kKeyMajorMaxG;
-  cudaError_t e = keymajor ? launch_k(attn_decode_kernel<true>, dim3(splits, a.n_kv, a.B),
-                                  dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, *a.map_k16,
-                                  *a.map_v16, p)
-                       : launch_k(attn_decode_kernel<false>, dim3(splits, a.n_kv, a.B),
-                                  dim3(DEC_THREADS), DEC_SMEM, st, 0, *a.map_k, *a.map_v, *a.map_k16,
-                                  *a.map_v16, p);
+  if (a.kv_fp8 && !keymajor) return cudaErrorInvalidValue;
+  const dim3 grid(splits, a.n_kv, a.B), block(DEC_THREADS);
+  cudaError_t e =
+      a.kv_fp8 ? launch_k(attn_decode_kernel<true, true>, grid, block, DEC_SMEM_F8, st, 0,
+                          *a.map_k, *a.map_v, *a.map_k16, *a.map_v16, p)
+      : keymajor ? launch_k(attn_decode_kernel<true, false>, grid, block, DEC_SMEM, st, 0,
+                            *a.map_k, *a.map_v, *a.map_k16, *a.map_v16, p)
+                 : launch_k(attn_decode_kernel<false, false>, grid, block, DEC_SMEM, st, 0,
+                            *a.map_k, *a.map_v, *a.map_k16, *a.map_v16, p);
   if (e != cudaSuccess || splits == 1) return e;
   const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
   return launch_k(attn_combine_kernel, dim3(a.B * a.n_q), dim3(AD), 0, st, 0,
                   (const float*)a.partial, a.positions, a.n_q, splits, kps, cap_keys, AD, a.out,
-                  a.out_lo, a.cu_rows);
+                  a.out_lo, a.cu_rows, p.v_scale);
 }
 
 int attn_decode_launches(int B, int n_kv, int max_keys, int sm_count, int dtype) {
@@ -1126,7 +1347,8 @@ cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_
   p.n_kv = a.n_kv;
   p.G = a.n_q / a.n_kv;
   p.n_qtiles = (a.T + PQ - 1) / PQ;
-  p.scale_log2 = kLog2e / sqrtf((float)AD);
+  p.scale_log2 = kLog2e / sqrtf((float)AD) * a.k_scale;
+  p.v_scale = a.v_scale;
   p.cu_rows = a.cu_rows;
   p.start_pos = a.start_pos;
   p.n_rows = a.cu_rows ? a.n_rows : a.B * a.T;

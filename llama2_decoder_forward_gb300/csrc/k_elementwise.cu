@@ -181,6 +181,15 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
   }
   const int ck = is_v ? c - qw - kw : c - qw;  // column within the K (or V) block
   const int g = ck / d, dd = ck % d;
+  uint8_t q8[8];
+  if (a.kv_fp8) {  // the cache holds e4m3(x / scale); the side buffers its e4m3 value
+    const float sc = is_v ? a.v_scale : a.k_scale;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      q8[k] = f32_to_e4m3(v[k] / sc);
+      o[k] = from_f32<T>(e4m3_to_f32(q8[k]));
+    }
+  }
   T* side = reinterpret_cast<T*>(is_v ? a.v_out : a.k_out);
   if (side) {
     T* dst = side + (size_t)r * kw + ck;
@@ -207,6 +216,14 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
       return;
     }
     slot = (((size_t)a.layer * a.n_pages + page) * a.n_kv + g) * a.page_size + pos % a.page_size;
+  }
+  if (a.kv_fp8) {
+    uint8_t* cache8 = reinterpret_cast<uint8_t*>(is_v ? a.v_cache : a.k_cache) + slot * d + dd;
+    uint2 w;
+    w.x = q8[0] | (q8[1] << 8) | (q8[2] << 16) | ((uint32_t)q8[3] << 24);
+    w.y = q8[4] | (q8[5] << 8) | (q8[6] << 16) | ((uint32_t)q8[7] << 24);
+    *reinterpret_cast<uint2*>(cache8) = w;
+    return;
   }
   T* cache = reinterpret_cast<T*>(is_v ? a.v_cache : a.k_cache) + slot * d + dd;
 #pragma unroll

@@ -163,11 +163,15 @@ __device__ __forceinline__ void rope_emit(const RopeAppendArgs& a, const RopeFea
     return;
   }
   const bool is_v = f.kind == 2;
+  const uint8_t q8 = a.kv_fp8 ? f32_to_e4m3(v / (is_v ? a.v_scale : a.k_scale)) : 0;
   bf16* side = reinterpret_cast<bf16*>(is_v ? a.v_out : a.k_out);
-  if (side) side[(size_t)r * a.n_kv * d + f.col] = hi;
+  if (side) side[(size_t)r * a.n_kv * d + f.col] = a.kv_fp8 ? __float2bfloat16_rn(e4m3_to_f32(q8)) : hi;
   if (t.kv >= 0) {
     const long long slot = t.kv + (long long)f.g * (a.page_size ? a.page_size : a.capacity);
-    reinterpret_cast<bf16*>(is_v ? a.v_cache : a.k_cache)[slot * d + f.dd] = hi;
+    if (a.kv_fp8)
+      reinterpret_cast<uint8_t*>(is_v ? a.v_cache : a.k_cache)[slot * d + f.dd] = q8;
+    else
+      reinterpret_cast<bf16*>(is_v ? a.v_cache : a.k_cache)[slot * d + f.dd] = hi;
   }
 }
 

@@ -83,7 +83,8 @@ extern "C" int llama_attention_decode_noalloc(const llama_config* cfg, const voi
                                               const llama_kv* kv, void* out, void* stream) {
   if (!cfg || !q || !positions || !out || !kv || !kv->k || !kv->v || B < 1)
     return LLAMA_ERR_INVALID_ARG;
-  if (cfg->dtype != LLAMA_BF16 || cfg->head_dim != 128) return LLAMA_ERR_UNSUPPORTED;
+  if (cfg->dtype != LLAMA_BF16 || cfg->head_dim != 128 || kv->kv_dtype != LLAMA_KV_MODEL)
+    return LLAMA_ERR_UNSUPPORTED;
   if (cfg->n_layers < 1 || cfg->n_q_heads < 1 || cfg->n_kv_heads < 1 || cfg->max_seq < 1 ||
       cfg->n_q_heads % cfg->n_kv_heads != 0 || layer < 0 || layer >= cfg->n_layers)
     return LLAMA_ERR_INVALID_ARG;
