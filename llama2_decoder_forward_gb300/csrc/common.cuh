@@ -35,10 +35,18 @@ __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
 __device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)q, __NV_E4M3)));
 }
-// Two E4M3 bytes (low byte first) as an f16x2 register (low half first).
+// The two low E4M3 bytes of q2 as an f16x2 register (byte 0 -> low half).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t q2) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(q2 & 0xffffu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+  uint32_t d;
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %1;\n cvt.rn.f16x2.e4m3x2 %0, a;\n}"
+      : "=r"(d) : "r"(q2));
+  return d;
+}
+// Four E4M3 bytes as two f16x2 registers: bytes 0, 1 -> lo; bytes 2, 3 -> hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t q4, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+      : "=r"(lo), "=r"(hi) : "r"(q4));
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

@@ -495,9 +495,9 @@ __device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* 
         ldsm_x4(kbase + swz128(row, chunk), r[0], r[1], r[2], r[3]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t lo_r = r[2 * h], hi_r = r[2 * h + 1];  // key rows g and g + 8
-          const uint32_t a[4] = {e4m3x2_to_f16x2(lo_r), e4m3x2_to_f16x2(hi_r),
-                                 e4m3x2_to_f16x2(lo_r >> 16), e4m3x2_to_f16x2(hi_r >> 16)};
+          uint32_t a[4];  // key rows g (r[2h]) and g + 8 (r[2h+1]); dims 4t, 4t+1 then 4t+2, 4t+3
+          e4m3x4_to_f16x2x2(r[2 * h], a[0], a[2]);
+          e4m3x4_to_f16x2x2(r[2 * h + 1], a[1], a[3]);
           const int kk = 2 * kp + h;
           mma_f16_16816(h ? sl : sh, a, qh[kk][0], qh[kk][1]);
         }
