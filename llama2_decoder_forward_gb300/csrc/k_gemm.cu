@@ -537,8 +537,10 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, b
   pl.tmem_cols = 32;
   while ((int)pl.tmem_cols < width) pl.tmem_cols <<= 1;
   const int stage_bytes = BM * BK * 2 * (dual ? 2 : 1) + pl.n_tile * BK * 2;
-  // two CTAs per SM while the tile is narrow and both fit in tensor memory
-  const bool two = pl.n_tile <= 128 && pl.tmem_cols <= 256;
+  // two CTAs per SM while both fit in tensor memory: narrow (decode) tiles,
+  // and the single-accumulator prefill tiles, whose epilogues then overlap
+  // the other CTA's K loop (two stages each)
+  const bool two = (pl.n_tile <= 128 && pl.tmem_cols <= 256) || (!dual && pl.n_tile == 256 && N > 512);
   const int budget = two ? 112 * 1024 : 224 * 1024;
   const int extra = rope ? 16 * pl.ncol : 0;
   pl.stages = std::max(2, std::min(8, (budget - 2048 - extra) / stage_bytes));
