@@ -63,7 +63,7 @@ int sm_count_or_default() {
 // Workspace layout (byte offsets from the workspace base).
 struct Layout {
   size_t status, rope, x, u, qkv, q, kside, vside, o, a, u_last, logits, ids, tok, pos, apart,
-      total;
+      ssq, total;
   size_t apart_bytes;
   int R;
 };
@@ -127,6 +127,8 @@ Layout make_layout(const llama_config* c, int sm_count) {
   L.apart_bytes = attn_decode_partial_bytes(c->max_batch, (int)nq, (int)d, c->max_seq, sm_count,
                                             (int)nkv);
   L.apart = take(std::max<size_t>(L.apart_bytes, 16));
+  // fused RMSNorm: per-(128-feature tile, row) sums of squares of the residual stream
+  L.ssq = take((H + 127) / 128 * (size_t)R * 4);
   L.total = off;
   return L;
 }
@@ -300,12 +302,35 @@ int do_rmsnorm(llama_ctx* c, const float* x, int rows, int stride, int offset, c
 
 // split: x holds the hi/lo pair layout of its N rows; out_lo: bf16 outputs also
 // store their remainder out_lo elements further on.
+// RMSNorm folded into the projections (bf16): the residual GEMM that updates
+// x also writes the next projection's input pair x * gamma and the tile sums
+// of x^2 (producer); the next projection scales each row by 1/rms from those
+// sums (consumer).
+struct NormFuse {
+  const void* gamma = nullptr;  // producer
+  void* out = nullptr;
+  size_t lo = 0;
+  bool consume = false;         // consumer
+};
+
 // rope: the Q/K/V projection's RoPE + cache-append epilogue (bf16 only).
 int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, const void* wu,
             int M, void* out, int ldo, int split = 0, size_t out_lo = 0,
-            const RopeAppendArgs* rope = nullptr) {
+            const RopeAppendArgs* rope = nullptr, const NormFuse* nf = nullptr) {
   GemmCall g{};
   g.rope = rope;
+  if (nf) {
+    float* ssq = c->at<float>(c->L.ssq);
+    g.norm_gamma = nf->gamma;
+    g.norm_out = nf->out;
+    g.norm_lo = nf->lo;
+    g.ssq_out = nf->gamma ? ssq : nullptr;
+    g.ssq_in = nf->consume ? ssq : nullptr;
+    g.ssq_tiles = (c->cfg.hidden + 127) / 128;
+    g.ssq_ld = c->L.R;
+    g.norm_h = c->cfg.hidden;
+    g.norm_eps = c->cfg.rms_eps;
+  }
   g.split = split;
   g.out_lo = out_lo;
   g.dtype = c->cfg.dtype;
@@ -550,14 +575,22 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   void* a = c->at<void>(c->L.a);
   const int lo = cf.dtype == LLAMA_BF16 ? round16(rows) : 0;
   const int sp = lo ? 1 : 0;
-  TRY(do_rmsnorm(c, x, rows, 1, 0, lw.attn_norm, u, lo));
+  // bf16: the RMSNorms after the first ride on the residual GEMMs (the layers
+  // run in order, so layer l > 0 finds its normalised input pair and the row
+  // sums left by layer l - 1's down projection)
+  const bool fuse = cf.dtype == LLAMA_BF16;
+  NormFuse consume;
+  consume.consume = true;
+  const NormFuse* qkv_nf = fuse && l > 0 ? &consume : nullptr;
+  if (!qkv_nf) TRY(do_rmsnorm(c, x, rows, 1, 0, lw.attn_norm, u, lo));
   void* ks = prefill ? c->at<void>(c->L.kside) : nullptr;
   void* vs = prefill ? c->at<void>(c->L.vside) : nullptr;
   const int rps = prefill ? T : 1;
   const int32_t* pos = prefill ? nullptr : positions;
   const size_t q_lo = (size_t)lo * nq * d;
   if (rm) {  // extend: RoPE/append, then attention over the cache
-    TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
+    TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp,
+                0, nullptr, qkv_nf));
     TRY(do_rope_append(c, qkv, rows, 1, nullptr, l, kv, q, nullptr, nullptr, q_lo, rm));
     TRY(do_attn_extend(c, q, rows, *rm, l, kv, o, q_lo, lo));  // pieces of 2+ rows
     TRY(do_attn_decode(c, q, rm->start_pos, rm->B, l, kv, o, q_lo, q_lo, rm->cu_rows));  // 1 row
@@ -568,10 +601,11 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
     // tensor pipe for longer than the separate pass over the fp32 rows takes.
     const RopeAppendArgs ra = rope_args(c, nullptr, rps, pos, l, kv, q, ks, vs, q_lo);
     TRY(do_gemm(c, kEpiRope, u, rows, H, lw.wqkv, nullptr, qkv_rows, nullptr, qkv_rows, sp, 0,
-                &ra));
+                &ra, qkv_nf));
     TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
   } else {
-    TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp));
+    TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp,
+                0, nullptr, qkv_nf));
     TRY(do_rope_append(c, qkv, rows, rps, pos, l, kv, q, ks, vs, q_lo));
     const bool f8 = kv->kv_dtype == LLAMA_KV_E4M3;  // side buffers hold unscaled E4M3 values
     if (prefill)
@@ -580,10 +614,27 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
     else
       TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
   }
-  TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H, sp));
-  TRY(do_rmsnorm(c, x, rows, 1, 0, lw.ffn_norm, u, lo));
-  TRY(do_gemm(c, LLAMA_EPI_SWIGLU, u, rows, H, lw.w_gate, lw.w_up, I, a, I, sp, (size_t)lo * I));
-  TRY(do_gemm(c, LLAMA_EPI_RESID_F32, a, rows, I, lw.w_down, nullptr, H, x, H, sp));
+  if (fuse) {
+    NormFuse ffn;  // O projection + residual, then the pre-FFN norm's input pair
+    ffn.gamma = lw.ffn_norm;
+    ffn.out = u;
+    ffn.lo = (size_t)lo * H;
+    TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H, sp, 0, nullptr,
+                &ffn));
+    TRY(do_gemm(c, LLAMA_EPI_SWIGLU, u, rows, H, lw.w_gate, lw.w_up, I, a, I, sp, (size_t)lo * I,
+                nullptr, &consume));
+    NormFuse next;  // down projection + residual, then the next layer's pre-attention pair
+    next.gamma = l + 1 < cf.n_layers ? c->layers[l + 1].attn_norm : nullptr;
+    next.out = u;
+    next.lo = (size_t)lo * H;
+    TRY(do_gemm(c, LLAMA_EPI_RESID_F32, a, rows, I, lw.w_down, nullptr, H, x, H, sp, 0, nullptr,
+                next.gamma ? &next : nullptr));
+  } else {
+    TRY(do_gemm(c, LLAMA_EPI_RESID_F32, o, rows, nq * d, lw.wo, nullptr, H, x, H, sp));
+    TRY(do_rmsnorm(c, x, rows, 1, 0, lw.ffn_norm, u, lo));
+    TRY(do_gemm(c, LLAMA_EPI_SWIGLU, u, rows, H, lw.w_gate, lw.w_up, I, a, I, sp, (size_t)lo * I));
+    TRY(do_gemm(c, LLAMA_EPI_RESID_F32, a, rows, I, lw.w_down, nullptr, H, x, H, sp));
+  }
   return LLAMA_OK;
 }
 

@@ -108,6 +108,18 @@ struct GemmCall {
                               // bf16(v - bf16(v)), L = round16(N); both are multiplied
   size_t out_lo;              // bf16 outputs: also store the remainder out_lo elements on
   const RopeAppendArgs* rope; // kEpiRope: where the rotated Q and the K/V rows go
+  // Fused RMSNorm (bf16). Producer (RESID_F32): also store the bf16 pair of
+  // x_new * norm_gamma[m] in norm_out ([N][M] hi, norm_lo elements further
+  // lo) and the sum of x_new^2 over each 128-feature tile in
+  // ssq_out[tile][ssq_ld]. Consumer: scale row n's outputs by
+  // 1 / sqrt(sum over ssq_tiles of ssq_in[t][n] / norm_h + norm_eps).
+  const void* norm_gamma = nullptr;
+  void* norm_out = nullptr;
+  size_t norm_lo = 0;
+  float* ssq_out = nullptr;
+  const float* ssq_in = nullptr;
+  int ssq_tiles = 0, ssq_ld = 0, norm_h = 0;
+  float norm_eps = 0.f;
   void* out;
   int ldo;
   uint32_t* status;

@@ -36,6 +36,14 @@ constexpr int kMaxDynSmem = 232448;  // 227 KB per CTA
 
 struct TcParams {
   RopeAppendArgs rope;  // kEpiRope only
+  // fused RMSNorm (see GemmCall)
+  const bf16* norm_gamma;
+  bf16* norm_out;
+  size_t norm_lo;
+  float* ssq_out;
+  const float* ssq_in;
+  int ssq_tiles, ssq_ld;
+  float norm_inv_h, norm_eps;
   int M, N, K;
   int n_tile, num_kb, splits, n_tiles;
   int stages;
@@ -190,6 +198,35 @@ __device__ __forceinline__ void load_acc16(uint32_t tq, int col, int lo, float (
 
 // Split-K cluster reduction: CTA k of the cluster finishes columns
 // [c_beg, c_end) of the tile; a work item is 4 consecutive rows of one column.
+// Sums of 16 values over the 32 lanes of a warp (v[j] summed over lanes, for
+// every j) in 16 shuffles: each halving step keeps half of the indices and
+// adds the partner lane's copies of them. On return lane l holds the sum for
+// index 8*b4 + 4*b3 + 2*b2 + b1 (b_i: bit i of l); lanes l and l ^ 1 agree.
+__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane, int& index) {
+  float a8[8], a4[4], a2[2];
+  const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4, h1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = h4 ? v[i] : v[i + 8];
+    a8[i] = (h4 ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = h3 ? a8[i] : a8[i + 4];
+    a4[i] = (h3 ? a8[i + 4] : a8[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = h2 ? a4[i] : a4[i + 2];
+    a2[i] = (h2 ? a4[i + 2] : a4[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  const float send = h1 ? a2[0] : a2[1];
+  float a1 = (h1 ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, send, 2);
+  a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+  index = (h4 ? 8 : 0) + (h3 ? 4 : 0) + (h2 ? 2 : 0) + (h1 ? 1 : 0);
+  return a1;
+}
+
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 struct RedSlice {
@@ -222,6 +259,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(accf + 1);
   // kEpiRope: the tile's tokens (ncol entries after the 256-byte barrier block)
   TokInfo* tok = reinterpret_cast<TokInfo*>(smem + (size_t)S * stage_bytes + 256);
+  // RMSNorm scales of the tile's rows (consumers), after the token table
+  float* scl = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes + 256 +
+                                        (EPI == kEpiRope ? 16 * p.ncol : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
@@ -344,8 +384,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
         const int r = tile_n * p.ncol + i;
         tok[i] = r < p.N ? rope_token(p.rope, r) : TokInfo{-1, -1, 0};
       }
-      epi_bar();
     }
+    if (p.ssq_in) {  // RMSNorm scale of each row: its tile sums, added in tile order
+      for (int i = threadIdx.x - 64; i < p.ncol; i += 128) {
+        const int r = tile_n * p.ncol + i;
+        float ss = 0.f;
+        if (r < p.N)
+          for (int tt = 0; tt < p.ssq_tiles; ++tt) ss += p.ssq_in[(size_t)tt * p.ssq_ld + r];
+        scl[i] = 1.0f / sqrtf(ss * p.norm_inv_h + p.norm_eps);
+      }
+    }
+    if (EPI == kEpiRope || p.ssq_in) epi_bar();
     const bool ok = mbar_wait(accf, 0, p.status);
     tc_fence_after();
     if (ok && !ctl[1]) {
@@ -362,6 +411,43 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           float g[16], u[16];
           load_acc16(tq, c0, p.lo, g);
           if (DUAL) load_acc16(tq, up + c0, p.lo, u);
+          if (p.ssq_in) {  // the input rows were normalised up to this scale
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              g[j] *= scl[c0 + j];
+              if (DUAL) u[j] *= scl[c0 + j];
+            }
+          }
+          if (EPI == LLAMA_EPI_RESID_F32 && p.norm_gamma) {
+            // x_new, its normalised-input pair for the next projection, and
+            // the per-row sums of squares of this tile's 128 features
+            float* o = reinterpret_cast<float*>(p.out);
+            const bool row_ok = gm < p.M;
+            const float gam = row_ok ? __bfloat162float(p.norm_gamma[gm]) : 0.f;
+            float res[16], ss[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              res[j] = (row_ok && c0 + j < nvalid) ? o[(size_t)(n0 + c0 + j) * p.ldo + gm] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float xn = res[j] + g[j];
+              ss[j] = 0.f;
+              if (row_ok && c0 + j < nvalid) {
+                const size_t idx = (size_t)(n0 + c0 + j) * p.ldo + gm;
+                o[idx] = xn;
+                const float y = xn * gam;
+                const bf16 hi = __float2bfloat16_rn(y);
+                p.norm_out[idx] = hi;
+                p.norm_out[idx + p.norm_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
+                ss[j] = xn * xn;
+              }
+            }
+            int jx;
+            const float tot = warp_sum16(ss, lane, jx);
+            if ((lane & 1) == 0)  // [4 quadrants][ncol] column sums of this warp's 32 rows
+              reinterpret_cast<float*>(smem)[q * p.ncol + c0 + jx] = tot;
+            continue;
+          }
           if (EPI == kEpiRope) {
             float partner[16];  // the RoPE partner feature sits in the neighbouring lane
 #pragma unroll
@@ -398,6 +484,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
         }
       } else {
         // this split's sums -> shared memory, column-major [col][128 rows]
+        // (the direct path's norm sums are finished below)
         float* red = reinterpret_cast<float*>(smem);
         for (int c0 = 0; c0 < p.ncol; c0 += 16) {
           float g[16];
@@ -411,6 +498,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           }
         }
       }
+    }
+    if (EPI == LLAMA_EPI_RESID_F32 && p.norm_gamma && p.splits == 1) {
+      epi_bar();  // every quadrant's column sums are in shared memory
+      const int n0 = tile_n * p.ncol;
+      const float* wsum = reinterpret_cast<const float*>(smem);
+      for (int i = threadIdx.x - 64; i < p.ncol; i += 128)
+        if (ok && !ctl[1] && n0 + i < p.N)
+          p.ssq_out[(size_t)tile_m * p.ssq_ld + n0 + i] =
+              wsum[i] + wsum[p.ncol + i] + wsum[2 * p.ncol + i] + wsum[3 * p.ncol + i];
     }
   }
   if (p.splits > 1) {
@@ -444,6 +540,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
             if (DUAL) { u[0] += uv[s2].x; u[1] += uv[s2].y; u[2] += uv[s2].z; u[3] += uv[s2].w; }
           }
         const int gm0 = tile_m * BM + rq;
+        if (p.ssq_in) {
+          const float sc = scl[c];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            g[e] *= sc;
+            u[e] *= sc;
+          }
+        }
         if (EPI == kEpiRope) {  // rows gm0..gm0+3: two complete RoPE pairs
           const TokInfo ti = tok[c];
           const RopeFeat f0 = rope_feat(p.rope, gm0);
@@ -466,6 +570,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (gm0 + e < p.M) o[e] = res[e] + g[e];
+          if (p.norm_gamma) {  // normalised-input pair and this tile's sum of squares
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (gm0 + e < p.M) {
+                const float xn = res[e] + g[e];
+                const float y = xn * __bfloat162float(p.norm_gamma[gm0 + e]);
+                const bf16 hi = __float2bfloat16_rn(y);
+                const size_t idx = (size_t)c * p.ldo + gm0 + e;
+                p.norm_out[idx] = hi;
+                p.norm_out[idx + p.norm_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
+                ss += xn * xn;
+              }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if ((threadIdx.x & 31) == 0) p.ssq_out[(size_t)tile_m * p.ssq_ld + c] = ss;
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
@@ -527,7 +648,8 @@ int gemm_n_tile(int N, int split) {
 
 // rope: the Q/K/V epilogue's token table (16 bytes per tile column) follows
 // the barrier block.
-static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, bool rope) {
+static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, bool rope,
+                      bool scale) {
   Plan pl{};
   pl.n_tile = gemm_n_tile(N, split);
   pl.lo = split ? pl.n_tile / 2 : 0;
@@ -542,7 +664,7 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, b
   // the other CTA's K loop (two stages each)
   const bool two = (pl.n_tile <= 128 && pl.tmem_cols <= 256) || (!dual && pl.n_tile == 256 && N > 512);
   const int budget = two ? 112 * 1024 : 224 * 1024;
-  const int extra = rope ? 16 * pl.ncol : 0;
+  const int extra = (rope ? 16 * pl.ncol : 0) + (scale ? 4 * pl.ncol : 0);
   pl.stages = std::max(2, std::min(8, (budget - 2048 - extra) / stage_bytes));
   pl.smem = (size_t)pl.stages * stage_bytes + 1024 + 256 + extra;
   pl.ctas_per_sm = std::max(1, std::min(two ? 2 : 1, (int)(233472 / (pl.smem + 1024))));
@@ -592,6 +714,15 @@ template <int EPI>
 static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st) {
   TcParams p;
   if (g.rope) p.rope = *g.rope;
+  p.norm_gamma = reinterpret_cast<const bf16*>(g.norm_gamma);
+  p.norm_out = reinterpret_cast<bf16*>(g.norm_out);
+  p.norm_lo = g.norm_lo;
+  p.ssq_out = g.ssq_out;
+  p.ssq_in = g.ssq_in;
+  p.ssq_tiles = g.ssq_tiles;
+  p.ssq_ld = g.ssq_ld;
+  p.norm_inv_h = g.norm_h > 0 ? 1.0f / (float)g.norm_h : 0.f;
+  p.norm_eps = g.norm_eps;
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
@@ -630,7 +761,8 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st) {
     }
   }
   const bool dual = g.epi == LLAMA_EPI_SWIGLU;
-  const Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count, g.epi == kEpiRope);
+  const Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count, g.epi == kEpiRope,
+                            g.ssq_in != nullptr);
   if (pl.n_tile != g.n_tile) return cudaErrorInvalidValue;
   switch (g.epi) {
     case LLAMA_EPI_STORE_F32: return launch_tc<LLAMA_EPI_STORE_F32>(g, pl, st);
