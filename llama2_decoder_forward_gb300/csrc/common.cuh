@@ -135,14 +135,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
-// Bring a tile of a 3D tensor into L2 without a shared-memory destination.
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int32_t x, int32_t y,
-                                                   int32_t z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -240,13 +232,6 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
 __device__ __forceinline__ void split_pack(float v0, float v1, uint32_t& hi, uint32_t& rem) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
   const __nv_bfloat162 r = __floats2bfloat162_rn(v0 - __low2float(h), v1 - __high2float(h));
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  rem = *reinterpret_cast<const uint32_t*>(&r);
-}
-// The same as an f16 pair (hi = f16(v), rem = f16(v - hi)).
-__device__ __forceinline__ void split_pack_f16(float v0, float v1, uint32_t& hi, uint32_t& rem) {
-  const __half2 h = __floats2half2_rn(v0, v1);
-  const __half2 r = __floats2half2_rn(v0 - __low2float(h), v1 - __high2float(h));
   hi = *reinterpret_cast<const uint32_t*>(&h);
   rem = *reinterpret_cast<const uint32_t*>(&r);
 }
