@@ -554,16 +554,20 @@ __device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* 
                 vsub + key * 128 + ((((off >> 4) ^ (key & 7))) << 4) + (off & 15));
           }
       }
-      // O^T += V^T P^T over 8 m-tiles of permuted dims
+      // O^T += V^T P^T over 8 m-tiles of permuted dims; one byte permute
+      // gathers the key pairs of two m-tiles (bytes j and j + 1 of both keys)
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int h = mt >> 2, j = mt & 3;
-        const uint32_t sel = (uint32_t)j | ((uint32_t)(4 + j) << 4);
-        const uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(w[0][h][0], w[1][h][0], sel)),
-                               e4m3x2_to_f16x2(__byte_perm(w[0][h][1], w[1][h][1], sel)),
-                               e4m3x2_to_f16x2(__byte_perm(w[2][h][0], w[3][h][0], sel)),
-                               e4m3x2_to_f16x2(__byte_perm(w[2][h][1], w[3][h][1], sel))};
-        mma_f16_16816(oacc[mt], a, bh0, bh1);
+      for (int mp = 0; mp < 4; ++mp) {  // m-tiles 2mp and 2mp + 1
+        const int h = mp >> 1, j = (mp & 1) * 2;
+        const uint32_t sel = (uint32_t)j | ((uint32_t)(4 + j) << 4) | ((uint32_t)(j + 1) << 8) |
+                             ((uint32_t)(5 + j) << 12);
+        uint32_t a0[4], a1[4];
+        e4m3x4_to_f16x2x2(__byte_perm(w[0][h][0], w[1][h][0], sel), a0[0], a1[0]);
+        e4m3x4_to_f16x2x2(__byte_perm(w[0][h][1], w[1][h][1], sel), a0[1], a1[1]);
+        e4m3x4_to_f16x2x2(__byte_perm(w[2][h][0], w[3][h][0], sel), a0[2], a1[2]);
+        e4m3x4_to_f16x2x2(__byte_perm(w[2][h][1], w[3][h][1], sel), a0[3], a1[3]);
+        mma_f16_16816(oacc[2 * mp], a0, bh0, bh1);
+        mma_f16_16816(oacc[2 * mp + 1], a1, bh0, bh1);
       }
     }
     __syncwarp();
