@@ -355,7 +355,8 @@ def run_prefill(args):
     dev = torch.device("cuda", 0)
     __graft_entry__.build()
     Bp, Tp, cap = 8, 512, 768
-    shape = synth.LLAMA2_7B
+    # fewer layers: the same kernels and launch shapes in a few GB (profiling)
+    shape = synth.LLAMA2_7B.with_(n_layers=args.layers)
     g = torch.Generator(device=dev)
     g.manual_seed(1004)
 
@@ -401,7 +402,8 @@ def run_prefill(args):
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (random-init 7B weights, uniform ids)",
-            "config": {"workload": "llama2-7b prefill, 8 sequences x 512 tokens, 32 layers + LM head on last rows"},
+            "config": {"workload": "llama2-7b prefill, 8 sequences x 512 tokens, %d layers + LM head on last rows"
+                                   % shape.n_layers},
             "roofline": {"kernel": "gemm_tc_kernel (all prefill projections)", "bound": "tensor",
                          "achieved": g_tf, "peak": tflops, "unit": "TFLOP/s", "frac": g_tf / tflops,
                          "peak_source": peak_kind, "traffic": None,
@@ -594,6 +596,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="model", choices=["model", "layer", "prefill", "extend"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="prefill workload: decoder layers (fewer for a small profiling case)")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels directly")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
                     help="KV-cache storage (e4m3: the FP8 cache; not the headline configuration)")
