@@ -345,7 +345,7 @@ __device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float mnew = fmaxf(m_run[j], mx);
-        corr[j] = mnew == -INFINITY ? 1.f : exp2f(m_run[j] - mnew);
+        corr[j] = mnew == m_run[j] ? 1.f : exp2f(m_run[j] - mnew);  // unchanged max: exactly 1
         m_run[j] = mnew;
       }
       float pv[4];
@@ -356,12 +356,15 @@ __device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint
       }
       l_run[0] = l_run[0] * corr[0] + pv[0] + pv[2];
       l_run[1] = l_run[1] * corr[1] + pv[1] + pv[3];
+      // once the running maxima settle most sub-tiles leave them unchanged
+      if (__any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f)) {
 #pragma unroll
-      for (int dt = 0; dt < 8; ++dt) {
-        oacc[dt][0] *= corr[0];
-        oacc[dt][1] *= corr[1];
-        oacc[dt][2] *= corr[0];
-        oacc[dt][3] *= corr[1];
+        for (int dt = 0; dt < 8; ++dt) {
+          oacc[dt][0] *= corr[0];
+          oacc[dt][1] *= corr[1];
+          oacc[dt][2] *= corr[0];
+          oacc[dt][3] *= corr[1];
+        }
       }
       // P^T as the B operand (16 keys x 8 heads): transpose the two 8x8 halves
       uint32_t p0h, p0l, p1h, p1l;
@@ -477,6 +480,7 @@ __device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* 
       const int nvalid = min(SUBK, kend - k0);
       const uint32_t kbase = smem_u32(st + warp * F8_SUB);
       const uint8_t* vsub = st + F8_TILE + warp * F8_SUB;
+      const uint32_t vbase = smem_u32(vsub);
       if (nvalid < SUBK) {  // V rows past the last key may hold anything: zero them
         const int nz = (SUBK - nvalid) * 8;
         for (int i = lane; i < nz; i += 32)
@@ -484,6 +488,19 @@ __device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* 
                                     (i & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
         __syncwarp();
+      }
+      // V words (loaded first, used after the softmax): keys 2t, 2t+1, 2t+8, 2t+9; dims 64h + 32e + 4(l/4) .. +3
+      uint32_t w[4][2][2];
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const int key = (kq & 1) + 2 * t4 + (kq >> 1) * 8;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int off = 64 * h + 32 * e + 4 * hq;
+            w[kq][h][e] = lds32(vbase + key * 128 + (((off >> 4) ^ (key & 7)) << 4) + (off & 15));
+          }
       }
       // S^T (16 keys x 8 heads), even and odd k-steps in separate chains
       float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
@@ -517,7 +534,7 @@ __device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* 
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float mnew = fmaxf(m_run[j], mx);
-        corr[j] = mnew == -INFINITY ? 1.f : exp2f(m_run[j] - mnew);
+        corr[j] = mnew == m_run[j] ? 1.f : exp2f(m_run[j] - mnew);  // unchanged max: exactly 1
         m_run[j] = mnew;
       }
       float pv[4];
@@ -528,32 +545,21 @@ __device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* 
       }
       l_run[0] = l_run[0] * corr[0] + pv[0] + pv[2];
       l_run[1] = l_run[1] * corr[1] + pv[1] + pv[3];
+      // once the running maxima settle most sub-tiles leave them unchanged
+      if (__any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f)) {
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        oacc[mt][0] *= corr[0];
-        oacc[mt][1] *= corr[1];
-        oacc[mt][2] *= corr[0];
-        oacc[mt][3] *= corr[1];
+        for (int mt = 0; mt < 8; ++mt) {
+          oacc[mt][0] *= corr[0];
+          oacc[mt][1] *= corr[1];
+          oacc[mt][2] *= corr[0];
+          oacc[mt][3] *= corr[1];
+        }
       }
       // P^T as the B operand (16 keys x 8 heads), f16
       const __half2 p0 = __floats2half2_rn(pv[0], pv[1]);  // keys 0-7
       const __half2 p1 = __floats2half2_rn(pv[2], pv[3]);  // keys 8-15
       const uint32_t bh0 = movmatrix_t(*reinterpret_cast<const uint32_t*>(&p0));
       const uint32_t bh1 = movmatrix_t(*reinterpret_cast<const uint32_t*>(&p1));
-      // V words: keys 2t, 2t+1, 2t+8, 2t+9; dims 64h + 32e + 4(l/4) .. +3
-      uint32_t w[4][2][2];
-#pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const int key = (kq & 1) + 2 * t4 + (kq >> 1) * 8;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int off = 64 * h + 32 * e + 4 * hq;
-            w[kq][h][e] = *reinterpret_cast<const uint32_t*>(
-                vsub + key * 128 + ((((off >> 4) ^ (key & 7))) << 4) + (off & 15));
-          }
-      }
       // O^T += V^T P^T over 8 m-tiles of permuted dims; one byte permute
       // gathers the key pairs of two m-tiles (bytes j and j + 1 of both keys)
 #pragma unroll
