@@ -250,6 +250,14 @@ int llama_sync_status(llama_ctx* ctx);
 /* Flags (LLAMA_FLAG_*) seen by the last llama_sync_status. */
 uint32_t llama_last_device_flags(const llama_ctx* ctx);
 
+/* Test of the timeout path: enqueue one kernel whose bounded wait, the one
+ * every pipelined kernel uses, waits on a shared-memory barrier that nothing
+ * completes. After limit_us microseconds (1 .. 1000000) it sets
+ * LLAMA_FLAG_WAIT_TIMEOUT and returns; the next llama_sync_status reports
+ * LLAMA_ERR_DEVICE_CHECK and the context stays usable. INVALID_ARG for a
+ * limit outside that range. Asynchronous. */
+int llama_check_wait_timeout(llama_ctx* ctx, int32_t limit_us);
+
 /* Static description of a status code. */
 const char* llama_strerror(int status);
 

@@ -82,6 +82,7 @@ _SIGS = {
     "llama_graph_launch": (c_int32, [c_void_p]),
     "llama_sync_status": (c_int32, [c_void_p]),
     "llama_last_device_flags": (ctypes.c_uint32, [c_void_p]),
+    "llama_check_wait_timeout": (c_int32, [c_void_p, c_int32]),
     "llama_strerror": (ctypes.c_char_p, [c_int32]),
     "llama_free": (c_int32, [c_void_p]),
     "llama_profile_enable": (c_int32, [c_void_p, ctypes.c_uint32]),
@@ -310,6 +311,10 @@ class Model:
     def sync_status(self):
         rc = lib().llama_sync_status(self.ctx)
         return rc, lib().llama_last_device_flags(self.ctx)
+
+    def check_wait_timeout(self, limit_us):
+        """Enqueue the bounded-wait check (a wait that runs out after limit_us)."""
+        self._chk(lib().llama_check_wait_timeout(self.ctx, int(limit_us)), "llama_check_wait_timeout")
 
     # ---- profiling
     def profile(self, kinds):

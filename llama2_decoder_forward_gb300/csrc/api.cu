@@ -983,6 +983,13 @@ int llama_sync_status(llama_ctx* c) {
 
 uint32_t llama_last_device_flags(const llama_ctx* c) { return c ? c->last_flags : 0u; }
 
+int llama_check_wait_timeout(llama_ctx* c, int32_t limit_us) {
+  TRY(check_ctx(c));
+  if (limit_us < 1 || limit_us > 1000000) return LLAMA_ERR_INVALID_ARG;
+  c->launches++;
+  return cuda_rc(launch_wait_check(c->status, (uint64_t)limit_us * 1000u, c->stream));
+}
+
 int llama_profile_enable(llama_ctx* c, uint32_t mask) {
   TRY(check_ctx(c));
   c->prof_mask = mask;

@@ -86,6 +86,8 @@ cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double the
 cudaError_t launch_rope_append(int dtype, const RopeAppendArgs& a, int rows, cudaStream_t st);
 cudaError_t launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st);
 cudaError_t launch_advance_positions(int32_t* positions, int B, cudaStream_t st);
+// One bounded wait that nothing completes: sets LLAMA_FLAG_WAIT_TIMEOUT after limit_ns.
+cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, cudaStream_t st);
 
 // ------------------------------------------------------------------ GEMM
 // y[n, m] (epilogue) sum_k x[n, k] * w[m, k]; x has N rows, w has M rows.

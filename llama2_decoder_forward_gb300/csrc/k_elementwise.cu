@@ -320,6 +320,25 @@ cudaError_t launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaS
 }  // namespace llgb
 
 namespace llgb {
+// Check of the bounded device wait: one thread waits, with the helper every
+// pipeline uses, on a shared-memory mbarrier whose phase nothing completes.
+// The wait runs out after limit_ns, sets LLAMA_FLAG_WAIT_TIMEOUT in the
+// status word and the kernel returns normally.
+__global__ void wait_check_kernel(uint32_t* status, uint64_t limit_ns) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait(&bar, 0, status, limit_ns);
+  }
+}
+
+cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, cudaStream_t st) {
+  return launch_k(wait_check_kernel, dim3(1), dim3(32), 0, st, 0, status, limit_ns);
+}
+
 cudaError_t launch_advance_positions(int32_t* positions, int B, cudaStream_t st) {
   return launch_k(advance_positions_kernel, dim3((B + 127) / 128), dim3(128), 0, st, 0, positions, B);
 }

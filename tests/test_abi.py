@@ -68,6 +68,7 @@ def test_null_context_and_arguments_rejected(lib):
     assert lib.llama_decode_step(None, None, None, 1, ctypes.byref(kv), None, None) == 1
     assert lib.llama_prefill(None, None, 1, 1, ctypes.byref(kv), None, None) == 1
     assert lib.llama_sync_status(None) == 1
+    assert lib.llama_check_wait_timeout(None, 1000) == 1
     assert lib.llama_free(None) == 1
     assert lib.llama_launch_count(None) == 0
     sp = binding.Sampling(1.0, 0, 1.0, 1.0)

@@ -1,8 +1,9 @@
 """Whole-model and whole-layer parity with the CPU oracle on the pages'
 workloads: the tiny fp32 model (greedy ids bit-exact, logits within 1e-4),
 single 7B- and 70B-shaped layers (decode and prefill) and ragged paged decode
-(MHA and GQA), plus device-side range checks."""
+(MHA and GQA), plus device-side range checks and the bounded-wait timeout."""
 import math
+import time
 
 import numpy as np
 import pytest
@@ -244,6 +245,33 @@ def test_device_range_checks_flag_and_skip():
     m.decode_step(torch.tensor([1, 2], dtype=torch.int32, device="cuda"),
                   torch.tensor([0, 0], dtype=torch.int32, device="cuda"), kv, lg)
     assert m.sync_status() == (0, 0)
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    # a device wait on a barrier that nothing completes: the kernel flags the
+    # timeout and returns; the host reads the flag and the next step is correct
+    need_gpu()
+    shape = _small_bf16()
+    B, T, cap = 2, 6, 32
+    w = synth.model_weights(shape, 12)
+    m = binding.Model(shape, to_dev(w), max_batch=B, max_tokens=B * T, max_seq=cap)
+    with pytest.raises(binding.LlamaError, match="INVALID_ARG"):
+        m.check_wait_timeout(0)
+    with pytest.raises(binding.LlamaError, match="INVALID_ARG"):
+        m.check_wait_timeout(2_000_000)
+    t0 = time.perf_counter()
+    m.check_wait_timeout(20_000)  # 20 ms
+    rc, flags = m.sync_status()
+    took = time.perf_counter() - t0
+    assert rc == 5 and flags == binding.FLAG_WAIT_TIMEOUT
+    assert 0.015 < took < 5.0
+    toks = synth.token_ids(B, T, shape.vocab, 12)
+    kv = binding.KVCache(shape, batch=B, capacity=cap)
+    lg = torch.empty(B, shape.vocab, device="cuda")
+    m.prefill(toks.cuda(), kv, lg)
+    assert m.sync_status() == (0, 0)
+    want = O.Model(shape, w, B, cap).prefill(toks.numpy())[:, -1]
+    assert_close(lg, want, BF16_TOL, "prefill after a timed-out wait")
 
 
 def test_host_checks_reject_bad_sizes():
