@@ -63,6 +63,8 @@ typedef enum llama_dtype { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
 #define LLAMA_FLAG_POS_RANGE 0x2u     /* position outside the cache */
 #define LLAMA_FLAG_PAGE_RANGE 0x4u    /* page id outside [0, n_pages) */
 #define LLAMA_FLAG_WAIT_TIMEOUT 0x8u  /* a bounded device wait expired */
+#define LLAMA_FLAG_INDEX 0x10u        /* bounds-check builds only: a kernel's shared-memory
+                                         layout or an index invariant failed its check */
 
 /* Model and sizing. Values of the size table ("Llama2架构与推理全解析" §1.6):
  * 7B = {32, 4096, 32, 32, 128, 11008, 32000}, 70B = {80, 8192, 64, 8, 128,
@@ -257,6 +259,12 @@ uint32_t llama_last_device_flags(const llama_ctx* ctx);
  * LLAMA_ERR_DEVICE_CHECK and the context stays usable. INVALID_ARG for a
  * limit outside that range. Asynchronous. */
 int llama_check_wait_timeout(llama_ctx* ctx, int32_t limit_us);
+
+/* 1 when the library was compiled with LLAMA_BOUNDS_CHECK (kernels check
+ * their shared-memory layout against the launch's dynamic shared memory and
+ * their index invariants, set LLAMA_FLAG_INDEX and skip the work on a
+ * failure), else 0. */
+int32_t llama_bounds_checked(void);
 
 /* Static description of a status code. */
 const char* llama_strerror(int status);

@@ -10,7 +10,11 @@ from __future__ import annotations
 import ctypes
 import os
 
-from .build import LIB
+from .build import CHECKED_LIB
+from .build import LIB as _MAIN_LIB
+
+# LLAMA_GB300_BOUNDS_CHECK=1 selects the bounds-check build of the same sources
+LIB = CHECKED_LIB if os.environ.get("LLAMA_GB300_BOUNDS_CHECK") == "1" else _MAIN_LIB
 
 c_int32 = ctypes.c_int32
 c_void_p = ctypes.c_void_p
@@ -20,7 +24,7 @@ EPI_STORE_F32, EPI_RESID_F32, EPI_STORE_T, EPI_SWIGLU = 0, 1, 2, 3
 EPI_SPLIT_X = 16  # OR-ed flag: x (and bf16 outputs) in the hi/lo pair layout
 KERNELS = ("rmsnorm", "gemm", "rope_append", "attn_decode", "attn_prefill", "embed", "argmax",
            "sample")
-FLAG_TOKEN_RANGE, FLAG_POS_RANGE, FLAG_PAGE_RANGE, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
+FLAG_TOKEN_RANGE, FLAG_POS_RANGE, FLAG_PAGE_RANGE, FLAG_WAIT_TIMEOUT, FLAG_INDEX = 1, 2, 4, 8, 16
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OUT_OF_RANGE", 4: "CUDA",
           5: "DEVICE_CHECK", 6: "WORKSPACE"}
 
@@ -83,6 +87,7 @@ _SIGS = {
     "llama_sync_status": (c_int32, [c_void_p]),
     "llama_last_device_flags": (ctypes.c_uint32, [c_void_p]),
     "llama_check_wait_timeout": (c_int32, [c_void_p, c_int32]),
+    "llama_bounds_checked": (c_int32, []),
     "llama_strerror": (ctypes.c_char_p, [c_int32]),
     "llama_free": (c_int32, [c_void_p]),
     "llama_profile_enable": (c_int32, [c_void_p, ctypes.c_uint32]),
@@ -114,8 +119,8 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB):
-            raise RuntimeError("libllama_gb300.so is not built (run llama2_decoder_forward_gb300"
-                               ".build.build_library() or __graft_entry__.build())")
+            raise RuntimeError("%s is not built (run llama2_decoder_forward_gb300.build."
+                               "build_library() or __graft_entry__.build())" % os.path.basename(LIB))
         l = ctypes.CDLL(LIB)
         for name, (res, args) in _SIGS.items():
             f = getattr(l, name)

@@ -16,6 +16,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libllama_gb300.so")
+# The same sources with -DLLAMA_BOUNDS_CHECK=1: kernels check their shared-
+# memory layouts and index invariants and flag LLAMA_FLAG_INDEX (tests only).
+CHECKED_BUILD = os.path.join(BUILD, "checked")
+CHECKED_LIB = os.path.join(CHECKED_BUILD, "libllama_gb300_checked.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,18 +45,21 @@ def _stale(target, sources):
     return any(os.path.getmtime(s) > t for s in sources)
 
 
-def build_library(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build_library(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile the library (checked=True: the bounds-check build) and return its path."""
+    bdir, lib_path = (CHECKED_BUILD, CHECKED_LIB) if checked else (BUILD, LIB)
+    extra = ["-DLLAMA_BOUNDS_CHECK=1"] if checked else []
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = _deps()
     nvcc = _nvcc()
     jobs = []
     objs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(bdir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + deps):
-            jobs.append([nvcc, *ARCH, *FLAGS, "-c", s, "-o", o])
+            jobs.append([nvcc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -65,9 +72,9 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        run([nvcc, *ARCH, "-shared", "-o", LIB, *objs])
-    return LIB
+    if force or jobs or _stale(lib_path, objs):
+        run([nvcc, *ARCH, "-shared", "-o", lib_path, *objs])
+    return lib_path
 
 
 if __name__ == "__main__":

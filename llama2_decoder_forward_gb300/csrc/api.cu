@@ -983,6 +983,14 @@ int llama_sync_status(llama_ctx* c) {
 
 uint32_t llama_last_device_flags(const llama_ctx* c) { return c ? c->last_flags : 0u; }
 
+int32_t llama_bounds_checked(void) {
+#if defined(LLAMA_BOUNDS_CHECK) && LLAMA_BOUNDS_CHECK
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 int llama_check_wait_timeout(llama_ctx* c, int32_t limit_us) {
   TRY(check_ctx(c));
   if (limit_us < 1 || limit_us > 1000000) return LLAMA_ERR_INVALID_ARG;

@@ -63,6 +63,39 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// ------------------------------------------------------------------ bounds-check builds
+// Compiled with -DLLAMA_BOUNDS_CHECK=1 the kernels check what a sanitizer
+// would: their shared-memory layout against the dynamic shared memory of the
+// launch, and index invariants the host is trusted with otherwise. A failed
+// check sets LLAMA_FLAG_INDEX and the caller skips the work. In other builds
+// every check is the constant true.
+#ifndef LLAMA_BOUNDS_CHECK
+#define LLAMA_BOUNDS_CHECK 0
+#endif
+__device__ __forceinline__ bool bc_ok(bool cond, uint32_t* status) {
+#if LLAMA_BOUNDS_CHECK
+  if (!cond) {
+    flag(status, LLAMA_FLAG_INDEX);
+    return false;
+  }
+#endif
+  return true;
+}
+// [p, p + bytes) inside this CTA's dynamic shared memory, p a multiple of align
+__device__ __forceinline__ bool bc_smem(const void* p, uint32_t bytes, uint32_t align,
+                                        uint32_t* status) {
+#if LLAMA_BOUNDS_CHECK
+  extern __shared__ __align__(16) uint8_t llgb_dyn_smem[];
+  uint32_t size;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(size));
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(llgb_dyn_smem));
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  return bc_ok(a >= base && a + bytes <= base + size && (a & (align - 1)) == 0, status);
+#else
+  return true;
+#endif
+}
+
 // 32-bit shared-memory load by shared-window address (a realigned dynamic
 // shared-memory pointer is otherwise read through generic addressing)
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {

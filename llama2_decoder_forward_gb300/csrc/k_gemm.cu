@@ -269,6 +269,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   const int kb0 = (int)(((long long)split * p.num_kb) / p.splits);
   const int kb1 = (int)(((long long)(split + 1) * p.num_kb) / p.splits);
 
+  {  // bounds-check builds: the layout fits the launch, the split sums fit the
+     // stages they reuse, output rows fit their stride (same for every CTA)
+    const uint32_t tables = 256 + (EPI == kEpiRope ? 16 * p.ncol : 0) + (p.ssq_in ? 4 * p.ncol : 0);
+    const uint32_t staged = p.splits > 1 ? (uint32_t)p.ncol * BM * 4 * (DUAL ? 2 : 1)
+                                         : (EPI == LLAMA_EPI_RESID_F32 ? 16u * p.ncol : 0u);
+    uint32_t* st = threadIdx.x == 0 ? p.status : nullptr;
+    const bool fits = bc_smem(smem, (uint32_t)S * stage_bytes + tables, 1024, st);
+    const bool red_fits = bc_ok(staged <= (uint32_t)S * stage_bytes, st);
+    const bool rows_fit = bc_ok(EPI == kEpiRope || p.M <= p.ldo, st);
+    if (!fits || !red_fits || !rows_fit) {
+      grid_dep_wait();
+      return;
+    }
+  }
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);

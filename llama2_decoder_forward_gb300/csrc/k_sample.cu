@@ -102,6 +102,12 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 1) sample_kernel(SampleArgs a)
   grid_dep_launch();
   extern __shared__ float e_sm[];  // [CH][512] unnormalised probabilities, then the bitmap
   uint32_t* seen = reinterpret_cast<uint32_t*>(e_sm + CH * SAMPLE_THREADS);
+  // bounds-check builds: the probabilities and the bitmap fit the launch, and
+  // the row fits the chunks
+  if (!bc_smem(e_sm, (uint32_t)(CH * SAMPLE_THREADS * 4 + ((a.V + 31) >> 5) * 4), 4,
+               threadIdx.x == 0 ? a.status : nullptr) ||
+      !bc_ok(a.V <= CH * SAMPLE_THREADS, threadIdx.x == 0 ? a.status : nullptr))
+    return;
   __shared__ int red_i[kSampleWarps];
   __shared__ float red_f[kSampleWarps];
   __shared__ uint32_t red_u[kSampleWarps];

@@ -83,3 +83,14 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="not built"):
         binding.lib()
+
+
+def test_bounds_check_build_exports_everything_and_reports_itself(lib):
+    from llama2_decoder_forward_gb300 import build as b
+    path = b.build_library(checked=True)
+    checked = ctypes.CDLL(path)
+    for n in sorted(_declared()):
+        assert hasattr(checked, n), n
+    checked.llama_bounds_checked.restype = ctypes.c_int32
+    assert checked.llama_bounds_checked() == 1
+    assert lib.llama_bounds_checked() == 0
