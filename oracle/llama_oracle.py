@@ -33,14 +33,18 @@ design notes):
   * The KV cache holds K and V in the model's storage type: the pages keep the
     cache in half precision to halve its memory ("Llama2架构全景解析" §2.1),
     so a bf16 model's cache stores each value rounded to bf16 (nearest, ties
-    to even) and an fp32 model's cache rounds to fp32; attention reads the
-    stored values. This is the only rounding in the oracle (cache_dtype="f64"
-    turns it off).
+    to even) and an fp32 model's cache rounds to fp32; an FP8 cache (FP8 is
+    named as a latency option in "Llama2架构全景解析" §3.2) stores
+    E4M3(value / scale) * scale, nearest with ties to even, saturating at
+    +-448. Attention reads the stored values. This is the only rounding in
+    the oracle (cache_dtype="f64" turns it off).
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py
-(closed forms, invariants, library routines, brute force); the end-to-end
-logits on random weights have no printed value to match and rest on the pinned
-parts plus the decode-equals-prefill and paged-equals-contiguous checks.
+(closed forms, invariants, library routines, brute force). The end-to-end
+logits on random weights have no printed value to match (end-to-end parity
+unpinned as a whole): they rest on the pinned parts plus the
+decode-equals-prefill, extend-equals-prefill and paged-equals-contiguous
+checks.
 """
 from __future__ import annotations
 
