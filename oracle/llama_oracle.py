@@ -103,6 +103,28 @@ def cache_store(values: np.ndarray, cache_dtype: str, scale: float = 1.0) -> np.
     return np.asarray(values, dtype=f64)
 
 
+def quantize_rows_e4m3(w: np.ndarray):
+    """FP8 E4M3 weights with one scale per output row (row m of a [out, in]
+    matrix; FP8 as the latency option of "Llama2架构全景解析" §3.2, reading
+    R29): s_m = max_k |w[m, k]| / 448 (1 for an all-zero row) and
+    code[m, k] = e4m3(w[m, k] / s_m), so the largest entry of every row maps
+    to +-448. The scale and the quotient are fp32 operations (the
+    quantisation kernel's precision; they decide the integer code), the
+    rounding to E4M3 is nearest with ties to even. Returns (codes as E4M3
+    values in float64, scales as float64 holding fp32 values); the weight the
+    model then uses is codes * scales[:, None]."""
+    w32 = np.asarray(w, dtype=np.float32)
+    amax = np.max(np.abs(w32), axis=1)
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = (w32 / s[:, None]).astype(np.float32)
+    return round_to_e4m3(q.astype(f64)), s.astype(f64)
+
+
+def dequantize_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """The weight an E4M3 matrix stands for: code * row scale, exactly."""
+    return np.asarray(codes, dtype=f64) * np.asarray(scales, dtype=f64)[:, None]
+
+
 def _kv_store(cdt, k, v):
     """K and V as stored: cdt is a storage type, or ("e4m3", k_scale, v_scale)."""
     if isinstance(cdt, tuple):

@@ -530,3 +530,55 @@ def test_e4m3_cache_stores_scaled_values_and_decode_still_equals_prefill():
     k = m.K[0][:, :, :9] / 0.05  # every stored K is an E4M3 value times the scale
     np.testing.assert_allclose(O.round_to_e4m3(k), k, rtol=1e-14, atol=0)
     assert len(np.unique(np.round(np.abs(k[k != 0]), 9))) < 250  # at most 2 x 126 finite magnitudes
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) weights, row scales
+
+def test_quantize_rows_e4m3_hand_rows():
+    w = np.array([[0.5, -1.0, 0.25, 0.0],
+                  [0.0, 0.0, 0.0, 0.0],
+                  [3.0, 0.01, -0.75, 1.5]])
+    codes, s = O.quantize_rows_e4m3(w)
+    np.testing.assert_array_equal(s, np.float32([1 / 448, 1.0, 3 / 448]).astype(np.float64))
+    np.testing.assert_array_equal(codes[0], [224.0, -448.0, 112.0, 0.0])
+    np.testing.assert_array_equal(codes[1], [0.0, 0.0, 0.0, 0.0])
+    # 0.01 / (3/448) = 1.4933 -> 1.5; -0.75 / (3/448) = -112; 1.5 -> 224
+    np.testing.assert_array_equal(codes[2], [448.0, 1.5, -112.0, 224.0])
+
+
+def test_quantize_rows_e4m3_matches_library_cast_and_maps_row_max_to_448():
+    rng = np.random.default_rng(32)
+    w = (rng.standard_normal((37, 300)) * 0.02).astype(np.float32)  # non-square: rows are outputs
+    w[5] *= 1000.0
+    w[9] = 0.0
+    codes, s = O.quantize_rows_e4m3(w)
+    wt = torch.from_numpy(w)
+    st = torch.where(wt.abs().amax(1) > 0, wt.abs().amax(1) / 448.0, torch.ones(37))
+    lib = (wt / st[:, None]).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(s, st.double().numpy())
+    np.testing.assert_array_equal(codes, lib)
+    nz = np.abs(w).max(1) > 0
+    np.testing.assert_array_equal(np.abs(codes[nz]).max(1), np.full(nz.sum(), 448.0))
+    assert np.all(codes[9] == 0) and s[9] == 1.0
+
+
+def test_dequantized_rows_are_within_half_an_e4m3_step():
+    rng = np.random.default_rng(33)
+    w = rng.standard_normal((64, 512)) * 0.02
+    codes, s = O.quantize_rows_e4m3(w)
+    deq = O.dequantize_rows(codes, s)
+    # half the spacing: 2^-4 relative for normals, 2^-10 * s below 2^-6 * s
+    bound = np.maximum(np.abs(w) * 2.0**-4, s[:, None] * 2.0**-10) * (1 + 1e-6)
+    assert np.all(np.abs(w - deq) <= bound)
+    assert np.abs(w - deq).max() > 0  # it does quantise
+
+
+def test_row_scales_factor_out_of_the_projection():
+    # y[n, m] = s_m * sum_k u[n, k] code[m, k]: the row scale can be applied to
+    # the accumulator after the contraction
+    rng = np.random.default_rng(34)
+    w = rng.standard_normal((24, 40)) * 0.05
+    u = rng.standard_normal((7, 40))
+    codes, s = O.quantize_rows_e4m3(w)
+    np.testing.assert_allclose(O.linear(u, O.dequantize_rows(codes, s)), (u @ codes.T) * s[None, :],
+                               rtol=1e-13, atol=1e-15)
