@@ -131,7 +131,7 @@ def replica_result(ms_per_step, tokens_per_step, device=None):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def build_model(workload, device, kv_e4m3=False):
+def build_model(workload, device, kv_e4m3=False, w_e4m3=False):
     import torch
     from llama2_decoder_forward_gb300 import binding, synth
 
@@ -151,6 +151,9 @@ def build_model(workload, device, kv_e4m3=False):
         layers.append({"attn_norm": rn(H, std=0.1, mean=1.0), "wqkv": rn(shape.qkv_rows, H),
                        "wo": rn(H, H), "ffn_norm": rn(H, std=0.1, mean=1.0), "w_gate": rn(I, H),
                        "w_up": rn(I, H), "w_down": rn(H, I)})
+    if w_e4m3:  # E4M3 projections with row scales, quantised on the device
+        layers = [binding.quantize_layer_e4m3(lw) for lw in layers]
+        torch.cuda.synchronize()
     w = {"layers": layers}
     if workload == "model":
         w.update(embed=rn(V, H), final_norm=rn(H, std=0.1, mean=1.0), lm_head=rn(V, H))
@@ -185,7 +188,8 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     __graft_entry__.build()
-    shape, model, kv = build_model(args.workload, dev, kv_e4m3=args.kv == "e4m3")
+    shape, model, kv = build_model(args.workload, dev, kv_e4m3=args.kv == "e4m3",
+                                   w_e4m3=args.weights == "e4m3")
     torch.cuda.synchronize()  # inputs are drawn on the default stream; the model runs on its own
     g = torch.Generator(device=dev)
     g.manual_seed(7)
@@ -298,7 +302,10 @@ def run_gpu(args):
     kv_bytes = B * shape.n_kv_heads * (CTX + 1) * shape.head_dim * 2 * kv_elem  # K and V per layer
     attn_avg = attn_ms / max(attn_n, 1)
     achieved = kv_bytes / (attn_avg * 1e-3) / 1e9
-    wbytes = (shape.qkv_rows + shape.hidden) * shape.hidden * 2 + 3 * shape.hidden * shape.intermediate * 2
+    w_rows = shape.qkv_rows + shape.hidden + 3 * shape.intermediate  # wqkv, wo, gate, up, down
+    w_elems = (shape.qkv_rows + shape.hidden) * shape.hidden + 3 * shape.hidden * shape.intermediate
+    # bf16 weights, or E4M3 bytes plus one fp32 scale per row
+    wbytes = w_elems * 2 if args.weights == "bf16" else w_elems + 4 * w_rows
     lm_bytes = shape.vocab * shape.hidden * 2 if args.workload == "model" else 0
     step_bytes = L * (wbytes + kv_bytes) + lm_bytes
     line = {
@@ -312,13 +319,14 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if args.kv == "bf16" else "bf16 (KV cache e4m3)",
+        "dtype": "bf16" + ("" if args.kv == "bf16" else " (KV cache e4m3)") +
+                 ("" if args.weights == "bf16" else " (projection weights e4m3)"),
         "data": "synthetic (random-init 7B weights N(0,0.02), cache N(0,1), uniform token ids)",
         "config": {"workload": ("llama2-7b decode step: 32 layers + embedding + LM head + greedy, "
                                 "batch 32, 1024 cached positions, contiguous KV")
                    if args.workload == "model" else
                    "one llama2-7b decoder layer, decode step, batch 32, 1024 cached positions",
-                   "batch": B, "context": CTX, "kv_cache": args.kv, "l2": "inputs larger than L2 (%.1f GB per step)" % (step_bytes / 1e9),
+                   "batch": B, "context": CTX, "kv_cache": args.kv, "weights": args.weights, "l2": "inputs larger than L2 (%.1f GB per step)" % (step_bytes / 1e9),
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "launch": "cuda graph of the step" if use_graph else "direct launches"},
         "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
@@ -601,6 +609,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels directly")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
                     help="KV-cache storage (e4m3: the FP8 cache; not the headline configuration)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "e4m3"],
+                    help="projection weights (e4m3: FP8 with row scales; not the headline "
+                         "configuration)")
     args = ap.parse_args()
     global B_WORKLOAD
     B_WORKLOAD = args.workload

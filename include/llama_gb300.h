@@ -84,7 +84,18 @@ typedef struct llama_config {
   int32_t max_tokens;    /* most prompt rows (B*T) in one prefill call */
   int32_t max_seq;       /* positions 0 .. max_seq-1 may be used (RoPE table size) */
   int32_t has_embed_head;/* 1: token ids in, logits out; 0: hidden in/out only */
+  int32_t weight_dtype;  /* projection weights (wqkv, wo, w_gate, w_up, w_down):
+                            LLAMA_W_MODEL in the config's dtype, or LLAMA_W_E4M3 */
 } llama_config;
+
+/* Projection weights as FP8 E4M3 (bf16 models only; FP8 as the latency option
+ * of "Llama2架构全景解析" §3.2): each matrix is [rows, cols] bytes plus an fp32
+ * scale per row, row m standing for e4m3(byte) * scale[m]
+ * (llama_quantize_rows_e4m3 makes both from bf16). Activations, norms, the
+ * embedding and the LM head keep the config's dtype. The GEMMs stream one
+ * byte per weight and apply the row scale to their accumulators. */
+#define LLAMA_W_MODEL 0
+#define LLAMA_W_E4M3 1
 
 /* One layer's weights (device pointers, dtype of the config).
  *   attn_norm, ffn_norm : [H]                       RMSNorm gains
@@ -92,6 +103,8 @@ typedef struct llama_config {
  *   wo                  : [H, n_q d]
  *   w_gate, w_up        : [I, H]
  *   w_down              : [H, I]
+ *   *_scale             : fp32 [rows of that matrix], weight_dtype LLAMA_W_E4M3
+ *                         only (the matrices are then E4M3 bytes); else ignored
  * The pointers must stay valid for the life of the context. */
 typedef struct llama_layer_weights {
   const void* attn_norm;
@@ -101,6 +114,11 @@ typedef struct llama_layer_weights {
   const void* w_gate;
   const void* w_up;
   const void* w_down;
+  const float* wqkv_scale;
+  const float* wo_scale;
+  const float* w_gate_scale;
+  const float* w_up_scale;
+  const float* w_down_scale;
 } llama_layer_weights;
 
 /* Whole-model weights. embed and lm_head are separate [V, H] matrices (the
@@ -244,6 +262,16 @@ int llama_graph_capture_decode(llama_ctx* ctx, const int32_t* tokens, int32_t* p
                                int32_t advance);
 /* Replay the captured step on the context's stream. */
 int llama_graph_launch(llama_ctx* ctx);
+
+/* E4M3 weights with one scale per row, on the device: for each row m of the
+ * bf16 matrix w [rows, cols], scales[m] = max_k |w[m,k]| / 448 (1 for an
+ * all-zero row) and codes[m,k] = e4m3(w[m,k] / scales[m]), nearest with ties
+ * to even, saturating at +-448 (fp32 arithmetic). w, codes: 16-byte aligned,
+ * cols a multiple of 16; codes [rows, cols] bytes, scales [rows] fp32.
+ * stream is a cudaStream_t (NULL: the legacy default stream). Asynchronous;
+ * INVALID_ARG for null or misaligned pointers or bad sizes. */
+int llama_quantize_rows_e4m3(const void* w, int32_t rows, int32_t cols, void* codes,
+                             float* scales, void* stream);
 
 /* Synchronise the stream, then read and clear the device status word.
  * Returns LLAMA_OK, LLAMA_ERR_CUDA or LLAMA_ERR_DEVICE_CHECK. */

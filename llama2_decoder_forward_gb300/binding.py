@@ -34,12 +34,16 @@ class LlamaConfig(ctypes.Structure):
                 ("n_kv_heads", c_int32), ("head_dim", c_int32), ("intermediate", c_int32),
                 ("vocab", c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
                 ("dtype", c_int32), ("max_batch", c_int32), ("max_tokens", c_int32),
-                ("max_seq", c_int32), ("has_embed_head", c_int32)]
+                ("max_seq", c_int32), ("has_embed_head", c_int32), ("weight_dtype", c_int32)]
+
+
+LAYER_MATS = ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
+PROJECTIONS = ("wqkv", "wo", "w_gate", "w_up", "w_down")
+W_MODEL, W_E4M3 = 0, 1
 
 
 class LayerWeights(ctypes.Structure):
-    _fields_ = [(n, c_void_p) for n in
-                ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")]
+    _fields_ = [(n, c_void_p) for n in LAYER_MATS] + [(n + "_scale", c_void_p) for n in PROJECTIONS]
 
 
 class Weights(ctypes.Structure):
@@ -87,6 +91,8 @@ _SIGS = {
     "llama_sync_status": (c_int32, [c_void_p]),
     "llama_last_device_flags": (ctypes.c_uint32, [c_void_p]),
     "llama_check_wait_timeout": (c_int32, [c_void_p, c_int32]),
+    "llama_quantize_rows_e4m3": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_void_p,
+                                           c_void_p]),
     "llama_bounds_checked": (c_int32, []),
     "llama_strerror": (ctypes.c_char_p, [c_int32]),
     "llama_free": (c_int32, [c_void_p]),
@@ -154,11 +160,36 @@ def _stream_handle(stream):
     return c_void_p(s.cuda_stream)
 
 
-def make_config(shape, max_batch, max_tokens, max_seq, has_embed_head=True) -> LlamaConfig:
+def make_config(shape, max_batch, max_tokens, max_seq, has_embed_head=True,
+                weight_dtype=W_MODEL) -> LlamaConfig:
     return LlamaConfig(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
                        shape.head_dim, shape.intermediate, shape.vocab if has_embed_head else 0,
                        shape.rms_eps, shape.rope_theta, F32 if shape.dtype == "f32" else BF16,
-                       max_batch, max_tokens, max_seq, 1 if has_embed_head else 0)
+                       max_batch, max_tokens, max_seq, 1 if has_embed_head else 0, weight_dtype)
+
+
+def quantize_rows_e4m3(w, stream=None):
+    """E4M3 codes (uint8 [rows, cols]) and per-row fp32 scales of a bf16 device
+    matrix, by the library's quantiser (llama_quantize_rows_e4m3)."""
+    import torch
+    w = w.contiguous()
+    rows, cols = w.shape
+    codes = torch.empty(rows, cols, dtype=torch.uint8, device=w.device)
+    scales = torch.empty(rows, dtype=torch.float32, device=w.device)
+    rc = lib().llama_quantize_rows_e4m3(_p(w), rows, cols, _p(codes), _p(scales),
+                                        _stream_handle(stream))
+    if rc:
+        raise LlamaError(rc, "llama_quantize_rows_e4m3")
+    return codes, scales
+
+
+def quantize_layer_e4m3(lw, stream=None):
+    """A layer's weight dict with its five projections as E4M3 codes plus
+    "<name>_scale" row scales (norm gains unchanged)."""
+    out = dict(lw)
+    for n in PROJECTIONS:
+        out[n], out[n + "_scale"] = quantize_rows_e4m3(lw[n], stream)
+    return out
 
 
 def workspace_bytes(cfg: LlamaConfig) -> int:
@@ -217,16 +248,19 @@ class Model:
         import torch
         self.shape = shape
         self.weights = weights  # keep the tensors alive
-        self.cfg = make_config(shape, max_batch, max_tokens, max_seq, has_embed_head)
-        nbytes = workspace_bytes(self.cfg)
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         layers = weights["layers"]
         if len(layers) != shape.n_layers:
             raise ValueError("shape has %d layers, weights have %d" % (shape.n_layers, len(layers)))
+        # E4M3 projections (quantize_layer_e4m3) carry "<name>_scale" entries
+        w8 = "wqkv_scale" in layers[0]
+        self.cfg = make_config(shape, max_batch, max_tokens, max_seq, has_embed_head,
+                               W_E4M3 if w8 else W_MODEL)
+        nbytes = workspace_bytes(self.cfg)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         arr = (LayerWeights * len(layers))()
         for i, lw in enumerate(layers):
-            arr[i] = LayerWeights(*[lw[n].data_ptr() for n in
-                                    ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")])
+            scales = [lw[n + "_scale"].data_ptr() if w8 else None for n in PROJECTIONS]
+            arr[i] = LayerWeights(*([lw[n].data_ptr() for n in LAYER_MATS] + scales))
         self._layers_arr = arr
         w = Weights(_p(weights.get("embed")), _p(weights.get("final_norm")), _p(weights.get("lm_head")),
                     ctypes.cast(arr, ctypes.POINTER(LayerWeights)))

@@ -77,11 +77,17 @@ int check_config(const llama_config* c) {
   if (c->has_embed_head != 0 && c->has_embed_head != 1) return LLAMA_ERR_INVALID_ARG;
   if (c->has_embed_head && c->vocab < 1) return LLAMA_ERR_INVALID_ARG;
   if (c->dtype != LLAMA_F32 && c->dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
+  if (c->weight_dtype != LLAMA_W_MODEL && c->weight_dtype != LLAMA_W_E4M3)
+    return LLAMA_ERR_INVALID_ARG;
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return LLAMA_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads != 0) return LLAMA_ERR_INVALID_ARG;
   if (c->head_dim % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
   // 16-byte row pitches for TMA and vector loads
   if (c->hidden % 8 != 0 || c->intermediate % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (c->weight_dtype == LLAMA_W_E4M3) {  // byte rows: 16-byte pitches for TMA
+    if (c->dtype != LLAMA_BF16 || c->hidden % 16 != 0 || c->intermediate % 16 != 0)
+      return LLAMA_ERR_UNSUPPORTED;
+  }
   if (c->dtype == LLAMA_BF16) {
     if (c->head_dim != 128) return LLAMA_ERR_UNSUPPORTED;
     if (c->n_q_heads / c->n_kv_heads > 16) return LLAMA_ERR_UNSUPPORTED;
@@ -154,6 +160,8 @@ struct llama_ctx {
   uint32_t* status = nullptr;
   float2* rope = nullptr;
   std::map<Key2, CUtensorMap> maps;
+  // E4M3 projection weights: weight pointer -> its per-row scales
+  std::map<const void*, const float*> wscale;
   uint32_t prof_mask = 0;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[LLAMA_KERNEL_COUNT];
   size_t ev_used[LLAMA_KERNEL_COUNT] = {};
@@ -185,6 +193,25 @@ const CUtensorMap* map2d(llama_ctx* c, const void* ptr, uint64_t rows, uint64_t 
   CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return nullptr;
+  return &c->maps.emplace(k, m).first->second;
+}
+
+// 2D row-major [rows, cols] byte tensor (E4M3 weights), box {64, 128}, no
+// swizzle (the GEMM converts the tile to bf16 itself).
+const CUtensorMap* map2d_u8(llama_ctx* c, const void* ptr, uint64_t rows, uint64_t cols) {
+  Key2 k{ptr, 5, rows, cols, 128, 0, 0};
+  auto it = c->maps.find(k);
+  if (it != c->maps.end()) return &it->second;
+  CUtensorMap m;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return nullptr;
   return &c->maps.emplace(k, m).first->second;
@@ -349,8 +376,23 @@ int do_gemm(llama_ctx* c, int epi, const void* x, int N, int K, const void* w, c
     if (!aligned16(x) || !aligned16(w) || (wu && !aligned16(wu))) return LLAMA_ERR_INVALID_ARG;
     trim_maps(c);
     g.n_tile = gemm_n_tile(N, split);
-    g.map_w = map2d(c, w, M, K, 128);
-    g.map_up = wu ? map2d(c, wu, M, K, 128) : nullptr;
+    if (!c->wscale.empty()) {  // E4M3 projection weights
+      auto iw = c->wscale.find(w);
+      if (iw != c->wscale.end()) g.w_scale = iw->second;
+      if (wu) {
+        auto iu = c->wscale.find(wu);
+        if (iu != c->wscale.end()) g.u_scale = iu->second;
+      }
+      if ((wu != nullptr) && ((g.w_scale != nullptr) != (g.u_scale != nullptr)))
+        return LLAMA_ERR_INVALID_ARG;
+    }
+    if (g.w_scale) {
+      g.map_w = map2d_u8(c, w, M, K);
+      g.map_up = wu ? map2d_u8(c, wu, M, K) : nullptr;
+    } else {
+      g.map_w = map2d(c, w, M, K, 128);
+      g.map_up = wu ? map2d(c, wu, M, K, 128) : nullptr;
+    }
     g.map_x = map2d(c, x, split ? (uint64_t)round16(N) + N : (uint64_t)N, K,
                     gemm_box_rows(N, split));
     if (!g.map_w || !g.map_x || (wu && !g.map_up)) return LLAMA_ERR_CUDA;
@@ -691,11 +733,18 @@ int llama_init(const llama_config* cfg, const llama_weights* w, void* workspace,
   if (!w->layers) return LLAMA_ERR_INVALID_ARG;
   if (cfg->has_embed_head && (!w->embed || !w->final_norm || !w->lm_head))
     return LLAMA_ERR_INVALID_ARG;
+  const bool w8 = cfg->weight_dtype == LLAMA_W_E4M3;
   for (int l = 0; l < cfg->n_layers; ++l) {
     const llama_layer_weights& lw = w->layers[l];
     const void* ps[7] = {lw.attn_norm, lw.wqkv, lw.wo, lw.ffn_norm, lw.w_gate, lw.w_up, lw.w_down};
     for (const void* p : ps)
       if (!p || !aligned16(p)) return LLAMA_ERR_INVALID_ARG;
+    if (w8) {
+      const float* sc[5] = {lw.wqkv_scale, lw.wo_scale, lw.w_gate_scale, lw.w_up_scale,
+                            lw.w_down_scale};
+      for (const float* p : sc)
+        if (!p || (reinterpret_cast<uintptr_t>(p) % 4) != 0) return LLAMA_ERR_INVALID_ARG;
+    }
   }
   if (cfg->has_embed_head && (!aligned16(w->embed) || !aligned16(w->lm_head)))
     return LLAMA_ERR_INVALID_ARG;
@@ -741,10 +790,21 @@ int llama_init(const llama_config* cfg, const llama_weights* w, void* workspace,
     const uint64_t H = cfg->hidden, d = cfg->head_dim, nq = cfg->n_q_heads,
                    nkv = cfg->n_kv_heads, I = cfg->intermediate;
     for (const auto& lw : c->layers) {
-      if (!map2d(c, lw.wqkv, (nq + 2 * nkv) * d, H, 128) || !map2d(c, lw.wo, H, nq * d, 128) ||
-          !map2d(c, lw.w_gate, I, H, 128) || !map2d(c, lw.w_up, I, H, 128) ||
-          !map2d(c, lw.w_down, H, I, 128))
+      if (w8) {
+        c->wscale[lw.wqkv] = lw.wqkv_scale;
+        c->wscale[lw.wo] = lw.wo_scale;
+        c->wscale[lw.w_gate] = lw.w_gate_scale;
+        c->wscale[lw.w_up] = lw.w_up_scale;
+        c->wscale[lw.w_down] = lw.w_down_scale;
+        if (!map2d_u8(c, lw.wqkv, (nq + 2 * nkv) * d, H) || !map2d_u8(c, lw.wo, H, nq * d) ||
+            !map2d_u8(c, lw.w_gate, I, H) || !map2d_u8(c, lw.w_up, I, H) ||
+            !map2d_u8(c, lw.w_down, H, I))
+          rc = LLAMA_ERR_CUDA;
+      } else if (!map2d(c, lw.wqkv, (nq + 2 * nkv) * d, H, 128) ||
+                 !map2d(c, lw.wo, H, nq * d, 128) || !map2d(c, lw.w_gate, I, H, 128) ||
+                 !map2d(c, lw.w_up, I, H, 128) || !map2d(c, lw.w_down, H, I, 128)) {
         rc = LLAMA_ERR_CUDA;
+      }
     }
     if (cfg->has_embed_head && !map2d(c, c->lm_head, cfg->vocab, H, 128)) rc = LLAMA_ERR_CUDA;
   }
@@ -989,6 +1049,16 @@ int32_t llama_bounds_checked(void) {
 #else
   return 0;
 #endif
+}
+
+int llama_quantize_rows_e4m3(const void* w, int32_t rows, int32_t cols, void* codes,
+                             float* scales, void* stream) {
+  if (!w || !codes || !scales || rows < 1 || cols < 16 || cols % 16 != 0)
+    return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) % 4) != 0)
+    return LLAMA_ERR_INVALID_ARG;
+  return cuda_rc(launch_quantize_rows_e4m3(w, rows, cols, codes, scales,
+                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int llama_check_wait_timeout(llama_ctx* c, int32_t limit_us) {

@@ -86,6 +86,9 @@ cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, double the
 cudaError_t launch_rope_append(int dtype, const RopeAppendArgs& a, int rows, cudaStream_t st);
 cudaError_t launch_argmax(const float* logits, int B, int V, int32_t* ids, cudaStream_t st);
 cudaError_t launch_advance_positions(int32_t* positions, int B, cudaStream_t st);
+// E4M3 rows of a bf16 [rows, cols] matrix with per-row scales (cols % 16 == 0).
+cudaError_t launch_quantize_rows_e4m3(const void* w, int rows, int cols, void* codes,
+                                      float* scales, cudaStream_t st);
 // One bounded wait that nothing completes: sets LLAMA_FLAG_WAIT_TIMEOUT after limit_ns.
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, cudaStream_t st);
 
@@ -122,6 +125,11 @@ struct GemmCall {
   const float* ssq_in = nullptr;
   int ssq_tiles = 0, ssq_ld = 0, norm_h = 0;
   float norm_eps = 0.f;
+  // E4M3 weights (bf16 path): map_w / map_up are byte tensors, box {64, 128},
+  // no swizzle; row m stands for code * w_scale[m] (u_scale[m] for W_up).
+  // Null: bf16 weights.
+  const float* w_scale = nullptr;
+  const float* u_scale = nullptr;
   void* out;
   int ldo;
   uint32_t* status;

@@ -335,6 +335,54 @@ __global__ void wait_check_kernel(uint32_t* status, uint64_t limit_ns) {
   }
 }
 
+// E4M3 weights, one CTA per row: the row's largest magnitude (exact in fp32),
+// scale = amax / 448 (1 for an all-zero row), then every value divided by the
+// scale (IEEE fp32 division) and rounded to E4M3, nearest even, saturating.
+__global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const bf16* __restrict__ w,
+                                                                  int cols,
+                                                                  uint8_t* __restrict__ codes,
+                                                                  float* __restrict__ scales) {
+  grid_dep_wait();
+  grid_dep_launch();
+  __shared__ float red[8];
+  const size_t row = blockIdx.x;
+  const bf16* src = w + row * cols;
+  float amax = 0.f;
+  for (int k = threadIdx.x * 8; k < cols; k += 256 * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + k);
+    const bf16* e = reinterpret_cast<const bf16*>(&v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(__bfloat162float(e[j])));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const float s = amax > 0.f ? amax / 448.0f : 1.0f;
+  if (threadIdx.x == 0) scales[row] = s;
+  uint8_t* dst = codes + row * cols;
+  for (int k = threadIdx.x * 8; k < cols; k += 256 * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + k);
+    const bf16* e = reinterpret_cast<const bf16*>(&v);
+    uint32_t b[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      b[j >> 2] |= (uint32_t)f32_to_e4m3(__bfloat162float(e[j]) / s) << (8 * (j & 3));
+    *reinterpret_cast<uint2*>(dst + k) = make_uint2(b[0], b[1]);
+  }
+}
+
+cudaError_t launch_quantize_rows_e4m3(const void* w, int rows, int cols, void* codes,
+                                      float* scales, cudaStream_t st) {
+  // a plain launch: the stream may be the legacy default stream
+  quantize_rows_e4m3_kernel<<<rows, 256, 0, st>>>(reinterpret_cast<const bf16*>(w), cols,
+                                                  reinterpret_cast<uint8_t*>(codes), scales);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wait_check(uint32_t* status, uint64_t limit_ns, cudaStream_t st) {
   return launch_k(wait_check_kernel, dim3(1), dim3(32), 0, st, 0, status, limit_ns);
 }

@@ -47,11 +47,16 @@ struct TcParams {
   int M, N, K;
   int n_tile, num_kb, splits, n_tiles;
   int stages;
+  int nconv;  // W8: converted-tile buffers (1 or 2)
   uint32_t tmem_cols;
   int lo;      // >0 (hi/lo mode): TMEM column offset of the remainder product (= ncol)
   int lo_rows; // hi/lo mode: activation row r's remainder is row lo_rows + r
   int ncol;    // output columns one tile produces (n_tile, or n_tile / 2 in the hi/lo mode)
   size_t out_lo;  // >0: bf16 outputs also write their remainder out_lo elements further
+  // E4M3 weights (W8 kernels): row m of W (and of W_up) stands for
+  // code * w_scale[m] (u_scale[m]); the scale multiplies the accumulator
+  const float* w_scale;
+  const float* u_scale;
   void* out;
   int ldo;
   uint32_t* status;
@@ -240,7 +245,47 @@ __device__ __forceinline__ RedSlice red_slice(const TcParams& p, int k) {
   return r;
 }
 
-template <int EPI>
+// E4M3 weight tile -> bf16 tile for the MMA. The source is the TMA box of
+// 128 rows x 64 bytes without swizzle (row r at r * 64); the destination is
+// the 128-row x 64-element bf16 tile in the 128-byte-swizzle layout the bf16
+// path loads by TMA (16-byte chunk j of row r at r * 128 + ((j ^ (r & 7)) << 4)).
+// Thread t of the 128 takes 16 bytes (quarter q = t % 4) of rows t / 4 + 32i:
+// a warp reads 512 contiguous bytes, and each group of 8 threads writes the
+// even chunks of one row and the odd chunks of the next, so neither side has
+// bank conflicts. E4M3 values are exact in f16 and in bf16.
+__device__ __forceinline__ void e4m3_tile_to_bf16(uint32_t src, uint32_t dst, int t) {
+  const int q = t & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 32 + (t >> 2);
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(src + r * 64 + q * 16));
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t lo, hi;  // f16 pairs of bytes (0, 1) and (2, 3)
+      e4m3x4_to_f16x2x2(w[j], lo, hi);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      const __nv_bfloat162 ab = __floats2bfloat162_rn(a.x, a.y);
+      const __nv_bfloat162 bb = __floats2bfloat162_rn(b.x, b.y);
+      o[2 * j] = *reinterpret_cast<const uint32_t*>(&ab);
+      o[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&bb);
+    }
+    const uint32_t row = dst + r * 128;
+    const uint32_t c0 = (uint32_t)((2 * q) ^ (r & 7)) << 4, c1 = (uint32_t)((2 * q + 1) ^ (r & 7)) << 4;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + c0), "r"(o[0]), "r"(o[1]),
+                 "r"(o[2]), "r"(o[3])
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + c1), "r"(o[4]), "r"(o[5]),
+                 "r"(o[6]), "r"(o[7])
+                 : "memory");
+  }
+}
+
+template <int EPI, bool W8>
 __global__ void __launch_bounds__(GEMM_THREADS, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
                    const __grid_constant__ CUtensorMap tmX, TcParams p) {
@@ -248,20 +293,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t a_bytes = BM * BK * 2;
+  // weight tiles as loaded: bf16, or E4M3 bytes (W8)
+  const uint32_t a_bytes = BM * BK * (W8 ? 1 : 2);
   const uint32_t b_bytes = (uint32_t)p.n_tile * BK * 2;
   const uint32_t stage_bytes = a_bytes * (DUAL ? 2 : 1) + b_bytes;
   const int S = p.stages;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
+  // W8: p.nconv buffers of converted bf16 weight tiles (gate then up) after the stages
+  const uint32_t conv_bytes = W8 ? BM * BK * 2 * (DUAL ? 2 : 1) : 0;
+  const int NC = W8 ? p.nconv : 0;
+  uint8_t* conv = smem + (size_t)S * stage_bytes;
+  uint8_t* bar_block = conv + (size_t)NC * conv_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(bar_block);
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
   // ctl[0]: TMEM base address, ctl[1]: abort, ctl[2]: this CTA reduces the tile
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(accf + 1);
+  // W8: converted buffer c is full (128 converter arrivals) / free (MMA commit)
+  uint64_t* cfull = accf + 3;
+  uint64_t* cempty = cfull + 2;
   // kEpiRope: the tile's tokens (ncol entries after the 256-byte barrier block)
-  TokInfo* tok = reinterpret_cast<TokInfo*>(smem + (size_t)S * stage_bytes + 256);
+  TokInfo* tok = reinterpret_cast<TokInfo*>(bar_block + 256);
   // RMSNorm scales of the tile's rows (consumers), after the token table
-  float* scl = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes + 256 +
-                                        (EPI == kEpiRope ? 16 * p.ncol : 0));
+  float* scl = reinterpret_cast<float*>(bar_block + 256 + (EPI == kEpiRope ? 16 * p.ncol : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
@@ -275,8 +328,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
     const uint32_t staged = p.splits > 1 ? (uint32_t)p.ncol * BM * 4 * (DUAL ? 2 : 1)
                                          : (EPI == LLAMA_EPI_RESID_F32 ? 16u * p.ncol : 0u);
     uint32_t* st = threadIdx.x == 0 ? p.status : nullptr;
-    const bool fits = bc_smem(smem, (uint32_t)S * stage_bytes + tables, 1024, st);
-    const bool red_fits = bc_ok(staged <= (uint32_t)S * stage_bytes, st);
+    const uint32_t body = (uint32_t)S * stage_bytes + (uint32_t)NC * conv_bytes;
+    const bool fits = bc_smem(smem, body + tables, 1024, st) &&
+                      bc_ok(16u * S + 56u <= 256u, st) &&  // barrier block
+                      bc_ok(!W8 || NC == 1 || NC == 2, st);
+    const bool red_fits = bc_ok(staged <= body, st);
     const bool rows_fit = bc_ok(EPI == kEpiRope || p.M <= p.ldo, st);
     if (!fits || !red_fits || !rows_fit) {
       grid_dep_wait();
@@ -292,6 +348,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
     mbar_init(accf, 1);
     ctl[1] = 0;
     ctl[2] = 0;
+    if (W8) {
+      for (int c = 0; c < NC; ++c) {
+        mbar_init(&cfull[c], 128);
+        mbar_init(&cempty[c], 1);
+      }
+    }
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
     if (DUAL) tma_prefetch_desc(&tmU);
@@ -364,17 +426,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   } else if (warp == 1) {
     if (lane == 0) {  // ---------------- MMA issuer
       const uint32_t idesc = idesc_bf16_f32(BM, p.n_tile);
-      int s = 0;
-      uint32_t ph = 0;
+      int s = 0, c = 0;
+      uint32_t ph = 0, cph = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (ctl[1] || !mbar_wait(&full[s], ph, p.status)) {
+        if (ctl[1] || !mbar_wait(&full[s], ph, p.status) ||
+            (W8 && !mbar_wait(&cfull[c], cph, p.status))) {
           ctl[1] = 1;
           break;
         }
         tc_fence_after();
         const uint32_t a0 = smem_u32(smem + (size_t)s * stage_bytes);
-        const uint64_t da = smem_desc_sw128(a0);
-        const uint64_t du = smem_desc_sw128(a0 + a_bytes);
+        // weights: the stage's bf16 tiles, or (W8) the converted buffer
+        const uint32_t w0 = W8 ? smem_u32(conv + (size_t)c * conv_bytes) : a0;
+        const uint32_t up_off = W8 ? BM * BK * 2 : a_bytes;
+        const uint64_t da = smem_desc_sw128(w0);
+        const uint64_t du = smem_desc_sw128(w0 + up_off);
         const uint64_t db = smem_desc_sw128(a0 + a_bytes * (DUAL ? 2 : 1));
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {  // advance 32 bytes (16 bf16) along K
@@ -383,6 +449,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           if (DUAL) tc_mma_f16(tmem + p.n_tile, du + 2 * k, db + 2 * k, idesc, acc);
         }
         tc_commit(&empty[s]);
+        if (W8) {
+          tc_commit(&cempty[c]);
+          if (++c == NC) {
+            c = 0;
+            cph ^= 1;
+          }
+        }
         if (++s == S) {
           s = 0;
           ph ^= 1;
@@ -392,6 +465,35 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
       mbar_wait(accf, 0, p.status);  // every MMA retired before teardown
     }
   } else {  // ---------------- epilogue warps 2..5
+    if (W8) {
+      // first the weight converters: every stage's E4M3 tiles to bf16, in
+      // k-block order, into the conversion buffers (weights only: no
+      // dependency on the previous kernel)
+      const int t = threadIdx.x - 64;
+      int s = 0, c = 0;
+      uint32_t ph = 0, cph = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (ctl[1] || !mbar_wait(&full[s], ph, p.status) ||
+            !mbar_wait(&cempty[c], cph ^ 1, p.status)) {
+          ctl[1] = 1;
+          break;
+        }
+        const uint32_t src = smem_u32(smem + (size_t)s * stage_bytes);
+        const uint32_t dst = smem_u32(conv + (size_t)c * conv_bytes);
+        e4m3_tile_to_bf16(src, dst, t);
+        if (DUAL) e4m3_tile_to_bf16(src + a_bytes, dst + BM * BK * 2, t);
+        fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+        mbar_arrive(&cfull[c]);
+        if (++c == NC) {
+          c = 0;
+          cph ^= 1;
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
     grid_dep_wait();  // the residual and the outputs belong to the previous kernels' order
     grid_dep_launch();
     if (EPI == kEpiRope) {  // token table, filled while the MMAs run
@@ -422,10 +524,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
         const int n0 = tile_n * p.ncol;
         const int nvalid = min(p.ncol, p.N - n0);
         const RopeFeat rf = EPI == kEpiRope ? rope_feat(p.rope, min(gm, p.M - 1)) : RopeFeat{};
+        const float wsc = W8 ? p.w_scale[min(gm, p.M - 1)] : 1.f;
+        const float usc = W8 && DUAL ? p.u_scale[min(gm, p.M - 1)] : 1.f;
         for (int c0 = 0; c0 < nvalid; c0 += 16) {
           float g[16], u[16];
           load_acc16(tq, c0, p.lo, g);
           if (DUAL) load_acc16(tq, up + c0, p.lo, u);
+          if (W8) {  // E4M3 weights: the row scale (before any use of the sums)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              g[j] *= wsc;
+              if (DUAL) u[j] *= usc;
+            }
+          }
           if (p.ssq_in) {  // the input rows were normalised up to this scale
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -555,6 +666,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
             if (DUAL) { u[0] += uv[s2].x; u[1] += uv[s2].y; u[2] += uv[s2].z; u[3] += uv[s2].w; }
           }
         const int gm0 = tile_m * BM + rq;
+        if (W8) {  // E4M3 weights: the row scales of the split-ordered sums
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int m = min(gm0 + e, p.M - 1);
+            g[e] *= p.w_scale[m];
+            if (DUAL) u[e] *= p.u_scale[m];
+          }
+        }
         if (p.ssq_in) {
           const float sc = scl[c];
 #pragma unroll
@@ -649,7 +768,7 @@ __global__ void gemm_f32_kernel(const float* __restrict__ x, const float* __rest
 
 // ------------------------------------------------------------------ planning
 struct Plan {
-  int n_tile, ncol, lo, lo_rows, stages, splits, m_tiles, n_tiles, num_kb, ctas_per_sm;
+  int n_tile, ncol, lo, lo_rows, stages, nconv, splits, m_tiles, n_tiles, num_kb, ctas_per_sm;
   size_t smem;
   uint32_t tmem_cols;
 };
@@ -664,7 +783,7 @@ int gemm_n_tile(int N, int split) {
 // rope: the Q/K/V epilogue's token table (16 bytes per tile column) follows
 // the barrier block.
 static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, bool rope,
-                      bool scale) {
+                      bool scale, bool w8) {
   Plan pl{};
   pl.n_tile = gemm_n_tile(N, split);
   pl.lo = split ? pl.n_tile / 2 : 0;
@@ -673,15 +792,22 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, b
   const int width = pl.n_tile * (dual ? 2 : 1);  // accumulator columns
   pl.tmem_cols = 32;
   while ((int)pl.tmem_cols < width) pl.tmem_cols <<= 1;
-  const int stage_bytes = BM * BK * 2 * (dual ? 2 : 1) + pl.n_tile * BK * 2;
+  const int stage_bytes = BM * BK * (w8 ? 1 : 2) * (dual ? 2 : 1) + pl.n_tile * BK * 2;
   // two CTAs per SM while both fit in tensor memory: narrow (decode) tiles,
   // and the single-accumulator prefill tiles, whose epilogues then overlap
   // the other CTA's K loop (two stages each)
   const bool two = (pl.n_tile <= 128 && pl.tmem_cols <= 256) || (!dual && pl.n_tile == 256 && N > 512);
   const int budget = two ? 112 * 1024 : 224 * 1024;
   const int extra = (rope ? 16 * pl.ncol : 0) + (scale ? 4 * pl.ncol : 0);
-  pl.stages = std::max(2, std::min(8, (budget - 2048 - extra) / stage_bytes));
-  pl.smem = (size_t)pl.stages * stage_bytes + 1024 + 256 + extra;
+  // E4M3 weights: buffers of converted bf16 tiles besides the (smaller)
+  // stages; two while three stages still fit, else one (converting a k-block
+  // takes far less time than streaming its bytes)
+  const int conv1 = w8 ? BM * BK * 2 * (dual ? 2 : 1) : 0;
+  pl.nconv = w8 ? 2 : 0;
+  if (w8 && (budget - 2048 - extra - 2 * conv1) / stage_bytes < 3) pl.nconv = 1;
+  const int conv = pl.nconv * conv1;
+  pl.stages = std::max(2, std::min(w8 ? 12 : 8, (budget - 2048 - extra - conv) / stage_bytes));
+  pl.smem = (size_t)pl.stages * stage_bytes + conv + 1024 + 256 + extra;
   pl.ctas_per_sm = std::max(1, std::min(two ? 2 : 1, (int)(233472 / (pl.smem + 1024))));
   pl.m_tiles = (M + BM - 1) / BM;
   pl.n_tiles = (N + pl.ncol - 1) / pl.ncol;
@@ -694,7 +820,7 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, b
   // latency and the cluster reduction).
   constexpr int kFixedKb = 4;
   const size_t red_bytes = (size_t)pl.ncol * (dual ? 2 : 1) * BM * sizeof(float);
-  const bool can_split = pl.n_tiles == 1 && red_bytes <= (size_t)pl.stages * stage_bytes;
+  const bool can_split = pl.n_tiles == 1 && red_bytes <= (size_t)pl.stages * stage_bytes + conv;
   const int max_split = can_split ? std::min(8, pl.num_kb) : 1;
   long best = -1;
   pl.splits = 1;
@@ -712,8 +838,11 @@ static Plan make_plan(int M, int N, int K, bool dual, int split, int sm_count, b
 
 template <int EPI>
 static cudaError_t set_attr() {
-  return cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kMaxDynSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_tc_kernel<EPI, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 
 cudaError_t gemm_prepare() {
@@ -725,7 +854,7 @@ cudaError_t gemm_prepare() {
   return set_attr<LLAMA_EPI_SWIGLU>();
 }
 
-template <int EPI>
+template <int EPI, bool W8>
 static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st) {
   TcParams p;
   if (g.rope) p.rope = *g.rope;
@@ -746,17 +875,25 @@ static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st)
   p.splits = pl.splits;
   p.n_tiles = pl.n_tiles;
   p.stages = pl.stages;
+  p.nconv = pl.nconv;
   p.tmem_cols = pl.tmem_cols;
   p.lo = pl.lo;
   p.lo_rows = pl.lo_rows;
   p.ncol = pl.ncol;
   p.out_lo = g.out_lo;
+  p.w_scale = g.w_scale;
+  p.u_scale = g.u_scale;
   p.out = g.out;
   p.ldo = g.ldo;
   p.status = g.status;
   const CUtensorMap* up = g.map_up ? g.map_up : g.map_w;
-  return launch_k(gemm_tc_kernel<EPI>, dim3(pl.n_tiles, pl.m_tiles, pl.splits),
+  return launch_k(gemm_tc_kernel<EPI, W8>, dim3(pl.n_tiles, pl.m_tiles, pl.splits),
                   dim3(GEMM_THREADS), pl.smem, st, pl.splits, *g.map_w, *up, *g.map_x, p);
+}
+
+template <int EPI>
+static cudaError_t launch_tc(const GemmCall& g, const Plan& pl, cudaStream_t st) {
+  return g.w_scale ? launch_tc<EPI, true>(g, pl, st) : launch_tc<EPI, false>(g, pl, st);
 }
 
 template <int EPI>
@@ -776,8 +913,9 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st) {
     }
   }
   const bool dual = g.epi == LLAMA_EPI_SWIGLU;
+  if (g.w_scale && dual != (g.u_scale != nullptr)) return cudaErrorInvalidValue;
   const Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count, g.epi == kEpiRope,
-                            g.ssq_in != nullptr);
+                            g.ssq_in != nullptr, g.w_scale != nullptr);
   if (pl.n_tile != g.n_tile) return cudaErrorInvalidValue;
   switch (g.epi) {
     case LLAMA_EPI_STORE_F32: return launch_tc<LLAMA_EPI_STORE_F32>(g, pl, st);

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gpu_ops.py", "tests/test_gpu_model.py", "tests/test_gpu_extend.py",
-          "tests/test_gpu_sample.py", "tests/test_gpu_fp8.py"]
+          "tests/test_gpu_sample.py", "tests/test_gpu_fp8.py", "tests/test_gpu_w8.py"]
 
 
 def _env():
