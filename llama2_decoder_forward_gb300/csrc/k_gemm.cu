@@ -21,6 +21,10 @@
 // shared memory in split order (deterministic), each CTA finishing a slice of
 // the tile's columns.
 //
+// E4M3 weights (W8 instantiations): the weight tiles arrive as bytes, the
+// epilogue warps convert each to a bf16 tile in shared memory before the MMA
+// (E4M3 is exact in bf16), and the per-row scale multiplies the accumulator.
+//
 // fp32 path: plain CUDA-core FMAs in fp32 (no TF32), one thread per output.
 #include <algorithm>
 
