@@ -63,6 +63,27 @@ def test_workspace_bytes_and_config_checks(lib):
     assert lib.llama_workspace_bytes(ctypes.byref(tiny), ctypes.byref(n)) == 0
 
 
+def test_e4m3_weight_config_and_quantiser_argument_checks(lib):
+    n = ctypes.c_size_t()
+    w8 = _cfg(weight_dtype=binding.W_E4M3)
+    assert lib.llama_workspace_bytes(ctypes.byref(w8), ctypes.byref(n)) == 0
+    assert lib.llama_workspace_bytes(ctypes.byref(_cfg(weight_dtype=2)), ctypes.byref(n)) == 1
+    # E4M3 projections need a bf16 model and 16-byte rows of bytes
+    tiny = binding.make_config(synth.TINY, 1, 16, 32, weight_dtype=binding.W_E4M3)  # fp32
+    assert lib.llama_workspace_bytes(ctypes.byref(tiny), ctypes.byref(n)) == 2
+    assert lib.llama_workspace_bytes(ctypes.byref(_cfg(weight_dtype=1, intermediate=11000)),
+                                     ctypes.byref(n)) == 2
+    # the quantiser rejects bad arguments before touching the device
+    buf = ctypes.create_string_buffer(4096 + 16)
+    al = (ctypes.addressof(buf) + 15) // 16 * 16
+    q = lib.llama_quantize_rows_e4m3
+    assert q(None, 4, 64, al, al, None) == 1
+    assert q(al, 0, 64, al, al, None) == 1
+    assert q(al, 4, 40, al, al, None) == 1       # rows of 40 bytes
+    assert q(al + 8, 4, 64, al, al, None) == 1   # misaligned source
+    assert q(al, 4, 64, al, al + 2, None) == 1   # misaligned scales
+
+
 def test_null_context_and_arguments_rejected(lib):
     kv = binding.KV()
     assert lib.llama_decode_step(None, None, None, 1, ctypes.byref(kv), None, None) == 1
