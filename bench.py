@@ -27,6 +27,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Llama2-7B decode tokens/s (bs32, ctx1024); decode-step HBM GB/s vs peak"
+
+
+def workload_name(workload):
+    """The decode workload both arms (GPU and CPU oracle) report in config."""
+    if workload == "model":
+        return ("llama2-7b decode step: 32 layers + embedding + LM head + greedy, "
+                "batch 32, 1024 cached positions, contiguous KV")
+    return "one llama2-7b decoder layer, decode step, batch 32, 1024 cached positions"
 B, CTX, CAP = 32, 1024, 1040
 
 
@@ -322,10 +330,7 @@ def run_gpu(args):
         "dtype": "bf16" + ("" if args.kv == "bf16" else " (KV cache e4m3)") +
                  ("" if args.weights == "bf16" else " (projection weights e4m3)"),
         "data": "synthetic (random-init 7B weights N(0,0.02), cache N(0,1), uniform token ids)",
-        "config": {"workload": ("llama2-7b decode step: 32 layers + embedding + LM head + greedy, "
-                                "batch 32, 1024 cached positions, contiguous KV")
-                   if args.workload == "model" else
-                   "one llama2-7b decoder layer, decode step, batch 32, 1024 cached positions",
+        "config": {"workload": workload_name(args.workload),
                    "batch": B, "context": CTX, "kv_cache": args.kv, "weights": args.weights, "l2": "inputs larger than L2 (%.1f GB per step)" % (step_bytes / 1e9),
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "launch": "cuda graph of the step" if use_graph else "direct launches"},
@@ -587,8 +592,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "llama2-7b decode step, batch 32, 1024 cached positions (CPU oracle)",
-                       "batch": B, "context": CTX},
+            "config": {"workload": workload_name(args.workload), "batch": B, "context": CTX,
+                       "kv_cache": "bf16", "weights": "bf16", "parallelism": "CPU oracle, rank 0"},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
