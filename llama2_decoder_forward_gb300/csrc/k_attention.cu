@@ -622,11 +622,6 @@ __global__ void __launch_bounds__(DEC_THREADS, FP8 ? 3 : 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * SB);
   uint64_t* empty = full + NS;
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + NS);
-  static_assert((4 * 16 * AD + 128) * sizeof(float) <= NS * SB, "merge area exceeds the stages");
-  if (!bc_smem(smem, NS * SB + 256, 1024, threadIdx.x == 0 ? p.status : nullptr)) {
-    grid_dep_wait();  // bounds-check builds: the layout does not fit the launch
-    return;
-  }
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -880,9 +875,6 @@ __global__ void __launch_bounds__(PRE_THREADS, 2)
 
   grid_dep_wait();  // q, k, v come from the RoPE/append kernel
   grid_dep_launch();
-  if (!bc_smem(smem, 2 * PTILE + PSTAGES * 2 * PTILE + 256, 1024,
-               threadIdx.x == 0 ? p.status : nullptr))
-    return;  // bounds-check builds: the layout does not fit the launch
   const int qt = p.n_qtiles - 1 - (int)blockIdx.x;  // longest rows first
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / p.G;
