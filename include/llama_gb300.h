@@ -21,7 +21,9 @@
  *    workspace (llama_workspace_bytes).
  *  - Row-major storage everywhere. Projection weights are [out, in]
  *    (y = x W^T), which is the pages' x W with W stored [in, out].
- *  - dtype LLAMA_BF16: weights, gains, embedding, LM head, KV cache are bf16;
+ *  - dtype LLAMA_BF16: weights, gains, embedding, LM head, KV cache are bf16
+ *    (options: an FP8 E4M3 KV cache, llama_kv.kv_dtype, and E4M3 projection
+ *    weights with per-row scales, llama_config.weight_dtype);
  *    dtype LLAMA_F32: all of them are fp32. In both cases the residual
  *    stream (hidden) and the logits are fp32 and every reduction (GEMM,
  *    softmax, norm statistics) accumulates in fp32.
