@@ -241,6 +241,8 @@ class Model:
     weights: dict as produced by synth.model_weights / layer_weights, already
     on the GPU ({"embed", "final_norm", "lm_head", "layers": [...]}); a
     layer-only model passes {"layers": [...]} and has_embed_head=False.
+    Layers made by quantize_layer_e4m3 (E4M3 projections with row scales)
+    select weight_dtype LLAMA_W_E4M3.
     """
 
     def __init__(self, shape, weights, *, max_batch, max_tokens, max_seq, has_embed_head=True,
