@@ -35,13 +35,6 @@ __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
 __device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)q, __NV_E4M3)));
 }
-// The two low E4M3 bytes of q2 as an f16x2 register (byte 0 -> low half).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t q2) {
-  uint32_t d;
-  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %1;\n cvt.rn.f16x2.e4m3x2 %0, a;\n}"
-      : "=r"(d) : "r"(q2));
-  return d;
-}
 // Four E4M3 bytes as two f16x2 registers: bytes 0, 1 -> lo; bytes 2, 3 -> hi.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t q4, uint32_t& lo, uint32_t& hi) {
   asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
@@ -180,11 +173,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 
