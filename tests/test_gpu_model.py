@@ -293,6 +293,14 @@ def test_host_checks_reject_bad_sizes():
         m.decode_step(torch.zeros(2, dtype=torch.int32, device="cuda"),
                       torch.zeros(2, dtype=torch.int32, device="cuda"), bad, lg)
     assert e.value.rc == 1
+    # empty inputs: no sequences, or prompts of no tokens
+    none = torch.zeros(0, dtype=torch.int32, device="cuda")
+    with pytest.raises(binding.LlamaError) as e:
+        m.decode_step(none, none, kv, lg)
+    assert e.value.rc == 1
+    with pytest.raises(binding.LlamaError) as e:
+        m.prefill(torch.zeros(2, 0, dtype=torch.int32, device="cuda"), kv, lg)
+    assert e.value.rc == 1
 
 
 # --------------------------------------------------------------------------- CUDA graph replay
