@@ -516,49 +516,57 @@ def run_extend(args):
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
-class OracleSample:
-    """The oracle on a bounded sample: one 7B layer's decode step for the 32
-    sequences over a 1024-position cache (plus the LM head and greedy choice
-    for the full model), scaled to the whole step by the layer count. Inputs
-    are drawn once; only the oracle's arithmetic is timed."""
+class OracleStep:
+    """The oracle's whole decode step on `n_seq` of the 32 sequences. Model
+    workload: the embedding, all 32 decoder layers (each a full fp64
+    layer_decode over a 1024-position cache), the final RMSNorm, the LM head
+    and the greedy choice; layer workload: one layer_decode on a hidden
+    input. One layer's fp64 weights and one layer's cache serve every layer
+    call (32 distinct fp64 layers would need 52 GB of host memory; the
+    arithmetic of each call is the same). Inputs are drawn once; only the
+    oracle's arithmetic is timed."""
 
-    def __init__(self, workload):
+    def __init__(self, n_seq, workload="model"):
         import numpy as np
         import torch
         from llama2_decoder_forward_gb300 import synth
         from oracle import llama_oracle as O
 
         self.O = O
-        self.shape = shape = synth.LLAMA2_7B.with_(n_layers=1)
-        self.workload = workload
-        self.lw = {k: O.as64(v) for k, v in synth.layer_weights(shape, 1003, 0).items()}
-        self.x = O.as64(synth.hidden_input(B, shape.hidden, 1003))
-        self.K = O.as64(synth.cache_values((B, shape.n_kv_heads, CTX + 1, shape.head_dim), 1003,
+        self.n_seq = n_seq
+        self.model = workload == "model"
+        self.shape = shape = synth.LLAMA2_7B if self.model else synth.LLAMA2_7B.with_(n_layers=1)
+        one = shape.with_(n_layers=1)
+        self.lw = {k: O.as64(v) for k, v in synth.layer_weights(one, 1003, 0).items()}
+        self.K = O.as64(synth.cache_values((n_seq, shape.n_kv_heads, CTX + 1, shape.head_dim), 1003,
                                            torch.bfloat16, stream=0))
-        self.V = O.as64(synth.cache_values((B, shape.n_kv_heads, CTX + 1, shape.head_dim), 1003,
+        self.V = O.as64(synth.cache_values((n_seq, shape.n_kv_heads, CTX + 1, shape.head_dim), 1003,
                                            torch.bfloat16, stream=1))
-        self.pos = np.full(B, CTX)
-        self.lm = None
-        if workload == "model":
+        self.pos = np.full(n_seq, CTX)
+        if self.model:
             g = torch.Generator().manual_seed(5)
-            self.lm = O.as64((torch.randn(shape.vocab, shape.hidden, generator=g) * 0.02).to(torch.bfloat16))
-            self.fn = O.as64(synth.layer_weights(shape, 1004, 0)["attn_norm"])
-        self.n_layers = 32 if workload == "model" else 1
-        self.desc = ("one 7B layer's decode step for 32 sequences over 1024 cached positions in fp64, "
-                     "scaled x%d layers%s" % (self.n_layers, " + the LM head and greedy choice"
-                                              if self.lm is not None else ""))
+            rn = lambda *s: O.as64((torch.randn(*s, generator=g) * 0.02).to(torch.bfloat16))
+            self.embed = rn(shape.vocab, shape.hidden)
+            self.lm = rn(shape.vocab, shape.hidden)
+            self.fn = self.lw["ffn_norm"]
+            self.tokens = synth.token_ids(1, n_seq, shape.vocab, 1003).numpy()[0]
+            self.desc = ("the fp64 oracle's whole decode step (embedding, 32 layer decodes over "
+                         "1024 cached positions, final norm, LM head, greedy) for %d of the 32 "
+                         "sequences" % n_seq)
+        else:
+            self.x = O.as64(synth.hidden_input(n_seq, shape.hidden, 1003))
+            self.desc = ("the fp64 oracle's decode step of one 7B layer over 1024 cached "
+                         "positions for %d of the 32 sequences" % n_seq)
 
     def step_seconds(self):
         O = self.O
         t0 = time.perf_counter()
-        h = O.layer_decode(self.x, self.lw, self.shape, self.K, self.V, self.pos)
-        t_layer = time.perf_counter() - t0
-        t_head = 0.0
-        if self.lm is not None:
-            t0 = time.perf_counter()
+        h = O.embed(self.embed, self.tokens) if self.model else self.x
+        for _ in range(self.shape.n_layers):
+            h = O.layer_decode(h, self.lw, self.shape, self.K, self.V, self.pos)
+        if self.model:
             O.greedy(O.lm_head(h, self.fn, self.lm, self.shape.rms_eps))
-            t_head = time.perf_counter() - t0
-        return self.n_layers * t_layer + t_head
+        return time.perf_counter() - t0
 
 
 def _cores():
@@ -568,19 +576,57 @@ def _cores():
     return os.cpu_count()
 
 
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name") or line.startswith("CPU part"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _single_thread_seconds(n_seq, workload):
+    """One oracle step on one core (BLAS limited to one thread, in a fresh
+    process so the limit takes effect before numpy loads)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = "import bench; print(bench.OracleStep(%d, %r).step_seconds())" % (n_seq, workload)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                           text=True, timeout=300)
+        return float(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+
+
 def cpu_baseline(workload):
-    o = OracleSample(workload)
+    """Timed oracle on the host cores beside the GPU number: the whole step
+    for all 32 sequences (best of two), plus a one-core step on one sequence."""
+    o = OracleStep(B, workload)
     sec = min(o.step_seconds() for _ in range(2))
+    st = _single_thread_seconds(1, workload)
     return {"value": B / sec, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "cpu_model": _cpu_model(), "step_s": sec,
+            "single_thread": {"value": 1.0 / st if st else None, "unit": "tokens/s",
+                              "step_s": st, "sample": "the same step for 1 sequence on 1 core"},
             "sample": o.desc + " (best of 2)"}
+
+
+REF_SEQS = 8  # sequences per reference-arm step: a bounded sample of the batch of 32
 
 
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
         return
-    o = OracleSample(args.workload)
-    desc = o.desc
+    o = OracleStep(REF_SEQS, args.workload)
     for _ in range(args.warmup):
         o.step_seconds()
     t0 = time.perf_counter()
@@ -588,14 +634,15 @@ def run_reference(args):
     for _ in range(args.steps):
         total += o.step_seconds()
     ms = total / args.steps * 1e3
-    v = B / (ms * 1e-3)
+    v = REF_SEQS / (ms * 1e-3)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(args.workload), "batch": B, "context": CTX,
-                       "kv_cache": "bf16", "weights": "bf16", "parallelism": "CPU oracle, rank 0"},
+                       "kv_cache": "bf16", "weights": "bf16", "parallelism": "CPU oracle, rank 0",
+                       "sample": "%d of the %d sequences per step" % (REF_SEQS, B)},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-                             "sample": desc},
+                             "cpu_model": _cpu_model(), "sample": o.desc},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t0}
     print(json.dumps(line), flush=True)

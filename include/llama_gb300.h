@@ -363,7 +363,10 @@ int llama_op_rope_append(llama_ctx* ctx, const float* qkv, int32_t rows, int32_t
                          void* q_out, void* k_out, void* v_out);
 
 /* Decode attention over the cache (§2.3, §2.4, §1.5): q T [B, n_q, d] (rotated),
- * sequence b attends keys 0..positions[b] of layer `layer`; out T [B, n_q d]. */
+ * sequence b attends keys 0..positions[b] of layer `layer`; out T [B, n_q d].
+ * positions[b] must lie in [0, min(cache slots, max_seq)): a position outside
+ * sets LLAMA_FLAG_POS_RANGE and its output rows are undefined (a negative
+ * position gives zeros). */
 int llama_op_attention_decode(llama_ctx* ctx, const void* q, const int32_t* positions,
                               int32_t B, int32_t layer, const llama_kv* kv, void* out);
 
@@ -382,9 +385,12 @@ int llama_op_attention_decode(llama_ctx* ctx, const void* q, const int32_t* posi
  * address and sets kernel attributes; make that first call before any stream
  * capture. Calls share the array: calls that overlap on the GPU race and must
  * be serialised by the caller. Shapes whose partial sums would exceed 8 MiB
- * return LLAMA_ERR_OUT_OF_RANGE and enqueue nothing. bf16 and head_dim 128
- * only. Range problems in positions or the page table are still skipped on
- * the device but are not reported (there is no status word). */
+ * return LLAMA_ERR_OUT_OF_RANGE and enqueue nothing (the partial sums are
+ * sized for every slot of the cache: positions may go up to the cache's
+ * capacity - 1, whatever cfg->max_seq says). bf16 and head_dim 128 only.
+ * Range problems in positions or the page table are still skipped on the
+ * device but are not reported (there is no status word): a negative position
+ * gives zero output rows, a page id outside the pool reads zeros. */
 int llama_attention_decode_noalloc(const llama_config* cfg, const void* q,
                                    const int32_t* positions, int32_t B, int32_t layer,
                                    const llama_kv* kv, void* out, void* stream);

@@ -67,13 +67,20 @@ struct DecParams {
   // which is row cu_rows[b] of q and of the output (null: row b)
   const int32_t* cu_rows;
   float v_scale;  // FP8 cache: V bytes are e4m3 * v_scale (1 otherwise; K's scale is in scale_log2)
+  // keys the launch covers: min(cache slots, splits * keys_per_split)
+  int key_limit;
 };
 
-// Number of keys sequence b attends (positions[b] + 1), clamped to the cache;
-// out-of-range positions are flagged by the RoPE/append kernel.
-__device__ __forceinline__ int decode_keys(int pos, int cap_keys) {
-  if (pos < 0) return 0;
-  return min(pos + 1, cap_keys);
+// Number of keys sequence b attends (positions[b] + 1). A position below 0
+// or one whose keys the launch does not cover (past the cache, or past the
+// key range the split plan was sized for) is flagged; the sequence then
+// attends no keys (negative position) or the covered keys only.
+__device__ __forceinline__ int decode_keys(int pos, int key_limit, uint32_t* status, bool report) {
+  if (pos < 0 || pos + 1 > key_limit) {
+    if (report) flag(status, LLAMA_FLAG_POS_RANGE);
+    return pos < 0 ? 0 : key_limit;
+  }
+  return pos + 1;
 }
 
 // Row index (within one layer's [rows, d] view of the cache) of the 16-key
@@ -624,8 +631,9 @@ __global__ void __launch_bounds__(DEC_THREADS, FP8 ? 3 : 2)
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + NS);
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  static_assert((4 * 16 * AD + 128) * sizeof(float) <= (size_t)NS * SB,
+                "the 4-warp merge area (O, max, sum) aliases the stage ring");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
   int qrow = b;  // row of q and of the output
   if (p.cu_rows) {
     qrow = p.cu_rows[b];
@@ -635,11 +643,20 @@ __global__ void __launch_bounds__(DEC_THREADS, FP8 ? 3 : 2)
     }
   }
   // positions and the page table are caller inputs, complete before the step
-  const int n_keys = decode_keys(p.positions[b], cap_keys);
+  const int n_keys = decode_keys(p.positions[b], p.key_limit, p.status,
+                                 split == 0 && threadIdx.x == 0);
   const int kbeg = split * p.keys_per_split;
   const int kend = min(n_keys, kbeg + p.keys_per_split);
   if (kbeg >= kend) {  // this split has no keys (the merge skips it)
     grid_dep_wait();
+    if (p.splits == 1 && threadIdx.x < AD) {
+      // a sequence without keys: zero output rows, as the split merge writes
+      for (int r = 0; r < p.G; ++r) {
+        const size_t oh = (size_t)qrow * p.n_q + (size_t)g * p.G + r;
+        p.out[oh * AD + threadIdx.x] = __float2bfloat16_rn(0.f);
+        if (p.out_lo) p.out[oh * AD + threadIdx.x + p.out_lo] = __float2bfloat16_rn(0.f);
+      }
+    }
     return;
   }
   const int n_sub = (kend - kbeg + SUBK - 1) / SUBK;
@@ -779,7 +796,7 @@ __global__ void __launch_bounds__(DEC_THREADS, FP8 ? 3 : 2)
 // output by 2^(m_s - max m) and normalise.
 __global__ void attn_combine_kernel(const float* __restrict__ part,
                                     const int32_t* __restrict__ positions, int n_q, int splits,
-                                    int keys_per_split, int cap_keys, int d, void* out,
+                                    int keys_per_split, int key_limit, int d, void* out,
                                     size_t out_lo, const int32_t* cu_rows, float v_scale) {
   grid_dep_wait();
   grid_dep_launch();
@@ -790,7 +807,7 @@ __global__ void attn_combine_kernel(const float* __restrict__ part,
     if (cu_rows[b + 1] - cu_rows[b] != 1) return;
     oh = (size_t)cu_rows[b] * n_q + (bh - (size_t)b * n_q);
   }
-  const int n_keys = decode_keys(positions[b], cap_keys);
+  const int n_keys = decode_keys(positions[b], key_limit, nullptr, false);
   const int used = min(splits, (n_keys + keys_per_split - 1) / keys_per_split);
   const float* pp = part + (size_t)bh * splits * (d + 2);
   float M = -INFINITY;
@@ -1141,7 +1158,7 @@ __global__ void attn_decode_f32_kernel(const float* __restrict__ q, const int32_
   const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / (n_q / n_kv);
   const int cap_keys = page_size ? max_pages * page_size : capacity;
-  const int n = decode_keys(positions[b], cap_keys);
+  const int n = decode_keys(positions[b], cap_keys, nullptr, false);
   float* qs = sh;
   float* sc = sh + d;
   float* red = sc + cap_keys;
@@ -1311,6 +1328,8 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
   p.cu_rows = a.cu_rows;
   p.scale_log2 = kLog2e / sqrtf((float)AD) * (a.kv_fp8 ? a.k_scale : 1.f);
   p.v_scale = a.kv_fp8 ? a.v_scale : 1.f;
+  const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
+  p.key_limit = (int)std::min<long long>(cap_keys, (long long)splits * kps);
   const bool keymajor = p.G <= kKeyMajorMaxG;
   if (a.kv_fp8 && !keymajor) return cudaErrorInvalidValue;
   const dim3 grid(splits, a.n_kv, a.B), block(DEC_THREADS);
@@ -1322,9 +1341,8 @@ cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t 
                  : launch_k(attn_decode_kernel<false, false>, grid, block, DEC_SMEM, st, 0,
                             *a.map_k, *a.map_v, *a.map_k16, *a.map_v16, p);
   if (e != cudaSuccess || splits == 1) return e;
-  const int cap_keys = a.page_size ? a.max_pages * a.page_size : a.capacity;
   return launch_k(attn_combine_kernel, dim3(a.B * a.n_q), dim3(AD), 0, st, 0,
-                  (const float*)a.partial, a.positions, a.n_q, splits, kps, cap_keys, AD, a.out,
+                  (const float*)a.partial, a.positions, a.n_q, splits, kps, p.key_limit, AD, a.out,
                   a.out_lo, a.cu_rows, p.v_scale);
 }
 

@@ -117,7 +117,9 @@ extern "C" int llama_attention_decode_noalloc(const llama_config* cfg, const voi
   const int rc = setup_device(dev, &scratch);
   if (rc != LLAMA_OK) return rc;
 
-  const int max_keys = cap_keys < cfg->max_seq ? cap_keys : cfg->max_seq;
+  // The split plan covers every slot of the cache (not only max_seq of them):
+  // there is no status word here to report a position the plan would miss.
+  const int max_keys = cap_keys;
   const size_t need = llgb::attn_decode_partial_bytes(B, cfg->n_q_heads, (int)d,
                                                       max_keys < 1 ? 1 : max_keys, sms, (int)nkv);
   if (need > kNoAllocScratchBytes) return LLAMA_ERR_OUT_OF_RANGE;

@@ -1,13 +1,14 @@
 """Full Llama2-7B architecture (random-init bf16 weights): prefill 512 random
 ids per sequence at batch 8, then 256 greedy decode steps.
 
-The CPU oracle follows sequence 0, teacher-forced with the GPU's own choices
-(greedy paths of bf16 and fp64 arithmetic may part ways once two logits are
-within rounding of each other): one fp64 pass over the prompt plus the first
-four chosen ids gives the prefill's last-row logits and the logits of decode
-steps 1-4 (decoding a token equals the prefill row at its position). The far
-end (step 256) is checked against a fresh GPU prefill of the 768-token
-sequence, a property that holds at any size.
+The CPU oracle follows two sequences through all 32 layers, teacher-forced
+with the GPU's own choices (greedy paths of bf16 and fp64 arithmetic may part
+ways once two logits are within rounding of each other): one fp64 prefill of
+the prompt plus the first 256 chosen ids gives the prefill's last-row logits
+and the logits of every decode step (decoding a token equals the prefill row
+at its position, "Llama2架构与推理全解析" §2.4); steps 0-4, 64, 128 and 256
+are compared. Step 256 is also compared with a fresh GPU prefill of the
+768-token sequence, a property that holds at any size.
 """
 import numpy as np
 import pytest
@@ -50,20 +51,23 @@ def test_full_7b_prefill_and_greedy_decode():
     model.sync()
     assert_close(lg[steps, 0], f64(lg1)[0], BF16_TOL, "decode step 256 vs prefill of 768 tokens")
 
-    # oracle: sequence 0 through all 32 layers, teacher-forced
-    n_chk = 4
-    seq = np.concatenate([prompt[0].numpy(), gi[:n_chk, 0]])
-    Tn = len(seq)
-    h = O.embed(O.as64(w["embed"]), seq)[None]
-    K = np.zeros((1, shape.n_kv_heads, Tn, shape.head_dim))
+    # oracle: sequences 0 and 5 through all 32 layers, teacher-forced
+    chk = [0, 1, 2, 3, 4, 64, 128, 256]
+    seqs = [0, 5]
+    seq = np.stack([np.concatenate([prompt[b].numpy(), gi[:steps, b]]) for b in seqs])
+    Tn = seq.shape[1]
+    h = O.embed(O.as64(w["embed"]), seq)
+    K = np.zeros((len(seqs), shape.n_kv_heads, Tn, shape.head_dim))
     Vc = np.zeros_like(K)
     for lw in w["layers"]:
         h = O.layer_prefill(h, {k: O.as64(v) for k, v in lw.items()}, shape, K, Vc)
-    ref = O.lm_head(h[0, T - 1:], O.as64(w["final_norm"]), O.as64(w["lm_head"]), shape.rms_eps)
-    got = f64(lg[: n_chk + 1, 0])
-    assert_close(got, ref, BF16_TOL, "sequence 0 logits (prefill + 4 decode steps)")
+    rows = [T - 1 + s for s in chk]
+    ref = O.lm_head(h[:, rows], O.as64(w["final_norm"]), O.as64(w["lm_head"]), shape.rms_eps)
+    got = np.stack([f64(lg[chk, b]) for b in seqs])
+    assert_close(got, ref, BF16_TOL, "sequences 0 and 5: prefill and decode steps %s" % chk)
     # a GPU choice may differ from the oracle's only where the oracle's top two
     # logits are closer than the tolerance
-    top2 = np.sort(ref, -1)[:, -2:]
-    clear = top2[:, 1] - top2[:, 0] > BF16_TOL[0] + BF16_TOL[1] * np.abs(top2[:, 1])
-    assert np.all(gi[: n_chk + 1, 0][clear] == O.greedy(ref)[clear])
+    top2 = np.sort(ref, -1)[..., -2:]
+    clear = top2[..., 1] - top2[..., 0] > BF16_TOL[0] + BF16_TOL[1] * np.abs(top2[..., 1])
+    chosen = np.stack([gi[chk, b] for b in seqs])
+    assert np.all(chosen[clear] == O.greedy(ref)[clear])

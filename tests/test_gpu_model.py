@@ -308,7 +308,8 @@ def test_graph_replay_matches_direct_steps_and_runs_the_greedy_loop():
     need_gpu()
     shape = _small_bf16()
     B, T, cap, steps = 3, 12, 48, 6
-    w = to_dev(synth.model_weights(shape, 13))
+    w_cpu = synth.model_weights(shape, 13)
+    w = to_dev(w_cpu)
     stream = torch.cuda.Stream()
     m = binding.Model(shape, w, max_batch=B, max_tokens=B * T, max_seq=cap, stream=stream)
     toks = synth.token_ids(B, T, shape.vocab, 13).cuda()
@@ -342,3 +343,15 @@ def test_graph_replay_matches_direct_steps_and_runs_the_greedy_loop():
     for a, b in zip(direct_lg, graph_lg):
         np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
     assert int(pos_g[0]) == T + steps
+    # the replayed loop against the oracle, teacher-forced with the GPU's ids:
+    # one fp64 prefill of the prompt and the chosen ids gives every step's row
+    # (decoding a token equals the prefill row at its position, §2.4)
+    gi = torch.stack(graph_ids, 1).cpu().numpy()
+    seq = np.concatenate([toks.numpy(), gi[:, :steps]], axis=1)
+    ref = O.Model(shape, w_cpu, B, cap).prefill(seq)[:, T - 1:]
+    got = torch.stack(graph_lg, 1)
+    assert_close(got, ref, BF16_TOL, "graph replay logits vs oracle")
+    np.testing.assert_array_equal(gi, O.greedy(f64(got)))
+    top2 = np.sort(ref, -1)[..., -2:]
+    clear = top2[..., 1] - top2[..., 0] > BF16_TOL[0] + BF16_TOL[1] * np.abs(top2[..., 1])
+    assert np.all(gi[clear] == O.greedy(ref)[clear])

@@ -265,6 +265,28 @@ def test_attention_decode_many_splits():
     _decode_case(64, 8, [4096, 3000], False, 53)
 
 
+def test_attention_decode_positions_outside_the_planned_keys_are_flagged():
+    # max_seq 256 against a 1024-slot cache: the split plan covers 256 keys, so
+    # position 600 is flagged; a negative position gives zero rows and a flag;
+    # an in-range sequence of the same launch is unaffected
+    shape = L7.with_(n_q_heads=8, n_kv_heads=8)
+    m, _ = ctx_for(shape, max_batch=3, max_tokens=0, max_seq=256)
+    B, nq, d, cap = 3, 8, 128, 1024
+    positions = [100, -1, 600]
+    pos = torch.tensor(positions, dtype=torch.int32)
+    q = _randn((B, nq, d), 1.0, torch.bfloat16, 55)
+    k = synth.cache_values((1, B, 8, cap, d), 55, torch.bfloat16, stream=0)
+    v = synth.cache_values((1, B, 8, cap, d), 55, torch.bfloat16, stream=1)
+    kv = binding.KVCache(shape, batch=B, capacity=cap, k=k.cuda(), v=v.cuda())
+    out = torch.full((B, nq * d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    m.op_attention_decode(q.cuda(), pos.cuda(), 0, kv, out)
+    rc, flags = m.sync_status()
+    assert rc == 5 and flags & binding.FLAG_POS_RANGE
+    ref = O.gqa_attention(f64(q)[0], f64(k)[0, 0], f64(v)[0, 0], 101)
+    assert_close(out[0].view(nq, d), ref, BF16_TOL, "in-range sequence beside flagged ones")
+    assert torch.all(out[1] == 0)
+
+
 def test_attention_decode_f32():
     shape = synth.TINY
     m, _ = ctx_for(shape, max_batch=3, max_tokens=16, max_seq=64, n_layers=2)

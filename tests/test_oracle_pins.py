@@ -582,3 +582,56 @@ def test_row_scales_factor_out_of_the_projection():
     codes, s = O.quantize_rows_e4m3(w)
     np.testing.assert_allclose(O.linear(u, O.dequantize_rows(codes, s)), (u @ codes.T) * s[None, :],
                                rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- generation loop (§3.4)
+
+def test_generate_greedy_equals_prefill_of_the_extended_prompt():
+    # The generation loop feeds each greedy choice back at the next position
+    # ("Llama2架构与推理全解析" §3.4) and the cache only saves recompute (§2.4):
+    # step s's logits are the last row of a fresh prefill of the prompt
+    # followed by the first s chosen ids, and each id is its row's argmax.
+    shape = synth.TINY.with_(n_layers=1)
+    w = synth.model_weights(shape, 1011)
+    B, T, n = 2, 9, 5
+    prompt = synth.token_ids(B, T, shape.vocab, 1011).numpy()
+    ids, lg = O.generate_greedy(O.Model(shape, w, B, T + n + 1), prompt, n)
+    assert ids.shape == (B, n + 1) and lg.shape == (B, n + 1, shape.vocab)
+    for s in range(n + 1):
+        seq = np.concatenate([prompt, ids[:, :s]], axis=1)
+        ref = O.Model(shape, w, B, T + n + 1).prefill(seq)[:, -1]
+        np.testing.assert_allclose(lg[:, s], ref, rtol=1e-10, atol=1e-12)
+        top2 = np.sort(ref, -1)[:, -2:]
+        assert np.all(top2[:, 1] - top2[:, 0] > 1e-9)  # the choice is unambiguous
+        np.testing.assert_array_equal(ids[:, s], np.argmax(ref, -1))
+
+
+def _generate_position_off_by_one(model, prompt, n_steps):
+    prompt = np.asarray(prompt)
+    B, T = prompt.shape
+    lg = model.prefill(prompt)[:, -1]
+    ids, logits = [O.greedy(lg)], [lg]
+    for s in range(n_steps):
+        lg = model.decode(ids[-1], np.full(B, T + s + 1))
+        ids.append(O.greedy(lg))
+        logits.append(lg)
+    return np.stack(ids, 1), np.stack(logits, 1)
+
+
+def _generate_feeds_first_choice(model, prompt, n_steps):
+    prompt = np.asarray(prompt)
+    B, T = prompt.shape
+    lg = model.prefill(prompt)[:, -1]
+    ids, logits = [O.greedy(lg)], [lg]
+    for s in range(n_steps):
+        lg = model.decode(ids[0], np.full(B, T + s))
+        ids.append(O.greedy(lg))
+        logits.append(lg)
+    return np.stack(ids, 1), np.stack(logits, 1)
+
+
+@pytest.mark.parametrize("mutant", [_generate_position_off_by_one, _generate_feeds_first_choice])
+def test_generate_greedy_pin_catches_planted_mistakes(monkeypatch, mutant):
+    monkeypatch.setattr(O, "generate_greedy", mutant)
+    with pytest.raises(AssertionError):
+        test_generate_greedy_equals_prefill_of_the_extended_prompt()
