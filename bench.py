@@ -67,7 +67,9 @@ B_WORKLOAD = "model"
 
 
 class Clocks:
-    """nvidia-smi sampler for the timed region."""
+    """nvidia-smi sampler for the timed region: started before it (and waited
+    for until its first sample arrives), sampling every 20 ms; the summary
+    keeps the samples taken between mark_start() and mark_end()."""
 
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -76,29 +78,50 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.p = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def _read(self):
+        for line in self.p.stdout:
+            self.lines.append((time.perf_counter(), line))
 
     def __enter__(self):
+        import threading
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+            t = time.perf_counter()
+            while not self.lines and time.perf_counter() - t < 5:
+                time.sleep(0.01)
         except Exception:
             self.p = None
+        self.mark_start()
         return self
 
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
     def __exit__(self, *a):
-        self.out = ""
+        if self.t1 is None:
+            self.mark_end()
         if self.p:
+            time.sleep(0.05)
             self.p.terminate()
             try:
-                self.out = self.p.communicate(timeout=5)[0]
+                self.p.wait(timeout=5)
             except Exception:
                 self.p.kill()
 
     def summary(self):
         sm, mx, reasons = [], 0.0, set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in (self.out or "").splitlines():
+        window = [l for t, l in self.lines if self.t0 <= t <= self.t1 + 0.025]
+        for line in window:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 7:
                 continue
@@ -114,7 +137,7 @@ class Clocks:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         sm.sort()
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "interval_ms": 20}
 
 
 def _dist():
@@ -181,7 +204,180 @@ def build_model(workload, device, kv_e4m3=False, w_e4m3=False):
             t.view(-1, CAP, shape.head_dim)[:, CTX:].zero_()
     model = binding.Model(shape, w, max_batch=B, max_tokens=B, max_seq=CAP,
                           has_embed_head=(workload == "model"))
-    return shape, model, kv
+    return shape, model, kv, w
+
+
+def _time_ms(fn, stream, steps, warmup=3):
+    """Average device time of fn() over `steps` calls, CUDA events on `stream`
+    after `warmup` untimed calls."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def extra_workloads(dev, stream, w7, hbm, tflops):
+    """The other workloads of the scope table, each timed after the headline
+    decode step (not part of its timed region): the 8 x 512 prefill of the full
+    7B model, one 70B-shaped layer (decode at batch 32 over 4096 positions,
+    and a 4096-token prefill), and ragged paged decode on 7B layer shapes (MHA
+    and GQA; the attention alone per context-length bin too)."""
+    import torch
+    from llama2_decoder_forward_gb300 import binding, synth
+
+    out = {}
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+
+    def rn(*s, std=0.02, mean=0.0):
+        t = torch.randn(*s, generator=g, device=dev, dtype=torch.float32)
+        return t.mul_(std).add_(mean).to(torch.bfloat16)
+
+    def layer(shape, std):
+        H, I = shape.hidden, shape.intermediate
+        return {"attn_norm": rn(H, std=0.1, mean=1.0), "wqkv": rn(shape.qkv_rows, H, std=std),
+                "wo": rn(H, shape.n_q_heads * shape.head_dim, std=std),
+                "ffn_norm": rn(H, std=0.1, mean=1.0), "w_gate": rn(I, H, std=std),
+                "w_up": rn(I, H, std=std), "w_down": rn(H, I, std=std)}
+
+    def layer_params(shape):
+        H, I = shape.hidden, shape.intermediate
+        return shape.qkv_rows * H + H * shape.n_q_heads * shape.head_dim + 3 * H * I
+
+    def prof(model, fn, kinds, steps):
+        model.profile(kinds)
+        for _ in range(steps):
+            fn()
+        r = {k: model.profile_read(k) for k in kinds}
+        model.profile([])
+        model.sync()
+        return {k: (ms / steps, n / steps) for k, (ms, n) in r.items()}
+
+    # ---- full 7B prefill, 8 sequences x 512 tokens (the same weights)
+    shape = synth.LLAMA2_7B
+    Bp, Tp = 8, 512
+    m = binding.Model(shape, w7, max_batch=Bp, max_tokens=Bp * Tp, max_seq=768, stream=stream)
+    kvp = binding.KVCache(shape, batch=Bp, capacity=768)
+    toks = torch.randint(0, shape.vocab, (Bp, Tp), generator=g, device=dev, dtype=torch.int32)
+    lg = torch.empty(Bp, shape.vocab, device=dev)
+    ids = torch.empty(Bp, dtype=torch.int32, device=dev)
+    fn = lambda: m.prefill(toks, kvp, lg, ids)
+    ms = _time_ms(fn, stream, 5)
+    k = prof(m, fn, ["gemm", "attn_prefill"], 3)
+    rows = Bp * Tp
+    gflop = 2.0 * rows * layer_params(shape) * shape.n_layers + 2.0 * Bp * shape.vocab * shape.hidden
+    aflop = 4.0 * shape.n_q_heads * shape.head_dim * (Tp * (Tp + 1) / 2) * Bp * shape.n_layers
+    g_tf = gflop / (k["gemm"][0] * 1e-3) / 1e12
+    a_tf = aflop / (k["attn_prefill"][0] * 1e-3) / 1e12
+    out["prefill_7b"] = {
+        "workload": "llama2-7b prefill, 8 sequences x 512 random ids, 32 layers + LM head on last rows",
+        "tokens_per_s": rows / (ms * 1e-3), "ms": ms,
+        "gemm": {"tflops": g_tf, "frac": g_tf / tflops, "ms": k["gemm"][0], "launches": k["gemm"][1]},
+        "attention": {"tflops": a_tf, "frac": a_tf / tflops, "ms": k["attn_prefill"][0]}}
+    del m, kvp
+    torch.cuda.empty_cache()
+
+    # ---- one 70B-shaped layer: decode at batch 32 over 4096 positions, and a 4096-token prefill
+    s70 = synth.LLAMA2_70B.with_(n_layers=1)
+    w70 = {"layers": [layer(s70, 0.01)]}
+    S70, cap70 = 4096, 4112
+    m = binding.Model(s70, w70, max_batch=B, max_tokens=S70, max_seq=cap70, has_embed_head=False,
+                      stream=stream)
+    kv = binding.KVCache(s70, batch=B, capacity=cap70)
+    kv.k.normal_(generator=g)
+    kv.v.normal_(generator=g)
+    h0 = torch.randn(B, s70.hidden, generator=g, device=dev)
+    h = h0.clone()
+    pos = torch.full((B,), S70, dtype=torch.int32, device=dev)
+    fn = lambda: m.decode_hidden(h, pos, kv)
+    ms = _time_ms(fn, stream, 20)
+    k = prof(m, fn, ["attn_decode", "gemm"], 5)
+    kvb = B * s70.n_kv_heads * (S70 + 1) * s70.head_dim * 2 * 2
+    wb = layer_params(s70) * 2
+    out["layer_70b_decode"] = {
+        "workload": "one llama2-70b layer (64 q / 8 kv heads), decode at batch 32 over 4096 cached positions",
+        "ms": ms, "gbs": (wb + kvb) / (ms * 1e-3) / 1e9, "frac": (wb + kvb) / (ms * 1e-3) / 1e9 / hbm,
+        "algorithmic_bytes": wb + kvb,
+        "attention": {"gbs": kvb / (k["attn_decode"][0] * 1e-3) / 1e9,
+                      "frac": kvb / (k["attn_decode"][0] * 1e-3) / 1e9 / hbm},
+        "gemm": {"gbs": wb / (k["gemm"][0] * 1e-3) / 1e9,
+                 "frac": wb / (k["gemm"][0] * 1e-3) / 1e9 / hbm}}
+    kv1 = binding.KVCache(s70, batch=1, capacity=cap70)
+    x = torch.randn(S70, s70.hidden, generator=g, device=dev)
+    fn = lambda: m.prefill_hidden(x, 1, S70, kv1)
+    ms = _time_ms(fn, stream, 3)
+    k = prof(m, fn, ["gemm", "attn_prefill"], 2)
+    gflop = 2.0 * S70 * layer_params(s70)
+    aflop = 4.0 * s70.n_q_heads * s70.head_dim * (S70 * (S70 + 1) / 2)
+    g_tf = gflop / (k["gemm"][0] * 1e-3) / 1e12
+    a_tf = aflop / (k["attn_prefill"][0] * 1e-3) / 1e12
+    out["layer_70b_prefill_4096"] = {
+        "workload": "one llama2-70b layer, causal prefill of 4096 tokens at batch 1",
+        "tokens_per_s": S70 / (ms * 1e-3), "ms": ms,
+        "gemm": {"tflops": g_tf, "frac": g_tf / tflops, "ms": k["gemm"][0]},
+        "attention": {"tflops": a_tf, "frac": a_tf / tflops, "ms": k["attn_prefill"][0]}}
+    del m, kv, kv1, w70, x
+    torch.cuda.empty_cache()
+
+    # ---- ragged paged decode on 7B layer shapes, MHA and GQA (32 q / 8 kv)
+    lens = synth.ragged_lengths(64, 128, 4096, 1005)
+    n_pages = [(int(L) + 1 + 15) // 16 for L in lens]
+    table, total = synth.page_table(n_pages, max(n_pages), 1005)
+    table = table.to(dev)
+    posr = lens.to(dev)
+    base = layer(synth.LLAMA2_7B.with_(n_layers=1), 0.02)
+    rag = {}
+    for name, nkv in (("mha", 32), ("gqa", 8)):
+        s5 = synth.LLAMA2_7B.with_(n_layers=1)
+        lw = base if nkv == 32 else synth.gqa_variant(base, s5, nkv)
+        s5 = s5.with_(n_kv_heads=nkv)
+        m = binding.Model(s5, {"layers": [lw]}, max_batch=64, max_tokens=0, max_seq=max(n_pages) * 16,
+                          has_embed_head=False, stream=stream)
+        kvr = binding.KVCache(s5, n_pages=total, page_size=16, page_table=table)
+        kvr.k.normal_(generator=g)
+        kvr.v.normal_(generator=g)
+        h0 = torch.randn(64, s5.hidden, generator=g, device=dev)
+        h = h0.clone()
+        fn = lambda: m.decode_hidden(h, posr, kvr)
+        ms = _time_ms(fn, stream, 20)
+        kvb = int(sum(int(L) + 1 for L in lens)) * nkv * s5.head_dim * 2 * 2
+        wb = layer_params(s5) * 2
+        q = torch.randn(64, s5.n_q_heads, s5.head_dim, generator=g, device=dev).to(torch.bfloat16)
+        o = torch.empty(64, s5.n_q_heads * s5.head_dim, device=dev, dtype=torch.bfloat16)
+        am = _time_ms(lambda: m.op_attention_decode(q, posr, 0, kvr, o), stream, 20)
+        bins = []
+        for lo, hi in ((128, 1024), (1025, 2048), (2049, 3072), (3073, 4096)):
+            idx = [i for i, L in enumerate(lens.tolist()) if lo <= L <= hi]
+            if not idx:
+                continue
+            it = torch.tensor(idx, device=dev)
+            kb = binding.KVCache(s5, n_pages=total, page_size=16,
+                                 page_table=table[it].contiguous(), k=kvr.k, v=kvr.v)
+            qb, pb = q[it].contiguous(), posr[it].contiguous()
+            ob = o[: len(idx)]
+            bm = _time_ms(lambda: m.op_attention_decode(qb, pb, 0, kb, ob), stream, 20)
+            bb = int(sum(int(lens[i]) + 1 for i in idx)) * nkv * s5.head_dim * 4
+            bins.append({"lengths": [lo, hi], "sequences": len(idx), "ms": bm,
+                         "gbs": bb / (bm * 1e-3) / 1e9, "frac": bb / (bm * 1e-3) / 1e9 / hbm})
+        rag[name] = {"ms": ms, "gbs": (wb + kvb) / (ms * 1e-3) / 1e9,
+                     "frac": (wb + kvb) / (ms * 1e-3) / 1e9 / hbm,
+                     "attention": {"ms": am, "gbs": kvb / (am * 1e-3) / 1e9,
+                                   "frac": kvb / (am * 1e-3) / 1e9 / hbm},
+                     "attention_by_length": bins}
+        del m, kvr
+        torch.cuda.empty_cache()
+    out["ragged_paged_7b_layer"] = {
+        "workload": "one llama2-7b layer, 64 sequences with cached lengths uniform in [128, 4096], "
+                    "pages of 16 tokens in a random permutation, decode one token each",
+        **rag}
+    return out
 
 
 def run_gpu(args):
@@ -196,8 +392,8 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     __graft_entry__.build()
-    shape, model, kv = build_model(args.workload, dev, kv_e4m3=args.kv == "e4m3",
-                                   w_e4m3=args.weights == "e4m3")
+    shape, model, kv, w7 = build_model(args.workload, dev, kv_e4m3=args.kv == "e4m3",
+                                       w_e4m3=args.weights == "e4m3")
     torch.cuda.synchronize()  # inputs are drawn on the default stream; the model runs on its own
     g = torch.Generator(device=dev)
     g.manual_seed(7)
@@ -241,11 +437,14 @@ def run_gpu(args):
     barrier()
     n0 = model.launch_count()
     with Clocks(local) as clk:
+        barrier()
+        clk.mark_start()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         barrier()
+        clk.mark_end()
     launches = model.launch_count() - n0
     ms = e0.elapsed_time(e1) / args.steps
     model.sync()
@@ -351,6 +550,9 @@ def run_gpu(args):
         "clocks": clk.summary(),
         "e2e": e2e,
     }
+    if (args.workload == "model" and args.kv == "bf16" and args.weights == "bf16"
+            and not args.no_extra):
+        line["workloads"] = extra_workloads(dev, stream, w7, hbm, tflops)
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload)
     print(json.dumps(line), flush=True)
@@ -659,6 +861,8 @@ def main():
     ap.add_argument("--layers", type=int, default=32,
                     help="prefill workload: decoder layers (fewer for a small profiling case)")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels directly")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads timed after the headline step")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
                     help="KV-cache storage (e4m3: the FP8 cache; not the headline configuration)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "e4m3"],
