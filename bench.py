@@ -211,6 +211,7 @@ def _time_ms(fn, stream, steps, warmup=3):
     """Average device time of fn() over `steps` calls, CUDA events on `stream`
     after `warmup` untimed calls."""
     import torch
+    torch.cuda.synchronize()  # inputs drawn on the default stream are complete
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()

@@ -212,6 +212,9 @@ struct AttnPrefillArgs {
 };
 cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_t st);
 cudaError_t attn_prepare();
+// bf16 prefill attention on tcgen05 (k_prefill_tc.cu)
+cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t st);
+cudaError_t attn_prefill_tc_prepare();
 
 // ---- token sampling (k_sample.cu)
 struct SampleCall {

@@ -1278,8 +1278,10 @@ cudaError_t attn_prepare() {
   e = cudaFuncSetAttribute(attn_decode_kernel<true, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEC_SMEM_F8);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)PRE_SMEM);
+  e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)PRE_SMEM);
+  if (e != cudaSuccess) return e;
+  return attn_prefill_tc_prepare();
 }
 
 cudaError_t launch_attn_decode(int dtype, const AttnDecodeArgs& a, cudaStream_t st) {
@@ -1365,6 +1367,7 @@ cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_
                     a.n_q, a.n_kv, a.head_dim);
   }
   if (a.head_dim != AD) return cudaErrorInvalidValue;
+  return launch_attn_prefill_tc(a, st);
   PreParams p;
   p.q_lo_rows = a.q_lo_rows;
   p.out = (bf16*)a.out;

@@ -1,0 +1,478 @@
+// Causal prefill attention on the 5th-generation tensor cores (tcgen05):
+// scores q.k / sqrt(d), the causal mask, a numerically stable softmax and the
+// weighted sum of V ("Llama2架构与推理全解析" §2.1 prefill, §2.3 attention; §1.5
+// GQA: query head h reads K/V head h / G), computed FlashAttention-style so
+// the T x T score matrix never leaves the SM.
+//
+// One CTA per (128 query rows, query head, sequence); 192 threads:
+//   warp 0     TMA producer: the Q tile (and its bf16 remainder rows), then
+//              K and V tiles of 64 keys into a 3-stage mbarrier ring;
+//   warp 1     tensor-memory owner and MMA issuer (one thread):
+//              S_j = Q K_j^T into one of two S buffers in tensor memory,
+//              O += P_j V_j into the O accumulator in tensor memory;
+//   warps 2-5  softmax: each thread owns one query row (its tensor-memory
+//              lane), reads S_j with tcgen05.ld, masks, keeps the running max
+//              and sum, writes P_j (bf16, as a hi/lo pair when Q is one) to
+//              shared memory in the MMA operand layout, and at the end reads
+//              O, divides by the sum and stores the output rows.
+// The MMA of S_{j+1} runs while the softmax works on S_j. The running max is
+// applied lazily: O and the sum are rescaled (in tensor memory) only when a
+// row's max grows by more than 2^8, otherwise P keeps the older max, which
+// leaves the normalised result unchanged. Key tiles past the diagonal are
+// skipped; the diagonal tile and the last partial tile are masked per key.
+//
+// Operand layouts (all 128-byte swizzled, as TMA writes them):
+//   Q  A operand, K-major: [128 rows][64 dims] per dim half;
+//   K  B operand, K-major: [64 keys][64 dims] per dim half;
+//   P  A operand, K-major: [128 rows][64 keys];
+//   V  B operand, MN-major: [64 keys][64 dims] per dim half (the dims are the
+//      MMA's N, contiguous in memory); 8-key groups 1024 bytes apart, the two
+//      dim halves KV_HALF bytes apart.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace llgb {
+
+namespace {
+
+constexpr int TQ = 128;          // query rows per CTA: MMA M, one tensor-memory lane each
+constexpr int TK = 64;           // keys per tile
+constexpr int TSUB = 16;         // keys per box of a 16-row (paged) cache view
+constexpr int TSTAGES = 3;
+constexpr int TC_THREADS = 192;
+constexpr uint32_t KV_HALF = TK * 128;     // 64 keys x 64 dims bf16: 8 KB
+constexpr uint32_t KV_TILE = 2 * KV_HALF;  // 64 keys x 128 dims: 16 KB
+constexpr uint32_t STAGE = 2 * KV_TILE;    // K tile then V tile: 32 KB
+constexpr uint32_t Q_HALF = TQ * 128;      // 128 rows x 64 dims: 16 KB
+constexpr uint32_t Q_TILE = 2 * Q_HALF;    // 32 KB; the remainder tile follows
+constexpr uint32_t P_TILE = TQ * 128;      // 128 rows x 64 keys: 16 KB; the remainder follows
+constexpr uint32_t OFF_P = 2 * Q_TILE;
+constexpr uint32_t OFF_ST = OFF_P + 2 * P_TILE;
+constexpr uint32_t OFF_BAR = OFF_ST + TSTAGES * STAGE;
+constexpr size_t TC_SMEM = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+constexpr uint32_t TMEM_COLS = 256;  // S buffers at columns 0 and 64, O at 128
+constexpr uint32_t O_COL = 128;
+constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more than 2^8
+
+struct TcPreParams {
+  bf16* out;
+  size_t out_lo;
+  uint32_t* status;
+  int q_lo_rows;  // > 0: Q rows have bf16 remainders at row q_lo_rows + r; P is a pair too
+  int T, n_q, n_kv, G, n_qtiles;
+  float scale_log2, v_scale;
+  const int32_t* cu_rows;
+  const int32_t* start_pos;
+  int n_rows;
+  int from_cache, box_rows, layer, page_size, capacity, batch_cap, n_pages, max_pages;
+  const int32_t* page_table;
+};
+
+// Shared-memory descriptor of an MN-major operand written by TMA with 128-byte
+// swizzling: 64 contiguous MN elements per 128-byte row, 8-row (K) groups 1024
+// bytes apart (stride byte offset), consecutive 64-element MN blocks `lbo`
+// bytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns per thread, registers -> tensor memory.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Cache row of the keys starting at k0 (a multiple of 16) of sequence b, K/V
+// head g; a page id outside the pool is flagged and mapped to rows TMA fills
+// with zeros.
+__device__ __forceinline__ int tc_kv_row(const TcPreParams& p, int b, int g, int k0) {
+  if (p.page_size == 0) return (b * p.n_kv + g) * p.capacity + k0;
+  const int pi = k0 / p.page_size;
+  const int page = pi < p.max_pages ? p.page_table[(size_t)b * p.max_pages + pi] : -1;
+  if (page < 0 || page >= p.n_pages) {
+    flag(p.status, LLAMA_FLAG_PAGE_RANGE);
+    return -4 * TSUB;
+  }
+  return (page * p.n_kv + g) * p.page_size + (k0 % p.page_size);
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
+                           const __grid_constant__ CUtensorMap mapK,
+                           const __grid_constant__ CUtensorMap mapV,
+                           const __grid_constant__ CUtensorMap mapK16,
+                           const __grid_constant__ CUtensorMap mapV16, TcPreParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* kvfull = qfull + 1;
+  uint64_t* kvempty = kvfull + TSTAGES;
+  uint64_t* sfull = kvempty + TSTAGES;  // [2] S_j is in tensor memory
+  uint64_t* sfree = sfull + 2;          // [2] the softmax has read S_j
+  uint64_t* pready = sfree + 2;         // P_j is in shared memory (O rescaled if needed)
+  uint64_t* odone = pready + 1;         // O += P_j V_j has completed
+  uint64_t* mfin = odone + 1;           // every MMA issued has completed (teardown)
+  // ctl[0]: tensor-memory base address, ctl[1]: abort
+  volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 1);
+  const bool pair = p.q_lo_rows > 0;
+
+  grid_dep_wait();  // q, k, v come from the RoPE/append kernel
+  grid_dep_launch();
+  const int qt = p.n_qtiles - 1 - (int)blockIdx.x;  // longest rows first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int g = h / p.G;
+  const int q0 = qt * TQ;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rowbase = p.cu_rows ? p.cu_rows[b] : b * p.T;
+  const int n_b = p.cu_rows ? p.cu_rows[b + 1] - rowbase : p.T;  // this sequence's rows
+  const int start = p.start_pos ? p.start_pos[b] : 0;             // position of its first row
+  if (q0 >= n_b) return;
+  if (p.cu_rows && p.from_cache && n_b == 1) return;  // single new rows: the decode kernel's
+  if (p.from_cache) {  // the sequence's keys must fit its cache slots
+    const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
+    if (start < 0 || start > cap_keys - n_b) {
+      if (threadIdx.x == 0) flag(p.status, LLAMA_FLAG_POS_RANGE);
+      return;
+    }
+  }
+  const int n_keys = start + n_b;  // keys 0 .. n_keys - 1 exist once the rows are appended
+  const int n_kt = (start + min(q0 + TQ, n_b) - 1) / TK + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qfull, 1);
+    for (int s = 0; s < TSTAGES; ++s) {
+      mbar_init(&kvfull[s], 1);
+      mbar_init(&kvempty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sfree[i], 4);
+    }
+    mbar_init(pready, 4);
+    mbar_init(odone, 1);
+    mbar_init(mfin, 1);
+    ctl[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(const_cast<uint32_t*>(ctl), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl[0];
+
+  if (warp == 0) {  // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      if (p.from_cache) {
+        tma_prefetch_desc(&mapK16);
+        tma_prefetch_desc(&mapV16);
+      }
+      mbar_arrive_expect_tx(qfull, pair ? 2 * Q_TILE : Q_TILE);
+      for (int t = 0; t < (pair ? 2 : 1); ++t) {
+        const int row0 = (t ? p.q_lo_rows : 0) + rowbase + q0;
+        for (int half = 0; half < 2; ++half)
+          for (int rb = 0; rb < 2; ++rb)
+            tma_load_3d(smem + t * Q_TILE + half * Q_HALF + rb * (Q_HALF / 2), &mapQ, qfull,
+                        64 * half, h, row0 + 64 * rb);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int kt = 0; kt < n_kt; ++kt) {
+        const int s = kt % TSTAGES;
+        const uint32_t ph = (kt / TSTAGES) & 1;
+        if (!mbar_wait(&kvempty[s], ph ^ 1, p.status)) {
+          ok = false;
+          ctl[1] = 1;
+          break;
+        }
+        uint8_t* ks = smem + OFF_ST + s * STAGE;
+        const int k0 = kt * TK, nvalid = min(TK, n_keys - k0);
+        if (!p.from_cache) {
+          mbar_arrive_expect_tx(&kvfull[s], STAGE);
+          tma_load_3d(ks, &mapK, &kvfull[s], 0, g, rowbase + k0);
+          tma_load_3d(ks + KV_HALF, &mapK, &kvfull[s], 64, g, rowbase + k0);
+          tma_load_3d(ks + KV_TILE, &mapV, &kvfull[s], 0, g, rowbase + k0);
+          tma_load_3d(ks + KV_TILE + KV_HALF, &mapV, &kvfull[s], 64, g, rowbase + k0);
+        } else if (p.box_rows == TK && nvalid == TK) {  // 64 contiguous keys: one box per half
+          const int row = tc_kv_row(p, b, g, k0);
+          mbar_arrive_expect_tx(&kvfull[s], STAGE);
+          tma_load_3d(ks, &mapK, &kvfull[s], 0, row, p.layer);
+          tma_load_3d(ks + KV_HALF, &mapK, &kvfull[s], 64, row, p.layer);
+          tma_load_3d(ks + KV_TILE, &mapV, &kvfull[s], 0, row, p.layer);
+          tma_load_3d(ks + KV_TILE + KV_HALF, &mapV, &kvfull[s], 64, row, p.layer);
+        } else {  // 16-key boxes, only those holding keys of this sequence
+          const int nsub = (nvalid + TSUB - 1) / TSUB;
+          mbar_arrive_expect_tx(&kvfull[s], nsub * 4 * (TSUB * 128));
+          for (int j = 0; j < nsub; ++j) {
+            const int row = tc_kv_row(p, b, g, k0 + j * TSUB);
+            uint8_t* kd = ks + j * TSUB * 128;
+            tma_load_3d(kd, &mapK16, &kvfull[s], 0, row, p.layer);
+            tma_load_3d(kd + KV_HALF, &mapK16, &kvfull[s], 64, row, p.layer);
+            tma_load_3d(kd + KV_TILE, &mapV16, &kvfull[s], 0, row, p.layer);
+            tma_load_3d(kd + KV_TILE + KV_HALF, &mapV16, &kvfull[s], 64, row, p.layer);
+          }
+        }
+        ++issued;
+      }
+      mbar_wait(qfull, 0, p.status);  // no copy may still be in flight when the CTA exits
+      if (!ok) {
+        for (int t = issued - 1; t >= 0 && t >= issued - TSTAGES; --t)
+          mbar_wait(&kvfull[t % TSTAGES], (t / TSTAGES) & 1, p.status);
+      }
+    }
+  } else if (warp == 1) {  // -------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(TQ, TK);
+      const uint32_t id_o = idesc_bf16_f32(TQ, 128) | (1u << 16);  // B (V) MN-major
+      const uint32_t qa = smem_u32(smem), pa = smem_u32(smem + OFF_P);
+      bool ok = mbar_wait(qfull, 0, p.status);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % TSTAGES;
+        if (ctl[1] || !mbar_wait(&kvfull[s], (j / TSTAGES) & 1, p.status)) return false;
+        if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(smem + OFF_ST + s * STAGE);
+        const uint32_t d = tmem + (uint32_t)(j & 1) * TK;
+        for (int t = 0; t < (pair ? 2 : 1); ++t)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // 16 dims per MMA
+            const uint32_t off = (uint32_t)(kk & 3) * 32;  // 32 bytes along K within a swizzle row
+            const uint64_t da = smem_desc_sw128(qa + t * Q_TILE + (kk >> 2) * Q_HALF + off);
+            const uint64_t db = smem_desc_sw128(kb + (kk >> 2) * KV_HALF + off);
+            tc_mma_f16(d, da, db, id_s, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+        tc_commit(&sfull[j & 1]);
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        if (ctl[1] || !mbar_wait(pready, j & 1, p.status)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + OFF_ST + (j % TSTAGES) * STAGE + KV_TILE);
+        for (int t = 0; t < (pair ? 2 : 1); ++t)
+#pragma unroll
+          for (int kk = 0; kk < TK / 16; ++kk) {  // 16 keys per MMA
+            const uint64_t da = smem_desc_sw128(pa + t * P_TILE + kk * 32);
+            const uint64_t db = smem_desc_sw128_mn(vb + kk * 2048, KV_HALF);
+            tc_mma_f16(tmem + O_COL, da, db, id_o, (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
+          }
+        tc_commit(odone);
+        tc_commit(&kvempty[j % TSTAGES]);
+        return true;
+      };
+      for (int j = 0; ok && j < n_kt; ++j) {
+        ok = issue_s(j);
+        if (ok && j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) ok = issue_pv(n_kt - 1);
+      if (!ok) ctl[1] = 1;
+      tc_commit(mfin);
+      mbar_wait(mfin, 0, p.status);  // every MMA retired before the tensor memory is freed
+    }
+  } else {  // --------------------------------------------------------- softmax warps
+    const int quad = warp & 3;  // tensor-memory lane quadrant this warp may access
+    const int r = quad * 32 + lane;
+    const int qrow = q0 + r;
+    const int qpos = start + qrow;
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+    uint8_t* pbase = smem + OFF_P;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      if (ctl[1] || !mbar_wait(&sfull[j & 1], (j >> 1) & 1, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[TK];
+      {
+        uint32_t u[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16(tl + (uint32_t)(j & 1) * TK + 16 * c, u[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sv[16 * c + i] = __uint_as_float(u[c][i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[j & 1]);
+      const int k0 = j * TK;
+      // a tile below the CTA's first row and inside the sequence needs no mask
+      const bool full = k0 + TK - 1 <= start + q0 && k0 + TK <= n_keys;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < TK; ++c) {
+        float v = sv[c] * p.scale_log2;
+        if (!full && (k0 + c > qpos || k0 + c >= n_keys)) v = -INFINITY;
+        sv[c] = v;
+        mt = fmaxf(mt, v);
+      }
+      // O += P_{j-1} V_{j-1} has completed: O may be rescaled, P overwritten
+      if (j >= 1) {
+        if (!mbar_wait(odone, (j - 1) & 1, p.status)) {
+          ok = false;
+          ctl[1] = 1;
+          break;
+        }
+        tc_fence_after();
+      }
+      const float m_new = fmaxf(m_used, mt);
+      const bool need = m_new > m_used + kRescaleLog2;  // also the first finite max
+      const float f = m_used == -INFINITY ? 0.f : exp2f(m_used - m_new);
+      if (__any_sync(0xffffffffu, need && j > 0)) {  // rescale this warp's O rows
+        const float fo = need ? f : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t u[16];
+          tmem_ld16(tl + O_COL + 16 * c, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * fo);
+          tmem_st16(tl + O_COL + 16 * c, u);
+        }
+        tmem_st_wait();
+      }
+      if (need) {
+        l *= f;
+        m_used = m_new;
+      }
+      float ls = 0.f;
+      const float mu = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+      for (int c = 0; c < TK; ++c) {
+        const float e = exp2f(sv[c] - mu);  // exp2(-inf) = 0 for masked keys
+        sv[c] = e;
+        ls += e;
+      }
+      l += ls;
+      const int nvalid = min(TK, n_keys - k0);
+      if (nvalid < TK) {
+        // V rows past the last key may hold anything (P is 0 there, but
+        // 0 * NaN is not): zero them before the MMA reads the tile
+        uint8_t* vt = smem + OFF_ST + (j % TSTAGES) * STAGE + KV_TILE;
+        const int nz = (TK - nvalid) * 16;
+        for (int i = threadIdx.x - 64; i < nz; i += 128) {
+          const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
+          *reinterpret_cast<uint4*>(vt + half * KV_HALF + row * 128 + chunk * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // P row r (and its remainder) in the 128-byte-swizzled K-major layout
+#pragma unroll
+      for (int c8 = 0; c8 < TK / 8; ++c8) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_pack(sv[8 * c8 + 2 * i], sv[8 * c8 + 2 * i + 1], hi[i], lo[i]);
+        const uint32_t a = smem_u32(pbase) + (uint32_t)r * 128u + ((uint32_t)(c8 ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(hi[0]), "r"(hi[1]),
+                     "r"(hi[2]), "r"(hi[3])
+                     : "memory");
+        if (pair)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + P_TILE), "r"(lo[0]),
+                       "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
+                       : "memory");
+      }
+      fence_proxy_async_smem();  // the MMA reads P (and the zeroed V rows) through the async proxy
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pready);
+    }
+    // ---- epilogue: O / l for this thread's row
+    if (ok && !ctl[1] && mbar_wait(odone, (n_kt - 1) & 1, p.status)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? p.v_scale / l : 0.f;
+      const bool row_ok = qrow < n_b && rowbase + qrow < p.n_rows;
+      bf16* dst = p.out + (size_t)(rowbase + qrow) * p.n_q * 128 + (size_t)h * 128;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t u[16];
+        tmem_ld16(tl + O_COL + 16 * c, u);
+        tmem_ld_wait();
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          split_pack(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv, hi[i], lo[i]);
+        if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
+          d4[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          d4[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+          if (p.out_lo) {
+            uint4* l4 = reinterpret_cast<uint4*>(dst + 16 * c + p.out_lo);
+            l4[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            l4[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+          }
+        }
+      }
+    } else {
+      ctl[1] = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t attn_prefill_tc_prepare() {
+  return cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)TC_SMEM);
+}
+
+cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t st) {
+  if (a.head_dim != 128) return cudaErrorInvalidValue;
+  if (a.from_cache && (!a.map_k16 || !a.map_v16)) return cudaErrorInvalidValue;
+  TcPreParams p;
+  p.out = (bf16*)a.out;
+  p.out_lo = a.out_lo;
+  p.status = a.status;
+  p.q_lo_rows = a.q_lo_rows;
+  p.T = a.T;
+  p.n_q = a.n_q;
+  p.n_kv = a.n_kv;
+  p.G = a.n_q / a.n_kv;
+  p.n_qtiles = (a.T + TQ - 1) / TQ;
+  p.scale_log2 = 1.4426950408889634f / sqrtf(128.f) * a.k_scale;
+  p.v_scale = a.v_scale;
+  p.cu_rows = a.cu_rows;
+  p.start_pos = a.start_pos;
+  p.n_rows = a.cu_rows ? a.n_rows : a.B * a.T;
+  p.from_cache = a.from_cache;
+  p.box_rows = a.box_rows == TK ? TK : TSUB;
+  p.layer = a.layer;
+  p.page_size = a.page_size;
+  p.capacity = a.capacity;
+  p.batch_cap = a.batch_cap;
+  p.n_pages = a.n_pages;
+  p.max_pages = a.max_pages;
+  p.page_table = a.page_table;
+  const CUtensorMap* k16 = a.from_cache ? a.map_k16 : a.map_k;
+  const CUtensorMap* v16 = a.from_cache ? a.map_v16 : a.map_v;
+  return launch_k(attn_prefill_tc_kernel, dim3(p.n_qtiles, a.n_q, a.B), dim3(TC_THREADS), TC_SMEM,
+                  st, 0, *a.map_q, *a.map_k, *a.map_v, *k16, *v16, p);
+}
+
+}  // namespace llgb

@@ -347,7 +347,7 @@ def test_graph_replay_matches_direct_steps_and_runs_the_greedy_loop():
     # one fp64 prefill of the prompt and the chosen ids gives every step's row
     # (decoding a token equals the prefill row at its position, §2.4)
     gi = torch.stack(graph_ids, 1).cpu().numpy()
-    seq = np.concatenate([toks.numpy(), gi[:, :steps]], axis=1)
+    seq = np.concatenate([toks.cpu().numpy(), gi[:, :steps]], axis=1)
     ref = O.Model(shape, w_cpu, B, cap).prefill(seq)[:, T - 1:]
     got = torch.stack(graph_lg, 1)
     assert_close(got, ref, BF16_TOL, "graph replay logits vs oracle")
