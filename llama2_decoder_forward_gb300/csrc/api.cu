@@ -29,6 +29,11 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // the KV cache holds single bf16 values. (The extra MMA work is free while
 // decode is bound by weight bytes; it doubles the prefill's tensor work.)
 inline int round16(int v) { return (v + 15) / 16 * 16; }
+// Remainder-row offset of the pair layout for `rows` activation rows: 0 when
+// the context carries single bf16 operands (or is fp32).
+inline int pair_rows(const llama_config& cf, int rows) {
+  return cf.dtype == LLAMA_BF16 && cf.act_dtype == LLAMA_ACT_PAIR ? round16(rows) : 0;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
@@ -79,6 +84,7 @@ int check_config(const llama_config* c) {
   if (c->dtype != LLAMA_F32 && c->dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
   if (c->weight_dtype != LLAMA_W_MODEL && c->weight_dtype != LLAMA_W_E4M3)
     return LLAMA_ERR_INVALID_ARG;
+  if (c->act_dtype != LLAMA_ACT_PAIR && c->act_dtype != LLAMA_ACT_BF16) return LLAMA_ERR_INVALID_ARG;
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return LLAMA_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads != 0) return LLAMA_ERR_INVALID_ARG;
   if (c->head_dim % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
@@ -615,7 +621,7 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   void* q = c->at<void>(c->L.q);
   void* o = c->at<void>(c->L.o);
   void* a = c->at<void>(c->L.a);
-  const int lo = cf.dtype == LLAMA_BF16 ? round16(rows) : 0;
+  const int lo = pair_rows(cf, rows);
   const int sp = lo ? 1 : 0;
   // bf16: the RMSNorms after the first ride on the residual GEMMs (the layers
   // run in order, so layer l > 0 finds its normalised input pair and the row
@@ -686,7 +692,7 @@ int run_head(llama_ctx* c, const float* x, int B, int stride, int offset, float*
              int32_t* next_ids, const int32_t* row_end = nullptr, int n_in = 0) {
   const llama_config& cf = c->cfg;
   void* ul = c->at<void>(c->L.u_last);
-  const int lo = cf.dtype == LLAMA_BF16 ? round16(B) : 0;
+  const int lo = pair_rows(cf, B);
   TRY(do_rmsnorm(c, x, B, stride, offset, c->final_norm, ul, lo, row_end, n_in));
   TRY(do_gemm(c, LLAMA_EPI_STORE_F32, ul, B, cf.hidden, c->lm_head, nullptr, cf.vocab, logits,
               cf.vocab, lo ? 1 : 0));

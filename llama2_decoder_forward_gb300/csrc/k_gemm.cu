@@ -568,7 +568,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
                 const float y = xn * gam;
                 const bf16 hi = __float2bfloat16_rn(y);
                 p.norm_out[idx] = hi;
-                p.norm_out[idx + p.norm_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
+                if (p.norm_lo)
+                  p.norm_out[idx + p.norm_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
                 ss[j] = xn * xn;
               }
             }
@@ -718,7 +719,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
                 const bf16 hi = __float2bfloat16_rn(y);
                 const size_t idx = (size_t)c * p.ldo + gm0 + e;
                 p.norm_out[idx] = hi;
-                p.norm_out[idx + p.norm_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
+                if (p.norm_lo)
+                  p.norm_out[idx + p.norm_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
                 ss += xn * xn;
               }
 #pragma unroll
