@@ -224,6 +224,33 @@ def _time_ms(fn, stream, steps, warmup=3):
     return e0.elapsed_time(e1) / steps
 
 
+def prefill_70b_layer_numbers(m, x, kv, stream, tflops, steps=3):
+    """Prefill of 4096 rows through one 70B-shaped layer: tokens/s, and the
+    GEMMs' and the attention's algorithmic TFLOP/s against the bf16 peak
+    (the attention counts the unmasked half, 4 n_q d T(T+1)/2)."""
+    from llama2_decoder_forward_gb300 import synth
+    s70 = synth.LLAMA2_70B
+    T = x.shape[0]
+    fn = lambda: m.prefill_hidden(x, 1, T, kv)
+    ms = _time_ms(fn, stream, steps)
+    m.profile(["gemm", "attn_prefill"])
+    for _ in range(2):
+        fn()
+    gm, _ = m.profile_read("gemm")
+    am, _ = m.profile_read("attn_prefill")
+    m.profile([])
+    m.sync()
+    gm, am = gm / 2, am / 2
+    H, I = s70.hidden, s70.intermediate
+    gflop = 2.0 * T * (s70.qkv_rows * H + H * s70.n_q_heads * s70.head_dim + 3 * H * I)
+    aflop = 4.0 * s70.n_q_heads * s70.head_dim * (T * (T + 1) / 2)
+    g_tf = gflop / (gm * 1e-3) / 1e12
+    a_tf = aflop / (am * 1e-3) / 1e12
+    return {"tokens_per_s": T / (ms * 1e-3), "ms": ms,
+            "gemm": {"tflops": g_tf, "frac": g_tf / tflops, "ms": gm},
+            "attention": {"tflops": a_tf, "frac": a_tf / tflops, "ms": am}}
+
+
 def extra_workloads(dev, stream, w7, hbm, tflops):
     """The other workloads of the scope table, each timed after the headline
     decode step (not part of its timed region): the 8 x 512 prefill of the full
@@ -312,19 +339,14 @@ def extra_workloads(dev, stream, w7, hbm, tflops):
                  "frac": wb / (k["gemm"][0] * 1e-3) / 1e9 / hbm}}
     kv1 = binding.KVCache(s70, batch=1, capacity=cap70)
     x = torch.randn(S70, s70.hidden, generator=g, device=dev)
-    fn = lambda: m.prefill_hidden(x, 1, S70, kv1)
-    ms = _time_ms(fn, stream, 3)
-    k = prof(m, fn, ["gemm", "attn_prefill"], 2)
-    gflop = 2.0 * S70 * layer_params(s70)
-    aflop = 4.0 * s70.n_q_heads * s70.head_dim * (S70 * (S70 + 1) / 2)
-    g_tf = gflop / (k["gemm"][0] * 1e-3) / 1e12
-    a_tf = aflop / (k["attn_prefill"][0] * 1e-3) / 1e12
-    out["layer_70b_prefill_4096"] = {
-        "workload": "one llama2-70b layer, causal prefill of 4096 tokens at batch 1",
-        "tokens_per_s": S70 / (ms * 1e-3), "ms": ms,
-        "gemm": {"tflops": g_tf, "frac": g_tf / tflops, "ms": k["gemm"][0]},
-        "attention": {"tflops": a_tf, "frac": a_tf / tflops, "ms": k["attn_prefill"][0]}}
-    del m, kv, kv1, w70, x
+    pre = {"workload": "one llama2-70b layer, causal prefill of 4096 tokens at batch 1"}
+    for act in ("bf16", "pair"):
+        ma = m if act == "pair" else binding.Model(s70, w70, max_batch=1, max_tokens=S70,
+                                                   max_seq=cap70, has_embed_head=False,
+                                                   stream=stream, act=act)
+        pre[act] = prefill_70b_layer_numbers(ma, x, kv1, stream, tflops)
+    out["layer_70b_prefill_4096"] = pre
+    del m, ma, kv, kv1, w70, x
     torch.cuda.empty_cache()
 
     # ---- ragged paged decode on 7B layer shapes, MHA and GQA (32 q / 8 kv)
@@ -630,6 +652,45 @@ def run_prefill(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill70(args):
+    """One 70B-shaped layer, causal prefill of 4096 tokens at batch 1 (the
+    prefill half of the 70B-layer workload), activation operands as --act
+    says; for profiling the prefill GEMMs and attention at that size."""
+    import torch
+    import __graft_entry__
+    from llama2_decoder_forward_gb300 import binding, synth
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    __graft_entry__.build()
+    s70 = synth.LLAMA2_70B.with_(n_layers=1)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1002)
+
+    def rn(*s, std=0.01, mean=0.0):
+        t = torch.randn(*s, generator=g, device=dev, dtype=torch.float32)
+        return t.mul_(std).add_(mean).to(torch.bfloat16)
+
+    H, I, T = s70.hidden, s70.intermediate, 4096
+    w = {"layers": [{"attn_norm": rn(H, std=0.1, mean=1.0), "wqkv": rn(s70.qkv_rows, H),
+                     "wo": rn(H, H), "ffn_norm": rn(H, std=0.1, mean=1.0), "w_gate": rn(I, H),
+                     "w_up": rn(I, H), "w_down": rn(H, I)}]}
+    stream = torch.cuda.Stream(device=dev)
+    m = binding.Model(s70, w, max_batch=1, max_tokens=T, max_seq=T + 16, has_embed_head=False,
+                      stream=stream, act=args.act)
+    kv = binding.KVCache(s70, batch=1, capacity=T + 16)
+    x = torch.randn(T, H, generator=g, device=dev)
+    hbm, tflops, peak_kind = _peaks()
+    with Clocks(0) as clk:
+        r = prefill_70b_layer_numbers(m, x, kv, stream, tflops, steps=args.steps)
+    line = {"metric": "Llama2-70B layer prefill tokens/s (4096 tokens)", "value": r["tokens_per_s"],
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": 3, "ms_per_step": r["ms"],
+            "higher_is_better": True, "dtype": "bf16 (activation operands: %s)" % args.act,
+            "data": "synthetic", "config": {"workload": "one llama2-70b layer, causal prefill of 4096 tokens"},
+            "kernels": r, "peak_tflops": tflops, "peak_source": peak_kind, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def run_extend(args):
     """One continuous-batching step on the full 7B model: 28 sequences decode
     one token at position 1024 while 4 others feed a 256-token prompt piece
@@ -857,7 +918,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="model", choices=["model", "layer", "prefill", "extend"])
+    ap.add_argument("--workload", default="model",
+                    choices=["model", "layer", "prefill", "prefill70", "extend"])
+    ap.add_argument("--act", default="pair", choices=["pair", "bf16"],
+                    help="prefill70 workload: activation operands (hi/lo pair or single bf16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=32,
                     help="prefill workload: decoder layers (fewer for a small profiling case)")
@@ -880,6 +944,8 @@ def main():
         run_prefill(args)
     elif args.workload == "extend":
         run_extend(args)
+    elif args.workload == "prefill70":
+        run_prefill70(args)
     else:
         run_gpu(args)
 

@@ -13,9 +13,7 @@
 // warps' (max, sum, O) are merged through shared memory; with several key
 // splits a small kernel merges the splits the same way.
 //
-// Prefill (bf16): FlashAttention-style: one CTA per (64 query rows, head,
-// sequence); K/V tiles of 64 keys via TMA, key tiles past the diagonal are
-// skipped, the diagonal tile is masked.
+// Prefill (bf16) runs on the tcgen05 tensor cores (k_prefill_tc.cu).
 //
 // fp32 configs use plain CUDA-core kernels (exact fp32, exp on the CUDA
 // math library) for both phases.
@@ -831,319 +829,6 @@ __global__ void attn_combine_kernel(const float* __restrict__ part,
   }
 }
 
-// ======================================================================== prefill (bf16)
-constexpr int PQ = 64;  // query rows per CTA
-constexpr int PK = 64;  // keys per tile
-constexpr int PSTAGES = 2;
-constexpr int PRE_THREADS = 160;
-constexpr uint32_t PHALF = PK * 128;       // 64 rows x 64 dims bf16 = 8 KB
-constexpr uint32_t PTILE = 2 * PHALF;      // 64 x 128 = 16 KB
-constexpr size_t PRE_SMEM = 2 * PTILE + PSTAGES * 2 * PTILE + 1024 + 256;
-
-struct PreParams {
-  int q_lo_rows;
-  bf16* out;
-  size_t out_lo;
-  uint32_t* status;
-  int T, n_q, n_kv, G, n_qtiles;
-  float scale_log2;
-  // Packed sequences (extend): sequence b owns rows cu_rows[b] .. cu_rows[b+1]-1
-  // at positions start_pos[b], start_pos[b] + 1, ...; null: T rows per
-  // sequence at positions 0 .. T-1.
-  const int32_t* cu_rows;
-  const int32_t* start_pos;
-  int n_rows;  // rows of Q and of the output
-  // K/V source: 0 = per-row buffers [rows, n_kv, d]; 1 = the KV cache (all
-  // keys 0 .. position of the row, earlier pieces included)
-  int from_cache, box_rows, layer, page_size, capacity, batch_cap, n_pages, max_pages;
-  const int32_t* page_table;
-  float v_scale;  // V values are the stored ones times this (K's scale is in scale_log2)
-};
-
-// Cache row of the keys starting at k0 (a multiple of 16) of sequence b, K/V
-// head g; a page id outside the pool is flagged and mapped to rows TMA fills
-// with zeros.
-__device__ __forceinline__ int pre_kv_row(const PreParams& p, int b, int g, int k0) {
-  if (p.page_size == 0) return (b * p.n_kv + g) * p.capacity + k0;
-  const int pi = k0 / p.page_size;
-  const int page = pi < p.max_pages ? p.page_table[(size_t)b * p.max_pages + pi] : -1;
-  if (page < 0 || page >= p.n_pages) {
-    flag(p.status, LLAMA_FLAG_PAGE_RANGE);
-    return -4 * SUBK;
-  }
-  return (page * p.n_kv + g) * p.page_size + (k0 % p.page_size);
-}
-
-__global__ void __launch_bounds__(PRE_THREADS, 2)
-    attn_prefill_kernel(const __grid_constant__ CUtensorMap mapQ,
-                        const __grid_constant__ CUtensorMap mapK,
-                        const __grid_constant__ CUtensorMap mapV,
-                        const __grid_constant__ CUtensorMap mapK16,
-                        const __grid_constant__ CUtensorMap mapV16, PreParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* qs = smem;           // Q tile; its bf16 remainders follow at qs + PTILE
-  uint8_t* kvs = smem + 2 * PTILE;  // stage s: K at s*2*PTILE, V at s*2*PTILE + PTILE
-  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + 2 * PTILE + PSTAGES * 2 * PTILE);
-  uint64_t* full = qfull + 1;
-  uint64_t* empty = full + PSTAGES;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(empty + PSTAGES);
-
-  grid_dep_wait();  // q, k, v come from the RoPE/append kernel
-  grid_dep_launch();
-  const int qt = p.n_qtiles - 1 - (int)blockIdx.x;  // longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int g = h / p.G;
-  const int q0 = qt * PQ;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rowbase = p.cu_rows ? p.cu_rows[b] : b * p.T;
-  const int n_b = p.cu_rows ? p.cu_rows[b + 1] - rowbase : p.T;  // this sequence's rows
-  const int start = p.start_pos ? p.start_pos[b] : 0;             // position of its first row
-  if (q0 >= n_b) return;
-  if (p.cu_rows && p.from_cache && n_b == 1) return;  // single new rows: the decode kernel's
-  if (p.from_cache) {  // the sequence's keys must fit its cache slots
-    const int cap_keys = p.page_size ? p.max_pages * p.page_size : p.capacity;
-    if (start < 0 || start > cap_keys - n_b) {
-      if (threadIdx.x == 0) flag(p.status, LLAMA_FLAG_POS_RANGE);
-      return;
-    }
-  }
-  const int n_keys = start + n_b;  // keys 0 .. n_keys - 1 exist once the rows are appended
-  const int n_kt = (start + min(q0 + PQ, n_b) - 1) / PK + 1;
-
-  if (threadIdx.x == 0) {
-    mbar_init(qfull, 1);
-    for (int s = 0; s < PSTAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == 4) {  // producer
-    if (lane == 0) {
-      tma_prefetch_desc(&mapQ);
-      tma_prefetch_desc(&mapK);
-      tma_prefetch_desc(&mapV);
-      if (p.from_cache) {
-        tma_prefetch_desc(&mapK16);
-        tma_prefetch_desc(&mapV16);
-      }
-      mbar_arrive_expect_tx(qfull, p.q_lo_rows ? 2 * PTILE : PTILE);
-      tma_load_3d(qs, &mapQ, qfull, 0, h, rowbase + q0);
-      tma_load_3d(qs + PHALF, &mapQ, qfull, 64, h, rowbase + q0);
-      if (p.q_lo_rows) {
-        tma_load_3d(qs + PTILE, &mapQ, qfull, 0, h, p.q_lo_rows + rowbase + q0);
-        tma_load_3d(qs + PTILE + PHALF, &mapQ, qfull, 64, h, p.q_lo_rows + rowbase + q0);
-      }
-      int issued = 0;
-      bool ok = true;
-      for (int kt = 0; kt < n_kt; ++kt) {
-        const int s = kt % PSTAGES;
-        const uint32_t ph = (kt / PSTAGES) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, p.status)) {
-          ok = false;
-          *abort_flag = 1;
-          break;
-        }
-        uint8_t* ks = kvs + s * 2 * PTILE;
-        const int k0 = kt * PK, nvalid = min(PK, n_keys - k0);
-        if (!p.from_cache) {
-          mbar_arrive_expect_tx(&full[s], 2 * PTILE);
-          tma_load_3d(ks, &mapK, &full[s], 0, g, rowbase + k0);
-          tma_load_3d(ks + PHALF, &mapK, &full[s], 64, g, rowbase + k0);
-          tma_load_3d(ks + PTILE, &mapV, &full[s], 0, g, rowbase + k0);
-          tma_load_3d(ks + PTILE + PHALF, &mapV, &full[s], 64, g, rowbase + k0);
-        } else if (p.box_rows == PK && nvalid == PK) {  // 64 contiguous keys: one box per half
-          const int row = pre_kv_row(p, b, g, k0);
-          mbar_arrive_expect_tx(&full[s], 2 * PTILE);
-          tma_load_3d(ks, &mapK, &full[s], 0, row, p.layer);
-          tma_load_3d(ks + PHALF, &mapK, &full[s], 64, row, p.layer);
-          tma_load_3d(ks + PTILE, &mapV, &full[s], 0, row, p.layer);
-          tma_load_3d(ks + PTILE + PHALF, &mapV, &full[s], 64, row, p.layer);
-        } else {  // 16-key boxes, only those holding keys of this sequence
-          const int nsub = (nvalid + SUBK - 1) / SUBK;
-          mbar_arrive_expect_tx(&full[s], nsub * 4 * HALF_BYTES);
-          for (int j = 0; j < nsub; ++j) {
-            const int row = pre_kv_row(p, b, g, k0 + j * SUBK);
-            uint8_t* kd = ks + j * HALF_BYTES;
-            tma_load_3d(kd, &mapK16, &full[s], 0, row, p.layer);
-            tma_load_3d(kd + PHALF, &mapK16, &full[s], 64, row, p.layer);
-            tma_load_3d(kd + PTILE, &mapV16, &full[s], 0, row, p.layer);
-            tma_load_3d(kd + PTILE + PHALF, &mapV16, &full[s], 64, row, p.layer);
-          }
-        }
-        ++issued;
-      }
-      mbar_wait(qfull, 0, p.status);
-      if (!ok) {
-        for (int t = issued - 1; t >= 0 && t >= issued - PSTAGES; --t)
-          mbar_wait(&full[t % PSTAGES], (t / PSTAGES) & 1, p.status);
-      }
-    }
-    return;
-  }
-
-  // consumers: warp w owns query rows q0 + 16w .. q0 + 16w + 15
-  const int mi = lane >> 3, rr = lane & 7;
-  const int r0 = lane >> 2;
-  const int myrow0 = q0 + warp * 16 + r0;  // rows myrow0 and myrow0 + 8
-  if (!mbar_wait(qfull, 0, p.status)) *abort_flag = 1;
-  uint32_t qa[8][4];
-  const uint32_t qb = smem_u32(qs);
-  const int q_row = warp * 16 + ((mi & 1) << 3) + rr;
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const int chunk = (kk & 3) * 2 + (mi >> 1);
-    ldsm_x4(qb + (kk >> 2) * PHALF + swz128(q_row, chunk), qa[kk][0], qa[kk][1], qa[kk][2],
-            qa[kk][3]);
-  }
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  float oacc[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-
-  for (int kt = 0; kt < n_kt; ++kt) {
-    const int s = kt % PSTAGES;
-    const uint32_t ph = (kt / PSTAGES) & 1;
-    if (*abort_flag) break;
-    if (!mbar_wait(&full[s], ph, p.status)) {
-      *abort_flag = 1;
-      break;
-    }
-    const int nvalid = min(PK, n_keys - kt * PK);
-    if (nvalid < PK) {
-      // V rows past the last key may hold anything (P is 0 there, but 0 * NaN
-      // is not): every warp zeroes all of them itself, so no warp waits for
-      // another (they all store the same zeros)
-      uint8_t* vt = kvs + s * 2 * PTILE + PTILE;
-      const int nz = (PK - nvalid) * 16;
-      for (int i = lane; i < nz; i += 32) {
-        const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
-        *reinterpret_cast<uint4*>(vt + half * PHALF + row * 128 + chunk * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
-    const uint32_t kb = smem_u32(kvs + s * 2 * PTILE);
-    const uint32_t vb = kb + PTILE;
-    float sc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t ql[4];  // remainder fragment of Q, read again from shared memory
-      if (p.q_lo_rows)
-        ldsm_x4(qb + PTILE + (kk >> 2) * PHALF + swz128(q_row, (kk & 3) * 2 + (mi >> 1)), ql[0],
-                ql[1], ql[2], ql[3]);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int row = np * 16 + ((mi >> 1) << 3) + rr;
-        const int chunk = (kk & 3) * 2 + (mi & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + (kk >> 2) * PHALF + swz128(row, chunk), b0, b1, b2, b3);
-        mma_bf16_16816(sc[2 * np], qa[kk], b0, b1);
-        mma_bf16_16816(sc[2 * np + 1], qa[kk], b2, b3);
-        if (p.q_lo_rows) {
-          mma_bf16_16816(sc[2 * np], ql, b0, b1);
-          mma_bf16_16816(sc[2 * np + 1], ql, b2, b3);
-        }
-      }
-    }
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int key = kt * PK + nb * 8 + 2 * (lane & 3) + (i & 1);
-        const int qpos = start + myrow0 + (i >= 2 ? 8 : 0);
-        const float v = (key <= qpos && key < n_keys) ? sc[nb][i] * p.scale_log2 : -INFINITY;
-        sc[nb][i] = v;
-        mx[i >> 1] = fmaxf(mx[i >> 1], v);
-      }
-    float corr[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
-      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
-      const float mnew = fmaxf(mrow[hh], mx[hh]);
-      corr[hh] = mnew == -INFINITY ? 1.f : exp2f(mrow[hh] - mnew);
-      mrow[hh] = mnew;
-    }
-    float ps[2] = {0.f, 0.f};
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int hh = i >> 1;
-        const float pv = mrow[hh] == -INFINITY ? 0.f : exp2f(sc[nb][i] - mrow[hh]);
-        sc[nb][i] = pv;
-        ps[hh] += pv;
-      }
-    lrow[0] = lrow[0] * corr[0] + ps[0];
-    lrow[1] = lrow[1] * corr[1] + ps[1];
-#pragma unroll
-    for (int dn = 0; dn < 16; ++dn) {
-      oacc[dn][0] *= corr[0];
-      oacc[dn][1] *= corr[0];
-      oacc[dn][2] *= corr[1];
-      oacc[dn][3] *= corr[1];
-    }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      // P as a bf16 pair: O += P_hi V + P_lo V
-      uint32_t pa[4], pl[4];
-      split_pack(sc[2 * ks][0], sc[2 * ks][1], pa[0], pl[0]);
-      split_pack(sc[2 * ks][2], sc[2 * ks][3], pa[1], pl[1]);
-      split_pack(sc[2 * ks + 1][0], sc[2 * ks + 1][1], pa[2], pl[2]);
-      split_pack(sc[2 * ks + 1][2], sc[2 * ks + 1][3], pa[3], pl[3]);
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        const int c16 = dp * 2 + (mi >> 1);
-        const int row = ks * 16 + ((mi & 1) << 3) + rr;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + (c16 >> 3) * PHALF + swz128(row, c16 & 7), b0, b1, b2, b3);
-        mma_bf16_16816(oacc[2 * dp], pa, b0, b1);
-        mma_bf16_16816(oacc[2 * dp + 1], pa, b2, b3);
-        mma_bf16_16816(oacc[2 * dp], pl, b0, b1);
-        mma_bf16_16816(oacc[2 * dp + 1], pl, b2, b3);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-  }
-  if (*abort_flag) return;
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    lrow[hh] += __shfl_xor_sync(0xffffffffu, lrow[hh], 1);
-    lrow[hh] += __shfl_xor_sync(0xffffffffu, lrow[hh], 2);
-  }
-  const size_t ld = (size_t)p.n_q * AD;
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    const int row = myrow0 + hh * 8;
-    if (row >= n_b || rowbase + row >= p.n_rows) continue;
-    const float inv = lrow[hh] > 0.f ? p.v_scale / lrow[hh] : 0.f;
-    bf16* dst = p.out + (size_t)(rowbase + row) * ld + (size_t)h * AD;
-#pragma unroll
-    for (int dn = 0; dn < 16; ++dn) {
-      const int col = dn * 8 + 2 * (lane & 3);
-      const float v0 = oacc[dn][2 * hh] * inv, v1 = oacc[dn][2 * hh + 1] * inv;
-      const uint32_t hi = pack_bf16(v0, v1);
-      *reinterpret_cast<uint32_t*>(dst + col) = hi;
-      if (p.out_lo) {
-        const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&hi);
-        *reinterpret_cast<uint32_t*>(dst + col + p.out_lo) =
-            pack_bf16(v0 - __low2float(h2), v1 - __high2float(h2));
-      }
-    }
-  }
-}
-
 // ======================================================================== fp32 CUDA-core kernels
 // Decode: one CTA per (query head, sequence); scores in shared memory.
 __global__ void attn_decode_f32_kernel(const float* __restrict__ q, const int32_t* positions,
@@ -1278,9 +963,6 @@ cudaError_t attn_prepare() {
   e = cudaFuncSetAttribute(attn_decode_kernel<true, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEC_SMEM_F8);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)PRE_SMEM);
-  if (e != cudaSuccess) return e;
   return attn_prefill_tc_prepare();
 }
 
@@ -1366,37 +1048,7 @@ cudaError_t launch_attn_prefill(int dtype, const AttnPrefillArgs& a, cudaStream_
                     (const float*)a.q, (const float*)a.k, (const float*)a.v, (float*)a.out, a.T,
                     a.n_q, a.n_kv, a.head_dim);
   }
-  if (a.head_dim != AD) return cudaErrorInvalidValue;
   return launch_attn_prefill_tc(a, st);
-  PreParams p;
-  p.q_lo_rows = a.q_lo_rows;
-  p.out = (bf16*)a.out;
-  p.out_lo = a.out_lo;
-  p.status = a.status;
-  p.T = a.T;
-  p.n_q = a.n_q;
-  p.n_kv = a.n_kv;
-  p.G = a.n_q / a.n_kv;
-  p.n_qtiles = (a.T + PQ - 1) / PQ;
-  p.scale_log2 = kLog2e / sqrtf((float)AD) * a.k_scale;
-  p.v_scale = a.v_scale;
-  p.cu_rows = a.cu_rows;
-  p.start_pos = a.start_pos;
-  p.n_rows = a.cu_rows ? a.n_rows : a.B * a.T;
-  p.from_cache = a.from_cache;
-  p.box_rows = a.box_rows == PK ? PK : SUBK;
-  p.layer = a.layer;
-  p.page_size = a.page_size;
-  p.capacity = a.capacity;
-  p.batch_cap = a.batch_cap;
-  p.n_pages = a.n_pages;
-  p.max_pages = a.max_pages;
-  p.page_table = a.page_table;
-  if (a.from_cache && (!a.map_k16 || !a.map_v16)) return cudaErrorInvalidValue;
-  const CUtensorMap* k16 = a.from_cache ? a.map_k16 : a.map_k;
-  const CUtensorMap* v16 = a.from_cache ? a.map_v16 : a.map_v;
-  return launch_k(attn_prefill_kernel, dim3(p.n_qtiles, a.n_q, a.B), dim3(PRE_THREADS), PRE_SMEM,
-                  st, 0, *a.map_q, *a.map_k, *a.map_v, *k16, *v16, p);
 }
 
 }  // namespace llgb
