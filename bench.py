@@ -339,14 +339,10 @@ def extra_workloads(dev, stream, w7, hbm, tflops):
                  "frac": wb / (k["gemm"][0] * 1e-3) / 1e9 / hbm}}
     kv1 = binding.KVCache(s70, batch=1, capacity=cap70)
     x = torch.randn(S70, s70.hidden, generator=g, device=dev)
-    pre = {"workload": "one llama2-70b layer, causal prefill of 4096 tokens at batch 1"}
-    for act in ("bf16", "pair"):
-        ma = m if act == "pair" else binding.Model(s70, w70, max_batch=1, max_tokens=S70,
-                                                   max_seq=cap70, has_embed_head=False,
-                                                   stream=stream, act=act)
-        pre[act] = prefill_70b_layer_numbers(ma, x, kv1, stream, tflops)
-    out["layer_70b_prefill_4096"] = pre
-    del m, ma, kv, kv1, w70, x
+    out["layer_70b_prefill_4096"] = {
+        "workload": "one llama2-70b layer, causal prefill of 4096 tokens at batch 1",
+        **prefill_70b_layer_numbers(m, x, kv1, stream, tflops)}
+    del m, kv, kv1, w70, x
     torch.cuda.empty_cache()
 
     # ---- ragged paged decode on 7B layer shapes, MHA and GQA (32 q / 8 kv)
@@ -654,8 +650,8 @@ def run_prefill(args):
 
 def run_prefill70(args):
     """One 70B-shaped layer, causal prefill of 4096 tokens at batch 1 (the
-    prefill half of the 70B-layer workload), activation operands as --act
-    says; for profiling the prefill GEMMs and attention at that size."""
+    prefill half of the 70B-layer workload), for profiling the prefill GEMMs
+    and attention at that size."""
     import torch
     import __graft_entry__
     from llama2_decoder_forward_gb300 import binding, synth
@@ -677,7 +673,7 @@ def run_prefill70(args):
                      "w_up": rn(I, H), "w_down": rn(H, I)}]}
     stream = torch.cuda.Stream(device=dev)
     m = binding.Model(s70, w, max_batch=1, max_tokens=T, max_seq=T + 16, has_embed_head=False,
-                      stream=stream, act=args.act)
+                      stream=stream)
     kv = binding.KVCache(s70, batch=1, capacity=T + 16)
     x = torch.randn(T, H, generator=g, device=dev)
     hbm, tflops, peak_kind = _peaks()
@@ -685,7 +681,7 @@ def run_prefill70(args):
         r = prefill_70b_layer_numbers(m, x, kv, stream, tflops, steps=args.steps)
     line = {"metric": "Llama2-70B layer prefill tokens/s (4096 tokens)", "value": r["tokens_per_s"],
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": 3, "ms_per_step": r["ms"],
-            "higher_is_better": True, "dtype": "bf16 (activation operands: %s)" % args.act,
+            "higher_is_better": True, "dtype": "bf16",
             "data": "synthetic", "config": {"workload": "one llama2-70b layer, causal prefill of 4096 tokens"},
             "kernels": r, "peak_tflops": tflops, "peak_source": peak_kind, "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
@@ -920,8 +916,6 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="model",
                     choices=["model", "layer", "prefill", "prefill70", "extend"])
-    ap.add_argument("--act", default="pair", choices=["pair", "bf16"],
-                    help="prefill70 workload: activation operands (hi/lo pair or single bf16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=32,
                     help="prefill workload: decoder layers (fewer for a small profiling case)")

@@ -88,25 +88,8 @@ typedef struct llama_config {
   int32_t has_embed_head;/* 1: token ids in, logits out; 0: hidden in/out only */
   int32_t weight_dtype;  /* projection weights (wqkv, wo, w_gate, w_up, w_down):
                             LLAMA_W_MODEL in the config's dtype, or LLAMA_W_E4M3 */
-  int32_t act_dtype;     /* bf16 models: how GEMM inputs and attention queries are
-                            carried, LLAMA_ACT_PAIR (default) or LLAMA_ACT_BF16 */
 } llama_config;
 
-/* Precision of the bf16 activation operands (bf16 models; ignored for fp32).
- * LLAMA_ACT_PAIR: every tensor-core operand that is an activation (the
- *   RMSNorm outputs, the attention output and the SwiGLU output as GEMM
- *   inputs; the queries and the softmax weights inside attention) is a pair
- *   hi = bf16(v), lo = bf16(v - hi) and both are multiplied, about 16
- *   significant bits. It costs twice the tensor work of a bf16 operand: free
- *   in decode, which is bound by memory, but it halves the prefill GEMMs'
- *   algorithmic rate. Deep stacks of random-weight layers amplify rounding
- *   enough that 32 layers need it to stay within 2e-2 + 1e-2 |logit| of an
- *   exact forward pass.
- * LLAMA_ACT_BF16: each of those operands is one bf16 value (the usual bf16
- *   inference arithmetic; the decode attention still keeps its softmax
- *   weights as a pair). */
-#define LLAMA_ACT_PAIR 0
-#define LLAMA_ACT_BF16 1
 
 /* Projection weights as FP8 E4M3 (bf16 models only; FP8 as the latency option
  * of "Llama2架构全景解析" §3.2): each matrix is [rows, cols] bytes plus an fp32

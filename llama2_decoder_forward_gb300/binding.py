@@ -34,15 +34,12 @@ class LlamaConfig(ctypes.Structure):
                 ("n_kv_heads", c_int32), ("head_dim", c_int32), ("intermediate", c_int32),
                 ("vocab", c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
                 ("dtype", c_int32), ("max_batch", c_int32), ("max_tokens", c_int32),
-                ("max_seq", c_int32), ("has_embed_head", c_int32), ("weight_dtype", c_int32),
-                ("act_dtype", c_int32)]
+                ("max_seq", c_int32), ("has_embed_head", c_int32), ("weight_dtype", c_int32)]
 
 
 LAYER_MATS = ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
 PROJECTIONS = ("wqkv", "wo", "w_gate", "w_up", "w_down")
 W_MODEL, W_E4M3 = 0, 1
-# activation operands of bf16 models: "pair" (hi/lo, about 16 bits) or "bf16" (single)
-ACT = {"pair": 0, "bf16": 1}
 
 
 class LayerWeights(ctypes.Structure):
@@ -164,12 +161,11 @@ def _stream_handle(stream):
 
 
 def make_config(shape, max_batch, max_tokens, max_seq, has_embed_head=True,
-                weight_dtype=W_MODEL, act="pair") -> LlamaConfig:
+                weight_dtype=W_MODEL) -> LlamaConfig:
     return LlamaConfig(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
                        shape.head_dim, shape.intermediate, shape.vocab if has_embed_head else 0,
                        shape.rms_eps, shape.rope_theta, F32 if shape.dtype == "f32" else BF16,
-                       max_batch, max_tokens, max_seq, 1 if has_embed_head else 0, weight_dtype,
-                       ACT[act])
+                       max_batch, max_tokens, max_seq, 1 if has_embed_head else 0, weight_dtype)
 
 
 def quantize_rows_e4m3(w, stream=None):
@@ -246,12 +242,11 @@ class Model:
     on the GPU ({"embed", "final_norm", "lm_head", "layers": [...]}); a
     layer-only model passes {"layers": [...]} and has_embed_head=False.
     Layers made by quantize_layer_e4m3 (E4M3 projections with row scales)
-    select weight_dtype LLAMA_W_E4M3. act: "pair" (activation operands as
-    bf16 hi/lo pairs, the default) or "bf16" (single bf16 operands).
+    select weight_dtype LLAMA_W_E4M3.
     """
 
     def __init__(self, shape, weights, *, max_batch, max_tokens, max_seq, has_embed_head=True,
-                 stream=None, act="pair"):
+                 stream=None):
         import torch
         self.shape = shape
         self.weights = weights  # keep the tensors alive
@@ -261,7 +256,7 @@ class Model:
         # E4M3 projections (quantize_layer_e4m3) carry "<name>_scale" entries
         w8 = "wqkv_scale" in layers[0]
         self.cfg = make_config(shape, max_batch, max_tokens, max_seq, has_embed_head,
-                               W_E4M3 if w8 else W_MODEL, act)
+                               W_E4M3 if w8 else W_MODEL)
         nbytes = workspace_bytes(self.cfg)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         arr = (LayerWeights * len(layers))()

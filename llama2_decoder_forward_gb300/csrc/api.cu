@@ -29,10 +29,9 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // the KV cache holds single bf16 values. (The extra MMA work is free while
 // decode is bound by weight bytes; it doubles the prefill's tensor work.)
 inline int round16(int v) { return (v + 15) / 16 * 16; }
-// Remainder-row offset of the pair layout for `rows` activation rows: 0 when
-// the context carries single bf16 operands (or is fp32).
+// Remainder-row offset of the pair layout for `rows` activation rows (0 for fp32).
 inline int pair_rows(const llama_config& cf, int rows) {
-  return cf.dtype == LLAMA_BF16 && cf.act_dtype == LLAMA_ACT_PAIR ? round16(rows) : 0;
+  return cf.dtype == LLAMA_BF16 ? round16(rows) : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -84,7 +83,6 @@ int check_config(const llama_config* c) {
   if (c->dtype != LLAMA_F32 && c->dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
   if (c->weight_dtype != LLAMA_W_MODEL && c->weight_dtype != LLAMA_W_E4M3)
     return LLAMA_ERR_INVALID_ARG;
-  if (c->act_dtype != LLAMA_ACT_PAIR && c->act_dtype != LLAMA_ACT_BF16) return LLAMA_ERR_INVALID_ARG;
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return LLAMA_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads != 0) return LLAMA_ERR_INVALID_ARG;
   if (c->head_dim % 8 != 0) return LLAMA_ERR_UNSUPPORTED;

@@ -61,10 +61,6 @@ def test_workspace_bytes_and_config_checks(lib):
     assert lib.llama_workspace_bytes(None, ctypes.byref(n)) == 1
     tiny = binding.make_config(synth.TINY, 1, 16, 32)
     assert lib.llama_workspace_bytes(ctypes.byref(tiny), ctypes.byref(n)) == 0
-    # activation operands: the pair (default) or single bf16; nothing else
-    assert lib.llama_workspace_bytes(ctypes.byref(_cfg(act_dtype=1)), ctypes.byref(n)) == 0
-    assert lib.llama_workspace_bytes(ctypes.byref(_cfg(act_dtype=2)), ctypes.byref(n)) == 1
-    assert binding.make_config(synth.LLAMA2_7B, 1, 1, 1, act="bf16").act_dtype == 1
 
 
 def test_e4m3_weight_config_and_quantiser_argument_checks(lib):

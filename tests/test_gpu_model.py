@@ -52,7 +52,7 @@ def test_tiny_fp32_greedy_generation():
 
 
 # --------------------------------------------------------------------------- single layers
-def _layer_decode_case(shape, std, B, S, seed, paged_lengths=None, n_kv_variant=None, act="pair"):
+def _layer_decode_case(shape, std, B, S, seed, paged_lengths=None, n_kv_variant=None):
     need_gpu()
     lw = synth.layer_weights(shape, seed, 0, std=std)
     if n_kv_variant:
@@ -80,7 +80,7 @@ def _layer_decode_case(shape, std, B, S, seed, paged_lengths=None, n_kv_variant=
         max_seq = max(n_pages) * 16
     pos = torch.tensor(lengths, dtype=torch.int32)
     m = binding.Model(shape, to_dev({"layers": [lw]}), max_batch=B, max_tokens=0, max_seq=max_seq,
-                      has_embed_head=False, act=act)
+                      has_embed_head=False)
     h = x.cuda()
     m.decode_hidden(h, pos.cuda(), kv)
     m.sync()
@@ -99,36 +99,6 @@ def _layer_decode_case(shape, std, B, S, seed, paged_lengths=None, n_kv_variant=
         refk = Kp[pages, :, pos.numpy() % 16]
     assert_close(newk, refk, BF16_TOL, "appended K")
     return assert_close(h, ref, BF16_TOL, "layer output")
-
-
-@pytest.mark.parametrize("big", [False, True])
-def test_layer_decode_single_bf16_operands(big):
-    # the single-bf16 operand mode on the single-layer workloads: 7B at batch
-    # 32 over 1024 positions, 70B (GQA 64/8) over 4096
-    if big:
-        _layer_decode_case(synth.LLAMA2_70B.with_(n_layers=1), 0.01, 32, 4096, 1002, act="bf16")
-    else:
-        _layer_decode_case(synth.LLAMA2_7B.with_(n_layers=1), 0.02, 32, 1024, 1001, act="bf16")
-
-
-def test_small_model_single_bf16_operands_prefill_and_decode():
-    # two layers with single bf16 operands stay within the bf16 bound
-    need_gpu()
-    shape = _small_bf16()
-    B, T, cap = 3, 40, 64
-    w = synth.model_weights(shape, 19)
-    toks = synth.token_ids(B, T + 1, shape.vocab, 19)
-    m = binding.Model(shape, to_dev(w), max_batch=B, max_tokens=B * T, max_seq=cap, act="bf16")
-    kv = binding.KVCache(shape, batch=B, capacity=cap)
-    lg_p = torch.empty(B, shape.vocab, device="cuda")
-    lg_d = torch.empty(B, shape.vocab, device="cuda")
-    m.prefill(toks[:, :T].contiguous().cuda(), kv, lg_p)
-    pos = torch.full((B,), T, dtype=torch.int32, device="cuda")
-    m.decode_step(toks[:, T].contiguous().cuda(), pos, kv, lg_d)
-    m.sync()
-    ref = O.Model(shape, w, B, cap).prefill(toks.numpy())
-    assert_close(lg_p, ref[:, T - 1], BF16_TOL, "single-bf16 prefill")
-    assert_close(lg_d, ref[:, T], BF16_TOL, "single-bf16 decode after prefill")
 
 
 def test_layer_7b_decode_bs32_ctx1024():
@@ -158,8 +128,7 @@ def test_ragged_paged_gqa_decode_bs160():
                        paged_lengths=lengths.tolist(), n_kv_variant=8)
 
 
-@pytest.mark.parametrize("act", ["pair", "bf16"])
-def test_layer_70b_prefill_4096_sampled_rows(act):
+def test_layer_70b_prefill_4096_sampled_rows():
     need_gpu()
     shape = synth.LLAMA2_70B.with_(n_layers=1)
     seed, T = 1002, 4096
@@ -167,7 +136,7 @@ def test_layer_70b_prefill_4096_sampled_rows(act):
     x = synth.hidden_input(T, shape.hidden, seed)
     kv = binding.KVCache(shape, batch=1, capacity=T)
     m = binding.Model(shape, to_dev({"layers": [lw]}), max_batch=1, max_tokens=T, max_seq=T,
-                      has_embed_head=False, act=act)
+                      has_embed_head=False)
     h = x.cuda()
     m.prefill_hidden(h, 1, T, kv)
     m.sync()
