@@ -4,17 +4,21 @@
 // GQA: query head h reads K/V head h / G), computed FlashAttention-style so
 // the T x T score matrix never leaves the SM.
 //
-// One CTA per (128 query rows, query head, sequence); 192 threads:
+// One CTA per (128 query rows, query head, sequence); 320 threads:
 //   warp 0     TMA producer: the Q tile (and its bf16 remainder rows), then
 //              K and V tiles of 64 keys into a 3-stage mbarrier ring;
 //   warp 1     tensor-memory owner and MMA issuer (one thread):
 //              S_j = Q K_j^T into one of two S buffers in tensor memory,
 //              O += P_j V_j into the O accumulator in tensor memory;
-//   warps 2-5  softmax: each thread owns one query row (its tensor-memory
-//              lane), reads S_j with tcgen05.ld, masks, keeps the running max
-//              and sum, writes P_j (bf16, as a hi/lo pair when Q is one) to
-//              shared memory in the MMA operand layout, and at the end reads
-//              O, divides by the sum and stores the output rows.
+//   warps 2-9  softmax, two groups of four warps: a thread of group k owns
+//              one query row (its tensor-memory lane) and keys 32k .. 32k+31
+//              of every tile. It reads its half of S_j with tcgen05.ld,
+//              masks, exchanges the row's tile maximum with its partner in the
+//              other group through shared memory, keeps the running max and
+//              its half of the sum, writes its half of P_j (bf16, as a hi/lo
+//              pair when Q is one) to shared memory in the MMA operand layout,
+//              rescales and at the end normalises and stores its 64 of the
+//              row's 128 output dims.
 // The MMA of S_{j+1} runs while the softmax works on S_j. The running max is
 // applied lazily: O and the sum are rescaled (in tensor memory) only when a
 // row's max grows by more than 2^8, otherwise P keeps the older max, which
@@ -41,7 +45,7 @@ constexpr int TQ = 128;          // query rows per CTA: MMA M, one tensor-memory
 constexpr int TK = 64;           // keys per tile
 constexpr int TSUB = 16;         // keys per box of a 16-row (paged) cache view
 constexpr int TSTAGES = 3;
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 320;  // producer, MMA issuer, two softmax warpgroups
 constexpr uint32_t KV_HALF = TK * 128;     // 64 keys x 64 dims bf16: 8 KB
 constexpr uint32_t KV_TILE = 2 * KV_HALF;  // 64 keys x 128 dims: 16 KB
 constexpr uint32_t STAGE = 2 * KV_TILE;    // K tile then V tile: 32 KB
@@ -51,7 +55,12 @@ constexpr uint32_t P_TILE = TQ * 128;      // 128 rows x 64 keys: 16 KB; the rem
 constexpr uint32_t OFF_P = 2 * Q_TILE;
 constexpr uint32_t OFF_ST = OFF_P + 2 * P_TILE;
 constexpr uint32_t OFF_BAR = OFF_ST + TSTAGES * STAGE;
-constexpr size_t TC_SMEM = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+// exchange area of the two softmax groups: fp32 [3][2 groups][128 rows] (the
+// tile maxima, double-buffered by tile parity, then the final sums) and int
+// [2][2 groups][4 quadrants] "this warp is on track" flags
+constexpr uint32_t OFF_X = OFF_BAR + 256;
+constexpr uint32_t OFF_XOK = OFF_X + 3 * 2 * 128 * 4;
+constexpr size_t TC_SMEM = OFF_XOK + 2 * 2 * 4 * 4 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 256;  // S buffers at columns 0 and 64, O at 128
 constexpr uint32_t O_COL = 128;
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more than 2^8
@@ -95,6 +104,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2^x on the special-function unit (the PTX ex2.approx instruction; inputs
+// below the fp32 range give 0, -inf gives 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The two softmax warps that own the same 32 rows (one per group) meet here.
+// Both always pass the same sequence of these barriers: every decision to
+// leave the tile loop is taken right after one, from flags both warps read.
+__device__ __forceinline__ void pair_bar(int quad) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
 }
 
 // Cache row of the keys starting at k0 (a multiple of 16) of sequence b, K/V
@@ -162,9 +186,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sfree[i], 4);
+      mbar_init(&sfree[i], 8);
     }
-    mbar_init(pready, 4);
+    mbar_init(pready, 8);
     mbar_init(odone, 1);
     mbar_init(mfin, 1);
     ctl[1] = 0;
@@ -287,67 +311,83 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_wait(mfin, 0, p.status);  // every MMA retired before the tensor memory is freed
     }
   } else {  // --------------------------------------------------------- softmax warps
-    const int quad = warp & 3;  // tensor-memory lane quadrant this warp may access
+    const int quad = warp & 3;          // tensor-memory lane quadrant this warp may access
+    const int grp = (warp - 2) >> 2;    // 0: keys 0-31 of a tile, O dims 0-63; 1: the rest
     const int r = quad * 32 + lane;
     const int qrow = q0 + r;
     const int qpos = start + qrow;
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-    uint8_t* pbase = smem + OFF_P;
-    float m_used = -INFINITY, l = 0.f;
+    float* xch = reinterpret_cast<float*>(smem + OFF_X);           // [3][2][128]
+    volatile int* xok = reinterpret_cast<volatile int*>(smem + OFF_XOK);  // [2][2][4]
+    const uint32_t prow = smem_u32(smem + OFF_P) + (uint32_t)r * 128u;
+    const float c = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;  // m_used: the row's reference max, log2 units
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
-      if (ctl[1] || !mbar_wait(&sfull[j & 1], (j >> 1) & 1, p.status)) {
+      const bool good =
+          __all_sync(0xffffffffu, ok && !ctl[1] && mbar_wait(&sfull[j & 1], (j >> 1) & 1, p.status));
+      float sv[32];
+      float pm = -INFINITY;
+      if (good) {
+        tc_fence_after();
+        uint32_t u[2][16];
+        const uint32_t col = (uint32_t)(j & 1) * TK + 32u * grp;
+        tmem_ld16(tl + col, u[0]);
+        tmem_ld16(tl + col + 16, u[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          sv[i] = __uint_as_float(u[0][i]);
+          sv[16 + i] = __uint_as_float(u[1][i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfree[j & 1]);
+        const int k0 = j * TK + 32 * grp;  // this thread's first key of the tile
+        // a tile below the CTA's first row and inside the sequence needs no mask
+        const bool full = j * TK + TK - 1 <= start + q0 && j * TK + TK <= n_keys;
+        if (!full) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (k0 + i > qpos || k0 + i >= n_keys) sv[i] = -INFINITY;
+        }
+        float mx[4] = {sv[0], sv[1], sv[2], sv[3]};  // raw scores; the scale is positive
+#pragma unroll
+        for (int i = 4; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], sv[i]);
+        pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      }
+      const int xb = (j & 1) * 2;
+      xch[(xb + grp) * 128 + r] = pm;
+      if (lane == 0) xok[(xb + grp) * 4 + quad] = good ? 1 : 0;
+      pair_bar(quad);
+      if (!xok[xb * 4 + quad] || !xok[(xb + 1) * 4 + quad]) {  // both warps leave together
         ok = false;
         break;
       }
-      tc_fence_after();
-      float sv[TK];
-      {
-        uint32_t u[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(tl + (uint32_t)(j & 1) * TK + 16 * c, u[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) sv[16 * c + i] = __uint_as_float(u[c][i]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sfree[j & 1]);
-      const int k0 = j * TK;
-      // a tile below the CTA's first row and inside the sequence needs no mask
-      const bool full = k0 + TK - 1 <= start + q0 && k0 + TK <= n_keys;
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < TK; ++c) {
-        float v = sv[c] * p.scale_log2;
-        if (!full && (k0 + c > qpos || k0 + c >= n_keys)) v = -INFINITY;
-        sv[c] = v;
-        mt = fmaxf(mt, v);
-      }
+      const float mt = fmaxf(xch[xb * 128 + r], xch[(xb + 1) * 128 + r]) * c;  // row tile max, log2
       // O += P_{j-1} V_{j-1} has completed: O may be rescaled, P overwritten
       if (j >= 1) {
-        if (!mbar_wait(odone, (j - 1) & 1, p.status)) {
-          ok = false;
+        if (!__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, p.status))) {
+          ok = false;  // the next tile's flags take both warps out of the loop
           ctl[1] = 1;
-          break;
+          continue;
         }
         tc_fence_after();
       }
       const float m_new = fmaxf(m_used, mt);
       const bool need = m_new > m_used + kRescaleLog2;  // also the first finite max
-      const float f = m_used == -INFINITY ? 0.f : exp2f(m_used - m_new);
-      if (__any_sync(0xffffffffu, need && j > 0)) {  // rescale this warp's O rows
+      const float f = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
+      if (__any_sync(0xffffffffu, need && j > 0)) {  // rescale this thread's 64 O dims
         const float fo = need ? f : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int q = 0; q < 4; ++q) {
           uint32_t u[16];
-          tmem_ld16(tl + O_COL + 16 * c, u);
+          const uint32_t oc = O_COL + 64u * grp + 16u * q;
+          tmem_ld16(tl + oc, u);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * fo);
-          tmem_st16(tl + O_COL + 16 * c, u);
+          tmem_st16(tl + oc, u);
         }
         tmem_st_wait();
       }
@@ -355,34 +395,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         l *= f;
         m_used = m_new;
       }
-      float ls = 0.f;
       const float mu = m_used == -INFINITY ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < TK; ++c) {
-        const float e = exp2f(sv[c] - mu);  // exp2(-inf) = 0 for masked keys
-        sv[c] = e;
-        ls += e;
+      for (int i = 0; i < 32; ++i) {
+        const float e = ex2(fmaf(sv[i], c, -mu));  // masked keys: -inf -> 0
+        sv[i] = e;
+        ls[i & 3] += e;
       }
-      l += ls;
-      const int nvalid = min(TK, n_keys - k0);
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      const int nvalid = min(TK, n_keys - j * TK);
       if (nvalid < TK) {
         // V rows past the last key may hold anything (P is 0 there, but
         // 0 * NaN is not): zero them before the MMA reads the tile
         uint8_t* vt = smem + OFF_ST + (j % TSTAGES) * STAGE + KV_TILE;
         const int nz = (TK - nvalid) * 16;
-        for (int i = threadIdx.x - 64; i < nz; i += 128) {
+        for (int i = threadIdx.x - 64; i < nz; i += 256) {
           const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
           *reinterpret_cast<uint4*>(vt + half * KV_HALF + row * 128 + chunk * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      // P row r (and its remainder) in the 128-byte-swizzled K-major layout
+      // this thread's 32 keys of P row r (and the remainder) in the
+      // 128-byte-swizzled K-major layout: 16-byte chunks 4 grp .. 4 grp + 3
 #pragma unroll
-      for (int c8 = 0; c8 < TK / 8; ++c8) {
+      for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) split_pack(sv[8 * c8 + 2 * i], sv[8 * c8 + 2 * i + 1], hi[i], lo[i]);
-        const uint32_t a = smem_u32(pbase) + (uint32_t)r * 128u + ((uint32_t)(c8 ^ (r & 7)) << 4);
+        for (int i = 0; i < 4; ++i) split_pack(sv[8 * c4 + 2 * i], sv[8 * c4 + 2 * i + 1], hi[i], lo[i]);
+        const uint32_t a = prow + ((uint32_t)((4 * grp + c4) ^ (r & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(hi[0]), "r"(hi[1]),
                      "r"(hi[2]), "r"(hi[3])
                      : "memory");
@@ -396,27 +437,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(pready);
     }
-    // ---- epilogue: O / l for this thread's row
-    if (ok && !ctl[1] && mbar_wait(odone, (n_kt - 1) & 1, p.status)) {
+    // ---- epilogue: this thread's 64 dims of O / l (l = both groups' halves)
+    const bool done = ok && !ctl[1] && mbar_wait(odone, (n_kt - 1) & 1, p.status);
+    xch[(4 + grp) * 128 + r] = l;
+    pair_bar(quad);
+    if (done && !ctl[1]) {
       tc_fence_after();
-      const float inv = l > 0.f ? p.v_scale / l : 0.f;
+      const float lt = xch[4 * 128 + r] + xch[5 * 128 + r];
+      const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
       const bool row_ok = qrow < n_b && rowbase + qrow < p.n_rows;
-      bf16* dst = p.out + (size_t)(rowbase + qrow) * p.n_q * 128 + (size_t)h * 128;
+      bf16* dst = p.out + (size_t)(rowbase + qrow) * p.n_q * 128 + (size_t)h * 128 + 64 * grp;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t u[16];
-        tmem_ld16(tl + O_COL + 16 * c, u);
+        tmem_ld16(tl + O_COL + 64u * grp + 16u * q, u);
         tmem_ld_wait();
         uint32_t hi[8], lo[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           split_pack(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv, hi[i], lo[i]);
         if (row_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * q);
           d4[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           d4[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
           if (p.out_lo) {
-            uint4* l4 = reinterpret_cast<uint4*>(dst + 16 * c + p.out_lo);
+            uint4* l4 = reinterpret_cast<uint4*>(dst + 16 * q + p.out_lo);
             l4[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             l4[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
           }
