@@ -52,15 +52,18 @@ constexpr uint32_t STAGE = 2 * KV_TILE;    // K tile then V tile: 32 KB
 constexpr uint32_t Q_HALF = TQ * 128;      // 128 rows x 64 dims: 16 KB
 constexpr uint32_t Q_TILE = 2 * Q_HALF;    // 32 KB; the remainder tile follows
 constexpr uint32_t P_TILE = TQ * 128;      // 128 rows x 64 keys: 16 KB; the remainder follows
+constexpr uint32_t P_BUF = 2 * P_TILE;     // one P buffer (hi and remainder); two alternate
 constexpr uint32_t OFF_P = 2 * Q_TILE;
-constexpr uint32_t OFF_ST = OFF_P + 2 * P_TILE;
+constexpr uint32_t OFF_ST = OFF_P + 2 * P_BUF;
 constexpr uint32_t OFF_BAR = OFF_ST + TSTAGES * STAGE;
-// exchange area of the two softmax groups: fp32 [3][2 groups][128 rows] (the
-// tile maxima, double-buffered by tile parity, then the final sums) and int
-// [2][2 groups][4 quadrants] "this warp is on track" flags
-constexpr uint32_t OFF_X = OFF_BAR + 256;
-constexpr uint32_t OFF_XOK = OFF_X + 3 * 2 * 128 * 4;
-constexpr size_t TC_SMEM = OFF_XOK + 2 * 2 * 4 * 4 + 1024;  // + alignment slack
+// exchange area of the two softmax groups: fp32 [2][2 groups][128 rows] (the
+// tile maxima, double-buffered by tile parity; after the loop the final sums
+// go to the buffer the last tile did not use) and int [2][2 groups][4
+// quadrants] "this warp is on track" flags
+constexpr uint32_t OFF_X = OFF_BAR + 128;
+constexpr uint32_t OFF_XOK = OFF_X + 2 * 2 * 128 * 4;
+constexpr size_t TC_SMEM = OFF_XOK + 2 * 2 * 4 * 4;  // the dynamic base is 1024-byte aligned (checked)
+static_assert(TC_SMEM <= 232448, "227 KB of shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 256;  // S buffers at columns 0 and 64, O at 128
 constexpr uint32_t O_COL = 128;
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more than 2^8
@@ -141,17 +144,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                            const __grid_constant__ CUtensorMap mapV,
                            const __grid_constant__ CUtensorMap mapK16,
                            const __grid_constant__ CUtensorMap mapV16, TcPreParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) flag(p.status, LLAMA_FLAG_INDEX);
+    grid_dep_wait();
+    return;
+  }
   uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* kvfull = qfull + 1;
   uint64_t* kvempty = kvfull + TSTAGES;
   uint64_t* sfull = kvempty + TSTAGES;  // [2] S_j is in tensor memory
   uint64_t* sfree = sfull + 2;          // [2] the softmax has read S_j
   uint64_t* pready = sfree + 2;         // P_j is in shared memory (O rescaled if needed)
-  uint64_t* odone = pready + 1;         // O += P_j V_j has completed
-  uint64_t* mfin = odone + 1;           // every MMA issued has completed (teardown)
+  uint64_t* odone = pready + 1;         // [2] O += P_j V_j has completed (buffer j & 1 free)
+  uint64_t* mfin = odone + 2;           // every MMA issued has completed (teardown)
   // ctl[0]: tensor-memory base address, ctl[1]: abort
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 1);
   const bool pair = p.q_lo_rows > 0;
@@ -189,7 +196,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&sfree[i], 8);
     }
     mbar_init(pready, 8);
-    mbar_init(odone, 1);
+    mbar_init(&odone[0], 1);
+    mbar_init(&odone[1], 1);
     mbar_init(mfin, 1);
     ctl[1] = 0;
     fence_mbar_init();
@@ -290,14 +298,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (ctl[1] || !mbar_wait(pready, j & 1, p.status)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + OFF_ST + (j % TSTAGES) * STAGE + KV_TILE);
+        const uint32_t pj = pa + (uint32_t)(j & 1) * P_BUF;
         for (int t = 0; t < (pair ? 2 : 1); ++t)
 #pragma unroll
           for (int kk = 0; kk < TK / 16; ++kk) {  // 16 keys per MMA
-            const uint64_t da = smem_desc_sw128(pa + t * P_TILE + kk * 32);
+            const uint64_t da = smem_desc_sw128(pj + t * P_TILE + kk * 32);
             const uint64_t db = smem_desc_sw128_mn(vb + kk * 2048, KV_HALF);
             tc_mma_f16(tmem + O_COL, da, db, id_o, (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
           }
-        tc_commit(odone);
+        tc_commit(&odone[j & 1]);
         tc_commit(&kvempty[j % TSTAGES]);
         return true;
       };
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
     float* xch = reinterpret_cast<float*>(smem + OFF_X);           // [3][2][128]
     volatile int* xok = reinterpret_cast<volatile int*>(smem + OFF_XOK);  // [2][2][4]
-    const uint32_t prow = smem_u32(smem + OFF_P) + (uint32_t)r * 128u;
+    const uint32_t prow0 = smem_u32(smem + OFF_P) + (uint32_t)r * 128u;
     const float c = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;  // m_used: the row's reference max, log2 units
     bool ok = true;
@@ -365,19 +374,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         break;
       }
       const float mt = fmaxf(xch[xb * 128 + r], xch[(xb + 1) * 128 + r]) * c;  // row tile max, log2
-      // O += P_{j-1} V_{j-1} has completed: O may be rescaled, P overwritten
-      if (j >= 1) {
-        if (!__all_sync(0xffffffffu, mbar_wait(odone, (j - 1) & 1, p.status))) {
+      // PV_j commits to odone[j & 1]; a wait below is for phase (t >> 1) of
+      // the tile t it names, and tile t - 2 was waited for one tile earlier,
+      // so the barrier is never two phases behind and parity identifies it
+      const float m_new = fmaxf(m_used, mt);
+      const bool need = m_new > m_used + kRescaleLog2;  // also the first finite max
+      const float f = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
+      const bool rescale = __any_sync(0xffffffffu, need && j > 0);
+      // the P buffer of tile j - 2 is reused; a rescale needs every earlier PV done
+      const int wt = rescale ? j - 1 : j - 2;
+      if (wt >= 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&odone[wt & 1], (wt >> 1) & 1, p.status))) {
           ok = false;  // the next tile's flags take both warps out of the loop
           ctl[1] = 1;
           continue;
         }
         tc_fence_after();
       }
-      const float m_new = fmaxf(m_used, mt);
-      const bool need = m_new > m_used + kRescaleLog2;  // also the first finite max
-      const float f = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
-      if (__any_sync(0xffffffffu, need && j > 0)) {  // rescale this thread's 64 O dims
+      if (rescale) {  // rescale this thread's 64 O dims
         const float fo = need ? f : 1.f;
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
@@ -423,7 +437,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) split_pack(sv[8 * c4 + 2 * i], sv[8 * c4 + 2 * i + 1], hi[i], lo[i]);
-        const uint32_t a = prow + ((uint32_t)((4 * grp + c4) ^ (r & 7)) << 4);
+        const uint32_t a = prow0 + (uint32_t)(j & 1) * P_BUF + ((uint32_t)((4 * grp + c4) ^ (r & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(hi[0]), "r"(hi[1]),
                      "r"(hi[2]), "r"(hi[3])
                      : "memory");
@@ -438,12 +452,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (lane == 0) mbar_arrive(pready);
     }
     // ---- epilogue: this thread's 64 dims of O / l (l = both groups' halves)
-    const bool done = ok && !ctl[1] && mbar_wait(odone, (n_kt - 1) & 1, p.status);
-    xch[(4 + grp) * 128 + r] = l;
+    const int last = n_kt - 1;
+    const bool done = ok && !ctl[1] && mbar_wait(&odone[last & 1], (last >> 1) & 1, p.status);
+    const int xs = (n_kt & 1) * 2;  // the exchange buffer the last tile did not use
+    xch[(xs + grp) * 128 + r] = l;
     pair_bar(quad);
     if (done && !ctl[1]) {
       tc_fence_after();
-      const float lt = xch[4 * 128 + r] + xch[5 * 128 + r];
+      const float lt = xch[xs * 128 + r] + xch[(xs + 1) * 128 + r];
       const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
       const bool row_ok = qrow < n_b && rowbase + qrow < p.n_rows;
       bf16* dst = p.out + (size_t)(rowbase + qrow) * p.n_q * 128 + (size_t)h * 128 + 64 * grp;
