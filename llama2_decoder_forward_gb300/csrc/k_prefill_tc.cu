@@ -6,7 +6,9 @@
 //
 // One CTA per (128 query rows, query head, sequence); 320 threads:
 //   warp 0     TMA producer: the Q tile (and its bf16 remainder rows), then
-//              K and V tiles of 64 keys into a 3-stage mbarrier ring;
+//              K and V tiles of 64 keys into two mbarrier rings (4 K slots,
+//              freed as soon as S_j is computed; 2 V slots, freed after
+//              O += P_j V_j), deep enough to cover the load latency;
 //   warp 1     tensor-memory owner and MMA issuer (one thread):
 //              S_j = Q K_j^T into one of two S buffers in tensor memory,
 //              O += P_j V_j into the O accumulator in tensor memory;
@@ -44,23 +46,24 @@ namespace {
 constexpr int TQ = 128;          // query rows per CTA: MMA M, one tensor-memory lane each
 constexpr int TK = 64;           // keys per tile
 constexpr int TSUB = 16;         // keys per box of a 16-row (paged) cache view
-constexpr int TSTAGES = 3;
+constexpr int KSTAGES = 4;  // K tiles in flight (a slot frees once S_j is computed)
+constexpr int VSTAGES = 2;  // V tiles (a slot frees once O += P_j V_j is computed)
 constexpr int TC_THREADS = 320;  // producer, MMA issuer, two softmax warpgroups
 constexpr uint32_t KV_HALF = TK * 128;     // 64 keys x 64 dims bf16: 8 KB
-constexpr uint32_t KV_TILE = 2 * KV_HALF;  // 64 keys x 128 dims: 16 KB
-constexpr uint32_t STAGE = 2 * KV_TILE;    // K tile then V tile: 32 KB
+constexpr uint32_t KV_TILE = 2 * KV_HALF;  // 64 keys x 128 dims: 16 KB (one K or V slot)
 constexpr uint32_t Q_HALF = TQ * 128;      // 128 rows x 64 dims: 16 KB
 constexpr uint32_t Q_TILE = 2 * Q_HALF;    // 32 KB; the remainder tile follows
 constexpr uint32_t P_TILE = TQ * 128;      // 128 rows x 64 keys: 16 KB; the remainder follows
 constexpr uint32_t P_BUF = 2 * P_TILE;     // one P buffer (hi and remainder); two alternate
 constexpr uint32_t OFF_P = 2 * Q_TILE;
 constexpr uint32_t OFF_ST = OFF_P + 2 * P_BUF;
-constexpr uint32_t OFF_BAR = OFF_ST + TSTAGES * STAGE;
+constexpr uint32_t OFF_V = OFF_ST + KSTAGES * KV_TILE;  // the V slots follow the K slots
+constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * KV_TILE;
 // exchange area of the two softmax groups: fp32 [2][2 groups][128 rows] (the
 // tile maxima, double-buffered by tile parity; after the loop the final sums
 // go to the buffer the last tile did not use) and int [2][2 groups][4
 // quadrants] "this warp is on track" flags
-constexpr uint32_t OFF_X = OFF_BAR + 128;
+constexpr uint32_t OFF_X = OFF_BAR + 256;  // after 21 barriers and two control words
 constexpr uint32_t OFF_XOK = OFF_X + 2 * 2 * 128 * 4;
 constexpr size_t TC_SMEM = OFF_XOK + 2 * 2 * 4 * 4;  // the dynamic base is 1024-byte aligned (checked)
 static_assert(TC_SMEM <= 232448, "227 KB of shared memory per CTA");
@@ -152,15 +155,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     return;
   }
   uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* kvfull = qfull + 1;
-  uint64_t* kvempty = kvfull + TSTAGES;
-  uint64_t* sfull = kvempty + TSTAGES;  // [2] S_j is in tensor memory
+  uint64_t* kfull = qfull + 1;
+  uint64_t* kempty = kfull + KSTAGES;
+  uint64_t* vfull = kempty + KSTAGES;
+  uint64_t* vempty = vfull + VSTAGES;
+  uint64_t* sfull = vempty + VSTAGES;  // [2] S_j is in tensor memory
   uint64_t* sfree = sfull + 2;          // [2] the softmax has read S_j
   uint64_t* pready = sfree + 2;         // P_j is in shared memory (O rescaled if needed)
   uint64_t* odone = pready + 1;         // [2] O += P_j V_j has completed (buffer j & 1 free)
   uint64_t* mfin = odone + 2;           // every MMA issued has completed (teardown)
   // ctl[0]: tensor-memory base address, ctl[1]: abort
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 1);
+  static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 1 + 2 + 1) * 8 + 8 <= OFF_X - OFF_BAR,
+                "barrier block");
   const bool pair = p.q_lo_rows > 0;
 
   grid_dep_wait();  // q, k, v come from the RoPE/append kernel
@@ -187,9 +194,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
-    for (int s = 0; s < TSTAGES; ++s) {
-      mbar_init(&kvfull[s], 1);
-      mbar_init(&kvempty[s], 1);
+    for (int s = 0; s < KSTAGES; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+    }
+    for (int s = 0; s < VSTAGES; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
@@ -225,49 +236,51 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tma_load_3d(smem + t * Q_TILE + half * Q_HALF + rb * (Q_HALF / 2), &mapQ, qfull,
                         64 * half, h, row0 + 64 * rb);
       }
-      int issued = 0;
+      // K_j then V_j for every key tile j, each into its own ring
+      int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int kt = 0; kt < n_kt; ++kt) {
-        const int s = kt % TSTAGES;
-        const uint32_t ph = (kt / TSTAGES) & 1;
-        if (!mbar_wait(&kvempty[s], ph ^ 1, p.status)) {
-          ok = false;
-          ctl[1] = 1;
-          break;
-        }
-        uint8_t* ks = smem + OFF_ST + s * STAGE;
+      for (int kt = 0; kt < n_kt && ok; ++kt) {
         const int k0 = kt * TK, nvalid = min(TK, n_keys - k0);
-        if (!p.from_cache) {
-          mbar_arrive_expect_tx(&kvfull[s], STAGE);
-          tma_load_3d(ks, &mapK, &kvfull[s], 0, g, rowbase + k0);
-          tma_load_3d(ks + KV_HALF, &mapK, &kvfull[s], 64, g, rowbase + k0);
-          tma_load_3d(ks + KV_TILE, &mapV, &kvfull[s], 0, g, rowbase + k0);
-          tma_load_3d(ks + KV_TILE + KV_HALF, &mapV, &kvfull[s], 64, g, rowbase + k0);
-        } else if (p.box_rows == TK && nvalid == TK) {  // 64 contiguous keys: one box per half
-          const int row = tc_kv_row(p, b, g, k0);
-          mbar_arrive_expect_tx(&kvfull[s], STAGE);
-          tma_load_3d(ks, &mapK, &kvfull[s], 0, row, p.layer);
-          tma_load_3d(ks + KV_HALF, &mapK, &kvfull[s], 64, row, p.layer);
-          tma_load_3d(ks + KV_TILE, &mapV, &kvfull[s], 0, row, p.layer);
-          tma_load_3d(ks + KV_TILE + KV_HALF, &mapV, &kvfull[s], 64, row, p.layer);
-        } else {  // 16-key boxes, only those holding keys of this sequence
-          const int nsub = (nvalid + TSUB - 1) / TSUB;
-          mbar_arrive_expect_tx(&kvfull[s], nsub * 4 * (TSUB * 128));
-          for (int j = 0; j < nsub; ++j) {
-            const int row = tc_kv_row(p, b, g, k0 + j * TSUB);
-            uint8_t* kd = ks + j * TSUB * 128;
-            tma_load_3d(kd, &mapK16, &kvfull[s], 0, row, p.layer);
-            tma_load_3d(kd + KV_HALF, &mapK16, &kvfull[s], 64, row, p.layer);
-            tma_load_3d(kd + KV_TILE, &mapV16, &kvfull[s], 0, row, p.layer);
-            tma_load_3d(kd + KV_TILE + KV_HALF, &mapV16, &kvfull[s], 64, row, p.layer);
+        for (int isv = 0; isv < 2; ++isv) {
+          const int ns = isv ? VSTAGES : KSTAGES;
+          const int s = kt % ns;
+          uint64_t* fb = isv ? &vfull[s] : &kfull[s];
+          if (!mbar_wait(isv ? &vempty[s] : &kempty[s], ((kt / ns) & 1) ^ 1, p.status)) {
+            ok = false;
+            ctl[1] = 1;
+            break;
           }
+          uint8_t* dst = smem + (isv ? OFF_V : OFF_ST) + s * KV_TILE;
+          const CUtensorMap* m64 = isv ? &mapV : &mapK;
+          const CUtensorMap* m16 = isv ? &mapV16 : &mapK16;
+          if (!p.from_cache) {
+            mbar_arrive_expect_tx(fb, KV_TILE);
+            tma_load_3d(dst, m64, fb, 0, g, rowbase + k0);
+            tma_load_3d(dst + KV_HALF, m64, fb, 64, g, rowbase + k0);
+          } else if (p.box_rows == TK && nvalid == TK) {  // 64 contiguous keys: one box per half
+            const int row = tc_kv_row(p, b, g, k0);
+            mbar_arrive_expect_tx(fb, KV_TILE);
+            tma_load_3d(dst, m64, fb, 0, row, p.layer);
+            tma_load_3d(dst + KV_HALF, m64, fb, 64, row, p.layer);
+          } else {  // 16-key boxes, only those holding keys of this sequence
+            const int nsub = (nvalid + TSUB - 1) / TSUB;
+            mbar_arrive_expect_tx(fb, nsub * 2 * (TSUB * 128));
+            for (int jj = 0; jj < nsub; ++jj) {
+              const int row = tc_kv_row(p, b, g, k0 + jj * TSUB);
+              tma_load_3d(dst + jj * TSUB * 128, m16, fb, 0, row, p.layer);
+              tma_load_3d(dst + KV_HALF + jj * TSUB * 128, m16, fb, 64, row, p.layer);
+            }
+          }
+          if (isv) ++v_issued;
+          else ++k_issued;
         }
-        ++issued;
       }
       mbar_wait(qfull, 0, p.status);  // no copy may still be in flight when the CTA exits
       if (!ok) {
-        for (int t = issued - 1; t >= 0 && t >= issued - TSTAGES; --t)
-          mbar_wait(&kvfull[t % TSTAGES], (t / TSTAGES) & 1, p.status);
+        for (int t = k_issued - 1; t >= 0 && t >= k_issued - KSTAGES; --t)
+          mbar_wait(&kfull[t % KSTAGES], (t / KSTAGES) & 1, p.status);
+        for (int t = v_issued - 1; t >= 0 && t >= v_issued - VSTAGES; --t)
+          mbar_wait(&vfull[t % VSTAGES], (t / VSTAGES) & 1, p.status);
       }
     }
   } else if (warp == 1) {  // -------------------------------------------- MMA issuer
@@ -277,11 +290,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t qa = smem_u32(smem), pa = smem_u32(smem + OFF_P);
       bool ok = mbar_wait(qfull, 0, p.status);
       auto issue_s = [&](int j) -> bool {
-        const int s = j % TSTAGES;
-        if (ctl[1] || !mbar_wait(&kvfull[s], (j / TSTAGES) & 1, p.status)) return false;
+        const int s = j % KSTAGES;
+        if (ctl[1] || !mbar_wait(&kfull[s], (j / KSTAGES) & 1, p.status)) return false;
         if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status)) return false;
         tc_fence_after();
-        const uint32_t kb = smem_u32(smem + OFF_ST + s * STAGE);
+        const uint32_t kb = smem_u32(smem + OFF_ST + s * KV_TILE);
         const uint32_t d = tmem + (uint32_t)(j & 1) * TK;
         for (int t = 0; t < (pair ? 2 : 1); ++t)
 #pragma unroll
@@ -292,12 +305,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc_mma_f16(d, da, db, id_s, (t > 0 || kk > 0) ? 1u : 0u);
           }
         tc_commit(&sfull[j & 1]);
+        tc_commit(&kempty[s]);
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
-        if (ctl[1] || !mbar_wait(pready, j & 1, p.status)) return false;
+        const int s = j % VSTAGES;
+        if (ctl[1] || !mbar_wait(pready, j & 1, p.status) ||
+            !mbar_wait(&vfull[s], (j / VSTAGES) & 1, p.status))
+          return false;
         tc_fence_after();
-        const uint32_t vb = smem_u32(smem + OFF_ST + (j % TSTAGES) * STAGE + KV_TILE);
+        const uint32_t vb = smem_u32(smem + OFF_V + s * KV_TILE);
         const uint32_t pj = pa + (uint32_t)(j & 1) * P_BUF;
         for (int t = 0; t < (pair ? 2 : 1); ++t)
 #pragma unroll
@@ -307,7 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc_mma_f16(tmem + O_COL, da, db, id_o, (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
           }
         tc_commit(&odone[j & 1]);
-        tc_commit(&kvempty[j % TSTAGES]);
+        tc_commit(&vempty[s]);
         return true;
       };
       for (int j = 0; ok && j < n_kt; ++j) {
@@ -421,8 +438,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int nvalid = min(TK, n_keys - j * TK);
       if (nvalid < TK) {
         // V rows past the last key may hold anything (P is 0 there, but
-        // 0 * NaN is not): zero them before the MMA reads the tile
-        uint8_t* vt = smem + OFF_ST + (j % TSTAGES) * STAGE + KV_TILE;
+        // 0 * NaN is not): zero them, once V_j has landed, before the MMA
+        // reads the tile (V_{j+2} cannot land in this slot before O += P_j V_j)
+        if (!__all_sync(0xffffffffu, mbar_wait(&vfull[j % VSTAGES], (j / VSTAGES) & 1, p.status))) {
+          ok = false;
+          ctl[1] = 1;
+          continue;
+        }
+        uint8_t* vt = smem + OFF_V + (j % VSTAGES) * KV_TILE;
         const int nz = (TK - nvalid) * 16;
         for (int i = threadIdx.x - 64; i < nz; i += 256) {
           const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
