@@ -4,11 +4,12 @@
 // GQA: query head h reads K/V head h / G), computed FlashAttention-style so
 // the T x T score matrix never leaves the SM.
 //
-// One CTA per (128 query rows, query head, sequence); 320 threads:
-//   warp 0     TMA producer: the Q tile (and its bf16 remainder rows), then
-//              K and V tiles of 64 keys into two mbarrier rings (4 K slots,
-//              freed as soon as S_j is computed; 2 V slots, freed after
-//              O += P_j V_j), deep enough to cover the load latency;
+// One CTA per (128 query rows, query head, sequence); 352 threads:
+//   warp 0     TMA producer of the Q tile (and its bf16 remainder rows) and
+//              of the K tiles (64 keys each) into a 5-slot mbarrier ring; a
+//              slot frees as soon as S_j = Q K_j^T is computed;
+//   warp 10    TMA producer of the V tiles into a 3-slot ring; a slot frees
+//              once O += P_j V_j is computed;
 //   warp 1     tensor-memory owner and MMA issuer (one thread):
 //              S_j = Q K_j^T into one of two S buffers in tensor memory,
 //              O += P_j V_j into the O accumulator in tensor memory;
@@ -18,22 +19,30 @@
 //              masks, exchanges the row's tile maximum with its partner in the
 //              other group through shared memory, keeps the running max and
 //              its half of the sum, writes its half of P_j (bf16, as a hi/lo
-//              pair when Q is one) to shared memory in the MMA operand layout,
-//              rescales and at the end normalises and stores its 64 of the
-//              row's 128 output dims.
-// The MMA of S_{j+1} runs while the softmax works on S_j. The running max is
-// applied lazily: O and the sum are rescaled (in tensor memory) only when a
+//              pair when Q is one) into tensor memory, rescales O when needed
+//              and at the end normalises and stores its 64 of the row's 128
+//              output dims.
+// Q (copied once from the TMA tile by the softmax threads) and P are the MMAs'
+// A operands in tensor memory: shared memory only feeds K and V to the tensor
+// cores, whose operand reads from shared memory bound the S and PV products
+// otherwise. The MMA of S_{j+1} runs while the softmax works on S_j; P has two
+// buffers so the softmax of a tile does not wait for the previous tile's PV.
+// The running max is applied lazily: O and the sum are rescaled only when a
 // row's max grows by more than 2^8, otherwise P keeps the older max, which
 // leaves the normalised result unchanged. Key tiles past the diagonal are
 // skipped; the diagonal tile and the last partial tile are masked per key.
 //
-// Operand layouts (all 128-byte swizzled, as TMA writes them):
-//   Q  A operand, K-major: [128 rows][64 dims] per dim half;
-//   K  B operand, K-major: [64 keys][64 dims] per dim half;
-//   P  A operand, K-major: [128 rows][64 keys];
-//   V  B operand, MN-major: [64 keys][64 dims] per dim half (the dims are the
-//      MMA's N, contiguous in memory); 8-key groups 1024 bytes apart, the two
-//      dim halves KV_HALF bytes apart.
+// Operand layouts:
+//   Q  A operand in tensor memory: lane = query row, column c holds dims
+//      2c, 2c+1 (bf16 pair, lower dim in the low half); the remainder rows
+//      64 columns further;
+//   K  B operand in shared memory, K-major, 128-byte swizzled as TMA writes
+//      it: [64 keys][64 dims] per dim half;
+//   P  A operand in tensor memory: column c of a buffer holds keys 2c, 2c+1;
+//      the remainder 32 columns further;
+//   V  B operand in shared memory, MN-major: [64 keys][64 dims] per dim half
+//      (the dims are the MMA's N, contiguous in memory); 8-key groups 1024
+//      bytes apart, the two dim halves KV_HALF bytes apart.
 #include <algorithm>
 
 #include "common.cuh"
@@ -46,29 +55,30 @@ namespace {
 constexpr int TQ = 128;          // query rows per CTA: MMA M, one tensor-memory lane each
 constexpr int TK = 64;           // keys per tile
 constexpr int TSUB = 16;         // keys per box of a 16-row (paged) cache view
-constexpr int KSTAGES = 4;  // K tiles in flight (a slot frees once S_j is computed)
-constexpr int VSTAGES = 2;  // V tiles (a slot frees once O += P_j V_j is computed)
-constexpr int TC_THREADS = 320;  // producer, MMA issuer, two softmax warpgroups
+constexpr int KSTAGES = 5;       // K tiles in flight
+constexpr int VSTAGES = 3;       // V tiles in flight
+constexpr int TC_THREADS = 352;  // Q/K producer, MMA issuer, two softmax warpgroups, V producer
+constexpr int V_WARP = 10;
 constexpr uint32_t KV_HALF = TK * 128;     // 64 keys x 64 dims bf16: 8 KB
 constexpr uint32_t KV_TILE = 2 * KV_HALF;  // 64 keys x 128 dims: 16 KB (one K or V slot)
 constexpr uint32_t Q_HALF = TQ * 128;      // 128 rows x 64 dims: 16 KB
 constexpr uint32_t Q_TILE = 2 * Q_HALF;    // 32 KB; the remainder tile follows
-constexpr uint32_t P_TILE = TQ * 128;      // 128 rows x 64 keys: 16 KB; the remainder follows
-constexpr uint32_t P_BUF = 2 * P_TILE;     // one P buffer (hi and remainder); two alternate
-constexpr uint32_t OFF_P = 2 * Q_TILE;
-constexpr uint32_t OFF_ST = OFF_P + 2 * P_BUF;
-constexpr uint32_t OFF_V = OFF_ST + KSTAGES * KV_TILE;  // the V slots follow the K slots
+constexpr uint32_t OFF_K = 2 * Q_TILE;
+constexpr uint32_t OFF_V = OFF_K + KSTAGES * KV_TILE;
 constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * KV_TILE;
 // exchange area of the two softmax groups: fp32 [2][2 groups][128 rows] (the
 // tile maxima, double-buffered by tile parity; after the loop the final sums
 // go to the buffer the last tile did not use) and int [2][2 groups][4
 // quadrants] "this warp is on track" flags
-constexpr uint32_t OFF_X = OFF_BAR + 256;  // after 21 barriers and two control words
+constexpr uint32_t OFF_X = OFF_BAR + 256;
 constexpr uint32_t OFF_XOK = OFF_X + 2 * 2 * 128 * 4;
 constexpr size_t TC_SMEM = OFF_XOK + 2 * 2 * 4 * 4;  // the dynamic base is 1024-byte aligned (checked)
 static_assert(TC_SMEM <= 232448, "227 KB of shared memory per CTA");
-constexpr uint32_t TMEM_COLS = 256;  // S buffers at columns 0 and 64, O at 128
+// tensor-memory columns: S buffers, the O accumulator, Q (hi, remainder), P buffers
+constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 128;
+constexpr uint32_t Q_COL = 256;  // 64 columns hi, then 64 columns remainder
+constexpr uint32_t P_COL = 384;  // buffer b at P_COL + 64 b: 32 columns hi, 32 remainder
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more than 2^8
 
 struct TcPreParams {
@@ -97,6 +107,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t 
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate):
+// the A operand is read from tensor memory (row m = lane m).
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // 32 lanes x 32 bits, 16 consecutive columns per thread, registers -> tensor memory.
@@ -141,6 +163,54 @@ __device__ __forceinline__ int tc_kv_row(const TcPreParams& p, int b, int g, int
   return (page * p.n_kv + g) * p.page_size + (k0 % p.page_size);
 }
 
+// K or V tile of keys k0 .. k0 + nvalid - 1 into ring slot `dst`, completing
+// on barrier fb.
+__device__ __forceinline__ void load_kv_tile(const TcPreParams& p, const CUtensorMap* m64,
+                                             const CUtensorMap* m16, uint8_t* dst, uint64_t* fb,
+                                             int b, int g, int rowbase, int k0, int nvalid) {
+  if (!p.from_cache) {
+    mbar_arrive_expect_tx(fb, KV_TILE);
+    tma_load_3d(dst, m64, fb, 0, g, rowbase + k0);
+    tma_load_3d(dst + KV_HALF, m64, fb, 64, g, rowbase + k0);
+  } else if (p.box_rows == TK && nvalid == TK) {  // 64 contiguous keys: one box per half
+    const int row = tc_kv_row(p, b, g, k0);
+    mbar_arrive_expect_tx(fb, KV_TILE);
+    tma_load_3d(dst, m64, fb, 0, row, p.layer);
+    tma_load_3d(dst + KV_HALF, m64, fb, 64, row, p.layer);
+  } else {  // 16-key boxes, only those holding keys of this sequence
+    const int nsub = (nvalid + TSUB - 1) / TSUB;
+    mbar_arrive_expect_tx(fb, nsub * 2 * (TSUB * 128));
+    for (int jj = 0; jj < nsub; ++jj) {
+      const int row = tc_kv_row(p, b, g, k0 + jj * TSUB);
+      tma_load_3d(dst + jj * TSUB * 128, m16, fb, 0, row, p.layer);
+      tma_load_3d(dst + KV_HALF + jj * TSUB * 128, m16, fb, 64, row, p.layer);
+    }
+  }
+}
+
+// A producer's ring: every tile's K (or V) into slot kt % NS once the
+// consumer freed it; on an abort the copies in flight are waited for.
+template <int NS>
+__device__ __forceinline__ void produce_ring(const TcPreParams& p, const CUtensorMap* m64,
+                                             const CUtensorMap* m16, uint8_t* slots, uint64_t* full,
+                                             uint64_t* empty, volatile uint32_t* ctl, int n_kt,
+                                             int n_keys, int b, int g, int rowbase) {
+  int issued = 0;
+  for (int kt = 0; kt < n_kt; ++kt) {
+    const int s = kt % NS;
+    if (ctl[1] || !mbar_wait(&empty[s], ((kt / NS) & 1) ^ 1, p.status)) {
+      ctl[1] = 1;
+      for (int t = issued - 1; t >= 0 && t >= issued - NS; --t)
+        mbar_wait(&full[t % NS], (t / NS) & 1, p.status);
+      return;
+    }
+    const int k0 = kt * TK;
+    load_kv_tile(p, m64, m16, slots + s * KV_TILE, &full[s], b, g, rowbase, k0,
+                 min(TK, n_keys - k0));
+    ++issued;
+  }
+}
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                            const __grid_constant__ CUtensorMap mapK,
@@ -154,19 +224,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     grid_dep_wait();
     return;
   }
-  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* kfull = qfull + 1;
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // Q tile in shared memory
+  uint64_t* qtm = qfull + 1;             // Q copied into tensor memory (8 softmax warps)
+  uint64_t* kfull = qtm + 1;
   uint64_t* kempty = kfull + KSTAGES;
   uint64_t* vfull = kempty + KSTAGES;
   uint64_t* vempty = vfull + VSTAGES;
   uint64_t* sfull = vempty + VSTAGES;  // [2] S_j is in tensor memory
-  uint64_t* sfree = sfull + 2;          // [2] the softmax has read S_j
-  uint64_t* pready = sfree + 2;         // P_j is in shared memory (O rescaled if needed)
-  uint64_t* odone = pready + 1;         // [2] O += P_j V_j has completed (buffer j & 1 free)
-  uint64_t* mfin = odone + 2;           // every MMA issued has completed (teardown)
+  uint64_t* sfree = sfull + 2;         // [2] the softmax has read S_j
+  uint64_t* pready = sfree + 2;        // P_j is in tensor memory (O rescaled if needed)
+  uint64_t* odone = pready + 1;        // [2] O += P_j V_j has completed (P buffer j & 1 free)
+  uint64_t* mfin = odone + 2;          // every MMA issued has completed (teardown)
   // ctl[0]: tensor-memory base address, ctl[1]: abort
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 1);
-  static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 1 + 2 + 1) * 8 + 8 <= OFF_X - OFF_BAR,
+  static_assert((2 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 1 + 2 + 1) * 8 + 8 <= OFF_X - OFF_BAR,
                 "barrier block");
   const bool pair = p.q_lo_rows > 0;
 
@@ -194,6 +265,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
+    mbar_init(qtm, 8);
     for (int s = 0; s < KSTAGES; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
@@ -205,10 +277,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
       mbar_init(&sfree[i], 8);
+      mbar_init(&odone[i], 1);
     }
     mbar_init(pready, 8);
-    mbar_init(&odone[0], 1);
-    mbar_init(&odone[1], 1);
     mbar_init(mfin, 1);
     ctl[1] = 0;
     fence_mbar_init();
@@ -219,15 +290,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = ctl[0];
 
-  if (warp == 0) {  // ------------------------------------------------ TMA producer
+  if (warp == 0) {  // ----------------------------------------------- Q and K producer
     if (lane == 0) {
       tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(&mapK);
-      tma_prefetch_desc(&mapV);
-      if (p.from_cache) {
-        tma_prefetch_desc(&mapK16);
-        tma_prefetch_desc(&mapV16);
-      }
+      if (p.from_cache) tma_prefetch_desc(&mapK16);
       mbar_arrive_expect_tx(qfull, pair ? 2 * Q_TILE : Q_TILE);
       for (int t = 0; t < (pair ? 2 : 1); ++t) {
         const int row0 = (t ? p.q_lo_rows : 0) + rowbase + q0;
@@ -236,73 +303,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tma_load_3d(smem + t * Q_TILE + half * Q_HALF + rb * (Q_HALF / 2), &mapQ, qfull,
                         64 * half, h, row0 + 64 * rb);
       }
-      // K_j then V_j for every key tile j, each into its own ring
-      int k_issued = 0, v_issued = 0;
-      bool ok = true;
-      for (int kt = 0; kt < n_kt && ok; ++kt) {
-        const int k0 = kt * TK, nvalid = min(TK, n_keys - k0);
-        for (int isv = 0; isv < 2; ++isv) {
-          const int ns = isv ? VSTAGES : KSTAGES;
-          const int s = kt % ns;
-          uint64_t* fb = isv ? &vfull[s] : &kfull[s];
-          if (!mbar_wait(isv ? &vempty[s] : &kempty[s], ((kt / ns) & 1) ^ 1, p.status)) {
-            ok = false;
-            ctl[1] = 1;
-            break;
-          }
-          uint8_t* dst = smem + (isv ? OFF_V : OFF_ST) + s * KV_TILE;
-          const CUtensorMap* m64 = isv ? &mapV : &mapK;
-          const CUtensorMap* m16 = isv ? &mapV16 : &mapK16;
-          if (!p.from_cache) {
-            mbar_arrive_expect_tx(fb, KV_TILE);
-            tma_load_3d(dst, m64, fb, 0, g, rowbase + k0);
-            tma_load_3d(dst + KV_HALF, m64, fb, 64, g, rowbase + k0);
-          } else if (p.box_rows == TK && nvalid == TK) {  // 64 contiguous keys: one box per half
-            const int row = tc_kv_row(p, b, g, k0);
-            mbar_arrive_expect_tx(fb, KV_TILE);
-            tma_load_3d(dst, m64, fb, 0, row, p.layer);
-            tma_load_3d(dst + KV_HALF, m64, fb, 64, row, p.layer);
-          } else {  // 16-key boxes, only those holding keys of this sequence
-            const int nsub = (nvalid + TSUB - 1) / TSUB;
-            mbar_arrive_expect_tx(fb, nsub * 2 * (TSUB * 128));
-            for (int jj = 0; jj < nsub; ++jj) {
-              const int row = tc_kv_row(p, b, g, k0 + jj * TSUB);
-              tma_load_3d(dst + jj * TSUB * 128, m16, fb, 0, row, p.layer);
-              tma_load_3d(dst + KV_HALF + jj * TSUB * 128, m16, fb, 64, row, p.layer);
-            }
-          }
-          if (isv) ++v_issued;
-          else ++k_issued;
-        }
-      }
+      produce_ring<KSTAGES>(p, &mapK, &mapK16, smem + OFF_K, kfull, kempty, ctl, n_kt, n_keys, b,
+                            g, rowbase);
       mbar_wait(qfull, 0, p.status);  // no copy may still be in flight when the CTA exits
-      if (!ok) {
-        for (int t = k_issued - 1; t >= 0 && t >= k_issued - KSTAGES; --t)
-          mbar_wait(&kfull[t % KSTAGES], (t / KSTAGES) & 1, p.status);
-        for (int t = v_issued - 1; t >= 0 && t >= v_issued - VSTAGES; --t)
-          mbar_wait(&vfull[t % VSTAGES], (t / VSTAGES) & 1, p.status);
-      }
+    }
+  } else if (warp == V_WARP) {  // --------------------------------------- V producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapV);
+      if (p.from_cache) tma_prefetch_desc(&mapV16);
+      produce_ring<VSTAGES>(p, &mapV, &mapV16, smem + OFF_V, vfull, vempty, ctl, n_kt, n_keys, b,
+                            g, rowbase);
     }
   } else if (warp == 1) {  // -------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(TQ, TK);
       const uint32_t id_o = idesc_bf16_f32(TQ, 128) | (1u << 16);  // B (V) MN-major
-      const uint32_t qa = smem_u32(smem), pa = smem_u32(smem + OFF_P);
-      bool ok = mbar_wait(qfull, 0, p.status);
+      bool ok = mbar_wait(qtm, 0, p.status);
       auto issue_s = [&](int j) -> bool {
         const int s = j % KSTAGES;
         if (ctl[1] || !mbar_wait(&kfull[s], (j / KSTAGES) & 1, p.status)) return false;
         if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status)) return false;
         tc_fence_after();
-        const uint32_t kb = smem_u32(smem + OFF_ST + s * KV_TILE);
+        const uint32_t kb = smem_u32(smem + OFF_K + s * KV_TILE);
         const uint32_t d = tmem + (uint32_t)(j & 1) * TK;
         for (int t = 0; t < (pair ? 2 : 1); ++t)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // 16 dims per MMA
-            const uint32_t off = (uint32_t)(kk & 3) * 32;  // 32 bytes along K within a swizzle row
-            const uint64_t da = smem_desc_sw128(qa + t * Q_TILE + (kk >> 2) * Q_HALF + off);
-            const uint64_t db = smem_desc_sw128(kb + (kk >> 2) * KV_HALF + off);
-            tc_mma_f16(d, da, db, id_s, (t > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {  // 16 dims per MMA: 8 Q columns
+            const uint64_t db = smem_desc_sw128(kb + (kk >> 2) * KV_HALF + (kk & 3) * 32);
+            tc_mma_f16_ts(d, tmem + Q_COL + 64u * t + 8u * kk, db, id_s,
+                          (t > 0 || kk > 0) ? 1u : 0u);
           }
         tc_commit(&sfull[j & 1]);
         tc_commit(&kempty[s]);
@@ -315,13 +344,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + OFF_V + s * KV_TILE);
-        const uint32_t pj = pa + (uint32_t)(j & 1) * P_BUF;
+        const uint32_t pc = tmem + P_COL + 64u * (uint32_t)(j & 1);
         for (int t = 0; t < (pair ? 2 : 1); ++t)
 #pragma unroll
-          for (int kk = 0; kk < TK / 16; ++kk) {  // 16 keys per MMA
-            const uint64_t da = smem_desc_sw128(pj + t * P_TILE + kk * 32);
+          for (int kk = 0; kk < TK / 16; ++kk) {  // 16 keys per MMA: 8 P columns
             const uint64_t db = smem_desc_sw128_mn(vb + kk * 2048, KV_HALF);
-            tc_mma_f16(tmem + O_COL, da, db, id_o, (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_f16_ts(tmem + O_COL, pc + 32u * t + 8u * kk, db, id_o,
+                          (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
           }
         tc_commit(&odone[j & 1]);
         tc_commit(&vempty[s]);
@@ -343,12 +372,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int qrow = q0 + r;
     const int qpos = start + qrow;
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-    float* xch = reinterpret_cast<float*>(smem + OFF_X);           // [3][2][128]
+    float* xch = reinterpret_cast<float*>(smem + OFF_X);                  // [2][2][128]
     volatile int* xok = reinterpret_cast<volatile int*>(smem + OFF_XOK);  // [2][2][4]
-    const uint32_t prow0 = smem_u32(smem + OFF_P) + (uint32_t)r * 128u;
     const float c = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;  // m_used: the row's reference max, log2 units
     bool ok = true;
+    {  // Q row r (group 0) or its remainder (group 1) into tensor memory
+      const bool qok = __all_sync(0xffffffffu, mbar_wait(qfull, 0, p.status));
+      if (qok && (grp == 0 || pair)) {
+        const uint32_t qs = smem_u32(smem + grp * Q_TILE) + (uint32_t)r * 128u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // columns 16q .. 16q+15: dim half q/2, chunks 4(q&1)..+3
+          uint32_t u[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t a =
+                qs + (q >> 1) * Q_HALF + ((uint32_t)((4 * (q & 1) + i) ^ (r & 7)) << 4);
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(u[4 * i]), "=r"(u[4 * i + 1]), "=r"(u[4 * i + 2]), "=r"(u[4 * i + 3])
+                         : "r"(a));
+          }
+          tmem_st16(tl + Q_COL + 64u * grp + 16u * q, u);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qtm);
+      if (!qok) ok = false;
+    }
     for (int j = 0; j < n_kt; ++j) {
       const bool good =
           __all_sync(0xffffffffu, ok && !ctl[1] && mbar_wait(&sfull[j & 1], (j >> 1) & 1, p.status));
@@ -420,7 +472,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * fo);
           tmem_st16(tl + oc, u);
         }
-        tmem_st_wait();
       }
       if (need) {
         l *= f;
@@ -439,7 +490,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (nvalid < TK) {
         // V rows past the last key may hold anything (P is 0 there, but
         // 0 * NaN is not): zero them, once V_j has landed, before the MMA
-        // reads the tile (V_{j+2} cannot land in this slot before O += P_j V_j)
+        // reads the tile (V_{j+3} cannot land in this slot before O += P_j V_j)
         if (!__all_sync(0xffffffffu, mbar_wait(&vfull[j % VSTAGES], (j / VSTAGES) & 1, p.status))) {
           ok = false;
           ctl[1] = 1;
@@ -452,24 +503,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           *reinterpret_cast<uint4*>(vt + half * KV_HALF + row * 128 + chunk * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();  // the MMA reads V through the async proxy
       }
-      // this thread's 32 keys of P row r (and the remainder) in the
-      // 128-byte-swizzled K-major layout: 16-byte chunks 4 grp .. 4 grp + 3
+      {  // this thread's 32 keys of P row r (and the remainder) into tensor memory
+        uint32_t ph[16], pl[16];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) split_pack(sv[8 * c4 + 2 * i], sv[8 * c4 + 2 * i + 1], hi[i], lo[i]);
-        const uint32_t a = prow0 + (uint32_t)(j & 1) * P_BUF + ((uint32_t)((4 * grp + c4) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(hi[0]), "r"(hi[1]),
-                     "r"(hi[2]), "r"(hi[3])
-                     : "memory");
-        if (pair)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + P_TILE), "r"(lo[0]),
-                       "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
-                       : "memory");
+        for (int i = 0; i < 16; ++i) split_pack(sv[2 * i], sv[2 * i + 1], ph[i], pl[i]);
+        const uint32_t pc = tl + P_COL + 64u * (uint32_t)(j & 1) + 16u * grp;
+        tmem_st16(pc, ph);
+        if (pair) tmem_st16(pc + 32, pl);
       }
-      fence_proxy_async_smem();  // the MMA reads P (and the zeroed V rows) through the async proxy
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(pready);
@@ -494,7 +538,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint32_t hi[8], lo[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          split_pack(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv, hi[i], lo[i]);
+          split_pack(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv, hi[i],
+                     lo[i]);
         if (row_ok) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * q);
           d4[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
