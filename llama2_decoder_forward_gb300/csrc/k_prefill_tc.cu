@@ -318,21 +318,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(TQ, TK);
       const uint32_t id_o = idesc_bf16_f32(TQ, 128) | (1u << 16);  // B (V) MN-major
+      // descriptors of K slot 0 and V slot 0; a slot, a dim half or a K step
+      // moves the start-address field (address / 16) by a constant, so the
+      // issue loop is a few adds per MMA (issuing bounds these small MMAs)
+      const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_K));
+      const uint64_t vdesc0 = smem_desc_sw128_mn(smem_u32(smem + OFF_V), KV_HALF);
+      const uint32_t qcol = tmem + Q_COL;
       bool ok = mbar_wait(qtm, 0, p.status);
       auto issue_s = [&](int j) -> bool {
         const int s = j % KSTAGES;
         if (ctl[1] || !mbar_wait(&kfull[s], (j / KSTAGES) & 1, p.status)) return false;
         if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status)) return false;
         tc_fence_after();
-        const uint32_t kb = smem_u32(smem + OFF_K + s * KV_TILE);
+        const uint64_t kd = kdesc0 + (uint64_t)(s * (KV_TILE >> 4));
         const uint32_t d = tmem + (uint32_t)(j & 1) * TK;
-        for (int t = 0; t < (pair ? 2 : 1); ++t)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // 16 dims per MMA: 8 Q columns
-            const uint64_t db = smem_desc_sw128(kb + (kk >> 2) * KV_HALF + (kk & 3) * 32);
-            tc_mma_f16_ts(d, tmem + Q_COL + 64u * t + 8u * kk, db, id_s,
-                          (t > 0 || kk > 0) ? 1u : 0u);
-          }
+        for (int kk = 0; kk < 8; ++kk)  // 16 dims per MMA: 8 Q columns, 32 bytes of K rows
+          tc_mma_f16_ts(d, qcol + 8u * kk, kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16, id_s,
+                        kk > 0 ? 1u : 0u);
+        if (pair)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_f16_ts(d, qcol + 64u + 8u * kk, kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16,
+                          id_s, 1u);
         tc_commit(&sfull[j & 1]);
         tc_commit(&kempty[s]);
         return true;
@@ -343,15 +351,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             !mbar_wait(&vfull[s], (j / VSTAGES) & 1, p.status))
           return false;
         tc_fence_after();
-        const uint32_t vb = smem_u32(smem + OFF_V + s * KV_TILE);
+        const uint64_t vd = vdesc0 + (uint64_t)(s * (KV_TILE >> 4));
         const uint32_t pc = tmem + P_COL + 64u * (uint32_t)(j & 1);
-        for (int t = 0; t < (pair ? 2 : 1); ++t)
+        const uint32_t oc = tmem + O_COL;
 #pragma unroll
-          for (int kk = 0; kk < TK / 16; ++kk) {  // 16 keys per MMA: 8 P columns
-            const uint64_t db = smem_desc_sw128_mn(vb + kk * 2048, KV_HALF);
-            tc_mma_f16_ts(tmem + O_COL, pc + 32u * t + 8u * kk, db, id_o,
-                          (j > 0 || t > 0 || kk > 0) ? 1u : 0u);
-          }
+        for (int kk = 0; kk < TK / 16; ++kk)  // 16 keys per MMA: 8 P columns, two 8-key groups of V
+          tc_mma_f16_ts(oc, pc + 8u * kk, vd + kk * (2048 / 16), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        if (pair)
+#pragma unroll
+          for (int kk = 0; kk < TK / 16; ++kk)
+            tc_mma_f16_ts(oc, pc + 32u + 8u * kk, vd + kk * (2048 / 16), id_o, 1u);
         tc_commit(&odone[j & 1]);
         tc_commit(&vempty[s]);
         return true;
