@@ -37,6 +37,7 @@ constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int GEMM_THREADS = 192;
 constexpr int kMaxDynSmem = 232448;  // 227 KB per CTA
+constexpr int kRasterGroup = 16;     // activation tiles a group of consecutive CTAs shares
 
 struct TcParams {
   RopeAppendArgs rope;  // kEpiRope only
@@ -321,7 +322,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   float* scl = reinterpret_cast<float*>(bar_block + 256 + (EPI == kEpiRope ? 16 * p.ncol : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
+  const int split = blockIdx.z;
+  // Tile order (no K split): CTAs run in launch order, so consecutive ones
+  // take kRasterGroup activation tiles of one weight tile, then the same
+  // activation tiles of the next weight tile. The activations and weights the
+  // running CTAs read then stay in L2 instead of every wave streaming all the
+  // activation tiles from HBM again.
+  int tile_n = blockIdx.x, tile_m = blockIdx.y;
+  if (p.splits == 1 && gridDim.x > 1) {
+    const int id = blockIdx.y * gridDim.x + blockIdx.x;
+    const int per_group = kRasterGroup * (int)gridDim.y;
+    const int g0 = (id / per_group) * kRasterGroup;
+    const int gn = min(kRasterGroup, (int)gridDim.x - g0);
+    const int r = id - (id / per_group) * per_group;
+    tile_n = g0 + r % gn;
+    tile_m = r / gn;
+  }
 
   const int kb0 = (int)(((long long)split * p.num_kb) / p.splits);
   const int kb1 = (int)(((long long)(split + 1) * p.num_kb) / p.splits);
