@@ -128,10 +128,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Wait for the phase with the given parity to complete. Gives up after
 // limit_ns (kWaitLimitNs by default), flags LLAMA_FLAG_WAIT_TIMEOUT and
-// returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                          uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+// returns false. The timed loop is a separate, non-inlined function: kept
+// inline, the compiler may read the global timer on the fast path as well,
+// which makes a wait on an already completed phase cost about ten times a
+// bare try_wait.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                            uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -140,6 +142,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
+  return mbar_wait_slow(bar, parity, status, limit_ns);
 }
 
 // ------------------------------------------------------------------ TMA (bulk tensor copies)

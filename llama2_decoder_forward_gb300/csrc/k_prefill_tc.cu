@@ -4,15 +4,18 @@
 // GQA: query head h reads K/V head h / G), computed FlashAttention-style so
 // the T x T score matrix never leaves the SM.
 //
-// One CTA per (128 query rows, query head, sequence); 352 threads:
+// One CTA per (128 query rows, query head, sequence); 384 threads:
 //   warp 0     TMA producer of the Q tile (and its bf16 remainder rows) and
 //              of the K tiles (64 keys each) into a 5-slot mbarrier ring; a
 //              slot frees as soon as S_j = Q K_j^T is computed;
 //   warp 10    TMA producer of the V tiles into a 3-slot ring; a slot frees
 //              once O += P_j V_j is computed;
-//   warp 1     tensor-memory owner and MMA issuer (one thread):
-//              S_j = Q K_j^T into one of two S buffers in tensor memory,
-//              O += P_j V_j into the O accumulator in tensor memory;
+//   warp 1     tensor-memory owner; one thread issues the score MMAs
+//              S_j = Q K_j^T into one of two S buffers in tensor memory;
+//   warp 11    one thread issues O += P_j V_j into the O accumulator in
+//              tensor memory (two issuing threads, because issuing and the
+//              barrier waits between MMA groups, not the tensor pipe, bound
+//              a single thread at these small MMA shapes);
 //   warps 2-9  softmax, two groups of four warps: a thread of group k owns
 //              one query row (its tensor-memory lane) and keys 32k .. 32k+31
 //              of every tile. It reads its half of S_j with tcgen05.ld,
@@ -57,8 +60,9 @@ constexpr int TK = 64;           // keys per tile
 constexpr int TSUB = 16;         // keys per box of a 16-row (paged) cache view
 constexpr int KSTAGES = 5;       // K tiles in flight
 constexpr int VSTAGES = 3;       // V tiles in flight
-constexpr int TC_THREADS = 352;  // Q/K producer, MMA issuer, two softmax warpgroups, V producer
+constexpr int TC_THREADS = 384;  // Q/K producer, S issuer, two softmax warpgroups, V producer, PV issuer
 constexpr int V_WARP = 10;
+constexpr int PV_WARP = 11;
 constexpr uint32_t KV_HALF = TK * 128;     // 64 keys x 64 dims bf16: 8 KB
 constexpr uint32_t KV_TILE = 2 * KV_HALF;  // 64 keys x 128 dims: 16 KB (one K or V slot)
 constexpr uint32_t Q_HALF = TQ * 128;      // 128 rows x 64 dims: 16 KB
@@ -234,10 +238,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* sfree = sfull + 2;         // [2] the softmax has read S_j
   uint64_t* pready = sfree + 2;        // P_j is in tensor memory (O rescaled if needed)
   uint64_t* odone = pready + 1;        // [2] O += P_j V_j has completed (P buffer j & 1 free)
-  uint64_t* mfin = odone + 2;          // every MMA issued has completed (teardown)
+  uint64_t* mfin = odone + 2;          // [2] every S / PV MMA issued has completed (teardown)
   // ctl[0]: tensor-memory base address, ctl[1]: abort
-  volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 1);
-  static_assert((2 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 1 + 2 + 1) * 8 + 8 <= OFF_X - OFF_BAR,
+  volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 2);
+  static_assert((2 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 1 + 2 + 2) * 8 + 8 <= OFF_X - OFF_BAR,
                 "barrier block");
   const bool pair = p.q_lo_rows > 0;
 
@@ -280,7 +284,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&odone[i], 1);
     }
     mbar_init(pready, 8);
-    mbar_init(mfin, 1);
+    mbar_init(&mfin[0], 1);
+    mbar_init(&mfin[1], 1);
     ctl[1] = 0;
     fence_mbar_init();
   }
@@ -314,8 +319,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       produce_ring<VSTAGES>(p, &mapV, &mapV16, smem + OFF_V, vfull, vempty, ctl, n_kt, n_keys, b,
                             g, rowbase);
     }
-  } else if (warp == 1) {  // -------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == PV_WARP) {  // ---------------------------- MMA issuers
     if (lane == 0) {
+      const bool is_s = warp == 1;
       const uint32_t id_s = idesc_bf16_f32(TQ, TK);
       const uint32_t id_o = idesc_bf16_f32(TQ, 128) | (1u << 16);  // B (V) MN-major
       // descriptors of K slot 0 and V slot 0; a slot, a dim half or a K step
@@ -324,55 +330,55 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_K));
       const uint64_t vdesc0 = smem_desc_sw128_mn(smem_u32(smem + OFF_V), KV_HALF);
       const uint32_t qcol = tmem + Q_COL;
-      bool ok = mbar_wait(qtm, 0, p.status);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % KSTAGES;
-        if (ctl[1] || !mbar_wait(&kfull[s], (j / KSTAGES) & 1, p.status)) return false;
-        if (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status)) return false;
-        tc_fence_after();
-        const uint64_t kd = kdesc0 + (uint64_t)(s * (KV_TILE >> 4));
-        const uint32_t d = tmem + (uint32_t)(j & 1) * TK;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // 16 dims per MMA: 8 Q columns, 32 bytes of K rows
-          tc_mma_f16_ts(d, qcol + 8u * kk, kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16, id_s,
-                        kk > 0 ? 1u : 0u);
-        if (pair)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc_mma_f16_ts(d, qcol + 64u + 8u * kk, kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16,
-                          id_s, 1u);
-        tc_commit(&sfull[j & 1]);
-        tc_commit(&kempty[s]);
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        const int s = j % VSTAGES;
-        if (ctl[1] || !mbar_wait(pready, j & 1, p.status) ||
-            !mbar_wait(&vfull[s], (j / VSTAGES) & 1, p.status))
-          return false;
-        tc_fence_after();
-        const uint64_t vd = vdesc0 + (uint64_t)(s * (KV_TILE >> 4));
-        const uint32_t pc = tmem + P_COL + 64u * (uint32_t)(j & 1);
-        const uint32_t oc = tmem + O_COL;
-#pragma unroll
-        for (int kk = 0; kk < TK / 16; ++kk)  // 16 keys per MMA: 8 P columns, two 8-key groups of V
-          tc_mma_f16_ts(oc, pc + 8u * kk, vd + kk * (2048 / 16), id_o, (j > 0 || kk > 0) ? 1u : 0u);
-        if (pair)
-#pragma unroll
-          for (int kk = 0; kk < TK / 16; ++kk)
-            tc_mma_f16_ts(oc, pc + 32u + 8u * kk, vd + kk * (2048 / 16), id_o, 1u);
-        tc_commit(&odone[j & 1]);
-        tc_commit(&vempty[s]);
-        return true;
-      };
+      bool ok = !is_s || mbar_wait(qtm, 0, p.status);
       for (int j = 0; ok && j < n_kt; ++j) {
-        ok = issue_s(j);
-        if (ok && j >= 1) ok = issue_pv(j - 1);
+        if (is_s) {  // S_j = Q K_j^T
+          const int s = j % KSTAGES;
+          if (ctl[1] || !mbar_wait(&kfull[s], (j / KSTAGES) & 1, p.status) ||
+              (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kd = kdesc0 + (uint64_t)(s * (KV_TILE >> 4));
+          const uint32_t d = tmem + (uint32_t)(j & 1) * TK;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // 16 dims per MMA: 8 Q columns, 32 bytes of K rows
+            tc_mma_f16_ts(d, qcol + 8u * kk, kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16, id_s,
+                          kk > 0 ? 1u : 0u);
+          if (pair)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_f16_ts(d, qcol + 64u + 8u * kk,
+                            kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16, id_s, 1u);
+          tc_commit(&sfull[j & 1]);
+          tc_commit(&kempty[s]);
+        } else {  // O += P_j V_j
+          const int s = j % VSTAGES;
+          if (ctl[1] || !mbar_wait(pready, j & 1, p.status) ||
+              !mbar_wait(&vfull[s], (j / VSTAGES) & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vd = vdesc0 + (uint64_t)(s * (KV_TILE >> 4));
+          const uint32_t pc = tmem + P_COL + 64u * (uint32_t)(j & 1);
+          const uint32_t oc = tmem + O_COL;
+#pragma unroll
+          for (int kk = 0; kk < TK / 16; ++kk)  // 16 keys per MMA: 8 P columns, two 8-key V groups
+            tc_mma_f16_ts(oc, pc + 8u * kk, vd + kk * (2048 / 16), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          if (pair)
+#pragma unroll
+            for (int kk = 0; kk < TK / 16; ++kk)
+              tc_mma_f16_ts(oc, pc + 32u + 8u * kk, vd + kk * (2048 / 16), id_o, 1u);
+          tc_commit(&odone[j & 1]);
+          tc_commit(&vempty[s]);
+        }
       }
-      if (ok) ok = issue_pv(n_kt - 1);
       if (!ok) ctl[1] = 1;
-      tc_commit(mfin);
-      mbar_wait(mfin, 0, p.status);  // every MMA retired before the tensor memory is freed
+      uint64_t* fin = &mfin[is_s ? 0 : 1];
+      tc_commit(fin);
+      mbar_wait(fin, 0, p.status);  // this thread's MMAs retired before the tensor memory is freed
     }
   } else {  // --------------------------------------------------------- softmax warps
     const int quad = warp & 3;          // tensor-memory lane quadrant this warp may access
