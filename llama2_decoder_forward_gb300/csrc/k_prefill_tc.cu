@@ -202,10 +202,10 @@ __device__ __forceinline__ void produce_ring(const TcPreParams& p, const CUtenso
   int issued = 0;
   for (int kt = 0; kt < n_kt; ++kt) {
     const int s = kt % NS;
-    if (ctl[1] || !mbar_wait(&empty[s], ((kt / NS) & 1) ^ 1, p.status)) {
+    if (ctl[1] || !mbar_wait_ready(&empty[s], ((kt / NS) & 1) ^ 1, p.status)) {
       ctl[1] = 1;
       for (int t = issued - 1; t >= 0 && t >= issued - NS; --t)
-        mbar_wait(&full[t % NS], (t / NS) & 1, p.status);
+        mbar_wait_ready(&full[t % NS], (t / NS) & 1, p.status);
       return;
     }
     const int k0 = kt * TK;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       produce_ring<KSTAGES>(p, &mapK, &mapK16, smem + OFF_K, kfull, kempty, ctl, n_kt, n_keys, b,
                             g, rowbase);
-      mbar_wait(qfull, 0, p.status);  // no copy may still be in flight when the CTA exits
+      mbar_wait_ready(qfull, 0, p.status);  // no copy may still be in flight when the CTA exits
     }
   } else if (warp == V_WARP) {  // --------------------------------------- V producer
     if (lane == 0) {
@@ -330,12 +330,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_K));
       const uint64_t vdesc0 = smem_desc_sw128_mn(smem_u32(smem + OFF_V), KV_HALF);
       const uint32_t qcol = tmem + Q_COL;
-      bool ok = !is_s || mbar_wait(qtm, 0, p.status);
+      bool ok = !is_s || mbar_wait_ready(qtm, 0, p.status);
       for (int j = 0; ok && j < n_kt; ++j) {
         if (is_s) {  // S_j = Q K_j^T
           const int s = j % KSTAGES;
-          if (ctl[1] || !mbar_wait(&kfull[s], (j / KSTAGES) & 1, p.status) ||
-              (j >= 2 && !mbar_wait(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status))) {
+          if (ctl[1] || !mbar_wait_ready(&kfull[s], (j / KSTAGES) & 1, p.status) ||
+              (j >= 2 && !mbar_wait_ready(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status))) {
             ok = false;
             break;
           }
@@ -355,8 +355,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_commit(&kempty[s]);
         } else {  // O += P_j V_j
           const int s = j % VSTAGES;
-          if (ctl[1] || !mbar_wait(pready, j & 1, p.status) ||
-              !mbar_wait(&vfull[s], (j / VSTAGES) & 1, p.status)) {
+          if (ctl[1] || !mbar_wait_ready(pready, j & 1, p.status) ||
+              !mbar_wait_ready(&vfull[s], (j / VSTAGES) & 1, p.status)) {
             ok = false;
             break;
           }
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (!ok) ctl[1] = 1;
       uint64_t* fin = &mfin[is_s ? 0 : 1];
       tc_commit(fin);
-      mbar_wait(fin, 0, p.status);  // this thread's MMAs retired before the tensor memory is freed
+      mbar_wait_ready(fin, 0, p.status);  // this thread's MMAs retired before the tensor memory is freed
     }
   } else {  // --------------------------------------------------------- softmax warps
     const int quad = warp & 3;          // tensor-memory lane quadrant this warp may access
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     float m_used = -INFINITY, l = 0.f;  // m_used: the row's reference max, log2 units
     bool ok = true;
     {  // Q row r (group 0) or its remainder (group 1) into tensor memory
-      const bool qok = __all_sync(0xffffffffu, mbar_wait(qfull, 0, p.status));
+      const bool qok = __all_sync(0xffffffffu, mbar_wait_ready(qfull, 0, p.status));
       if (qok && (grp == 0 || pair)) {
         const uint32_t qs = smem_u32(smem + grp * Q_TILE) + (uint32_t)r * 128u;
 #pragma unroll
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int j = 0; j < n_kt; ++j) {
       const bool good =
-          __all_sync(0xffffffffu, ok && !ctl[1] && mbar_wait(&sfull[j & 1], (j >> 1) & 1, p.status));
+          __all_sync(0xffffffffu, ok && !ctl[1] && mbar_wait_ready(&sfull[j & 1], (j >> 1) & 1, p.status));
       float sv[32];
       float pm = -INFINITY;
       if (good) {
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // the P buffer of tile j - 2 is reused; a rescale needs every earlier PV done
       const int wt = rescale ? j - 1 : j - 2;
       if (wt >= 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&odone[wt & 1], (wt >> 1) & 1, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_ready(&odone[wt & 1], (wt >> 1) & 1, p.status))) {
           ok = false;  // the next tile's flags take both warps out of the loop
           ctl[1] = 1;
           continue;
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // V rows past the last key may hold anything (P is 0 there, but
         // 0 * NaN is not): zero them, once V_j has landed, before the MMA
         // reads the tile (V_{j+3} cannot land in this slot before O += P_j V_j)
-        if (!__all_sync(0xffffffffu, mbar_wait(&vfull[j % VSTAGES], (j / VSTAGES) & 1, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_ready(&vfull[j % VSTAGES], (j / VSTAGES) & 1, p.status))) {
           ok = false;
           ctl[1] = 1;
           continue;
@@ -535,7 +535,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     // ---- epilogue: this thread's 64 dims of O / l (l = both groups' halves)
     const int last = n_kt - 1;
-    const bool done = ok && !ctl[1] && mbar_wait(&odone[last & 1], (last >> 1) & 1, p.status);
+    const bool done = ok && !ctl[1] && mbar_wait_ready(&odone[last & 1], (last >> 1) & 1, p.status);
     const int xs = (n_kt & 1) * 2;  // the exchange buffer the last tile did not use
     xch[(xs + grp) * 128 + r] = l;
     pair_bar(quad);
