@@ -458,53 +458,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         break;
       }
       const float mt = fmaxf(xch[xb * 128 + r], xch[(xb + 1) * 128 + r]) * c;  // row tile max, log2
+      // PV_j commits to odone[j & 1]; a wait below is for phase (t >> 1) of
+      // the tile t it names, and tile t - 2 was waited for one tile earlier,
+      // so the barrier is never two phases behind and parity identifies it
       const float m_new = fmaxf(m_used, mt);
       const bool need = m_new > m_used + kRescaleLog2;  // also the first finite max
       const float f = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
       const bool rescale = __any_sync(0xffffffffu, need && j > 0);
-      if (need) {
-        l *= f;
-        m_used = m_new;
-      }
-      // P = 2^(s c - m) as bf16 pairs, before any wait on the tensor pipe
-      const float mu = m_used == -INFINITY ? 0.f : m_used;
-      uint32_t ph[16], pl[16];
-      {
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float e0 = ex2(fmaf(sv[2 * i], c, -mu));  // masked keys: -inf -> 0
-          const float e1 = ex2(fmaf(sv[2 * i + 1], c, -mu));
-          ls[(2 * i) & 3] += e0;
-          ls[(2 * i + 1) & 3] += e1;
-          split_pack(e0, e1, ph[i], pl[i]);
-        }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      }
-      const int nvalid = min(TK, n_keys - j * TK);
-      if (nvalid < TK) {
-        // V rows past the last key may hold anything (P is 0 there, but
-        // 0 * NaN is not): zero them, once V_j has landed, before the MMA
-        // reads the tile (V_{j+3} cannot land in this slot before O += P_j V_j)
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_ready(&vfull[j % VSTAGES], (j / VSTAGES) & 1, p.status))) {
-          ok = false;
-          ctl[1] = 1;
-          continue;
-        }
-        uint8_t* vt = smem + OFF_V + (j % VSTAGES) * KV_TILE;
-        const int nz = (TK - nvalid) * 16;
-        for (int i = threadIdx.x - 64; i < nz; i += 256) {
-          const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
-          *reinterpret_cast<uint4*>(vt + half * KV_HALF + row * 128 + chunk * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();  // the MMA reads V through the async proxy
-      }
-      // PV_j commits to odone[j & 1]; a wait below is for phase (t >> 1) of
-      // the tile t it names, and tile t - 2 was waited for one tile earlier,
-      // so the barrier is never two phases behind and parity identifies it.
-      // P_j reuses the buffer of tile j - 2; a rescale needs every earlier PV done.
+      // the P buffer of tile j - 2 is reused; a rescale needs every earlier PV done
       const int wt = rescale ? j - 1 : j - 2;
       if (wt >= 0) {
         if (!__all_sync(0xffffffffu, mbar_wait_ready(&odone[wt & 1], (wt >> 1) & 1, p.status))) {
@@ -527,7 +488,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tmem_st16(tl + oc, u);
         }
       }
+      if (need) {
+        l *= f;
+        m_used = m_new;
+      }
+      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float e = ex2(fmaf(sv[i], c, -mu));  // masked keys: -inf -> 0
+        sv[i] = e;
+        ls[i & 3] += e;
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      const int nvalid = min(TK, n_keys - j * TK);
+      if (nvalid < TK) {
+        // V rows past the last key may hold anything (P is 0 there, but
+        // 0 * NaN is not): zero them, once V_j has landed, before the MMA
+        // reads the tile (V_{j+3} cannot land in this slot before O += P_j V_j)
+        if (!__all_sync(0xffffffffu, mbar_wait_ready(&vfull[j % VSTAGES], (j / VSTAGES) & 1, p.status))) {
+          ok = false;
+          ctl[1] = 1;
+          continue;
+        }
+        uint8_t* vt = smem + OFF_V + (j % VSTAGES) * KV_TILE;
+        const int nz = (TK - nvalid) * 16;
+        for (int i = threadIdx.x - 64; i < nz; i += 256) {
+          const int row = nvalid + (i >> 4), half = (i >> 3) & 1, chunk = i & 7;
+          *reinterpret_cast<uint4*>(vt + half * KV_HALF + row * 128 + chunk * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // the MMA reads V through the async proxy
+      }
       {  // this thread's 32 keys of P row r (and the remainder) into tensor memory
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) split_pack(sv[2 * i], sv[2 * i + 1], ph[i], pl[i]);
         const uint32_t pc = tl + P_COL + 64u * (uint32_t)(j & 1) + 16u * grp;
         tmem_st16(pc, ph);
         if (pair) tmem_st16(pc + 32, pl);
