@@ -41,7 +41,7 @@ constexpr uint32_t DSTAGE_BYTES = 4 * TILE_HALF;       // K and V, two dim halve
 constexpr size_t DEC_SMEM = DSTAGES * DSTAGE_BYTES + 1024 + 256;
 // FP8 E4M3 cache: one byte per value, so a 64-key tile of K (or V) is one
 // 128-byte-swizzled box of 64 rows x 128 bytes; three CTAs per SM.
-constexpr int F8_STAGES = 4;
+constexpr int F8_STAGES = 3;
 constexpr uint32_t F8_TILE = DTILE * 128;  // K (or V) of 64 keys: 8 KB
 constexpr uint32_t F8_SUB = SUBK * 128;    // 16 keys: 2 KB
 constexpr uint32_t F8_STAGE = 2 * F8_TILE;
@@ -614,7 +614,7 @@ __device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* 
 }
 
 template <bool KEYMAJOR, bool FP8>
-__global__ void __launch_bounds__(DEC_THREADS, FP8 ? 3 : 2)
+__global__ void __launch_bounds__(DEC_THREADS, FP8 ? 4 : 2)
     attn_decode_kernel(const __grid_constant__ CUtensorMap mapK,
                        const __grid_constant__ CUtensorMap mapV,
                        const __grid_constant__ CUtensorMap mapK16,
