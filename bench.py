@@ -288,6 +288,56 @@ def extra_workloads(dev, stream, w7, hbm, tflops):
         model.sync()
         return {k: (ms / steps, n / steps) for k, (ms, n) in r.items()}
 
+    # ---- the FP8 options of the same decode step (not the headline configuration):
+    # an E4M3 KV cache, then E4M3 projection weights with row scales
+    def decode_variant(weights, kv, name):
+        m = binding.Model(synth.LLAMA2_7B, weights, max_batch=B, max_tokens=B, max_seq=CAP,
+                          stream=stream)
+        tok = torch.randint(0, synth.LLAMA2_7B.vocab, (B,), generator=g, device=dev,
+                            dtype=torch.int32)
+        pos = torch.full((B,), CTX, dtype=torch.int32, device=dev)
+        lg = torch.empty(B, synth.LLAMA2_7B.vocab, device=dev)
+        ids = torch.empty(B, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+        m.capture_decode(tok, pos, kv, lg, ids, advance=False)
+        ms = _time_ms(m.graph_launch, stream, 20)
+        m.profile(["attn_decode", "gemm"])
+        for _ in range(5):
+            m.decode_step(tok, pos, kv, lg, ids)
+        am, an = m.profile_read("attn_decode")
+        gm, _ = m.profile_read("gemm")
+        m.profile([])
+        m.sync()
+        return {"workload": name, "tokens_per_s": B / (ms * 1e-3), "ms": ms,
+                "attn_decode_ms": am / max(an, 1), "gemm_ms_per_step": gm / 5}
+
+    s7 = synth.LLAMA2_7B
+    kv8 = binding.KVCache(s7, batch=B, capacity=CAP, e4m3=(1.0 / 64, 1.0 / 64))
+    for t in (kv8.k, kv8.v):
+        view = t.view(-1, CAP, s7.head_dim)
+        for i in range(0, view.shape[0], 4096):
+            f = torch.randn(min(4096, view.shape[0] - i), CTX, s7.head_dim, generator=g,
+                            device=dev) * 64
+            view[i:i + 4096, :CTX] = f.clamp_(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        view[:, CTX:].zero_()
+    r = decode_variant(w7, kv8, "7B decode step as the headline, KV cache E4M3 (byte per value)")
+    kvb = B * s7.n_kv_heads * (CTX + 1) * s7.head_dim * 2  # K and V bytes of one layer
+    r["attn_decode_gbs"] = kvb / (r["attn_decode_ms"] * 1e-3) / 1e9
+    r["attn_decode_frac"] = r["attn_decode_gbs"] / hbm
+    out["decode_kv_e4m3"] = r
+    del kv8
+    torch.cuda.empty_cache()
+    w8 = dict(w7)
+    w8["layers"] = [binding.quantize_layer_e4m3(lw) for lw in w7["layers"]]
+    kvb16 = binding.KVCache(s7, batch=B, capacity=CAP)
+    for t in (kvb16.k, kvb16.v):
+        t.view(-1, CAP, s7.head_dim)[:, :CTX].normal_(generator=g)
+        t.view(-1, CAP, s7.head_dim)[:, CTX:].zero_()
+    out["decode_w_e4m3"] = decode_variant(
+        w8, kvb16, "7B decode step as the headline, projection weights E4M3 with row scales")
+    del w8, kvb16
+    torch.cuda.empty_cache()
+
     # ---- full 7B prefill, 8 sequences x 512 tokens (the same weights)
     shape = synth.LLAMA2_7B
     Bp, Tp = 8, 512
