@@ -236,12 +236,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* vempty = vfull + VSTAGES;
   uint64_t* sfull = vempty + VSTAGES;  // [2] S_j is in tensor memory
   uint64_t* sfree = sfull + 2;         // [2] the softmax has read S_j
-  uint64_t* pready = sfree + 2;        // P_j is in tensor memory (O rescaled if needed)
-  uint64_t* odone = pready + 1;        // [2] O += P_j V_j has completed (P buffer j & 1 free)
+  // [2] P_j is in tensor memory (O rescaled if needed). One per P buffer: the
+  // softmax may finish tile j + 1 before the PV thread looks at tile j, but
+  // never tile j + 2 (its P buffer waits for O += P_j V_j), so a buffer's
+  // barrier is at most one phase ahead of its waiter and parity identifies it
+  uint64_t* pready = sfree + 2;
+  uint64_t* odone = pready + 2;        // [2] O += P_j V_j has completed (P buffer j & 1 free)
   uint64_t* mfin = odone + 2;          // [2] every S / PV MMA issued has completed (teardown)
   // ctl[0]: tensor-memory base address, ctl[1]: abort
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 2);
-  static_assert((2 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 1 + 2 + 2) * 8 + 8 <= OFF_X - OFF_BAR,
+  static_assert((2 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 2 + 2 + 2) * 8 + 8 <= OFF_X - OFF_BAR,
                 "barrier block");
   const bool pair = p.q_lo_rows > 0;
 
@@ -283,7 +287,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&sfree[i], 8);
       mbar_init(&odone[i], 1);
     }
-    mbar_init(pready, 8);
+    mbar_init(&pready[0], 8);
+    mbar_init(&pready[1], 8);
     mbar_init(&mfin[0], 1);
     mbar_init(&mfin[1], 1);
     ctl[1] = 0;
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_commit(&kempty[s]);
         } else {  // O += P_j V_j
           const int s = j % VSTAGES;
-          if (ctl[1] || !mbar_wait_ready(pready, j & 1, p.status) ||
+          if (ctl[1] || !mbar_wait_ready(&pready[j & 1], (j >> 1) & 1, p.status) ||
               !mbar_wait_ready(&vfull[s], (j / VSTAGES) & 1, p.status)) {
             ok = false;
             break;
@@ -531,7 +536,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pready);
+      if (lane == 0) mbar_arrive(&pready[j & 1]);
     }
     // ---- epilogue: this thread's 64 dims of O / l (l = both groups' halves)
     const int last = n_kt - 1;
