@@ -182,3 +182,20 @@ def test_invalid_parameters_are_rejected(ctx7):
                 dict(repetition_penalty=0.0), dict(temperature=float("nan"))):
         with pytest.raises(RuntimeError, match="INVALID_ARG"):
             ctx7.sample(z, u, ids, **bad)
+
+
+def test_ties_at_the_thresholds_follow_the_index_order(ctx7):
+    # rows with long runs of equal logits: every entry tied (the radix search
+    # never shrinks the candidates), and a plateau straddling the top-k cut
+    B, V = 8, L7.vocab
+    z = torch.zeros(B, V)
+    z[1] = 0.25
+    z[2, ::3] = 1.0
+    z[3, 1000:1100] = 2.0
+    z[3, 5000:5040] = 3.0
+    z[4:] = torch.round(_logits(4, V, 306) * 2.0) / 2.0  # few distinct values
+    u = _uniforms(B, 306)
+    for params in (dict(temperature=1.0, top_k=50), dict(temperature=0.8, top_k=70, top_p=0.5),
+                   dict(temperature=1.0, top_p=0.3), dict(temperature=1.0, top_k=5000)):
+        got = _run(ctx7, z, u, params)
+        _check(z, u, params, got, max_band=1)
