@@ -329,10 +329,28 @@ __global__ void __launch_bounds__(SAMPLE_THREADS, 1) sample_kernel(SampleArgs a)
 
   // 3. top-k: radix select of the k-th largest key among the kept entries
   if (a.top_k > 0 && a.top_k < V) {
+    // Candidates: when k threads own entries, the keys >= L, the smallest of
+    // the largest keys of threads 0..k-1. Those k keys are >= L, so the k-th
+    // largest is too, and usually few keys pass (the search can then start on
+    // the list).
+    uint64_t cand = kept;
+    int n_cand = V;
+    if (a.top_k <= (V + CH - 1) / CH) {
+      uint32_t tmax = 0;
+#pragma unroll
+      for (int j = 0; j < CH; ++j)
+        if ((kept >> j) & 1ull) tmax = max(tmax, key[j]);
+      const uint32_t L = block_reduce(t < a.top_k ? tmax : 0xffffffffu, red_u,
+                                      [](uint32_t x, uint32_t y) { return min(x, y); });
+      cand = 0;
+#pragma unroll
+      for (int j = 0; j < CH; ++j) cand |= (uint64_t)(((kept >> j) & 1ull) && key[j] >= L) << j;
+      n_cand = -1;
+    }
     int above;
     uint64_t act;
-    const uint32_t kap = radix_select<CH>(key, kept, V, a.top_k, [](int) { return 1; }, hist_i,
-                                          tot_i, lkey, lw_i, red_i, above, act);
+    const uint32_t kap = radix_select<CH>(key, cand, n_cand, a.top_k, [](int) { return 1; },
+                                          hist_i, tot_i, lkey, lw_i, red_i, above, act);
     // kap is the k-th largest key: `above` entries exceed it, `act` equal it
     const int need = a.top_k - above;
     int rank = block_exclusive_scan(__popcll((long long)act), red_i);
