@@ -6,9 +6,9 @@
 //
 // One CTA per (128 query rows, query head, sequence); 384 threads:
 //   warp 0     TMA producer of the Q tile (and its bf16 remainder rows) and
-//              of the K tiles (64 keys each) into a 5-slot mbarrier ring; a
+//              of the K tiles (128 keys each) into a 3-slot mbarrier ring; a
 //              slot frees as soon as S_j = Q K_j^T is computed;
-//   warp 10    TMA producer of the V tiles into a 3-slot ring; a slot frees
+//   warp 10    TMA producer of the V tiles into a 2-slot ring; a slot frees
 //              once O += P_j V_j is computed;
 //   warp 1     tensor-memory owner; one thread issues the score MMAs
 //              S_j = Q K_j^T into one of two S buffers in tensor memory;
@@ -17,7 +17,7 @@
 //              barrier waits between MMA groups, not the tensor pipe, bound
 //              a single thread at these small MMA shapes);
 //   warps 2-9  softmax, two groups of four warps: a thread of group k owns
-//              one query row (its tensor-memory lane) and keys 32k .. 32k+31
+//              one query row (its tensor-memory lane) and keys 64k .. 64k+63
 //              of every tile. It reads its half of S_j with tcgen05.ld,
 //              masks, exchanges the row's tile maximum with its partner in the
 //              other group through shared memory, keeps the running max and
@@ -28,8 +28,11 @@
 // Q (copied once from the TMA tile by the softmax threads) and P are the MMAs'
 // A operands in tensor memory: shared memory only feeds K and V to the tensor
 // cores, whose operand reads from shared memory bound the S and PV products
-// otherwise. The MMA of S_{j+1} runs while the softmax works on S_j; P has two
-// buffers so the softmax of a tile does not wait for the previous tile's PV.
+// otherwise. S has two buffers, and P_j is written over S_j (each thread
+// replaces its own scores): the MMA of S_{j+1} runs while the softmax works on
+// S_j, and S_{j+2} reuses buffer j & 1 once O += P_j V_j has completed. With
+// 128-key tiles the score MMAs have N = 128, where one thread issues them
+// faster than the tensor pipe executes them (at N = 64 issuing bounded them).
 // The running max is applied lazily: O and the sum are rescaled only when a
 // row's max grows by more than 2^8, otherwise P keeps the older max, which
 // leaves the normalised result unchanged. Key tiles past the diagonal are
@@ -40,10 +43,11 @@
 //      2c, 2c+1 (bf16 pair, lower dim in the low half); the remainder rows
 //      64 columns further;
 //   K  B operand in shared memory, K-major, 128-byte swizzled as TMA writes
-//      it: [64 keys][64 dims] per dim half;
-//   P  A operand in tensor memory: column c of a buffer holds keys 2c, 2c+1;
-//      the remainder 32 columns further;
-//   V  B operand in shared memory, MN-major: [64 keys][64 dims] per dim half
+//      it: [128 keys][64 dims] per dim half;
+//   P  A operand in tensor memory, in the S buffer of its tile: keys 64k ..
+//      64k+63 at columns 64k .. 64k+31 (column c holds two consecutive keys),
+//      their remainders at columns 64k+32 .. 64k+63;
+//   V  B operand in shared memory, MN-major: [128 keys][64 dims] per dim half
 //      (the dims are the MMA's N, contiguous in memory); 8-key groups 1024
 //      bytes apart, the two dim halves KV_HALF bytes apart.
 #include <algorithm>
@@ -56,15 +60,16 @@ namespace llgb {
 namespace {
 
 constexpr int TQ = 128;          // query rows per CTA: MMA M, one tensor-memory lane each
-constexpr int TK = 64;           // keys per tile
+constexpr int TK = 128;          // keys per tile
+constexpr int TBOX = 64;         // rows of the Q/K/V boxes of the 64-row views
 constexpr int TSUB = 16;         // keys per box of a 16-row (paged) cache view
-constexpr int KSTAGES = 5;       // K tiles in flight
-constexpr int VSTAGES = 3;       // V tiles in flight
+constexpr int KSTAGES = 3;       // K tiles in flight
+constexpr int VSTAGES = 2;       // V tiles in flight
 constexpr int TC_THREADS = 384;  // Q/K producer, S issuer, two softmax warpgroups, V producer, PV issuer
 constexpr int V_WARP = 10;
 constexpr int PV_WARP = 11;
-constexpr uint32_t KV_HALF = TK * 128;     // 64 keys x 64 dims bf16: 8 KB
-constexpr uint32_t KV_TILE = 2 * KV_HALF;  // 64 keys x 128 dims: 16 KB (one K or V slot)
+constexpr uint32_t KV_HALF = TK * 128;     // 128 keys x 64 dims bf16: 16 KB
+constexpr uint32_t KV_TILE = 2 * KV_HALF;  // 128 keys x 128 dims: 32 KB (one K or V slot)
 constexpr uint32_t Q_HALF = TQ * 128;      // 128 rows x 64 dims: 16 KB
 constexpr uint32_t Q_TILE = 2 * Q_HALF;    // 32 KB; the remainder tile follows
 constexpr uint32_t OFF_K = 2 * Q_TILE;
@@ -78,11 +83,10 @@ constexpr uint32_t OFF_X = OFF_BAR + 256;
 constexpr uint32_t OFF_XOK = OFF_X + 2 * 2 * 128 * 4;
 constexpr size_t TC_SMEM = OFF_XOK + 2 * 2 * 4 * 4;  // the dynamic base is 1024-byte aligned (checked)
 static_assert(TC_SMEM <= 232448, "227 KB of shared memory per CTA");
-// tensor-memory columns: S buffers, the O accumulator, Q (hi, remainder), P buffers
+// tensor-memory columns: S (and P) buffers, the O accumulator, Q (hi, remainder)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t O_COL = 128;
-constexpr uint32_t Q_COL = 256;  // 64 columns hi, then 64 columns remainder
-constexpr uint32_t P_COL = 384;  // buffer b at P_COL + 64 b: 32 columns hi, 32 remainder
+constexpr uint32_t O_COL = 256;
+constexpr uint32_t Q_COL = 384;  // 64 columns hi, then 64 columns remainder
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more than 2^8
 
 struct TcPreParams {
@@ -168,26 +172,42 @@ __device__ __forceinline__ int tc_kv_row(const TcPreParams& p, int b, int g, int
 }
 
 // K or V tile of keys k0 .. k0 + nvalid - 1 into ring slot `dst`, completing
-// on barrier fb.
+// on barrier fb: per 64-key block one 64-row box per dim half when the view
+// has them and the block is full, else 16-key boxes for the keys the sequence
+// has.
 __device__ __forceinline__ void load_kv_tile(const TcPreParams& p, const CUtensorMap* m64,
                                              const CUtensorMap* m16, uint8_t* dst, uint64_t* fb,
                                              int b, int g, int rowbase, int k0, int nvalid) {
   if (!p.from_cache) {
     mbar_arrive_expect_tx(fb, KV_TILE);
-    tma_load_3d(dst, m64, fb, 0, g, rowbase + k0);
-    tma_load_3d(dst + KV_HALF, m64, fb, 64, g, rowbase + k0);
-  } else if (p.box_rows == TK && nvalid == TK) {  // 64 contiguous keys: one box per half
-    const int row = tc_kv_row(p, b, g, k0);
-    mbar_arrive_expect_tx(fb, KV_TILE);
-    tma_load_3d(dst, m64, fb, 0, row, p.layer);
-    tma_load_3d(dst + KV_HALF, m64, fb, 64, row, p.layer);
-  } else {  // 16-key boxes, only those holding keys of this sequence
-    const int nsub = (nvalid + TSUB - 1) / TSUB;
-    mbar_arrive_expect_tx(fb, nsub * 2 * (TSUB * 128));
-    for (int jj = 0; jj < nsub; ++jj) {
-      const int row = tc_kv_row(p, b, g, k0 + jj * TSUB);
-      tma_load_3d(dst + jj * TSUB * 128, m16, fb, 0, row, p.layer);
-      tma_load_3d(dst + KV_HALF + jj * TSUB * 128, m16, fb, 64, row, p.layer);
+    for (int rb = 0; rb < TK / TBOX; ++rb) {
+      tma_load_3d(dst + rb * TBOX * 128, m64, fb, 0, g, rowbase + k0 + rb * TBOX);
+      tma_load_3d(dst + KV_HALF + rb * TBOX * 128, m64, fb, 64, g, rowbase + k0 + rb * TBOX);
+    }
+    return;
+  }
+  uint32_t bytes = 0;
+  for (int rb = 0; rb < TK / TBOX; ++rb) {
+    const int nv = min(TBOX, nvalid - rb * TBOX);
+    if (nv > 0)
+      bytes += (p.box_rows == TBOX && nv == TBOX) ? 2 * TBOX * 128
+                                                  : 2 * ((nv + TSUB - 1) / TSUB) * TSUB * 128;
+  }
+  mbar_arrive_expect_tx(fb, bytes);
+  for (int rb = 0; rb < TK / TBOX; ++rb) {
+    const int nv = min(TBOX, nvalid - rb * TBOX);
+    uint8_t* d = dst + rb * TBOX * 128;
+    if (nv <= 0) break;
+    if (p.box_rows == TBOX && nv == TBOX) {
+      const int row = tc_kv_row(p, b, g, k0 + rb * TBOX);
+      tma_load_3d(d, m64, fb, 0, row, p.layer);
+      tma_load_3d(d + KV_HALF, m64, fb, 64, row, p.layer);
+    } else {
+      for (int jj = 0; jj < (nv + TSUB - 1) / TSUB; ++jj) {
+        const int row = tc_kv_row(p, b, g, k0 + rb * TBOX + jj * TSUB);
+        tma_load_3d(d + jj * TSUB * 128, m16, fb, 0, row, p.layer);
+        tma_load_3d(d + KV_HALF + jj * TSUB * 128, m16, fb, 64, row, p.layer);
+      }
     }
   }
 }
@@ -235,17 +255,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* vfull = kempty + KSTAGES;
   uint64_t* vempty = vfull + VSTAGES;
   uint64_t* sfull = vempty + VSTAGES;  // [2] S_j is in tensor memory
-  uint64_t* sfree = sfull + 2;         // [2] the softmax has read S_j
-  // [2] P_j is in tensor memory (O rescaled if needed). One per P buffer: the
+  // [2] P_j is in tensor memory (O rescaled if needed). One per buffer: the
   // softmax may finish tile j + 1 before the PV thread looks at tile j, but
-  // never tile j + 2 (its P buffer waits for O += P_j V_j), so a buffer's
-  // barrier is at most one phase ahead of its waiter and parity identifies it
-  uint64_t* pready = sfree + 2;
-  uint64_t* odone = pready + 2;        // [2] O += P_j V_j has completed (P buffer j & 1 free)
+  // never tile j + 2 (S_{j+2} waits for O += P_j V_j), so a buffer's barrier
+  // is at most one phase ahead of its waiter and parity identifies it
+  uint64_t* pready = sfull + 2;
+  uint64_t* odone = pready + 2;        // [2] O += P_j V_j has completed (buffer j & 1 free)
   uint64_t* mfin = odone + 2;          // [2] every S / PV MMA issued has completed (teardown)
   // ctl[0]: tensor-memory base address, ctl[1]: abort
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 2);
-  static_assert((2 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 2 + 2 + 2) * 8 + 8 <= OFF_X - OFF_BAR,
+  static_assert((2 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 2 + 2) * 8 + 8 <= OFF_X - OFF_BAR,
                 "barrier block");
   const bool pair = p.q_lo_rows > 0;
 
@@ -284,7 +303,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sfree[i], 8);
       mbar_init(&odone[i], 1);
     }
     mbar_init(&pready[0], 8);
@@ -337,10 +355,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t qcol = tmem + Q_COL;
       bool ok = !is_s || mbar_wait_ready(qtm, 0, p.status);
       for (int j = 0; ok && j < n_kt; ++j) {
-        if (is_s) {  // S_j = Q K_j^T
+        if (is_s) {  // S_j = Q K_j^T, into the buffer P_{j-2} leaves
           const int s = j % KSTAGES;
           if (ctl[1] || !mbar_wait_ready(&kfull[s], (j / KSTAGES) & 1, p.status) ||
-              (j >= 2 && !mbar_wait_ready(&sfree[j & 1], ((j - 2) >> 1) & 1, p.status))) {
+              (j >= 2 && !mbar_wait_ready(&odone[j & 1], ((j - 2) >> 1) & 1, p.status))) {
             ok = false;
             break;
           }
@@ -367,15 +385,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           tc_fence_after();
           const uint64_t vd = vdesc0 + (uint64_t)(s * (KV_TILE >> 4));
-          const uint32_t pc = tmem + P_COL + 64u * (uint32_t)(j & 1);
+          const uint32_t pc = tmem + TK * (uint32_t)(j & 1);
           const uint32_t oc = tmem + O_COL;
+          // 16 keys per MMA: 8 P columns (keys 64g + 16m .. at 64g + 8m), two 8-key V groups
 #pragma unroll
-          for (int kk = 0; kk < TK / 16; ++kk)  // 16 keys per MMA: 8 P columns, two 8-key V groups
-            tc_mma_f16_ts(oc, pc + 8u * kk, vd + kk * (2048 / 16), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < TK / 16; ++kk)
+            tc_mma_f16_ts(oc, pc + 64u * (kk >> 2) + 8u * (kk & 3), vd + kk * (2048 / 16), id_o,
+                          (j > 0 || kk > 0) ? 1u : 0u);
           if (pair)
 #pragma unroll
             for (int kk = 0; kk < TK / 16; ++kk)
-              tc_mma_f16_ts(oc, pc + 32u + 8u * kk, vd + kk * (2048 / 16), id_o, 1u);
+              tc_mma_f16_ts(oc, pc + 64u * (kk >> 2) + 32u + 8u * (kk & 3), vd + kk * (2048 / 16),
+                            id_o, 1u);
           tc_commit(&odone[j & 1]);
           tc_commit(&vempty[s]);
         }
@@ -424,34 +445,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int j = 0; j < n_kt; ++j) {
       const bool good =
           __all_sync(0xffffffffu, ok && !ctl[1] && mbar_wait_ready(&sfull[j & 1], (j >> 1) & 1, p.status));
-      float sv[32];
+      float sv[64];
       float pm = -INFINITY;
+      const uint32_t sc = (uint32_t)(j & 1) * TK + 64u * grp;  // this thread's S (then P) columns
       if (good) {
         tc_fence_after();
-        uint32_t u[2][16];
-        const uint32_t col = (uint32_t)(j & 1) * TK + 32u * grp;
-        tmem_ld16(tl + col, u[0]);
-        tmem_ld16(tl + col + 16, u[1]);
-        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          sv[i] = __uint_as_float(u[0][i]);
-          sv[16 + i] = __uint_as_float(u[1][i]);
+        for (int q = 0; q < 4; q += 2) {
+          uint32_t u[2][16];
+          tmem_ld16(tl + sc + 16u * q, u[0]);
+          tmem_ld16(tl + sc + 16u * q + 16u, u[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            sv[16 * q + i] = __uint_as_float(u[0][i]);
+            sv[16 * q + 16 + i] = __uint_as_float(u[1][i]);
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sfree[j & 1]);
-        const int k0 = j * TK + 32 * grp;  // this thread's first key of the tile
+        const int k0 = j * TK + 64 * grp;  // this thread's first key of the tile
         // a tile below the CTA's first row and inside the sequence needs no mask
         const bool full = j * TK + TK - 1 <= start + q0 && j * TK + TK <= n_keys;
         if (!full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 64; ++i)
             if (k0 + i > qpos || k0 + i >= n_keys) sv[i] = -INFINITY;
         }
         float mx[4] = {sv[0], sv[1], sv[2], sv[3]};  // raw scores; the scale is positive
 #pragma unroll
-        for (int i = 4; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], sv[i]);
+        for (int i = 4; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], sv[i]);
         pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
       const int xb = (j & 1) * 2;
@@ -463,25 +484,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         break;
       }
       const float mt = fmaxf(xch[xb * 128 + r], xch[(xb + 1) * 128 + r]) * c;  // row tile max, log2
-      // PV_j commits to odone[j & 1]; a wait below is for phase (t >> 1) of
-      // the tile t it names, and tile t - 2 was waited for one tile earlier,
-      // so the barrier is never two phases behind and parity identifies it
       const float m_new = fmaxf(m_used, mt);
       const bool need = m_new > m_used + kRescaleLog2;  // also the first finite max
       const float f = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
       const bool rescale = __any_sync(0xffffffffu, need && j > 0);
-      // the P buffer of tile j - 2 is reused; a rescale needs every earlier PV done
-      const int wt = rescale ? j - 1 : j - 2;
-      if (wt >= 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait_ready(&odone[wt & 1], (wt >> 1) & 1, p.status))) {
+      if (rescale) {
+        // O must not be in flight: wait for O += P_{j-1} V_{j-1}. PV_{j-3}
+        // completed before S_{j-1} was computed and PV_{j+1} needs this
+        // tile's P, so the barrier is on tile j - 3 or j - 1 and parity
+        // identifies it
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_ready(&odone[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status))) {
           ok = false;  // the next tile's flags take both warps out of the loop
           ctl[1] = 1;
           continue;
         }
         tc_fence_after();
-      }
-      if (rescale) {  // rescale this thread's 64 O dims
-        const float fo = need ? f : 1.f;
+        const float fo = need ? f : 1.f;  // rescale this thread's 64 O dims
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
           uint32_t u[16];
@@ -500,7 +519,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const float mu = m_used == -INFINITY ? 0.f : m_used;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 64; ++i) {
         const float e = ex2(fmaf(sv[i], c, -mu));  // masked keys: -inf -> 0
         sv[i] = e;
         ls[i & 3] += e;
@@ -510,7 +529,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (nvalid < TK) {
         // V rows past the last key may hold anything (P is 0 there, but
         // 0 * NaN is not): zero them, once V_j has landed, before the MMA
-        // reads the tile (V_{j+3} cannot land in this slot before O += P_j V_j)
+        // reads the tile (V_{j+2} cannot land in this slot before O += P_j V_j)
         if (!__all_sync(0xffffffffu, mbar_wait_ready(&vfull[j % VSTAGES], (j / VSTAGES) & 1, p.status))) {
           ok = false;
           ctl[1] = 1;
@@ -525,13 +544,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         fence_proxy_async_smem();  // the MMA reads V through the async proxy
       }
-      {  // this thread's 32 keys of P row r (and the remainder) into tensor memory
+      // this thread's 64 keys of P row r over its scores: keys at columns
+      // sc .. sc+31, the remainders at sc+32 .. sc+63 (all scores are in
+      // registers: tmem_ld_wait above)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
         uint32_t ph[16], pl[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) split_pack(sv[2 * i], sv[2 * i + 1], ph[i], pl[i]);
-        const uint32_t pc = tl + P_COL + 64u * (uint32_t)(j & 1) + 16u * grp;
-        tmem_st16(pc, ph);
-        if (pair) tmem_st16(pc + 32, pl);
+        for (int i = 0; i < 16; ++i) split_pack(sv[32 * hh + 2 * i], sv[32 * hh + 2 * i + 1], ph[i], pl[i]);
+        tmem_st16(tl + sc + 16u * hh, ph);
+        if (pair) tmem_st16(tl + sc + 32u + 16u * hh, pl);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -610,7 +632,7 @@ cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t st) {
   p.start_pos = a.start_pos;
   p.n_rows = a.cu_rows ? a.n_rows : a.B * a.T;
   p.from_cache = a.from_cache;
-  p.box_rows = a.box_rows == TK ? TK : TSUB;
+  p.box_rows = a.box_rows == TBOX ? TBOX : TSUB;
   p.layer = a.layer;
   p.page_size = a.page_size;
   p.capacity = a.capacity;
