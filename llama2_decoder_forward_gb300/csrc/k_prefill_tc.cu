@@ -25,23 +25,23 @@
 //              pair when Q is one) into tensor memory, rescales O when needed
 //              and at the end normalises and stores its 64 of the row's 128
 //              output dims.
-// Q (copied once from the TMA tile by the softmax threads) and P are the MMAs'
-// A operands in tensor memory: shared memory only feeds K and V to the tensor
-// cores, whose operand reads from shared memory bound the S and PV products
-// otherwise. S has two buffers, and P_j is written over S_j (each thread
-// replaces its own scores): the MMA of S_{j+1} runs while the softmax works on
-// S_j, and S_{j+2} reuses buffer j & 1 once O += P_j V_j has completed. With
-// 128-key tiles the score MMAs have N = 128, where one thread issues them
-// faster than the tensor pipe executes them (at N = 64 issuing bounded them).
+// Q is the score MMAs' A operand straight from its TMA tile in shared memory,
+// and P the PV MMAs' A operand in tensor memory. That leaves tensor memory for
+// three S buffers and the O accumulator. S has three buffers, and P_j is written over S_j (each thread
+// replaces its own scores): the MMAs of S_{j+1} and S_{j+2} run while the
+// softmax works on S_j, and S_{j+3} reuses buffer j % 3 once O += P_j V_j has
+// completed. With 128-key tiles the score MMAs have N = 128, where one thread
+// issues them faster than the tensor pipe executes them (at N = 64 issuing
+// bounded them).
 // The running max is applied lazily: O and the sum are rescaled only when a
 // row's max grows by more than 2^8, otherwise P keeps the older max, which
 // leaves the normalised result unchanged. Key tiles past the diagonal are
 // skipped; the diagonal tile and the last partial tile are masked per key.
 //
 // Operand layouts:
-//   Q  A operand in tensor memory: lane = query row, column c holds dims
-//      2c, 2c+1 (bf16 pair, lower dim in the low half); the remainder rows
-//      64 columns further;
+//   Q  A operand in shared memory, K-major, 128-byte swizzled as TMA writes
+//      it: [128 rows][64 dims] per dim half, the remainder tile Q_TILE
+//      further;
 //   K  B operand in shared memory, K-major, 128-byte swizzled as TMA writes
 //      it: [128 keys][64 dims] per dim half;
 //   P  A operand in tensor memory, in the S buffer of its tile: keys 64k ..
@@ -83,10 +83,10 @@ constexpr uint32_t OFF_X = OFF_BAR + 256;
 constexpr uint32_t OFF_XOK = OFF_X + 2 * 2 * 128 * 4;
 constexpr size_t TC_SMEM = OFF_XOK + 2 * 2 * 4 * 4;  // the dynamic base is 1024-byte aligned (checked)
 static_assert(TC_SMEM <= 232448, "227 KB of shared memory per CTA");
-// tensor-memory columns: S (and P) buffers, the O accumulator, Q (hi, remainder)
+// tensor-memory columns: three S (then P) buffers of 128 columns, the O accumulator
+constexpr int NSB = 3;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t O_COL = 256;
-constexpr uint32_t Q_COL = 384;  // 64 columns hi, then 64 columns remainder
+constexpr uint32_t O_COL = NSB * TK;
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more than 2^8
 
 struct TcPreParams {
@@ -249,22 +249,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     return;
   }
   uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // Q tile in shared memory
-  uint64_t* qtm = qfull + 1;             // Q copied into tensor memory (8 softmax warps)
-  uint64_t* kfull = qtm + 1;
+  uint64_t* kfull = qfull + 1;
   uint64_t* kempty = kfull + KSTAGES;
   uint64_t* vfull = kempty + KSTAGES;
   uint64_t* vempty = vfull + VSTAGES;
-  uint64_t* sfull = vempty + VSTAGES;  // [2] S_j is in tensor memory
-  // [2] P_j is in tensor memory (O rescaled if needed). One per buffer: the
-  // softmax may finish tile j + 1 before the PV thread looks at tile j, but
-  // never tile j + 2 (S_{j+2} waits for O += P_j V_j), so a buffer's barrier
-  // is at most one phase ahead of its waiter and parity identifies it
-  uint64_t* pready = sfull + 2;
-  uint64_t* odone = pready + 2;        // [2] O += P_j V_j has completed (buffer j & 1 free)
-  uint64_t* mfin = odone + 2;          // [2] every S / PV MMA issued has completed (teardown)
+  uint64_t* sfull = vempty + VSTAGES;  // [NSB] S_j is in tensor memory buffer j % NSB
+  // [NSB] P_j is in tensor memory (O rescaled if needed). One per buffer: the
+  // softmax may finish later tiles before the PV thread looks at tile j, but
+  // not tile j + NSB (S_{j+NSB} waits for O += P_j V_j), so a buffer's
+  // barrier is at most one phase ahead of its waiter and parity identifies it
+  uint64_t* pready = sfull + NSB;
+  uint64_t* odone = pready + NSB;      // [NSB] O += P_j V_j has completed (buffer j % NSB free)
+  uint64_t* mfin = odone + NSB;        // [2] every S / PV MMA issued has completed (teardown)
   // ctl[0]: tensor-memory base address, ctl[1]: abort
   volatile uint32_t* ctl = reinterpret_cast<volatile uint32_t*>(mfin + 2);
-  static_assert((2 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 2 + 2) * 8 + 8 <= OFF_X - OFF_BAR,
+  static_assert((1 + 2 * KSTAGES + 2 * VSTAGES + 3 * NSB + 2) * 8 + 8 <= OFF_X - OFF_BAR,
                 "barrier block");
   const bool pair = p.q_lo_rows > 0;
 
@@ -292,7 +291,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
-    mbar_init(qtm, 8);
     for (int s = 0; s < KSTAGES; ++s) {
       mbar_init(&kfull[s], 1);
       mbar_init(&kempty[s], 1);
@@ -301,12 +299,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSB; ++i) {
       mbar_init(&sfull[i], 1);
       mbar_init(&odone[i], 1);
+      mbar_init(&pready[i], 8);
     }
-    mbar_init(&pready[0], 8);
-    mbar_init(&pready[1], 8);
     mbar_init(&mfin[0], 1);
     mbar_init(&mfin[1], 1);
     ctl[1] = 0;
@@ -352,40 +349,43 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // issue loop is a few adds per MMA (issuing bounds these small MMAs)
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_K));
       const uint64_t vdesc0 = smem_desc_sw128_mn(smem_u32(smem + OFF_V), KV_HALF);
-      const uint32_t qcol = tmem + Q_COL;
-      bool ok = !is_s || mbar_wait_ready(qtm, 0, p.status);
+      // Q: the A operand of the score MMAs, read from its TMA tile (hi, then
+      // the remainder tile Q_TILE further)
+      const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem));
+      bool ok = !is_s || mbar_wait_ready(qfull, 0, p.status);
       for (int j = 0; ok && j < n_kt; ++j) {
-        if (is_s) {  // S_j = Q K_j^T, into the buffer P_{j-2} leaves
+        const int sb = j % NSB;
+        if (is_s) {  // S_j = Q K_j^T, into the buffer P_{j-NSB} leaves
           const int s = j % KSTAGES;
           if (ctl[1] || !mbar_wait_ready(&kfull[s], (j / KSTAGES) & 1, p.status) ||
-              (j >= 2 && !mbar_wait_ready(&odone[j & 1], ((j - 2) >> 1) & 1, p.status))) {
+              (j >= NSB && !mbar_wait_ready(&odone[sb], ((j - NSB) / NSB) & 1, p.status))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t kd = kdesc0 + (uint64_t)(s * (KV_TILE >> 4));
-          const uint32_t d = tmem + (uint32_t)(j & 1) * TK;
+          const uint32_t d = tmem + (uint32_t)sb * TK;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // 16 dims per MMA: 8 Q columns, 32 bytes of K rows
-            tc_mma_f16_ts(d, qcol + 8u * kk, kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16, id_s,
-                          kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)  // 16 dims per MMA: 32 bytes of Q and of K rows
+            tc_mma_f16(d, qdesc0 + ((kk >> 2) * Q_HALF + (kk & 3) * 32) / 16,
+                       kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16, id_s, kk > 0 ? 1u : 0u);
           if (pair)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_f16_ts(d, qcol + 64u + 8u * kk,
-                            kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16, id_s, 1u);
-          tc_commit(&sfull[j & 1]);
+              tc_mma_f16(d, qdesc0 + (Q_TILE + (kk >> 2) * Q_HALF + (kk & 3) * 32) / 16,
+                         kd + ((kk >> 2) * KV_HALF + (kk & 3) * 32) / 16, id_s, 1u);
+          tc_commit(&sfull[sb]);
           tc_commit(&kempty[s]);
         } else {  // O += P_j V_j
           const int s = j % VSTAGES;
-          if (ctl[1] || !mbar_wait_ready(&pready[j & 1], (j >> 1) & 1, p.status) ||
+          if (ctl[1] || !mbar_wait_ready(&pready[sb], (j / NSB) & 1, p.status) ||
               !mbar_wait_ready(&vfull[s], (j / VSTAGES) & 1, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t vd = vdesc0 + (uint64_t)(s * (KV_TILE >> 4));
-          const uint32_t pc = tmem + TK * (uint32_t)(j & 1);
+          const uint32_t pc = tmem + TK * (uint32_t)sb;
           const uint32_t oc = tmem + O_COL;
           // 16 keys per MMA: 8 P columns (keys 64g + 16m .. at 64g + 8m), two 8-key V groups
 #pragma unroll
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int kk = 0; kk < TK / 16; ++kk)
               tc_mma_f16_ts(oc, pc + 64u * (kk >> 2) + 32u + 8u * (kk & 3), vd + kk * (2048 / 16),
                             id_o, 1u);
-          tc_commit(&odone[j & 1]);
+          tc_commit(&odone[sb]);
           tc_commit(&vempty[s]);
         }
       }
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else {  // --------------------------------------------------------- softmax warps
     const int quad = warp & 3;          // tensor-memory lane quadrant this warp may access
-    const int grp = (warp - 2) >> 2;    // 0: keys 0-31 of a tile, O dims 0-63; 1: the rest
+    const int grp = (warp - 2) >> 2;    // 0: keys 0-63 of a tile, O dims 0-63; 1: the rest
     const int r = quad * 32 + lane;
     const int qrow = q0 + r;
     const int qpos = start + qrow;
@@ -418,36 +418,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const float c = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;  // m_used: the row's reference max, log2 units
     bool ok = true;
-    {  // Q row r (group 0) or its remainder (group 1) into tensor memory
-      const bool qok = __all_sync(0xffffffffu, mbar_wait_ready(qfull, 0, p.status));
-      if (qok && (grp == 0 || pair)) {
-        const uint32_t qs = smem_u32(smem + grp * Q_TILE) + (uint32_t)r * 128u;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // columns 16q .. 16q+15: dim half q/2, chunks 4(q&1)..+3
-          uint32_t u[16];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t a =
-                qs + (q >> 1) * Q_HALF + ((uint32_t)((4 * (q & 1) + i) ^ (r & 7)) << 4);
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(u[4 * i]), "=r"(u[4 * i + 1]), "=r"(u[4 * i + 2]), "=r"(u[4 * i + 3])
-                         : "r"(a));
-          }
-          tmem_st16(tl + Q_COL + 64u * grp + 16u * q, u);
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qtm);
-      if (!qok) ok = false;
-    }
     for (int j = 0; j < n_kt; ++j) {
       const bool good =
-          __all_sync(0xffffffffu, ok && !ctl[1] && mbar_wait_ready(&sfull[j & 1], (j >> 1) & 1, p.status));
+          __all_sync(0xffffffffu, ok && !ctl[1] && mbar_wait_ready(&sfull[j % NSB], (j / NSB) & 1, p.status));
       float sv[64];
       float pm = -INFINITY;
-      const uint32_t sc = (uint32_t)(j & 1) * TK + 64u * grp;  // this thread's S (then P) columns
+      const uint32_t sc = (uint32_t)(j % NSB) * TK + 64u * grp;  // this thread's S (then P) columns
       if (good) {
         tc_fence_after();
 #pragma unroll
@@ -489,12 +465,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const float f = m_used == -INFINITY ? 0.f : ex2(m_used - m_new);
       const bool rescale = __any_sync(0xffffffffu, need && j > 0);
       if (rescale) {
-        // O must not be in flight: wait for O += P_{j-1} V_{j-1}. PV_{j-3}
-        // completed before S_{j-1} was computed and PV_{j+1} needs this
-        // tile's P, so the barrier is on tile j - 3 or j - 1 and parity
+        // O must not be in flight: wait for O += P_{j-1} V_{j-1}. PV_{j-1-NSB}
+        // completed before S_{j-1} was computed and PV_{j-1+NSB} needs a later
+        // tile's P, so the barrier is on tile j - 1 - NSB or j - 1 and parity
         // identifies it
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_ready(&odone[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_ready(&odone[(j - 1) % NSB],
+                                                     ((j - 1) / NSB) & 1, p.status))) {
           ok = false;  // the next tile's flags take both warps out of the loop
           ctl[1] = 1;
           continue;
@@ -558,11 +534,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&pready[j & 1]);
+      if (lane == 0) mbar_arrive(&pready[j % NSB]);
     }
     // ---- epilogue: this thread's 64 dims of O / l (l = both groups' halves)
     const int last = n_kt - 1;
-    const bool done = ok && !ctl[1] && mbar_wait_ready(&odone[last & 1], (last >> 1) & 1, p.status);
+    const bool done =
+        ok && !ctl[1] && mbar_wait_ready(&odone[last % NSB], (last / NSB) & 1, p.status);
     const int xs = (n_kt & 1) * 2;  // the exchange buffer the last tile did not use
     xch[(xs + grp) * 128 + r] = l;
     pair_bar(quad);
