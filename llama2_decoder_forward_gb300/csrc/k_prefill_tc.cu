@@ -426,18 +426,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t sc = (uint32_t)(j % NSB) * TK + 64u * grp;  // this thread's S (then P) columns
       if (good) {
         tc_fence_after();
+        uint32_t u[4][16];
 #pragma unroll
-        for (int q = 0; q < 4; q += 2) {
-          uint32_t u[2][16];
-          tmem_ld16(tl + sc + 16u * q, u[0]);
-          tmem_ld16(tl + sc + 16u * q + 16u, u[1]);
-          tmem_ld_wait();
+        for (int q = 0; q < 4; ++q) tmem_ld16(tl + sc + 16u * q, u[q]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            sv[16 * q + i] = __uint_as_float(u[0][i]);
-            sv[16 * q + 16 + i] = __uint_as_float(u[1][i]);
-          }
-        }
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sv[16 * q + i] = __uint_as_float(u[q][i]);
         const int k0 = j * TK + 64 * grp;  // this thread's first key of the tile
         // a tile below the CTA's first row and inside the sequence needs no mask
         const bool full = j * TK + TK - 1 <= start + q0 && j * TK + TK <= n_keys;
@@ -492,15 +488,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         l *= f;
         m_used = m_new;
       }
-      const float mu = m_used == -INFINITY ? 0.f : m_used;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float e = ex2(fmaf(sv[i], c, -mu));  // masked keys: -inf -> 0
-        sv[i] = e;
-        ls[i & 3] += e;
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       const int nvalid = min(TK, n_keys - j * TK);
       if (nvalid < TK) {
         // V rows past the last key may hold anything (P is 0 there, but
@@ -520,17 +507,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         fence_proxy_async_smem();  // the MMA reads V through the async proxy
       }
-      // this thread's 64 keys of P row r over its scores: keys at columns
-      // sc .. sc+31, the remainders at sc+32 .. sc+63 (all scores are in
-      // registers: tmem_ld_wait above)
+      // e = 2^(s c - m) and this thread's 64 keys of P row r over its scores
+      // (keys at columns sc .. sc+31, the remainders at sc+32 .. sc+63; all
+      // scores are in registers), one 32-key half at a time so the packing
+      // and stores of one half overlap the exponentials of the other
+      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int i = 32 * hh; i < 32 * hh + 32; ++i) {
+          const float e = ex2(fmaf(sv[i], c, -mu));  // masked keys: -inf -> 0
+          sv[i] = e;
+          ls[i & 3] += e;
+        }
         uint32_t ph[16], pl[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) split_pack(sv[32 * hh + 2 * i], sv[32 * hh + 2 * i + 1], ph[i], pl[i]);
         tmem_st16(tl + sc + 16u * hh, ph);
         if (pair) tmem_st16(tl + sc + 32u + 16u * hh, pl);
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
