@@ -18,8 +18,10 @@
 //      the top: each pass counts the keys that still match the threshold's
 //      prefix in 16 buckets of their next 4 bits and keeps the bucket where
 //      the count from the top reaches k (once the tied keys fit, they move to
-//      a short list that the remaining passes read instead); ties at the
-//      threshold are kept in ascending index order;
+//      a short list that the remaining passes read instead); the candidates
+//      start as the keys >= the smallest of the first k threads' maxima, a
+//      bound the k-th largest key cannot be below; ties at the threshold are
+//      kept in ascending index order;
 //   4. e = exp(s - max s) over the kept entries;
 //   5. top-p: the same radix select over the kept mass (sum of e per bucket)
 //      finds the smallest prefix of the descending order whose mass reaches
@@ -27,8 +29,8 @@
 //      mass is still short of it;
 //   6. draw: u * sum(e) is located in the running sum of e in ascending
 //      vocabulary order (the last kept entry if rounding leaves none).
-// Bucket totals are per-thread parts in shared memory added in thread order,
-// and every other reduction and scan also runs in a fixed order, so a draw is
+// Bucket totals are per-thread parts in shared memory added in a fixed
+// order, and so is every other reduction and scan, so a draw is
 // reproducible.
 #include <climits>
 
