@@ -42,6 +42,15 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t q4, uint32_t& lo, uin
       : "=r"(lo), "=r"(hi) : "r"(q4));
 }
 
+// 2^x on the special-function unit (the PTX ex2.approx instruction: about
+// 2^-22 relative error; results below the normal fp32 range give 0, -inf
+// gives 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -193,7 +193,7 @@ __device__ __forceinline__ void decode_consume_mma(const DecParams& p, uint8_t* 
         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
         const float mnew = fmaxf(mrow[h], mx[h]);
-        corr[h] = mnew == -INFINITY ? 1.f : exp2f(mrow[h] - mnew);
+        corr[h] = mnew == -INFINITY ? 1.f : ex2(mrow[h] - mnew);
         mrow[h] = mnew;
       }
       float ps[2] = {0.f, 0.f};
@@ -202,7 +202,7 @@ __device__ __forceinline__ void decode_consume_mma(const DecParams& p, uint8_t* 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int h = i >> 1;
-          const float pv = mrow[h] == -INFINITY ? 0.f : exp2f(sc[nb][i] - mrow[h]);
+          const float pv = mrow[h] == -INFINITY ? 0.f : ex2(sc[nb][i] - mrow[h]);
           sc[nb][i] = pv;
           ps[h] += pv;
         }
@@ -350,14 +350,14 @@ __device__ __forceinline__ void decode_consume_keymajor(const DecParams& p, uint
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float mnew = fmaxf(m_run[j], mx);
-        corr[j] = mnew == m_run[j] ? 1.f : exp2f(m_run[j] - mnew);  // unchanged max: exactly 1
+        corr[j] = mnew == m_run[j] ? 1.f : ex2(m_run[j] - mnew);  // unchanged max: exactly 1
         m_run[j] = mnew;
       }
       float pv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int j = i & 1;
-        pv[i] = m_run[j] == -INFINITY ? 0.f : exp2f(sv[i] - m_run[j]);
+        pv[i] = m_run[j] == -INFINITY ? 0.f : ex2(sv[i] - m_run[j]);
       }
       l_run[0] = l_run[0] * corr[0] + pv[0] + pv[2];
       l_run[1] = l_run[1] * corr[1] + pv[1] + pv[3];
@@ -539,14 +539,14 @@ __device__ __forceinline__ void decode_consume_fp8(const DecParams& p, uint8_t* 
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float mnew = fmaxf(m_run[j], mx);
-        corr[j] = mnew == m_run[j] ? 1.f : exp2f(m_run[j] - mnew);  // unchanged max: exactly 1
+        corr[j] = mnew == m_run[j] ? 1.f : ex2(m_run[j] - mnew);  // unchanged max: exactly 1
         m_run[j] = mnew;
       }
       float pv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int j = i & 1;
-        pv[i] = m_run[j] == -INFINITY ? 0.f : exp2f(sv[i] - m_run[j]);
+        pv[i] = m_run[j] == -INFINITY ? 0.f : ex2(sv[i] - m_run[j]);
       }
       l_run[0] = l_run[0] * corr[0] + pv[0] + pv[2];
       l_run[1] = l_run[1] * corr[1] + pv[1] + pv[3];

@@ -142,13 +142,6 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 2^x on the special-function unit (the PTX ex2.approx instruction; inputs
-// below the fp32 range give 0, -inf gives 0).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // The two softmax warps that own the same 32 rows (one per group) meet here.
 // Both always pass the same sequence of these barriers: every decision to
