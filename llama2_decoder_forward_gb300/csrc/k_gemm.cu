@@ -77,8 +77,13 @@ __device__ __forceinline__ void epi_apply(void* out, size_t idx, float g, float 
   } else if (EPI == LLAMA_EPI_RESID_F32) {
     reinterpret_cast<float*>(out)[idx] += g;
   } else {
-    // STORE_T: g; SWIGLU: silu(g) * u with silu(z) = z * sigmoid(z)
-    const float v = EPI == LLAMA_EPI_STORE_T ? g : g / (1.0f + expf(-g)) * u;
+    // STORE_T: g; SWIGLU: silu(g) * u with silu(z) = z / (1 + e^-z), the
+    // exponential as 2^(-z log2 e) on the special-function unit and the
+    // quotient by the fast division (relative errors near 2^-21, far below
+    // the 16 bits of the stored pair; z very negative: 2^+inf = inf and the
+    // quotient is 0)
+    const float v =
+        EPI == LLAMA_EPI_STORE_T ? g : __fdividef(g, 1.0f + ex2(-1.4426950408889634f * g)) * u;
     const T hi = from_f32<T>(v);
     reinterpret_cast<T*>(out)[idx] = hi;
     if (out_lo) reinterpret_cast<T*>(out)[idx + out_lo] = from_f32<T>(v - to_f32(hi));
