@@ -120,6 +120,31 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int max_seq, int hal
 // writes Q to q_out and K, V into the cache slot (and to k_out / v_out when
 // given). Positions outside the cache, or page ids outside the pool, set a
 // status flag and skip the cache write.
+// Eight consecutive values to dst: 16-byte stores when dst is 16-byte aligned
+// (always, for the layouts this library sets up), else element by element.
+__device__ __forceinline__ void store8(bf16* dst, const bf16 (&o)[8]) {
+  if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w[k] = (uint32_t)__bfloat16_as_ushort(o[2 * k]) |
+             ((uint32_t)__bfloat16_as_ushort(o[2 * k + 1]) << 16);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = o[k];
+  }
+}
+__device__ __forceinline__ void store8(float* dst, const float (&o)[8]) {
+  if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(o[4], o[5], o[6], o[7]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = o[k];
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
   grid_dep_wait();
@@ -171,11 +196,12 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
   for (int k = 0; k < 8; ++k) o[k] = from_f32<T>(v[k]);
   if (c < qw) {
     T* dst = reinterpret_cast<T*>(a.q_out) + (size_t)r * qw + c;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) dst[k] = o[k];
+    store8(dst, o);
     if (a.q_lo) {
+      T ol[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) dst[a.q_lo + k] = from_f32<T>(v[k] - to_f32(o[k]));
+      for (int k = 0; k < 8; ++k) ol[k] = from_f32<T>(v[k] - to_f32(o[k]));
+      store8(dst + a.q_lo, ol);
     }
     return;
   }
@@ -191,11 +217,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
     }
   }
   T* side = reinterpret_cast<T*>(is_v ? a.v_out : a.k_out);
-  if (side) {
-    T* dst = side + (size_t)r * kw + ck;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) dst[k] = o[k];
-  }
+  if (side) store8(side + (size_t)r * kw + ck, o);
   // cache slot
   size_t slot;
   if (a.page_size == 0) {
@@ -225,9 +247,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeAppendArgs a) {
     *reinterpret_cast<uint2*>(cache8) = w;
     return;
   }
-  T* cache = reinterpret_cast<T*>(is_v ? a.v_cache : a.k_cache) + slot * d + dd;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) cache[k] = o[k];
+  store8(reinterpret_cast<T*>(is_v ? a.v_cache : a.k_cache) + slot * d + dd, o);
 }
 
 // ------------------------------------------------------------------ greedy argmax
