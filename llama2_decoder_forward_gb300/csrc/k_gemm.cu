@@ -198,6 +198,88 @@ __device__ __forceinline__ void rope_emit(const RopeAppendArgs& a, const RopeFea
   }
 }
 
+// Four consecutive features f0 .. f0+3 of token row r (two whole RoPE pairs,
+// one kind, one head: f0.dd a multiple of 4) from their sums g, with the
+// pairs' angles cs (x, y: first pair; z, w: second): the same values as four
+// rope_emit calls, stored 8 bytes at a time where the destination allows.
+__device__ __forceinline__ void st4_bf16(bf16* dst, const float (&v)[4], bool lo_part) {
+  bf16 h[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const bf16 hi = __float2bfloat16_rn(v[e]);
+    h[e] = lo_part ? __float2bfloat16_rn(v[e] - __bfloat162float(hi)) : hi;
+  }
+  if ((reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+    const uint32_t w0 = (uint32_t)__bfloat16_as_ushort(h[0]) | ((uint32_t)__bfloat16_as_ushort(h[1]) << 16);
+    const uint32_t w1 = (uint32_t)__bfloat16_as_ushort(h[2]) | ((uint32_t)__bfloat16_as_ushort(h[3]) << 16);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dst[e] = h[e];
+  }
+}
+__device__ __forceinline__ void rope_emit4(const RopeAppendArgs& a, const RopeFeat& f0, int r,
+                                           const TokInfo& t, float4 cs, const float (&g)[4],
+                                           int valid) {
+  if (valid < 4) {  // a partial item at the end of the rows: element by element
+    for (int e = 0; e < valid; ++e) {
+      RopeFeat f = f0;
+      f.col += e;
+      f.dd += e;
+      f.odd = e & 1;
+      rope_emit(a, f, r, t, e < 2 ? make_float2(cs.x, cs.y) : make_float2(cs.z, cs.w), g[e],
+                g[e ^ 1]);
+    }
+    return;
+  }
+  const int d = a.head_dim;
+  float v[4];
+  if (f0.kind == 2) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = g[e];
+  } else {
+    v[0] = g[0] * cs.x - g[1] * cs.y;
+    v[1] = g[1] * cs.x + g[0] * cs.y;
+    v[2] = g[2] * cs.z - g[3] * cs.w;
+    v[3] = g[3] * cs.z + g[2] * cs.w;
+  }
+  if (f0.kind == 0) {
+    bf16* q = reinterpret_cast<bf16*>(a.q_out) + (size_t)r * a.n_q * d + f0.col;
+    st4_bf16(q, v, false);
+    if (a.q_lo) st4_bf16(q + a.q_lo, v, true);
+    return;
+  }
+  const bool is_v = f0.kind == 2;
+  if (a.kv_fp8) {  // the cache holds e4m3(x / scale); the side buffers its e4m3 value
+    const float sc = is_v ? a.v_scale : a.k_scale;
+    uint8_t q8[4];
+    float dq[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      q8[e] = f32_to_e4m3(v[e] / sc);
+      dq[e] = e4m3_to_f32(q8[e]);
+    }
+    bf16* side = reinterpret_cast<bf16*>(is_v ? a.v_out : a.k_out);
+    if (side) st4_bf16(side + (size_t)r * a.n_kv * d + f0.col, dq, false);
+    if (t.kv >= 0) {
+      const long long slot = t.kv + (long long)f0.g * (a.page_size ? a.page_size : a.capacity);
+      uint8_t* c8 = reinterpret_cast<uint8_t*>(is_v ? a.v_cache : a.k_cache) + slot * d + f0.dd;
+      if ((reinterpret_cast<uintptr_t>(c8) & 3u) == 0)
+        *reinterpret_cast<uint32_t*>(c8) = (uint32_t)q8[0] | ((uint32_t)q8[1] << 8) |
+                                           ((uint32_t)q8[2] << 16) | ((uint32_t)q8[3] << 24);
+      else
+        for (int e = 0; e < 4; ++e) c8[e] = q8[e];
+    }
+    return;
+  }
+  bf16* side = reinterpret_cast<bf16*>(is_v ? a.v_out : a.k_out);
+  if (side) st4_bf16(side + (size_t)r * a.n_kv * d + f0.col, v, false);
+  if (t.kv >= 0) {
+    const long long slot = t.kv + (long long)f0.g * (a.page_size ? a.page_size : a.capacity);
+    st4_bf16(reinterpret_cast<bf16*>(is_v ? a.v_cache : a.k_cache) + slot * d + f0.dd, v, false);
+  }
+}
+
 // 16 accumulator columns starting at col for this thread's TMEM lane; in the
 // hi/lo operand mode the column col + lo holds the product with the
 // remainders and is added.
@@ -712,16 +794,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           const TokInfo ti = tok[c];
           const RopeFeat f0 = rope_feat(p.rope, gm0);
           const float4 cs = rope_cs2(p.rope, f0, ti.pos);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            RopeFeat f = f0;
-            f.col += e;
-            f.dd += e;
-            f.odd = e & 1;
-            if (gm0 + e < p.M)
-              rope_emit(p.rope, f, c, ti, e < 2 ? make_float2(cs.x, cs.y) : make_float2(cs.z, cs.w),
-                        g[e], g[e ^ 1]);
-          }
+          rope_emit4(p.rope, f0, c, ti, cs, g, min(4, p.M - gm0));
         } else if (EPI == LLAMA_EPI_RESID_F32) {
           float* o = reinterpret_cast<float*>(p.out) + (size_t)c * p.ldo + gm0;
           float res[4];
