@@ -67,6 +67,14 @@ struct TcParams {
   uint32_t* status;
 };
 
+// silu(g) * u with silu(z) = z / (1 + e^-z): the exponential as 2^(-z log2 e)
+// on the special-function unit and the quotient by the fast division (relative
+// errors near 2^-21, far below the 16 bits of the stored pair; z very
+// negative: 2^+inf = inf and the quotient is 0).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + ex2(-1.4426950408889634f * g)) * u;
+}
+
 // Store one output element. For bf16 outputs with out_lo > 0 the value is
 // kept as a pair: hi = bf16(v) at idx and lo = bf16(v - hi) at idx + out_lo.
 template <int EPI, typename T>
@@ -77,13 +85,7 @@ __device__ __forceinline__ void epi_apply(void* out, size_t idx, float g, float 
   } else if (EPI == LLAMA_EPI_RESID_F32) {
     reinterpret_cast<float*>(out)[idx] += g;
   } else {
-    // STORE_T: g; SWIGLU: silu(g) * u with silu(z) = z / (1 + e^-z), the
-    // exponential as 2^(-z log2 e) on the special-function unit and the
-    // quotient by the fast division (relative errors near 2^-21, far below
-    // the 16 bits of the stored pair; z very negative: 2^+inf = inf and the
-    // quotient is 0)
-    const float v =
-        EPI == LLAMA_EPI_STORE_T ? g : __fdividef(g, 1.0f + ex2(-1.4426950408889634f * g)) * u;
+    const float v = EPI == LLAMA_EPI_STORE_T ? g : silu_mul(g, u);  // STORE_T: g
     const T hi = from_f32<T>(v);
     reinterpret_cast<T*>(out)[idx] = hi;
     if (out_lo) reinterpret_cast<T*>(out)[idx + out_lo] = from_f32<T>(v - to_f32(hi));
@@ -797,30 +799,59 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           rope_emit4(p.rope, f0, c, ti, cs, g, min(4, p.M - gm0));
         } else if (EPI == LLAMA_EPI_RESID_F32) {
           float* o = reinterpret_cast<float*>(p.out) + (size_t)c * p.ldo + gm0;
+          // a whole item with 16-byte aligned rows: vector loads and stores
+          const bool vec = gm0 + 4 <= p.M && (reinterpret_cast<uintptr_t>(o) & 15u) == 0;
           float res[4];
+          if (vec) {
+            const float4 r4 = *reinterpret_cast<const float4*>(o);
+            res[0] = r4.x; res[1] = r4.y; res[2] = r4.z; res[3] = r4.w;
+            *reinterpret_cast<float4*>(o) =
+                make_float4(res[0] + g[0], res[1] + g[1], res[2] + g[2], res[3] + g[3]);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) res[e] = gm0 + e < p.M ? o[e] : 0.f;
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (gm0 + e < p.M) o[e] = res[e] + g[e];
-          if (p.norm_gamma) {  // normalised-input pair and this tile's sum of squares
-            float ss = 0.f;
+            for (int e = 0; e < 4; ++e) res[e] = gm0 + e < p.M ? o[e] : 0.f;
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (gm0 + e < p.M) {
+              if (gm0 + e < p.M) o[e] = res[e] + g[e];
+          }
+          if (p.norm_gamma) {  // normalised-input pair and this tile's sum of squares
+            float ss = 0.f;
+            if (vec) {
+              float y[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
                 const float xn = res[e] + g[e];
-                const float y = xn * __bfloat162float(p.norm_gamma[gm0 + e]);
-                const bf16 hi = __float2bfloat16_rn(y);
-                const size_t idx = (size_t)c * p.ldo + gm0 + e;
-                p.norm_out[idx] = hi;
-                if (p.norm_lo)
-                  p.norm_out[idx + p.norm_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
+                y[e] = xn * __bfloat162float(p.norm_gamma[gm0 + e]);
                 ss += xn * xn;
               }
+              bf16* dst = p.norm_out + (size_t)c * p.ldo + gm0;
+              st4_bf16(dst, y, false);
+              if (p.norm_lo) st4_bf16(dst + p.norm_lo, y, true);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (gm0 + e < p.M) {
+                  const float xn = res[e] + g[e];
+                  const float y = xn * __bfloat162float(p.norm_gamma[gm0 + e]);
+                  const bf16 hi = __float2bfloat16_rn(y);
+                  const size_t idx = (size_t)c * p.ldo + gm0 + e;
+                  p.norm_out[idx] = hi;
+                  if (p.norm_lo)
+                    p.norm_out[idx + p.norm_lo] = __float2bfloat16_rn(y - __bfloat162float(hi));
+                  ss += xn * xn;
+                }
+            }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             if ((threadIdx.x & 31) == 0) p.ssq_out[(size_t)tile_m * p.ssq_ld + c] = ss;
           }
+        } else if (EPI == LLAMA_EPI_SWIGLU && gm0 + 4 <= p.M) {  // a whole item
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = silu_mul(g[e], u[e]);
+          bf16* dst = reinterpret_cast<bf16*>(p.out) + (size_t)c * p.ldo + gm0;
+          st4_bf16(dst, v, false);
+          if (p.out_lo) st4_bf16(dst + p.out_lo, v, true);
         } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
