@@ -205,6 +205,11 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile that
 // TMA wrote with CU_TENSOR_MAP_SWIZZLE_128B (rows of 128 bytes, 1024-byte

@@ -489,13 +489,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
       }
       // activation tile: one box of n_tile rows, or in the hi/lo mode the hi
       // rows and the remainder rows of the same ncol activations back to back
+      // activations are read by every weight tile's CTA: kept in L2 ahead of
+      // the streamed weights
+      const uint64_t pol_x = l2_policy_evict_last();
       auto load_x = [&](uint8_t* dst, uint64_t* bar, int kb) {
         if (p.lo) {
-          tma_load_2d(dst, &tmX, bar, kb * BK, tile_n * p.ncol);
-          tma_load_2d(dst + (uint32_t)p.ncol * BK * 2, &tmX, bar, kb * BK,
-                      p.lo_rows + tile_n * p.ncol);
+          tma_load_2d_hint(dst, &tmX, bar, kb * BK, tile_n * p.ncol, pol_x);
+          tma_load_2d_hint(dst + (uint32_t)p.ncol * BK * 2, &tmX, bar, kb * BK,
+                           p.lo_rows + tile_n * p.ncol, pol_x);
         } else {
-          tma_load_2d(dst, &tmX, bar, kb * BK, tile_n * p.n_tile);
+          tma_load_2d_hint(dst, &tmX, bar, kb * BK, tile_n * p.n_tile, pol_x);
         }
       };
       grid_dep_wait();
