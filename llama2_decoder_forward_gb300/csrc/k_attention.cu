@@ -676,6 +676,7 @@ __global__ void __launch_bounds__(DEC_THREADS, FP8 ? 4 : 2)
       tma_prefetch_desc(&mapV);
       tma_prefetch_desc(&mapK16);
       tma_prefetch_desc(&mapV16);
+      const uint64_t pol_kv = l2_policy_evict_first();  // the cache is streamed once
       int issued = 0;
       bool ok = true, waited = false;
       for (int t = 0; t < n_tiles; ++t) {
@@ -700,33 +701,34 @@ __global__ void __launch_bounds__(DEC_THREADS, FP8 ? 4 : 2)
           if (p.box_rows == DTILE && nsub == 4) {
             const int row = kv_row(p, b, g, kbeg + t * DTILE);
             mbar_arrive_expect_tx(&full[s], F8_STAGE);
-            tma_load_3d(st, &mapK, &full[s], 0, row, p.layer);
-            tma_load_3d(st + F8_TILE, &mapV, &full[s], 0, row, p.layer);
+            tma_load_3d_hint(st, &mapK, &full[s], 0, row, p.layer, pol_kv);
+            tma_load_3d_hint(st + F8_TILE, &mapV, &full[s], 0, row, p.layer, pol_kv);
           } else {
             mbar_arrive_expect_tx(&full[s], nsub * 2 * F8_SUB);
             for (int j = 0; j < nsub; ++j) {
               const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
-              tma_load_3d(st + j * F8_SUB, &mapK16, &full[s], 0, row, p.layer);
-              tma_load_3d(st + F8_TILE + j * F8_SUB, &mapV16, &full[s], 0, row, p.layer);
+              tma_load_3d_hint(st + j * F8_SUB, &mapK16, &full[s], 0, row, p.layer, pol_kv);
+              tma_load_3d_hint(st + F8_TILE + j * F8_SUB, &mapV16, &full[s], 0, row, p.layer,
+                               pol_kv);
             }
           }
         } else if (p.box_rows == DTILE && nsub == 4) {  // 64 contiguous keys: one box per half
           const int row = kv_row(p, b, g, kbeg + t * DTILE);
           mbar_arrive_expect_tx(&full[s], DSTAGE_BYTES);
-          tma_load_3d(st, &mapK, &full[s], 0, row, p.layer);
-          tma_load_3d(st + TILE_HALF, &mapK, &full[s], 64, row, p.layer);
-          tma_load_3d(st + 2 * TILE_HALF, &mapV, &full[s], 0, row, p.layer);
-          tma_load_3d(st + 3 * TILE_HALF, &mapV, &full[s], 64, row, p.layer);
+          tma_load_3d_hint(st, &mapK, &full[s], 0, row, p.layer, pol_kv);
+          tma_load_3d_hint(st + TILE_HALF, &mapK, &full[s], 64, row, p.layer, pol_kv);
+          tma_load_3d_hint(st + 2 * TILE_HALF, &mapV, &full[s], 0, row, p.layer, pol_kv);
+          tma_load_3d_hint(st + 3 * TILE_HALF, &mapV, &full[s], 64, row, p.layer, pol_kv);
         } else {
           mbar_arrive_expect_tx(&full[s], nsub * SUB_BYTES * 2);
           for (int j = 0; j < nsub; ++j) {
             const int row = kv_row(p, b, g, kbeg + (4 * t + j) * SUBK);
             uint8_t* kd = st + j * HALF_BYTES;
             uint8_t* vd = st + 2 * TILE_HALF + j * HALF_BYTES;
-            tma_load_3d(kd, &mapK16, &full[s], 0, row, p.layer);
-            tma_load_3d(kd + TILE_HALF, &mapK16, &full[s], 64, row, p.layer);
-            tma_load_3d(vd, &mapV16, &full[s], 0, row, p.layer);
-            tma_load_3d(vd + TILE_HALF, &mapV16, &full[s], 64, row, p.layer);
+            tma_load_3d_hint(kd, &mapK16, &full[s], 0, row, p.layer, pol_kv);
+            tma_load_3d_hint(kd + TILE_HALF, &mapK16, &full[s], 64, row, p.layer, pol_kv);
+            tma_load_3d_hint(vd, &mapV16, &full[s], 0, row, p.layer, pol_kv);
+            tma_load_3d_hint(vd + TILE_HALF, &mapV16, &full[s], 64, row, p.layer, pol_kv);
           }
         }
         ++issued;
