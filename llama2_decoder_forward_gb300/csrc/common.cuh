@@ -51,6 +51,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// SwiGLU: silu(g) * u with silu(z) = z / (1 + e^-z): the exponential as 2^(-z log2 e)
+// on the special-function unit and the quotient by the fast division (relative
+// errors near 2^-21, far below the 16 bits of the stored pair; z very
+// negative: 2^+inf = inf and the quotient is 0).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + ex2(-1.4426950408889634f * g)) * u;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -67,14 +67,6 @@ struct TcParams {
   uint32_t* status;
 };
 
-// silu(g) * u with silu(z) = z / (1 + e^-z): the exponential as 2^(-z log2 e)
-// on the special-function unit and the quotient by the fast division (relative
-// errors near 2^-21, far below the 16 bits of the stored pair; z very
-// negative: 2^+inf = inf and the quotient is 0).
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fdividef(g, 1.0f + ex2(-1.4426950408889634f * g)) * u;
-}
-
 // Store one output element. For bf16 outputs with out_lo > 0 the value is
 // kept as a pair: hi = bf16(v) at idx and lo = bf16(v - hi) at idx + out_lo.
 template <int EPI, typename T>
@@ -985,7 +977,8 @@ cudaError_t gemm_prepare() {
   if ((e = set_attr<LLAMA_EPI_RESID_F32>()) != cudaSuccess) return e;
   if ((e = set_attr<LLAMA_EPI_STORE_T>()) != cudaSuccess) return e;
   if ((e = set_attr<kEpiRope>()) != cudaSuccess) return e;
-  return set_attr<LLAMA_EPI_SWIGLU>();
+  if ((e = set_attr<LLAMA_EPI_SWIGLU>()) != cudaSuccess) return e;
+  return gemm_tm_prepare();
 }
 
 template <int EPI, bool W8>
@@ -1046,6 +1039,7 @@ cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st) {
       default: return launch_f32<LLAMA_EPI_SWIGLU>(g, st);
     }
   }
+  if (gemm_tm_applies(g)) return launch_gemm_tm(g, st);
   const bool dual = g.epi == LLAMA_EPI_SWIGLU;
   if (g.w_scale && dual != (g.u_scale != nullptr)) return cudaErrorInvalidValue;
   const Plan pl = make_plan(g.M, g.N, g.K, dual, g.split, g.sm_count, g.epi == kEpiRope,

@@ -131,6 +131,12 @@ def _pair(x):
     (4096, 100, 11008, "resid"),
     (32000, 8, 4096, "store_f32"),
     (1024, 1, 256, "store_t"),
+    # at least one 128-row x 256-feature tile per SM: the persistent kernel
+    # with the activation rows on the MMA's M side (ragged rows, features, K)
+    (12288, 1000, 4096, "store_f32"),
+    (4000, 1300, 4104, "resid"),
+    (2816, 1200, 4096, "swiglu"),
+    (4096, 1200, 1024, "store_t"),
 ])
 def test_linear_bf16_pair_operands(ctx7, M, N, K, epi):
     # fp32 activations carried as bf16 hi + lo: the product tracks the fp32 values
