@@ -688,7 +688,8 @@ def run_prefill(args):
             "data": "synthetic (random-init 7B weights, uniform ids)",
             "config": {"workload": "llama2-7b prefill, 8 sequences x 512 tokens, %d layers + LM head on last rows"
                                    % shape.n_layers},
-            "roofline": {"kernel": "gemm_tc_kernel (all prefill projections)", "bound": "tensor",
+            "roofline": {"kernel": "gemm_tm_kernel (prefill projections) + gemm_tc_kernel (LM head)",
+                         "bound": "tensor",
                          "achieved": g_tf, "peak": tflops, "unit": "TFLOP/s", "frac": g_tf / tflops,
                          "peak_source": peak_kind, "traffic": None,
                          "algorithmic_flops_per_step": gemm_flops, "launches_per_step": gemm_n / args.steps},
@@ -811,7 +812,8 @@ def run_extend(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init 7B weights, uniform ids, N(0,1) cache)",
             "config": {"workload": "llama2-7b extend step: 28 sequences decode at position 1024, 4 feed "
                                    "256-token prompt pieces at positions 512..767; one call, 1052 rows"},
-            "roofline": {"kernel": "gemm_tc_kernel (all projections of the 1052 rows)", "bound": "tensor",
+            "roofline": {"kernel": "gemm_tm_kernel (Q/K/V, gate/up) + gemm_tc_kernel (O, down, LM head)",
+                         "bound": "tensor",
                          "achieved": g_tf, "peak": tflops, "unit": "TFLOP/s", "frac": g_tf / tflops,
                          "peak_source": peak_kind, "traffic": None,
                          "algorithmic_flops_per_step": gemm_flops, "launches_per_step": gemm_n / args.steps},

@@ -634,21 +634,32 @@ int run_layer(llama_ctx* c, int l, float* x, int rows, int B, int T, const int32
   const int rps = prefill ? T : 1;
   const int32_t* pos = prefill ? nullptr : positions;
   const size_t q_lo = (size_t)lo * nq * d;
+  // prefill Q/K/V on the token-major GEMM (bf16 weights, prefill-sized rows)
+  const bool tm_qkv = prefill && cf.dtype == LLAMA_BF16 && d % 16 == 0 &&
+                      (c->wscale.empty() || c->wscale.find(lw.wqkv) == c->wscale.end()) &&
+                      gemm_tm_shape(kEpiRope, qkv_rows, rows, sp, c->sm_count);
   if (rm) {  // extend: RoPE/append, then attention over the cache
     TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp,
                 0, nullptr, qkv_nf));
     TRY(do_rope_append(c, qkv, rows, 1, nullptr, l, kv, q, nullptr, nullptr, q_lo, rm));
     TRY(do_attn_extend(c, q, rows, *rm, l, kv, o, q_lo, lo));  // pieces of 2+ rows
     TRY(do_attn_decode(c, q, rm->start_pos, rm->B, l, kv, o, q_lo, q_lo, rm->cu_rows));  // 1 row
-  } else if (cf.dtype == LLAMA_BF16 && !prefill) {
-    // Q/K/V projection with RoPE and the cache append in its epilogue. Prefill
-    // keeps them in a separate kernel: its GEMM runs one CTA per SM with the
-    // epilogue after the K loop, where the per-element work would stall the
-    // tensor pipe for longer than the separate pass over the fp32 rows takes.
+  } else if (cf.dtype == LLAMA_BF16 && (!prefill || tm_qkv)) {
+    // Q/K/V projection with RoPE and the cache append in its epilogue. A
+    // prefill takes it only on the persistent token-major GEMM, whose
+    // epilogue overlaps the next tile's MMAs; with one tile per CTA the
+    // per-element work stalled the tensor pipe for longer than the separate
+    // pass over the fp32 rows takes.
     const RopeAppendArgs ra = rope_args(c, nullptr, rps, pos, l, kv, q, ks, vs, q_lo);
     TRY(do_gemm(c, kEpiRope, u, rows, H, lw.wqkv, nullptr, qkv_rows, nullptr, qkv_rows, sp, 0,
                 &ra, qkv_nf));
-    TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
+    if (prefill) {
+      const bool f8 = kv->kv_dtype == LLAMA_KV_E4M3;
+      TRY(do_attn_prefill(c, q, ks, vs, B, T, o, q_lo, lo, f8 ? kv->k_scale : 1.f,
+                          f8 ? kv->v_scale : 1.f));
+    } else {
+      TRY(do_attn_decode(c, q, positions, B, l, kv, o, q_lo, q_lo));
+    }
   } else {
     TRY(do_gemm(c, LLAMA_EPI_STORE_F32, u, rows, H, lw.wqkv, nullptr, qkv_rows, qkv, qkv_rows, sp,
                 0, nullptr, qkv_nf));

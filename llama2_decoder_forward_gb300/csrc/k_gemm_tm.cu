@@ -19,14 +19,17 @@
 // accumulator (thread = token row, tcgen05.ld 32x32b) and apply the
 // epilogue: store fp32, add into the fp32 residual (and, for the fused
 // RMSNorm, store the next projection's input pair x * gamma and the per-row
-// sums of x^2 per 128 features), or silu(gate) * up as a bf16 pair. SwiGLU
-// loads 128 gate rows and the same 128 up rows as the two halves of B, so
+// sums of x^2 per 128 features), silu(gate) * up as a bf16 pair, or, for the
+// Q/K/V projection, RoPE and the KV-cache append (each thread holds whole
+// RoPE pairs of its token: features 2j and 2j + 1 are neighbouring
+// accumulator columns). SwiGLU loads 128 gate rows and the same 128 up rows as the two halves of B, so
 // columns 0..127 of the accumulator hold the gate sums and 128..255 the up
 // sums of the same features.
 #include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
+#include "rope_epi.cuh"
 
 namespace llgb {
 
@@ -45,6 +48,7 @@ constexpr int TM_GROUP = 16;  // activation tiles consecutive tiles share
 constexpr size_t TM_SMEM = (size_t)TM_STAGES * TM_STAGE_BYTES + 1024 + 256;
 
 struct TmParams {
+  RopeAppendArgs rope;  // kEpiRope only
   int M, N, K, num_kb;
   int lo_rows;  // activation row n's remainder is row lo_rows + n of the map
   int n_tok, n_feat, tiles;
@@ -148,6 +152,75 @@ __device__ __forceinline__ void st16_pair(bf16* dst, size_t lo, const float (&v)
         if (lo) dst[lo + j] = __ushort_as_bfloat16((uint16_t)((j & 1) ? rw >> 16 : rw & 0xFFFFu));
       }
   }
+}
+
+// The Q/K/V epilogue for 16 consecutive features m.. of token row n (one
+// head of one kind: m and the head size are multiples of 16) from their sums
+// g: RoPE on Q and K by the token's angle (feature pairs 2j, 2j + 1 rotated
+// together), Q to its bf16 pair buffer, K and V to the cache slot (bf16, or
+// E4M3 of x / scale) and to the side buffers when given. The same values as
+// the separate RoPE/append kernel and gemm_tc_kernel's epilogue.
+__device__ __forceinline__ void tm_rope16(const RopeAppendArgs& a, int n, int m, const TokInfo& ti,
+                                          const float (&g)[16]) {
+  const int d = a.head_dim, qw = a.n_q * d, kw = a.n_kv * d;
+  const int kind = m < qw ? 0 : (m < qw + kw ? 1 : 2);
+  const int col = m - (kind == 0 ? 0 : (kind == 1 ? qw : qw + kw));
+  const int gh = col / d, dd = col - gh * d;
+  float v[16];
+  if (kind == 2 || ti.pos < 0) {  // V, or a position outside the table (angle 0)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = g[j];
+  } else {
+    const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)ti.pos * (d / 2) + (dd >> 1));
+    // the separate RoPE kernel's expressions term for term, so that both
+    // round (and contract into FMAs) alike and write bit-identical values
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // pairs (4i, 4i+1) and (4i+2, 4i+3)
+      const float4 c = __ldg(cs + i);
+      const float x0 = g[4 * i], x1 = g[4 * i + 1], x2 = g[4 * i + 2], x3 = g[4 * i + 3];
+      v[4 * i] = x0 * c.x - x1 * c.y;
+      v[4 * i + 1] = x0 * c.y + x1 * c.x;
+      v[4 * i + 2] = x2 * c.z - x3 * c.w;
+      v[4 * i + 3] = x2 * c.w + x3 * c.z;
+    }
+  }
+  if (kind == 0) {
+    st16_pair(reinterpret_cast<bf16*>(a.q_out) + (size_t)n * qw + col, a.q_lo, v, 16);
+    return;
+  }
+  const bool is_v = kind == 2;
+  bf16* side = reinterpret_cast<bf16*>(is_v ? a.v_out : a.k_out);
+  const long long slot =
+      ti.kv < 0 ? -1 : ti.kv + (long long)gh * (a.page_size ? a.page_size : a.capacity);
+  if (a.kv_fp8) {  // the cache holds e4m3(x / scale); the side buffers its e4m3 value
+    const float sc = is_v ? a.v_scale : a.k_scale;
+    uint32_t w[4];
+    float dq[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[i] = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint8_t q8 = f32_to_e4m3(v[4 * i + e] / sc);
+        dq[4 * i + e] = e4m3_to_f32(q8);
+        w[i] |= (uint32_t)q8 << (8 * e);
+      }
+    }
+    if (side) st16_pair(side + (size_t)n * kw + col, 0, dq, 16);
+    if (slot >= 0) {
+      uint8_t* c8 = reinterpret_cast<uint8_t*>(is_v ? a.v_cache : a.k_cache) + slot * d + dd;
+      if ((reinterpret_cast<uintptr_t>(c8) & 15u) == 0) {
+        *reinterpret_cast<uint4*>(c8) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) c8[j] = (uint8_t)(w[j >> 2] >> (8 * (j & 3)));
+      }
+    }
+    return;
+  }
+  if (side) st16_pair(side + (size_t)n * kw + col, 0, v, 16);
+  if (slot >= 0)
+    st16_pair(reinterpret_cast<bf16*>(is_v ? a.v_cache : a.k_cache) + slot * d + dd, 0, v, 16);
 }
 
 }  // namespace
@@ -334,6 +407,8 @@ __global__ void __launch_bounds__(TM_THREADS, 1)
         for (int tt = 0; tt < p.ssq_tiles; ++tt) ss += p.ssq_in[(size_t)tt * p.ssq_ld + n];
         scl = 1.0f / sqrtf(ss * p.norm_inv_h + p.norm_eps);
       }
+      const TokInfo ti =
+          EPI == kEpiRope && row_ok ? rope_token(p.rope, n) : TokInfo{-1, -1, 0};
       const uint32_t tb = tq + (uint32_t)(b * TM_BN);
       const int m0 = feat * p.fw;
       const size_t row = (size_t)(row_ok ? n : 0) * p.ldo;
@@ -360,7 +435,9 @@ __global__ void __launch_bounds__(TM_THREADS, 1)
         const int m = m0 + c0;
         const int valid = row_ok ? min(16, p.M - m) : 0;
         if (valid <= 0) continue;
-        if (EPI == LLAMA_EPI_STORE_F32) {
+        if (EPI == kEpiRope) {
+          tm_rope16(p.rope, n, m, ti, g);
+        } else if (EPI == LLAMA_EPI_STORE_F32) {
           st16_f32(reinterpret_cast<float*>(p.out) + row + m, g, valid);
         } else if (EPI == LLAMA_EPI_RESID_F32) {
           float* o = reinterpret_cast<float*>(p.out) + row + m;
@@ -409,20 +486,31 @@ __global__ void __launch_bounds__(TM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host side
-bool gemm_tm_applies(const GemmCall& g) {
-  if (g.dtype != LLAMA_BF16 || !g.split || g.w_scale || g.rope) return false;
-  if (g.epi != LLAMA_EPI_STORE_F32 && g.epi != LLAMA_EPI_RESID_F32 &&
-      g.epi != LLAMA_EPI_STORE_T && g.epi != LLAMA_EPI_SWIGLU)
+bool gemm_tm_shape(int epi, int M, int N, int split, int sm_count) {
+  if (!split) return false;
+  if (epi != LLAMA_EPI_STORE_F32 && epi != LLAMA_EPI_RESID_F32 && epi != LLAMA_EPI_STORE_T &&
+      epi != LLAMA_EPI_SWIGLU && epi != kEpiRope)
     return false;
-  if (gemm_box_rows(g.N, g.split) != TM_BM || g.M > g.ldo) return false;  // 128-row boxes
-  const int fw = g.epi == LLAMA_EPI_SWIGLU ? 128 : TM_BN;
-  const long tiles = (long)((g.N + TM_BM - 1) / TM_BM) * ((g.M + fw - 1) / fw);
-  return tiles >= std::max(1, g.sm_count);  // at least one tile for every SM
+  if (gemm_box_rows(N, split) != TM_BM) return false;  // 128-row activation boxes
+  const int fw = epi == LLAMA_EPI_SWIGLU ? 128 : TM_BN;
+  const long tiles = (long)((N + TM_BM - 1) / TM_BM) * ((M + fw - 1) / fw);
+  return tiles >= std::max(1, sm_count);  // at least one tile for every SM
+}
+
+bool gemm_tm_applies(const GemmCall& g) {
+  if (g.dtype != LLAMA_BF16 || g.w_scale) return false;
+  if (g.epi == kEpiRope) {
+    if (!g.rope || g.rope->head_dim % 16 != 0) return false;
+  } else if (g.rope || g.M > g.ldo) {
+    return false;
+  }
+  return gemm_tm_shape(g.epi, g.M, g.N, g.split, g.sm_count);
 }
 
 template <int EPI>
 static cudaError_t launch_tm(const GemmCall& g, cudaStream_t st) {
   TmParams p{};
+  if (g.rope) p.rope = *g.rope;
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
@@ -458,6 +546,7 @@ cudaError_t launch_gemm_tm(const GemmCall& g, cudaStream_t st) {
     case LLAMA_EPI_STORE_F32: return launch_tm<LLAMA_EPI_STORE_F32>(g, st);
     case LLAMA_EPI_RESID_F32: return launch_tm<LLAMA_EPI_RESID_F32>(g, st);
     case LLAMA_EPI_STORE_T: return launch_tm<LLAMA_EPI_STORE_T>(g, st);
+    case kEpiRope: return launch_tm<kEpiRope>(g, st);
     default: return launch_tm<LLAMA_EPI_SWIGLU>(g, st);
   }
 }
@@ -470,6 +559,8 @@ cudaError_t gemm_tm_prepare() {
   if ((e = cudaFuncSetAttribute(gemm_tm_kernel<LLAMA_EPI_RESID_F32>, a, (int)TM_SMEM)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(gemm_tm_kernel<LLAMA_EPI_STORE_T>, a, (int)TM_SMEM)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(gemm_tm_kernel<kEpiRope>, a, (int)TM_SMEM)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(gemm_tm_kernel<LLAMA_EPI_SWIGLU>, a, (int)TM_SMEM);
 }

@@ -156,3 +156,29 @@ def test_extend_host_checks():
     m.extend(tk, cu, st, kv, lg, max_rows=3)
     rc, flags = m.sync_status()
     assert rc == 5 and flags & binding.FLAG_POS_RANGE
+
+
+def test_prefill_fused_qkv_epilogue_writes_the_cache_of_the_separate_pass():
+    # A 7B layer over 2 x 320 prompt rows. Prefill rotates Q/K and appends
+    # K/V in the token-major GEMM's epilogue; an extend step of the same
+    # whole prompts stores the fp32 Q/K/V sums and runs the separate RoPE
+    # kernel. Both round the same sums with the same expressions, so the
+    # cache (layer 0: no attention output in between) agrees bit for bit.
+    # (Extend steps take bf16 caches only; the fused E4M3 append is checked
+    # against the oracle in the FP8 tests.)
+    need_gpu()
+    shape, B, T, seed = L7, 2, 320, 2104
+    lw = synth.layer_weights(shape, seed, 0, std=0.02)
+    x = synth.hidden_input(B * T, shape.hidden, seed)
+    m = binding.Model(shape, to_dev({"layers": [lw]}), max_batch=B, max_tokens=B * T,
+                      max_seq=T, has_embed_head=False)
+    kv1 = binding.KVCache(shape, batch=B, capacity=T)
+    kv2 = binding.KVCache(shape, batch=B, capacity=T)
+    h1 = x.cuda()
+    m.prefill_hidden(h1, B, T, kv1)
+    h2 = x.cuda()
+    cu = torch.tensor([0, T, 2 * T], dtype=torch.int32, device="cuda")
+    m.extend_hidden(h2, cu, torch.zeros(B, dtype=torch.int32, device="cuda"), kv2)
+    m.sync()
+    assert torch.equal(kv1.k, kv2.k) and torch.equal(kv1.v, kv2.v)
+    assert_close(h1, f64(h2), BF16_TOL, "prefill and extend of the same prompts")

@@ -143,6 +143,32 @@ def test_layer_decode_7b_e4m3_cache():
     _near(got, K[np.arange(B), :, S], KS)
 
 
+def test_layer_prefill_7b_e4m3_cache_token_major_gemms():
+    # 640 prompt rows: the Q/K/V projection (with RoPE and the E4M3 append in
+    # its epilogue) and gate/up run on the persistent token-major GEMM, the O
+    # and down projections (80 tiles) on the other one
+    need_gpu()
+    shape, B, T, seed = L7, 2, 320, 2103
+    lw = synth.layer_weights(shape, seed, 0, std=0.02)
+    kv = binding.KVCache(shape, batch=B, capacity=T, e4m3=(KS, VS))
+    x = synth.hidden_input(B * T, shape.hidden, seed)
+    m = binding.Model(shape, to_dev({"layers": [lw]}), max_batch=B, max_tokens=B * T, max_seq=T,
+                      has_embed_head=False)
+    h = x.cuda()
+    m.prefill_hidden(h, B, T, kv)
+    m.sync()
+    rows = [0, 1, 127, 128, 255, 319]
+    K = np.zeros((B, shape.n_kv_heads, T, shape.head_dim))
+    V = np.zeros_like(K)
+    lw64 = {k: f64(v) for k, v in lw.items()}
+    ref = O.layer_prefill(f64(x).reshape(B, T, -1), lw64, shape, K, V, rows=rows,
+                          cache_dtype=("e4m3", KS, VS))
+    assert_close(f64(h).reshape(B, T, -1)[:, rows], ref, BF16_TOL, "prefill rows, e4m3 cache")
+    for t in (0, 200, 319):
+        _near(_e4m3_values(kv.k)[0][:, :, t] * KS, K[:, :, t], KS)
+        _near(_e4m3_values(kv.v)[0][:, :, t] * VS, V[:, :, t], VS)
+
+
 def test_prefill_then_decode_small_model_e4m3():
     need_gpu()
     shape = synth.Shape(2, 256, 4, 2, 128, 512, 512, dtype="bf16")
