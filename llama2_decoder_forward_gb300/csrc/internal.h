@@ -143,9 +143,9 @@ inline int gemm_box_rows(int N, int split) {
 }
 cudaError_t launch_gemm(const GemmCall& g, cudaStream_t st);
 cudaError_t gemm_prepare();  // sets kernel attributes once per process
-// Prefill-sized bf16 pair-operand projections (at least one 128-row x
-// 256-feature tile per SM): the persistent kernel with the activation rows on
-// the MMA's M side. launch_gemm takes this path whenever it applies.
+// Prefill-sized bf16 pair-operand projections (at least 0.9 tiles of 128
+// rows x 256 features per SM): the persistent kernel with the activation rows
+// on the MMA's M side. launch_gemm takes this path whenever it applies.
 bool gemm_tm_shape(int epi, int M, int N, int split, int sm_count);  // by shape alone
 bool gemm_tm_applies(const GemmCall& g);
 cudaError_t launch_gemm_tm(const GemmCall& g, cudaStream_t st);

@@ -494,7 +494,10 @@ bool gemm_tm_shape(int epi, int M, int N, int split, int sm_count) {
   if (gemm_box_rows(N, split) != TM_BM) return false;  // 128-row activation boxes
   const int fw = epi == LLAMA_EPI_SWIGLU ? 128 : TM_BN;
   const long tiles = (long)((N + TM_BM - 1) / TM_BM) * ((M + fw - 1) / fw);
-  return tiles >= std::max(1, sm_count);  // at least one tile for every SM
+  // about one tile for every SM or more: at 144 tiles on 152 SMs (the O and
+  // down projections of a 1052-row extend step) this kernel measured 2.7 %
+  // faster for the whole step than the weights-on-M tiles
+  return tiles * 10 >= 9L * std::max(1, sm_count);
 }
 
 bool gemm_tm_applies(const GemmCall& g) {

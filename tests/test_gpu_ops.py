@@ -139,6 +139,7 @@ def _pair(x):
     (4096, 1200, 1024, "store_t"),
     (2900, 1200, 4096, "swiglu"),      # ragged features with gate and up halves
     (12200, 1000, 4096, "store_f32"),  # M % 16 != 0: unaligned rows, element stores
+    (4096, 1100, 4096, "resid"),       # 144 tiles: one round on fewer CTAs than SMs
 ])
 def test_linear_bf16_pair_operands(ctx7, M, N, K, epi):
     # fp32 activations carried as bf16 hi + lo: the product tracks the fp32 values
